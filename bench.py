@@ -1,0 +1,484 @@
+"""Benchmark of the 3.25-bit codebook-quantised decode matmul on GB300.
+
+Workload (one "step"): the dense decode batch K=4096, N=12288 (a fused
+gate+up projection) called once at each of M = 1, 2, 4, 8 token rows, every
+call on a different copy of the packed weights (32 rotating copies, 657 MB,
+more than 4x the 129 MB L2, so weight bytes come from HBM).  Activations,
+a_scale and codebooks are seeded synthetic data of the pages' distributions.
+
+Metric: effective weight GB/s = packed weight bytes (3KN/8 + KN/32 + 8N per
+call) / time.  The timed region is K steps replayed from a CUDA graph, timed
+with CUDA events on the launching stream; per-kernel durations come from
+events between the kernels of the graph.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain C implementation under
+oracle/) on a bounded row sample of the same workload on the host cores.
+Under torchrun every rank runs its own replica (the matmul needs no
+exchange); value is the sum over ranks of the bytes processed divided by the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_codebook_quantized_gb300 import ops, synth  # noqa: E402
+
+K_DIM, N_DIM = 4096, 12288
+MS = (1, 2, 4, 8)
+ROTATE = 32
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "effective weight GB/s and % of GB300 HBM roofline per cbq_gemm call (M=1..64)"
+WORKLOAD = "decode_4096x12288: cbq_gemm at M=1,2,4,8, K=4096, N=12288 (fused gate+up)"
+
+
+def weight_bytes(N=N_DIM, K=K_DIM) -> int:
+    return 3 * K * N // 8 + K * N // 32 + 8 * N
+
+
+def call_bytes(M, N=N_DIM, K=K_DIM) -> int:
+    """Algorithmic bytes of one call: packed weights, activations, a_scale, y."""
+    return weight_bytes(N, K) + M * K + 4 * M + 4 * M * N
+
+
+# ---------------------------------------------------------------- helpers --
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws, backend):
+    if ws > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend)
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def reduce_max_sum(ws, t_max: float, units: float, device):
+    """(max over ranks of t_max, sum over ranks of units)."""
+    if ws == 1:
+        return t_max, units
+    t = torch.tensor([t_max], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for key in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if key in d:
+                    v = d[key]
+                    v = v.get("value", v) if isinstance(v, dict) else v
+                    return float(v), "measured (MEASURED_PEAKS.json hbm_gbs)"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader",
+                 "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1].split()[0]))
+                maxs.append(float(parts[2].split()[0]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sms) if sms else None,
+                "sm_max_mhz": max(maxs) if maxs else None,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_codebook_quantized_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """dram bytes per launch from the committed ncu summary of this workload,
+    or None when the summary is missing or the kernel sources changed since."""
+    p = os.path.join(ROOT, "profiles", "cbq_gemm_decode_4096x12288.md")
+    if not os.path.exists(p):
+        return None
+    src, per_m = None, {}
+    for line in open(p):
+        if line.startswith("kernel_source_sha256:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith(f"dram_bytes_per_launch[{kernel}]"):
+            k, v = line.split(":", 1)
+            per_m[k.split("M=")[1].rstrip("]").strip()] = float(v)
+    if src != kernel_source_hash() or not per_m:
+        return None
+    return per_m
+
+
+# --------------------------------------------------------------- our arm --
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(ws, "nccl")
+    dev = torch.device("cuda", local)
+    from bit_codebook_quantized_gb300 import build as _b
+    if rank == 0 or ws == 1:
+        _b.build()
+    barrier(ws)
+    _b.build()
+    ops.lib()
+
+    # ---- inputs, resident in HBM before the timed region --------------------
+    pw = synth.gen_weights(N_DIM, K_DIM, seed=1)
+    w0 = ops.PackedWeights.from_host(pw.codes, pw.scales, pw.codebooks, N_DIM, K_DIM, device=dev)
+    copies = [w0] + [ops.PackedWeights(w0.codes.clone(), w0.scales.clone(), w0.codebooks.clone(),
+                                       N_DIM, K_DIM) for _ in range(ROTATE - 1)]
+    acts = {M: torch.from_numpy(synth.gen_activations(M, K_DIM, seed=10 + M)).to(dev) for M in MS}
+    scs = {M: torch.from_numpy(synth.gen_a_scale(M, seed=20 + M, mode="uniform")).to(dev)
+           for M in MS}
+    ys = {M: torch.empty((M, N_DIM), dtype=torch.float32, device=dev) for M in MS}
+    stream = torch.cuda.Stream(device=dev)
+
+    call = [0]
+
+    def step():
+        for M in MS:
+            w = copies[call[0] % ROTATE]
+            call[0] += 1
+            ops.gemm(acts[M], scs[M], w, out=ys[M], stream=stream)
+
+    # ---- warm-up (untimed, eager) --------------------------------------------
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    stream.synchronize()
+    if ops.device_status(stream) != ops.OK:
+        raise RuntimeError("device status not ok after warm-up")
+
+    # ---- capture a graph of S steps with an event between every kernel -------
+    S = min(args.steps, 250)
+    while args.steps % S:
+        S -= 1
+    reps = args.steps // S
+    try:   # event-record nodes inside the graph time every kernel of the replay
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(S * len(MS) + 1)]
+    except TypeError:
+        evs = None
+    g = torch.cuda.CUDAGraph()
+    launches_before = ops.launch_count()
+    with torch.cuda.graph(g, stream=stream):
+        e = 0
+        if evs:
+            evs[e].record(stream)
+        for _ in range(S):
+            for M in MS:
+                w = copies[call[0] % ROTATE]
+                call[0] += 1
+                ops.gemm(acts[M], scs[M], w, out=ys[M], stream=stream)
+                e += 1
+                if evs:
+                    evs[e].record(stream)
+    launches_per_graph = ops.launch_count() - launches_before
+    g.replay()
+    stream.synchronize()
+
+    # ---- timed region ---------------------------------------------------------
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    elapsed_s = t0.elapsed_time(t1) / 1e3
+    st = ops.device_status(stream)
+    if st != ops.OK:
+        raise RuntimeError(f"device status {st} after timed region")
+
+    # per-kernel durations from the events of the last replay
+    if evs:
+        per_m_ms = {M: [] for M in MS}
+        for i in range(S * len(MS)):
+            per_m_ms[MS[i % len(MS)]].append(evs[i].elapsed_time(evs[i + 1]))
+        per_m_us = {M: 1e3 * float(np.mean(v)) for M, v in per_m_ms.items()}
+        kernel_timing = "event-record nodes between the kernels of the timed graph"
+    else:
+        per_m_us = time_per_m(stream, copies, acts, scs, ys, call)
+        kernel_timing = "separate graphs per M right after the timed region (no external events)"
+
+    units = args.steps * len(MS) * weight_bytes()
+    t_max, units_all = reduce_max_sum(ws, elapsed_s, units, dev)
+    value = units_all / t_max / 1e9
+
+    # ---- e2e through the public API with host buffers --------------------------
+    e2e = run_e2e(dev, stream, copies, args)
+
+    peak, peak_src = measured_peak()
+    per_call = []
+    for M in MS:
+        us = per_m_us[M]
+        per_call.append({"M": M, "us": round(us, 3),
+                         "weight_GBps": round(weight_bytes() / us / 1e3, 1),
+                         "roofline_frac": round(call_bytes(M) / us / 1e3 / peak, 4),
+                         "tokens_per_s": round(M / us * 1e6, 1)})
+    # dominant kernel: everything here runs in the small-M kernel
+    dom_bytes = sum(call_bytes(M) for M in MS) / len(MS)
+    dom_us = float(np.mean([per_m_us[M] for M in MS]))
+    traffic = profiled_traffic("gemv_kernel")
+    roof = {"bound": "hbm", "kernel": "gemv_kernel (M=1,2,4,8)",
+            "achieved": round(dom_bytes / dom_us / 1e3, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(dom_bytes / dom_us / 1e3 / peak, 4),
+            "traffic": (round(float(np.mean(list(traffic.values()))), 0) if traffic else None),
+            "algorithmic_bytes_per_launch": int(dom_bytes), "peak_source": peak_src}
+
+    cpu = None
+    if rank == 0 and ws == 1 and args.cpu_seconds > 0:
+        cpu = cpu_baseline(seconds=args.cpu_seconds)
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t_max * 1e3 / args.steps, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3", "data": "synthetic (seeded; packed 3-bit codes, E4M3 codebooks "
+                                    "and activations, E8M0 scales)",
+            "config": {"workload": WORKLOAD, "M": list(MS), "K": K_DIM, "N": N_DIM,
+                       "weight_bytes_per_call": weight_bytes(),
+                       "l2": f"inputs larger than L2: {ROTATE} rotating weight copies "
+                             f"({ROTATE * weight_bytes() / 1e6:.0f} MB) vs 129 MB L2",
+                       "timing": f"CUDA graph of {S} steps replayed {reps}x, CUDA events; "
+                                 f"per-kernel: {kernel_timing}",
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": roof, "per_call": per_call,
+            "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": int(launches_per_graph * reps),
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def time_per_m(stream, copies, acts, scs, ys, call, launches=200):
+    out = {}
+    for M in MS:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(launches):
+                ops.gemm(acts[M], scs[M], copies[call[0] % ROTATE], out=ys[M], stream=stream)
+                call[0] += 1
+        g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        stream.synchronize()
+        out[M] = 1e3 * a.elapsed_time(b) / launches
+    return out
+
+
+def run_e2e(dev, stream, copies, args):
+    """Same metric through the public API with host buffers: every step copies
+    the activations and a_scale from pinned host memory, runs cbq_gemm for
+    M = 1, 2, 4, 8 and reads every y back to pinned host memory."""
+    host_a = {M: torch.from_numpy(synth.gen_activations(M, K_DIM, seed=10 + M)).pin_memory()
+              for M in MS}
+    host_s = {M: torch.from_numpy(synth.gen_a_scale(M, seed=20 + M, mode="uniform")).pin_memory()
+              for M in MS}
+    host_y = {M: torch.empty((M, N_DIM), dtype=torch.float32).pin_memory() for M in MS}
+    dev_a = {M: torch.empty((M, K_DIM), dtype=torch.uint8, device=dev) for M in MS}
+    dev_s = {M: torch.empty(M, dtype=torch.float32, device=dev) for M in MS}
+    dev_y = {M: torch.empty((M, N_DIM), dtype=torch.float32, device=dev) for M in MS}
+    steps = max(20, min(args.steps, 500))
+    call = 0
+
+    def one():
+        nonlocal call
+        with torch.cuda.stream(stream):
+            for M in MS:
+                dev_a[M].copy_(host_a[M], non_blocking=True)
+                dev_s[M].copy_(host_s[M], non_blocking=True)
+                ops.gemm(dev_a[M], dev_s[M], copies[call % ROTATE], out=dev_y[M], stream=stream)
+                call += 1
+                host_y[M].copy_(dev_y[M], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        one()
+    t = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = time.perf_counter() - t
+    h2d = sum(M * K_DIM + 4 * M for M in MS)
+    d2h = sum(4 * M * N_DIM for M in MS)
+    return {"value": round(steps * len(MS) * weight_bytes() / dt / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(dt * 1e3 / steps, 4)}
+
+
+# ------------------------------------------------------- oracle (CPU) arm --
+
+def _oracle_step(o, pw, acts, scs, rows):
+    sel = np.arange(rows)
+    for M in MS:
+        o.gemm(acts[M], scs[M], pw.codes[sel], pw.scales[sel], pw.codebooks[sel], M, rows, K_DIM)
+
+
+def cpu_baseline(seconds: float):
+    """The oracle as it stands, on the host cores, on a row sample of the step."""
+    import oracle as o
+    pw = synth.gen_weights(N_DIM, K_DIM, seed=1)
+    acts = {M: synth.gen_activations(M, K_DIM, seed=10 + M) for M in MS}
+    scs = {M: synth.gen_a_scale(M, seed=20 + M, mode="uniform") for M in MS}
+    rows = 64
+    t = time.perf_counter()
+    _oracle_step(o, pw, acts, scs, rows)
+    probe = time.perf_counter() - t
+    rows = int(min(N_DIM, max(64, rows * seconds / max(probe, 1e-3))))
+    t = time.perf_counter()
+    _oracle_step(o, pw, acts, scs, rows)
+    dt = time.perf_counter() - t
+    units = len(MS) * weight_bytes() * rows / N_DIM
+    return {"value": round(units / dt / 1e9, 4), "unit": "GB/s", "cores": o.num_threads(),
+            "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of N={N_DIM} at each M in {list(MS)}, one pass "
+                      f"({dt:.1f} s); plain C, fp64, OpenMP over rows",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if ws > 1:
+        dist_init(ws, "gloo")
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+    import oracle as o
+    o.build()
+    pw = synth.gen_weights(N_DIM, K_DIM, seed=1)
+    acts = {M: synth.gen_activations(M, K_DIM, seed=10 + M) for M in MS}
+    scs = {M: synth.gen_a_scale(M, seed=20 + M, mode="uniform") for M in MS}
+    # size each step's row sample so warm-up + timed steps take about a minute
+    t = time.perf_counter()
+    _oracle_step(o, pw, acts, scs, 16)
+    per_row = (time.perf_counter() - t) / 16
+    total_steps = max(1, args.steps + args.warmup)
+    rows = int(min(N_DIM, max(1, 60.0 / total_steps / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        _oracle_step(o, pw, acts, scs, rows)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(o, pw, acts, scs, rows)
+    dt = time.perf_counter() - t
+    units = args.steps * len(MS) * weight_bytes() * rows / N_DIM
+    value = units / dt / 1e9
+    out = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "impl": "reference",
+           "config": {"workload": WORKLOAD, "M": list(MS), "K": K_DIM, "N": N_DIM},
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": o.num_threads(),
+                            "kind": "oracle",
+                            "sample": f"each step: rows 0..{rows - 1} of N={N_DIM} at every M"},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU-baseline budget on rank 0 (0 disables)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

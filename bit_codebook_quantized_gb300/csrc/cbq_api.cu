@@ -1,0 +1,239 @@
+// cbq_api.cu -- the C entry points declared in include/cbq.h: argument
+// checks, tensor-map encoding, kernel selection.  All device work is done by
+// the kernels in cbq_gemv.cu and cbq_umma.cu; this file launches them on the
+// caller's stream and never synchronises (except cbq_device_status).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "cbq_internal.h"
+
+namespace cbq {
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+struct DeviceInfo {
+  int sm_count = 0;
+  int supported = -1;  // -1 unknown, 0 no, 1 yes
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_dev_mutex;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int current_device_checked(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CBQ_EDEVICE;
+  std::lock_guard<std::mutex> lk(g_dev_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (d.supported < 0) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return CBQ_EDEVICE;
+    // The kernels are compiled for sm_103a only.
+    d.supported = (prop.major == 10 && prop.minor == 3) ? 1 : 0;
+    d.sm_count = prop.multiProcessorCount;
+  }
+  if (!d.supported) return CBQ_EDEVICE;
+  if (out) *out = &d;
+  return CBQ_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool weight_ok(const cbq_weight_t* w) {
+  return w && w->codes && w->scales && w->codebooks && aligned(w->codes, 16) &&
+         aligned(w->scales, 16) && aligned(w->codebooks, 16);
+}
+
+}  // namespace
+
+int device_sm_count() {
+  DeviceInfo* d = nullptr;
+  if (current_device_checked(&d) != CBQ_OK) return 1;
+  return d->sm_count;
+}
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int make_tmap_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch,
+                 uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return CBQ_ECUDA;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CBQ_OK : CBQ_ECUDA;
+}
+
+}  // namespace cbq
+
+using namespace cbq;
+
+extern "C" {
+
+int cbq_packed_sizes(int32_t N, int32_t K, size_t* codes_bytes, size_t* scales_bytes,
+                     size_t* codebook_bytes) {
+  if (N < 0 || K < 0 || K % 128 != 0) return CBQ_EINVAL;
+  const size_t n = static_cast<size_t>(N), k = static_cast<size_t>(K);
+  if (codes_bytes) *codes_bytes = 3 * k * n / 8;
+  if (scales_bytes) *scales_bytes = k * n / 32;
+  if (codebook_bytes) *codebook_bytes = 8 * n;
+  return CBQ_OK;
+}
+
+int cbq_pack(const float* W, int32_t N, int32_t K, uint8_t* codes, uint8_t* scales,
+             uint8_t* codebooks) {
+  if (N < 0 || K <= 0 || K % 128 != 0) return CBQ_EINVAL;
+  if (N == 0) return CBQ_OK;
+  if (!W || !codes || !scales || !codebooks) return CBQ_EINVAL;
+  return pack_host(W, N, K, codes, scales, codebooks);
+}
+
+int cbq_unpack(const cbq_weight_t* w, int32_t N, int32_t K, float* W_out, void* stream) {
+  if (N < 0 || K < 0 || K % 128 != 0) return CBQ_EINVAL;
+  if (N == 0 || K == 0) return CBQ_OK;
+  if (!weight_ok(w) || !W_out || !aligned(W_out, 16)) return CBQ_EINVAL;
+  int st = current_device_checked(nullptr);
+  if (st != CBQ_OK) return st;
+  return launch_unpack(w->codes, w->scales, w->codebooks, N, K, W_out,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w, int32_t M,
+                  int32_t N, int32_t K, float* y, void* stream, int32_t path) {
+  if (M < 0 || M > 64 || N < 0 || K < 0 || K % 128 != 0) return CBQ_EINVAL;
+  if (path < CBQ_PATH_AUTO || path > CBQ_PATH_MMA) return CBQ_EINVAL;
+  if (M == 0 || N == 0) return CBQ_OK;
+  if (!y || !aligned(y, 4)) return CBQ_EINVAL;
+  int st = current_device_checked(nullptr);
+  if (st != CBQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    return cudaMemsetAsync(y, 0, sizeof(float) * size_t(M) * size_t(N), s) == cudaSuccess
+               ? CBQ_OK
+               : CBQ_ECUDA;
+  }
+  if (!a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(w))
+    return CBQ_EINVAL;
+  if (path == CBQ_PATH_AUTO) path = CBQ_PATH_GEMV;
+  if (path == CBQ_PATH_GEMV) {
+    GemvParams p;
+    std::memset(&p, 0, sizeof(p));
+    st = make_tmap_2d(&p.tmap_codes, w->codes, uint64_t(K) * 3 / 8, uint64_t(N),
+                      uint64_t(K) * 3 / 8, 48, 16, false);
+    if (st != CBQ_OK) return st;
+    p.a = a;
+    p.a_scale = a_scale;
+    p.scales = w->scales;
+    p.codebooks = w->codebooks;
+    p.y = y;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    return launch_gemv(p, false, s);
+  }
+  UmmaParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.a = a;
+  p.a_scale = a_scale;
+  p.scales = w->scales;
+  p.codebooks = w->codebooks;
+  p.y = y;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  st = make_tmap_2d(&p.tmap_codes, w->codes, uint64_t(K) * 3 / 8, uint64_t(N),
+                    uint64_t(K) * 3 / 8, 48, 128, false);
+  if (st != CBQ_OK) return st;
+  return launch_umma(p, false, s);
+}
+
+int cbq_gemm(const uint8_t* a, const float* a_scale, const cbq_weight_t* w, int32_t M, int32_t N,
+             int32_t K, float* y, void* stream) {
+  return cbq_gemm_path(a, a_scale, w, M, N, K, y, stream, CBQ_PATH_AUTO);
+}
+
+int cbq_grouped_gemm(const uint8_t* a, const float* a_scale, const cbq_weight_t* experts,
+                     int32_t E, const int32_t* topk_idx, int32_t topk, int32_t M, int32_t N,
+                     int32_t K, float* y, void* stream) {
+  if (M < 0 || M > 64 || N < 0 || K < 0 || K % 128 != 0 || E < 1 || E > 4096 || topk < 1 ||
+      topk > 8 || topk > E)
+    return CBQ_EINVAL;
+  if (M == 0 || N == 0) return CBQ_OK;
+  if (!y || !aligned(y, 4) || !topk_idx || !aligned(topk_idx, 4)) return CBQ_EINVAL;
+  if (static_cast<int64_t>(E) * N > INT32_MAX) return CBQ_EINVAL;
+  int st = current_device_checked(nullptr);
+  if (st != CBQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    return cudaMemsetAsync(y, 0, sizeof(float) * size_t(M) * topk * size_t(N), s) == cudaSuccess
+               ? CBQ_OK
+               : CBQ_ECUDA;
+  }
+  if (!a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(experts))
+    return CBQ_EINVAL;
+  GemvParams p;
+  std::memset(&p, 0, sizeof(p));
+  st = make_tmap_2d(&p.tmap_codes, experts->codes, uint64_t(K) * 3 / 8, uint64_t(E) * N,
+                    uint64_t(K) * 3 / 8, 48, 16, false);
+  if (st != CBQ_OK) return st;
+  p.a = a;
+  p.a_scale = a_scale;
+  p.scales = experts->scales;
+  p.codebooks = experts->codebooks;
+  p.y = y;
+  p.topk_idx = topk_idx;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.E = E;
+  p.topk = topk;
+  return launch_gemv(p, true, s);
+}
+
+int cbq_device_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return CBQ_ECUDA;
+  unsigned v = take_status_gemv(s) | take_status_umma(s);
+  if (v & 1u) return CBQ_ETIMEOUT;
+  if (v & 2u) return CBQ_EROUTING;
+  return CBQ_OK;
+}
+
+uint64_t cbq_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* cbq_status_str(int status) {
+  switch (status) {
+    case CBQ_OK: return "ok";
+    case CBQ_EINVAL: return "invalid argument";
+    case CBQ_ECUDA: return "CUDA call failed";
+    case CBQ_EDEVICE: return "no supported GPU (needs sm_103)";
+    case CBQ_ETIMEOUT: return "a kernel gave up waiting; its output is incomplete";
+    case CBQ_EROUTING: return "routing indices out of range or repeated within a token";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,149 @@
+// cbq_device.cuh -- device-side building blocks shared by the libcbq kernels:
+// the 3-bit code decode, mbarrier / TMA wrappers with bounded waits, and the
+// library's sticky device status word.
+//
+// Format ("Hibana: Fast Agentic Inference on Unified-Memory Devices",
+// section "Model surgery / Three-bit weights"): a group of 32 weights is 12
+// bytes, a 96-bit little-endian number holding code j at bits 3j..3j+2; each
+// code indexes the row's 8-entry E4M3 codebook; one E8M0 scale per group.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace cbq {
+
+// Status bits a kernel can raise (each translation unit keeps its own sticky
+// word; cbq_device_status() collects and clears them).
+enum : unsigned { kErrTimeout = 1u, kErrRouting = 2u };
+
+// Bounded waits give up after this many SM clock cycles (~2 s at 2 GHz).
+constexpr long long kWaitLimitCycles = 4000000000LL;
+
+// ---------------------------------------------------------------------------
+// Decode: 8 codes (a 24-bit field) -> 8 E4M3 bytes through the codebook.
+// ---------------------------------------------------------------------------
+
+// Spread 8 packed 3-bit codes (bits 3j..3j+2 of f, j = 0..7; bits 24..31 of f
+// are ignored) so that code j lands in nibble j.  The result, and the result
+// shifted right by 16, are byte-permute selectors for codes 0-3 and 4-7.
+__device__ __forceinline__ uint32_t spread_codes8(uint32_t f) {
+  uint32_t lo = f & 0x00000FFFu;                  // codes 0-3
+  uint32_t hi = f & 0x00FFF000u;                  // codes 4-7
+  uint32_t h = lo + (hi << 4);                    // codes 4-7 -> bits 16..27
+  uint32_t t = h & 0x0FC00FC0u;                   // codes 2,3 and 6,7
+  h = h + t * 3u;                                 // move them up by 2 bits
+  t = h & 0x38383838u;                            // odd codes
+  return h + t;                                   // move them up by 1 bit
+}
+
+// Four E4M3 codebook bytes for the four codes held in nibbles 0..3 of `sel`
+// (each 0..7; nibble bit 3 clear).  cb_lo holds entries 0-3, cb_hi 4-7.
+__device__ __forceinline__ uint32_t lookup4(uint32_t cb_lo, uint32_t cb_hi, uint32_t sel) {
+  return __byte_perm(cb_lo, cb_hi, sel);
+}
+
+// E8M0 byte -> fp32 2^(s-127) (s = 0 gives the subnormal 2^-127).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+  return s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
+}
+
+// Twenty-four bits of a group starting at bit 24*t: codes 8t..8t+7.  The
+// group's three 32-bit words are w0, w1, w2.
+__device__ __forceinline__ uint32_t group_field(uint32_t w0, uint32_t w1, uint32_t w2, int t) {
+  switch (t) {
+    case 0: return w0;
+    case 1: return __funnelshift_r(w0, w1, 24);
+    case 2: return __funnelshift_r(w1, w2, 16);
+    default: return w2 >> 8;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory addresses, mbarriers, TMA.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+// Make mbarrier initialisation visible to the async (TMA / tensor-core) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// 2-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Named barrier over `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Warp-level FP8 MMA: D(16x8 f32) = A(16x32 e4m3, row) * B(32x8 e4m3, col) + C.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f), "f"(0.f), "f"(0.f),
+        "f"(0.f));
+}
+
+}  // namespace cbq

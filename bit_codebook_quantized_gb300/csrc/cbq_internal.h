@@ -1,0 +1,61 @@
+// cbq_internal.h -- host-side glue between the C entry points (cbq_api.cu)
+// and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/cbq.h"
+
+namespace cbq {
+
+// Kernel parameters of the small-M kernel (dense and grouped).
+struct alignas(128) GemvParams {
+  CUtensorMap tmap_codes;     // 2-D map over codes [rows][3K/8], box [16 rows][48 B]
+  const uint8_t* a;           // [M][K] E4M3
+  const float* a_scale;       // [M]
+  const uint8_t* scales;      // [rows][K/32]
+  const uint8_t* codebooks;   // [rows][8]
+  float* y;                   // dense [M][N]; grouped [M][topk][N]
+  const int32_t* topk_idx;    // grouped only: [M][topk]
+  int M, N, K;
+  int E, topk;                // grouped only
+};
+
+// Kernel parameters of the tcgen05 kernel (dense and grouped).
+struct alignas(128) UmmaParams {
+  CUtensorMap tmap_codes;     // 2-D map over codes [rows][3K/8], box [128 rows][48 B]
+  CUtensorMap tmap_act;       // 2-D map over activations [M][K], box [rows][128 B], 128B swizzle
+  const uint8_t* a;
+  const float* a_scale;
+  const uint8_t* scales;
+  const uint8_t* codebooks;
+  float* y;
+  const int32_t* topk_idx;
+  int M, N, K;
+  int E, topk;
+  int ksplit;                 // K-range split factor (cluster size along K)
+};
+
+int device_sm_count();
+void note_launch();
+
+// Encode a 2-D uint8 tensor map (rows x cols bytes, row pitch `pitch` bytes).
+int make_tmap_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                 uint64_t pitch, uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+
+int launch_gemv(const GemvParams& p, bool grouped, cudaStream_t stream);
+int launch_unpack(const uint8_t* codes, const uint8_t* scales, const uint8_t* codebooks, int N,
+                  int K, float* W, cudaStream_t stream);
+unsigned take_status_gemv(cudaStream_t stream);
+
+int launch_umma(const UmmaParams& p, bool grouped, cudaStream_t stream);
+unsigned take_status_umma(cudaStream_t stream);
+
+// Host quantiser (cbq_pack.cpp).
+int pack_host(const float* W, int N, int K, uint8_t* codes, uint8_t* scales,
+              uint8_t* codebooks);
+
+}  // namespace cbq

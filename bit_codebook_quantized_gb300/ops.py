@@ -1,0 +1,176 @@
+"""ctypes binding of libcbq (include/cbq.h).  Argument marshalling only: every
+step of the matmul runs in the library's CUDA kernels; torch supplies device
+memory and streams.  Each function has the name of its C entry point without
+the ``cbq_`` prefix.
+
+The library must have been built (``python -m bit_codebook_quantized_gb300.build``
+or ``__graft_entry__.build()``); loading raises ``CbqError`` otherwise.  There
+is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcbq.so")
+
+PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
+OK, EINVAL, ECUDA, EDEVICE, ETIMEOUT, EROUTING = 0, -1, -2, -3, -4, -5
+
+# Every symbol include/cbq.h declares.
+EXPORTS = ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path",
+           "cbq_grouped_gemm", "cbq_device_status", "cbq_launch_count", "cbq_status_str")
+
+
+class CbqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)} ({status})")
+
+
+class _Weight(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("codebooks", ctypes.c_void_p)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise CbqError(ECUDA, f"libcbq.so not built at {LIB_PATH}; run the build first")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        L.cbq_packed_sizes.argtypes = [i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz),
+                                       ctypes.POINTER(sz)]
+        L.cbq_pack.argtypes = [vp, i32, i32, vp, vp, vp]
+        L.cbq_unpack.argtypes = [ctypes.POINTER(_Weight), i32, i32, vp, vp]
+        L.cbq_gemm.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp]
+        L.cbq_gemm_path.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp, i32]
+        L.cbq_grouped_gemm.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, vp, i32, i32, i32,
+                                       i32, vp, vp]
+        L.cbq_device_status.argtypes = [vp]
+        L.cbq_launch_count.argtypes = []
+        L.cbq_launch_count.restype = ctypes.c_uint64
+        L.cbq_status_str.argtypes = [ctypes.c_int]
+        L.cbq_status_str.restype = ctypes.c_char_p
+        for name in ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path",
+                     "cbq_grouped_gemm", "cbq_device_status"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+        return L
+
+
+def status_str(status: int) -> str:
+    try:
+        return lib().cbq_status_str(int(status)).decode()
+    except CbqError:
+        return "library not loaded"
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise CbqError(status, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+@dataclass
+class PackedWeights:
+    """Packed matrix resident on the GPU (rows = N, or E*N for stacked experts)."""
+    codes: torch.Tensor      # uint8 [rows, 3K/8]
+    scales: torch.Tensor     # uint8 [rows, K/32]
+    codebooks: torch.Tensor  # uint8 [rows, 8]
+    N: int
+    K: int
+
+    @classmethod
+    def from_host(cls, codes: np.ndarray, scales: np.ndarray, codebooks: np.ndarray, N: int,
+                  K: int, device="cuda") -> "PackedWeights":
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(device)  # noqa: E731
+        return cls(t(codes), t(scales), t(codebooks), N, K)
+
+    def struct(self) -> _Weight:
+        return _Weight(self.codes.data_ptr(), self.scales.data_ptr(), self.codebooks.data_ptr())
+
+    @property
+    def nbytes(self) -> int:
+        return self.codes.numel() + self.scales.numel() + self.codebooks.numel()
+
+
+def packed_sizes(N: int, K: int) -> tuple[int, int, int]:
+    c, s, b = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().cbq_packed_sizes(N, K, ctypes.byref(c), ctypes.byref(s), ctypes.byref(b)),
+           "cbq_packed_sizes")
+    return c.value, s.value, b.value
+
+
+def pack(W: np.ndarray):
+    """Host quantiser: fp32 [N, K] -> (codes, scales, codebooks) numpy uint8."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    N, K = W.shape
+    cs, ss, bs = packed_sizes(N, K)
+    codes = np.zeros(cs, np.uint8)
+    scales = np.zeros(ss, np.uint8)
+    cbs = np.zeros(bs, np.uint8)
+    _check(lib().cbq_pack(W.ctypes.data, N, K, codes.ctypes.data, scales.ctypes.data,
+                          cbs.ctypes.data), "cbq_pack")
+    return codes.reshape(N, -1), scales.reshape(N, -1), cbs.reshape(N, 8)
+
+
+def unpack(w: PackedWeights, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty((w.N, w.K), dtype=torch.float32, device=w.codes.device)
+    ws = w.struct()
+    _check(lib().cbq_unpack(ctypes.byref(ws), w.N, w.K, out.data_ptr(), _stream(stream)),
+           "cbq_unpack")
+    return out
+
+
+def gemm(a: torch.Tensor, a_scale: torch.Tensor, w: PackedWeights,
+         out: torch.Tensor | None = None, path: int = PATH_AUTO, stream=None) -> torch.Tensor:
+    """y[M, N] = a_scale * (a[M, K] @ W^T); a is uint8 E4M3 bytes on the GPU."""
+    M = a.shape[0]
+    if out is None:
+        out = torch.empty((M, w.N), dtype=torch.float32, device=a.device)
+    ws = w.struct()
+    _check(lib().cbq_gemm_path(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(ws), M, w.N, w.K,
+                               out.data_ptr(), _stream(stream), path), "cbq_gemm")
+    return out
+
+
+def grouped_gemm(a: torch.Tensor, a_scale: torch.Tensor, experts: PackedWeights, E: int,
+                 topk_idx: torch.Tensor, out: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """y[M, topk, N] for stacked experts (experts.N = rows per expert)."""
+    M, topk = topk_idx.shape
+    if out is None:
+        out = torch.empty((M, topk, experts.N), dtype=torch.float32, device=a.device)
+    ws = experts.struct()
+    _check(lib().cbq_grouped_gemm(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(ws), E,
+                                  topk_idx.data_ptr(), topk, M, experts.N, experts.K,
+                                  out.data_ptr(), _stream(stream)), "cbq_grouped_gemm")
+    return out
+
+
+def device_status(stream=None) -> int:
+    return int(lib().cbq_device_status(_stream(stream)))
+
+
+def launch_count() -> int:
+    return int(lib().cbq_launch_count())

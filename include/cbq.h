@@ -1,0 +1,141 @@
+/*
+ * cbq.h -- C ABI of the 3.25-bit codebook-quantised matmul library (libcbq).
+ *
+ * Method: "Hibana: Fast Agentic Inference on Unified-Memory Devices",
+ * section "Model surgery / Three-bit weights": every group of 32 weights is a
+ * 3-bit index into an 8-entry FP8 codebook plus one 8-bit scale per group,
+ * 3 + 8/32 = 3.25 bits per weight, and the kernel looks the codes up and feeds
+ * FP8 tensor cores.  Section "Adaptive speculation / Expert sharing": a
+ * speculative-verify round of a mixture-of-experts layer reads only the
+ * experts its tokens route to.
+ *
+ * Packed format (fixed by this library; the pages leave it open):
+ *   codes     uint8 [rows][3K/8]  row-major over K; group g = k/32 of row n is
+ *             the 12 bytes at offset (n*K/32 + g)*12, read as a 96-bit
+ *             little-endian number with code j = k%32 at bits 3j..3j+2.
+ *   scales    uint8 [rows][K/32]  E8M0: value 2^(s-127); 255 (NaN) not allowed.
+ *   codebooks uint8 [rows][8]     OCP FP8 E4M3 ("fn"), one codebook per row.
+ *   w[n,k] = E4M3(codebooks[n][code(n,k)]) * 2^(scales[n][k/32] - 127)
+ *
+ * Matmul: activations a uint8 E4M3 [M][K] row-major, a_scale fp32 [M],
+ *   y[m,n] = a_scale[m] * sum_k E4M3(a[m,k]) * w[n,k]   (fp32 out [M][N]),
+ *   accumulated in fp32 on tensor cores; the summation order is free, so
+ *   results agree with an exact evaluation within 1e-3*a_scale*sum|a*w| + 1e-6.
+ *
+ * Conventions for every entry point:
+ *   - the caller owns every buffer; no entry point allocates device memory;
+ *   - device pointers must be 16-byte aligned (cudaMalloc gives 256);
+ *   - calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream) and never synchronise the host;
+ *   - the return value is CBQ_OK or a negative CBQ_E* code; on an argument
+ *     error nothing is launched; nothing throws across the ABI;
+ *   - requires an sm_103 (GB300) or sm_100 class GPU; K % 128 == 0.
+ */
+#ifndef CBQ_H
+#define CBQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CBQ_OK 0
+#define CBQ_EINVAL (-1)      /* bad argument: null/misaligned pointer, bad size */
+#define CBQ_ECUDA (-2)       /* a CUDA runtime/driver call failed */
+#define CBQ_EDEVICE (-3)     /* no supported GPU on the current device */
+#define CBQ_ETIMEOUT (-4)    /* a kernel gave up waiting (see cbq_device_status) */
+#define CBQ_EROUTING (-5)    /* grouped call: an expert id outside [0,E) or a
+                                token listing one expert twice was seen */
+
+/* Which kernel cbq_gemm_path runs. */
+#define CBQ_PATH_AUTO 0      /* M <= 4: GEMV kernel; M >= 5: tcgen05 kernel */
+#define CBQ_PATH_GEMV 1      /* register-decode + warp MMA kernel, any M <= 64 */
+#define CBQ_PATH_MMA 2       /* TMA + tcgen05 block-scaled FP8 kernel, any M <= 64 */
+
+/* One packed matrix in device memory (all three arrays 16-byte aligned). */
+typedef struct cbq_weight {
+    const uint8_t *codes;      /* [rows][3K/8]  */
+    const uint8_t *scales;     /* [rows][K/32]  */
+    const uint8_t *codebooks;  /* [rows][8]     */
+} cbq_weight_t;
+
+/* Byte sizes of the three packed arrays for an N x K matrix:
+ * 3KN/8, KN/32 and 8N (3.25 bits per weight plus an 8-byte codebook per row,
+ * section "Model surgery / Three-bit weights").  Any pointer may be NULL.
+ * Errors: CBQ_EINVAL if N < 0, K < 0 or K % 128 != 0. */
+int cbq_packed_sizes(int32_t N, int32_t K, size_t *codes_bytes,
+                     size_t *scales_bytes, size_t *codebook_bytes);
+
+/* Quantise fp32 weights W (HOST, [N][K] row-major) into the packed format
+ * (HOST outputs, sized by cbq_packed_sizes).  Runs on the calling thread, is
+ * deterministic, and implements the fitting rule this library fixes for the
+ * pages' "snap each group to a fitted 8-entry FP8 codebook":
+ *   1. per group of 32: s = clamp(127 + ceil(log2 max|w|), 0, 254), 127 if all
+ *      zero, so |w| / 2^(s-127) <= 1;
+ *   2. u = w / 2^(s-127);
+ *   3. per row, 1-D Lloyd with 8 centroids over u: start at the sorted values
+ *      at index floor((i+0.5)K/8); 16 rounds of nearest assignment (ties to the
+ *      lower index) and mean update in k order (empty clusters keep theirs);
+ *   4. round centroids to E4M3 (nearest, ties to even, saturate at 448), sort;
+ *   5. code = nearest rounded centroid (ties to the lower index).
+ * Not on the matmul path (weights are packed once, offline).
+ * Errors: CBQ_EINVAL on NULL pointers, N < 0, K <= 0 or K % 128 != 0, or a
+ * non-finite weight. */
+int cbq_pack(const float *W, int32_t N, int32_t K, uint8_t *codes,
+             uint8_t *scales, uint8_t *codebooks);
+
+/* Decode a packed matrix to fp32 W_out (DEVICE, [N][K]); every value is exact
+ * (an E4M3 value times a power of two).  One kernel launch on `stream`.
+ * Errors: CBQ_EINVAL (null/misaligned pointer, N < 0, K % 128 != 0),
+ * CBQ_EDEVICE, CBQ_ECUDA. */
+int cbq_unpack(const cbq_weight_t *w, int32_t N, int32_t K, float *W_out,
+               void *stream);
+
+/* y[M][N] = a_scale * (a[M][K] x W^T): the decode-step / verify-round matmul
+ * against packed weights.  a, a_scale, y and w's arrays are DEVICE pointers.
+ * 1 <= M <= 64 (M == 0 or N == 0 is a no-op); N >= 0; K % 128 == 0 (K == 0
+ * writes y = 0).  Picks the kernel by M (CBQ_PATH_AUTO); one launch.
+ * Errors: CBQ_EINVAL, CBQ_EDEVICE, CBQ_ECUDA. */
+int cbq_gemm(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
+             int32_t M, int32_t N, int32_t K, float *y, void *stream);
+
+/* Same as cbq_gemm with an explicit kernel choice (CBQ_PATH_*); used by the
+ * tests and the benchmark to exercise each kernel at every M. */
+int cbq_gemm_path(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
+                  int32_t M, int32_t N, int32_t K, float *y, void *stream,
+                  int32_t path);
+
+/* Mixture-of-experts verify round ("Adaptive speculation / Expert sharing"):
+ * the E experts are stacked in one packed matrix (expert e owns rows
+ * e*N .. e*N+N-1 of `experts`), topk_idx is DEVICE int32 [M][topk] and
+ *   y[t][j][:] = a_scale[t] * a[t] x W_{topk_idx[t][j]}^T   (fp32 [M][topk][N]),
+ * with no gate weight and no combine.  Only experts that appear in topk_idx
+ * are read from memory.  The routing is read on the device inside the one
+ * kernel launch.  1 <= M <= 64, 1 <= topk <= 8, 1 <= E <= 4096, each row of
+ * topk_idx must list distinct experts in [0, E); a violation seen on the
+ * device is reported by cbq_device_status as CBQ_EROUTING.
+ * Errors: CBQ_EINVAL, CBQ_EDEVICE, CBQ_ECUDA. */
+int cbq_grouped_gemm(const uint8_t *a, const float *a_scale,
+                     const cbq_weight_t *experts, int32_t E,
+                     const int32_t *topk_idx, int32_t topk, int32_t M,
+                     int32_t N, int32_t K, float *y, void *stream);
+
+/* Synchronise `stream`, then return and clear the sticky device status of
+ * this library on the current device: CBQ_OK, CBQ_ETIMEOUT (a kernel's
+ * bounded wait for a copy or a tensor-core op ran out; the kernel returned
+ * early and its output is incomplete) or CBQ_EROUTING. */
+int cbq_device_status(void *stream);
+
+/* Kernel launches made by this library since load (all entry points). */
+uint64_t cbq_launch_count(void);
+
+/* Human-readable text for a status code (static storage). */
+const char *cbq_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CBQ_H */

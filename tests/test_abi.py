@@ -1,0 +1,114 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, rejects bad arguments before touching the device, and its
+host quantiser matches the oracle's byte for byte."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from bit_codebook_quantized_gb300 import ops, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from bit_codebook_quantized_gb300 import build
+    build.build()
+    return ops.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "cbq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cbq_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared()
+    assert set(names) == set(ops.EXPORTS)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_packed_sizes_closed_form(L):
+    for N, K in [(1, 128), (2048, 2048), (12288, 4096), (5120, 25600), (151936, 2048), (0, 0)]:
+        c, s, b = ops.packed_sizes(N, K)
+        assert (c, s, b) == (3 * K * N // 8, K * N // 32, 8 * N)
+        assert c + s + b == oracle.packed_bytes(N, K)
+    with pytest.raises(ops.CbqError):
+        ops.packed_sizes(16, 96)
+    with pytest.raises(ops.CbqError):
+        ops.packed_sizes(-1, 128)
+
+
+def test_status_strings(L):
+    for s in (0, -1, -2, -3, -4, -5):
+        assert ops.status_str(s) and ops.status_str(s) != "unknown status"
+    assert ops.status_str(7) == "unknown status"
+
+
+def test_argument_errors_before_device(L):
+    w = ops._Weight(16, 16, 16)
+    p = ctypes.byref(w)
+    # K not a multiple of 128, M out of range, bad path, bad topk / E
+    assert L.cbq_gemm(16, 16, p, 1, 8, 96, 16, None) == ops.EINVAL
+    assert L.cbq_gemm(16, 16, p, 65, 8, 128, 16, None) == ops.EINVAL
+    assert L.cbq_gemm(16, 16, p, -1, 8, 128, 16, None) == ops.EINVAL
+    assert L.cbq_gemm_path(16, 16, p, 1, 8, 128, 16, None, 7) == ops.EINVAL
+    assert L.cbq_grouped_gemm(16, 16, p, 0, 16, 1, 1, 8, 128, 16, None) == ops.EINVAL
+    assert L.cbq_grouped_gemm(16, 16, p, 4, 16, 9, 1, 8, 128, 16, None) == ops.EINVAL
+    assert L.cbq_grouped_gemm(16, 16, p, 4, 16, 5, 1, 8, 128, 16, None) == ops.EINVAL
+    assert L.cbq_unpack(p, 8, 100, 16, None) == ops.EINVAL
+    # empty problems are no-ops that succeed without a device
+    assert L.cbq_gemm(0, 0, None, 0, 8, 128, 0, None) == ops.OK
+    assert L.cbq_gemm(0, 0, None, 4, 0, 128, 0, None) == ops.OK
+    assert L.cbq_unpack(None, 0, 128, None, None) == ops.OK
+    assert L.cbq_pack(None, 0, 128, None, None, None) == ops.OK
+    assert L.cbq_pack(None, 4, 128, None, None, None) == ops.EINVAL
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the no-GPU answer")
+def test_no_gpu_is_reported(L):
+    w = ops._Weight(16, 16, 16)
+    st = L.cbq_gemm(16, 16, ctypes.byref(w), 1, 8, 128, 16, None)
+    assert st == ops.EDEVICE
+
+
+def test_pack_rejects_non_finite(L):
+    W = np.zeros((2, 128), np.float32)
+    W[1, 5] = np.nan
+    with pytest.raises(ops.CbqError):
+        ops.pack(W)
+
+
+@pytest.mark.parametrize("N,K,seed", [(5, 128, 1), (9, 256, 2), (3, 512, 3)])
+def test_host_pack_matches_oracle_bytes(L, N, K, seed):
+    W = synth.gen_dense_weights_fp32(N, K, seed)
+    W[0, :32] = 0.0                                  # an all-zero group
+    W[1 % N, 40] = 3e-39                             # a subnormal weight
+    got = ops.pack(W)
+    want = oracle.pack(W)
+    for g_, w_ in zip(got, want):
+        assert np.array_equal(g_, w_)
+
+
+def test_host_pack_matches_oracle_on_few_valued_rows(L):
+    """Rows built from 8 values (many exact ties in the Lloyd rounds) pack to
+    the same bytes as the oracle."""
+    rng = synth.rng_for(77)
+    N, K = 3, 256
+    vals = [-1.0, -0.5, -0.25, 0.0, 0.125, 0.25, 0.5, 1.0]
+    W = np.empty((N, K), np.float32)
+    for n in range(N):
+        u = np.repeat(vals, K // 8)
+        rng.shuffle(u)
+        u[0::32] = [1.0, -1.0] * (K // 64)
+        W[n] = u * np.ldexp(1.0, np.repeat(rng.integers(100, 150, K // 32), 32) - 127)
+    codes, scales, cbs = ops.pack(W)
+    ocodes, oscales, ocbs = oracle.pack(W)
+    assert np.array_equal(codes, ocodes) and np.array_equal(scales, oscales)
+    assert np.array_equal(cbs, ocbs)

@@ -1,0 +1,192 @@
+"""GPU parity: the CUDA kernels against the CPU oracle on the same seeded
+inputs.  Bit-exact for unpack and for one-hot activations; fp32 results
+within |y - y_ref| <= 1e-3 * |a_scale| * sum|a*w| + 1e-6 elsewhere."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_codebook_quantized_gb300 import ops, synth
+from tests.gpu_util import Case, assert_close, ensure_built, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+PATHS = [ops.PATH_GEMV]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+# ---- unpack ------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K,lo,hi", [(37, 384, 120, 127), (300, 4096, 0, 254), (1, 128, 1, 1)])
+def test_unpack_bit_exact(N, K, lo, hi):
+    pw = synth.gen_weights(N, K, seed=N + K, scale_lo=lo, scale_hi=hi)
+    # include negative, subnormal and zero codebook entries
+    pw.codebooks[0] = [0x80, 0x00, 0x01, 0x07, 0x08, 0xB8, 0x7E, 0xFE][:8]
+    w = ops.PackedWeights.from_host(pw.codes, pw.scales, pw.codebooks, N, K)
+    W = ops.unpack(w)
+    torch.cuda.synchronize()
+    ref = oracle.unpack(pw.codes, pw.scales, pw.codebooks, N, K)
+    assert np.array_equal(W.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+# ---- small shapes, every M, both kernels ---------------------------------------
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 9, 16, 24, 33, 64])
+def test_gemm_small(path, M):
+    # N = 200: 12 full 16-row slabs + a ragged slab, and 1 full + 1 ragged 128-row tile
+    # K = 640: 5 chunks of 128, i.e. a ragged last pipeline stage
+    c = Case(M, 200, 640, seed=1000 + M)
+    y = c.run(path)
+    yref, b = c.oracle()
+    assert_close(y, yref, b, f"path {path} M {M}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("N,K", [(16, 128), (1, 128), (129, 256), (2048, 2048), (40, 25600)])
+def test_gemm_shapes(path, N, K):
+    c = Case(3, N, K, seed=N * 7 + K)
+    y = c.run(path)
+    yref, b = c.oracle()
+    assert_close(y, yref, b, f"path {path} N {N} K {K}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_one_hot_is_bit_exact(path):
+    N, K = 150, 512
+    c = Case(8, N, K, seed=5, scale_lo=100, scale_hi=150)
+    ks = [0, 1, 31, 32, 100, 255, 256, 511]
+    c.a[:] = 0
+    for m, k in enumerate(ks):
+        c.a[m, k] = 0x38                      # E4M3 1.0
+    c.s[:] = 1.0
+    y = c.run(path)
+    W = oracle.unpack(c.pw.codes, c.pw.scales, c.pw.codebooks, N, K)
+    for m, k in enumerate(ks):
+        assert np.array_equal(y[m].view(np.uint32), W[:, k].view(np.uint32)), (m, k)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_zero_codes_and_zero_codebook(path):
+    c = Case(4, 70, 384, seed=9)
+    c.pw.codes[:] = 0
+    y = c.run(path)
+    yref, b = c.oracle()
+    assert_close(y, yref, b, "all-zero codes")
+    c2 = Case(4, 70, 384, seed=9)
+    c2.pw.codebooks[:] = 0
+    assert np.all(c2.run(path) == 0)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_a_scale_linearity(path):
+    c = Case(5, 64, 256, seed=17)
+    y1 = c.run(path)
+    a, s, w = c.device()
+    y2 = ops.gemm(a, s * 2, w, path=path).cpu().numpy()
+    assert np.array_equal(y2, 2 * y1)
+
+
+def test_auto_path_matches_both_kernels():
+    for M in (1, 4, 5, 8, 16):
+        c = Case(M, 96, 256, seed=40 + M)
+        yref, b = c.oracle()
+        assert_close(c.run(ops.PATH_AUTO), yref, b, f"auto M {M}")
+
+
+def test_empty_and_zero_k():
+    a = torch.zeros((4, 128), dtype=torch.uint8, device="cuda")
+    s = torch.ones(4, device="cuda")
+    pw = synth.gen_weights(8, 128, 1)
+    w = ops.PackedWeights.from_host(pw.codes, pw.scales, pw.codebooks, 8, 0)
+    y = torch.full((4, 8), 7.0, device="cuda")
+    ops.gemm(a, s, w, out=y)                 # K = 0 -> y = 0
+    torch.cuda.synchronize()
+    assert torch.all(y == 0)
+    w0 = ops.PackedWeights.from_host(pw.codes, pw.scales, pw.codebooks, 0, 128)
+    ops.gemm(a, s, w0, out=y)                # N = 0 -> nothing happens
+    assert ops.device_status() == ops.OK
+
+
+# ---- full workload sizes, sampled rows -------------------------------------------
+
+FULL = ["gemv_2048", "decode_4096x12288_m1", "decode_4096x12288_m2", "decode_4096x12288_m4",
+        "decode_4096x12288_m8", "verify_up_5120x25600_m16", "verify_down_25600x5120_m16",
+        "vocab_head_2048x151936_m1", "vocab_head_2048x151936_m8", "vocab_head_2048x151936_m64"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    wl = synth.workloads()[name]
+    c = Case(wl.M, wl.N, wl.K, seed=zlib.crc32(name.encode()) % 1000, a_scale=wl.a_scale,
+             half_normal=wl.half_normal)
+    y = c.run(ops.PATH_AUTO)
+    rows = sample_rows(wl.N, 48, seed=3)
+    yref, b = c.oracle_rows(rows)
+    assert_close(y[:, rows], yref, b, name)
+    assert np.all(np.isfinite(y))
+    assert ops.device_status() == ops.OK
+
+
+# ---- grouped (MoE verify round) ---------------------------------------------------
+
+def _grouped_case(E, N, K, M, budget, topk, seed):
+    pw = synth.gen_weights(E * N, K, seed)
+    a = synth.gen_activations(M, K, seed + 1)
+    s = synth.gen_a_scale(M, seed + 2, "uniform")
+    idx = synth.gen_moe_routing(M, E, budget, topk, seed + 3)
+    return pw, a, s, idx
+
+
+def _run_grouped(pw, a, s, idx, E, N, K):
+    w = ops.PackedWeights.from_host(pw.codes, pw.scales, pw.codebooks, N, K)
+    y = ops.grouped_gemm(torch.from_numpy(a).cuda(), torch.from_numpy(s).cuda(), w, E,
+                         torch.from_numpy(idx).cuda())
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("E,N,K,M,budget,topk", [(12, 80, 256, 6, 4, 2), (16, 33, 384, 64, 16, 8),
+                                                  (5, 16, 128, 1, 1, 1)])
+def test_grouped_small(E, N, K, M, budget, topk):
+    pw, a, s, idx = _grouped_case(E, N, K, M, budget, topk, seed=E + N + M)
+    y = _run_grouped(pw, a, s, idx, E, N, K)
+    yref, b, reads = oracle.grouped_gemm(a, s, pw.codes, pw.scales, pw.codebooks, E, idx, M, N, K)
+    assert_close(y, yref, b, "grouped")
+    assert ops.device_status() == ops.OK
+
+
+def test_grouped_full_size_sampled():
+    wl = synth.workloads()["moe_verify_e128_2048x1536_m64"]
+    E, N, K, M = wl.experts, wl.N, wl.K, wl.M
+    pw, a, s, idx = _grouped_case(E, N, K, M, wl.budget, wl.topk, seed=321)
+    y = _run_grouped(pw, a, s, idx, E, N, K)
+    rows = sample_rows(N, 24, seed=4)
+    for t in range(0, M, 7):
+        for j in range(wl.topk):
+            e = int(idx[t, j])
+            sel = e * N + rows
+            yr, b = oracle.gemm(a[t:t + 1], s[t:t + 1], pw.codes[sel], pw.scales[sel],
+                                pw.codebooks[sel], 1, len(rows), K)
+            assert_close(y[t, j, rows][None], yr, b, f"token {t} slot {j}")
+    assert ops.device_status() == ops.OK
+
+
+def test_grouped_routing_errors_are_reported():
+    E, N, K, M = 4, 16, 128, 2
+    pw, a, s, idx = _grouped_case(E, N, K, M, 4, 2, seed=8)
+    bad = idx.copy()
+    bad[1, 0] = 9                              # outside [0, E)
+    _run_grouped(pw, a, s, bad, E, N, K)
+    assert ops.device_status() == ops.EROUTING
+    dup = idx.copy()
+    dup[0, 1] = dup[0, 0]                      # one token lists an expert twice
+    _run_grouped(pw, a, s, dup, E, N, K)
+    assert ops.device_status() == ops.EROUTING
+    assert ops.device_status() == ops.OK       # the status is cleared once read
