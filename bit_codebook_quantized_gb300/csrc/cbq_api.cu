@@ -137,7 +137,7 @@ int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w,
   }
   if (!a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(w))
     return CBQ_EINVAL;
-  if (path == CBQ_PATH_AUTO) path = CBQ_PATH_GEMV;
+  if (path == CBQ_PATH_AUTO) path = (M <= 4) ? CBQ_PATH_GEMV : CBQ_PATH_MMA;
   if (path == CBQ_PATH_GEMV) {
     GemvParams p;
     std::memset(&p, 0, sizeof(p));
@@ -175,12 +175,13 @@ int cbq_gemm(const uint8_t* a, const float* a_scale, const cbq_weight_t* w, int3
   return cbq_gemm_path(a, a_scale, w, M, N, K, y, stream, CBQ_PATH_AUTO);
 }
 
-int cbq_grouped_gemm(const uint8_t* a, const float* a_scale, const cbq_weight_t* experts,
-                     int32_t E, const int32_t* topk_idx, int32_t topk, int32_t M, int32_t N,
-                     int32_t K, float* y, void* stream) {
+int cbq_grouped_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* experts,
+                          int32_t E, const int32_t* topk_idx, int32_t topk, int32_t M, int32_t N,
+                          int32_t K, float* y, void* stream, int32_t path) {
   if (M < 0 || M > 64 || N < 0 || K < 0 || K % 128 != 0 || E < 1 || E > 4096 || topk < 1 ||
       topk > 8 || topk > E)
     return CBQ_EINVAL;
+  if (path < CBQ_PATH_AUTO || path > CBQ_PATH_MMA) return CBQ_EINVAL;
   if (M == 0 || N == 0) return CBQ_OK;
   if (!y || !aligned(y, 4) || !topk_idx || !aligned(topk_idx, 4)) return CBQ_EINVAL;
   if (static_cast<int64_t>(E) * N > INT32_MAX) return CBQ_EINVAL;
@@ -194,10 +195,29 @@ int cbq_grouped_gemm(const uint8_t* a, const float* a_scale, const cbq_weight_t*
   }
   if (!a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(experts))
     return CBQ_EINVAL;
-  GemvParams p;
+  if (path == CBQ_PATH_AUTO) path = (M <= 4) ? CBQ_PATH_GEMV : CBQ_PATH_MMA;
+  const uint64_t rows = uint64_t(E) * N, pitch = uint64_t(K) * 3 / 8;
+  if (path == CBQ_PATH_GEMV) {
+    GemvParams p;
+    std::memset(&p, 0, sizeof(p));
+    st = make_tmap_2d(&p.tmap_codes, experts->codes, pitch, rows, pitch, 48, 16, false);
+    if (st != CBQ_OK) return st;
+    p.a = a;
+    p.a_scale = a_scale;
+    p.scales = experts->scales;
+    p.codebooks = experts->codebooks;
+    p.y = y;
+    p.topk_idx = topk_idx;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.E = E;
+    p.topk = topk;
+    return launch_gemv(p, true, s);
+  }
+  UmmaParams p;
   std::memset(&p, 0, sizeof(p));
-  st = make_tmap_2d(&p.tmap_codes, experts->codes, uint64_t(K) * 3 / 8, uint64_t(E) * N,
-                    uint64_t(K) * 3 / 8, 48, 16, false);
+  st = make_tmap_2d(&p.tmap_codes, experts->codes, pitch, rows, pitch, 48, 128, false);
   if (st != CBQ_OK) return st;
   p.a = a;
   p.a_scale = a_scale;
@@ -210,7 +230,14 @@ int cbq_grouped_gemm(const uint8_t* a, const float* a_scale, const cbq_weight_t*
   p.K = K;
   p.E = E;
   p.topk = topk;
-  return launch_gemv(p, true, s);
+  return launch_umma(p, true, s);
+}
+
+int cbq_grouped_gemm(const uint8_t* a, const float* a_scale, const cbq_weight_t* experts,
+                     int32_t E, const int32_t* topk_idx, int32_t topk, int32_t M, int32_t N,
+                     int32_t K, float* y, void* stream) {
+  return cbq_grouped_gemm_path(a, a_scale, experts, E, topk_idx, topk, M, N, K, y, stream,
+                               CBQ_PATH_AUTO);
 }
 
 int cbq_device_status(void* stream) {

@@ -59,14 +59,20 @@ __device__ __forceinline__ bool status_set() {
   return *reinterpret_cast<volatile unsigned*>(&g_status_gemv) != 0u;
 }
 
+// Spin on an mbarrier phase.  After ~0.5 ms of waiting, give up at once if
+// another wait of this kernel already timed out; after kWaitLimitCycles,
+// raise kErrTimeout and give up.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  if (status_set()) return false;
-  long long t0 = clock64();
+  const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) {
-      raise(kErrTimeout);
-      return false;
+    const long long dt = clock64() - t0;
+    if (dt > (1LL << 20)) {
+      if (status_set()) return false;
+      if (dt > kWaitLimitCycles) {
+        raise(kErrTimeout);
+        return false;
+      }
     }
   }
   return true;

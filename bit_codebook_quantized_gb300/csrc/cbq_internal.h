@@ -27,7 +27,6 @@ struct alignas(128) GemvParams {
 // Kernel parameters of the tcgen05 kernel (dense and grouped).
 struct alignas(128) UmmaParams {
   CUtensorMap tmap_codes;     // 2-D map over codes [rows][3K/8], box [128 rows][48 B]
-  CUtensorMap tmap_act;       // 2-D map over activations [M][K], box [rows][128 B], 128B swizzle
   const uint8_t* a;
   const float* a_scale;
   const uint8_t* scales;
@@ -37,6 +36,8 @@ struct alignas(128) UmmaParams {
   int M, N, K;
   int E, topk;
   int ksplit;                 // K-range split factor (cluster size along K)
+  int b_bytes;                // shared bytes of the resident activation tile
+  int red_bytes;              // shared bytes of the split-K partial tiles (leader CTA)
 };
 
 int device_sm_count();

@@ -1,13 +1,556 @@
-// cbq_umma.cu -- verify-round kernel (TMA + tcgen05 block-scaled FP8 MMA).
-// Placeholder until the tcgen05 kernel lands: reports "invalid argument" so
-// that CBQ_PATH_MMA fails loudly instead of computing anything else.
+// cbq_umma.cu -- verify-round kernel of the codebook-quantised matmul:
+// TMA-staged packed codes, register decode to E4M3, block-scaled FP8 MMA on
+// the 5th-generation tensor cores (tcgen05) with fp32 accumulators in TMEM.
+//
+// "Hibana: Fast Agentic Inference on Unified-Memory Devices", section "Model
+// surgery / Three-bit weights": the kernel looks the 3-bit codes up in the
+// 8-entry FP8 codebook and feeds FP8 tensor cores; section "Adaptive
+// speculation": a verify round multiplies the drafted tokens of all requests
+// (M = 8..64 rows) by the same weights, and with "Expert sharing" reads only
+// the experts the round's tokens route to.
+//
+// Mapping to sm_103a (swap-AB: weight rows are the MMA's M = 128, token rows
+// its N = 16..64):
+//  * warp 0 (one lane) streams the tile's code bytes with 2-D TMA boxes of
+//    [128 rows][48 B] (128 k) into a 6-stage mbarrier ring;
+//  * warps 2..9 are two decoder warpgroups taking alternate k-tiles; thread
+//    = weight row.  A thread reads its row's 48 code bytes (3 conflict-free
+//    128-bit shared loads), spreads the codes to nibbles, turns them into
+//    E4M3 bytes with byte-permutes through the row's codebook (two
+//    registers), and writes them as 16-byte rows of 8x16 B core matrices,
+//    the tcgen05 K-major layout.  Its 4 E8M0 group-scale bytes go to TMEM as
+//    the MMA's A scale factors;
+//  * warp 1 (one lane) issues 4 tcgen05.mma kind::mxf8f6f4.block_scale
+//    (K = 32 each) per k-tile: A = decoded weights (smem), B = E4M3
+//    activations (smem, resident for the CTA's K range), scale A = the group
+//    scales, scale B = 2^0.  The E8M0 group scale is exactly the MX block
+//    scale of a 32-wide K block, so the tensor core applies it;
+//  * the decoder warps read the accumulator (tcgen05.ld), apply a_scale and
+//    store fp32 y.  Two accumulators alternate between tiles;
+//  * narrow problems split K over a thread-block cluster; the partial tiles
+//    are summed in the leader CTA's shared memory through DSMEM stores.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cstdint>
+
+#include "cbq_device.cuh"
 #include "cbq_internal.h"
 
 namespace cbq {
 
-int launch_umma(const UmmaParams&, bool, cudaStream_t) { return CBQ_EINVAL; }
-unsigned take_status_umma(cudaStream_t) { return 0u; }
+static __device__ unsigned g_status_umma = 0;
+
+namespace {
+
+constexpr int kRows = 128;                    // MMA M (weight rows per tile)
+constexpr int kCodeStage = kRows * 48;        // one k-tile of codes: 6 KB
+constexpr int kAStage = kRows * 128;          // one decoded k-tile: 16 KB
+constexpr int kCodeStages = 6;
+constexpr int kAStages = 3;
+constexpr int kDecWarps = 8;
+constexpr int kThreads = 64 + kDecWarps * 32;
+constexpr int kTmemCols = 256;
+constexpr int kAccCols = 64;                  // accumulator i at column 64 * i
+constexpr int kSfaCol = 128;                  // + 4 * A stage (4-column aligned)
+constexpr int kSfbCol = 160;                  // 8 columns of 2^0
+constexpr int kMaxExperts = 4096;
+constexpr int kMaxRouting = 64 * 8;
+constexpr int kMaxSmem = 232448;
+
+__device__ __forceinline__ void raise(unsigned bits) { atomicOr(&g_status_umma, bits); }
+__device__ __forceinline__ bool status_set() {
+  return *reinterpret_cast<volatile unsigned*>(&g_status_umma) != 0u;
+}
+
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+  auto tw = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (tw()) return true;
+  const long long t0 = clock64();
+  while (!tw()) {
+    const long long dt = clock64() - t0;
+    if (dt > (1LL << 20)) {
+      if (status_set()) return false;
+      if (dt > kWaitLimitCycles) {
+        raise(kErrTimeout);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Shared-memory carve-up (byte offsets), identical on host and device.
+struct Layout {
+  int codes, a, b, red, bars, route, total;
+  __host__ __device__ Layout(int b_bytes, int red_bytes, bool grouped) {
+    codes = 0;
+    a = codes + kCodeStages * kCodeStage;
+    b = a + kAStages * kAStage;
+    red = b + b_bytes;
+    bars = red + red_bytes;
+    route = bars + 256;
+    total = route + (grouped ? (kMaxRouting * 4 + 64 * 4 + 16 + kMaxExperts * 2 + kMaxExperts) : 0);
+  }
+};
+
+// Decode one group (three 32-bit words) of a row: 32 E4M3 bytes as two
+// 16-byte halves (codes 0-15 and 16-31).
+__device__ __forceinline__ void decode_group(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t cb_lo,
+                                             uint32_t cb_hi, uint4& lo, uint4& hi) {
+  const uint32_t s0 = spread_codes8(w0);
+  const uint32_t s1 = spread_codes8(__funnelshift_r(w0, w1, 24));
+  const uint32_t s2 = spread_codes8(__funnelshift_r(w1, w2, 16));
+  const uint32_t s3 = spread_codes8(w2 >> 8);
+  lo.x = lookup4(cb_lo, cb_hi, s0);
+  lo.y = lookup4(cb_lo, cb_hi, s0 >> 16);
+  lo.z = lookup4(cb_lo, cb_hi, s1);
+  lo.w = lookup4(cb_lo, cb_hi, s1 >> 16);
+  hi.x = lookup4(cb_lo, cb_hi, s2);
+  hi.y = lookup4(cb_lo, cb_hi, s2 >> 16);
+  hi.z = lookup4(cb_lo, cb_hi, s3);
+  hi.w = lookup4(cb_lo, cb_hi, s3 >> 16);
+}
+
+template <int NTOK, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant__ UmmaParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const Layout L(p.b_bytes, p.red_bytes, GROUPED);
+  uint8_t* codes_s = smem + L.codes;
+  uint8_t* a_s = smem + L.a;
+  uint8_t* b_s = smem + L.b;
+  float* red_s = reinterpret_cast<float*>(smem + L.red);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* codes_full = bars;
+  uint64_t* codes_empty = codes_full + kCodeStages;
+  uint64_t* a_full = codes_empty + kCodeStages;
+  uint64_t* a_empty = a_full + kAStages;
+  uint64_t* acc_full = a_empty + kAStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* b_full = acc_empty + 2;
+  uint64_t* red_full = b_full + 1;
+  uint64_t* red_free = red_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_free + 1);
+  int* misc = reinterpret_cast<int*>(tmem_slot + 2);     // [0] list count, [1] experts used
+  int32_t* topk_s = reinterpret_cast<int32_t*>(smem + L.route);
+  int32_t* list_tok = topk_s + kMaxRouting;              // token | slot << 8
+  uint16_t* used_list = reinterpret_cast<uint16_t*>(list_tok + 64 + 4);
+  uint8_t* used_flag = reinterpret_cast<uint8_t*>(used_list + kMaxExperts);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cs = p.ksplit;
+  const int rank = cs > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cluster_id = blockIdx.x / cs, n_clusters = gridDim.x / cs;
+  const int nkt = p.K / 128;
+  const int kt0 = rank * nkt / cs, kt1 = (rank + 1) * nkt / cs;
+  const int tiles = (p.N + kRows - 1) / kRows;
+
+  if (tid == 0) {
+    for (int i = 0; i < kCodeStages; ++i) {
+      mbar_init(&codes_full[i], 1);
+      mbar_init(&codes_empty[i], 4);
+    }
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(&a_full[i], 4);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kDecWarps);
+    }
+    mbar_init(b_full, kDecWarps);
+    mbar_init(red_full, (cs > 1 ? cs - 1 : 1) * kDecWarps * 32);
+    mbar_init(red_free, kDecWarps * 32);
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&p.tmap_codes);
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+
+  // ---- which units does this CTA own? ----
+  int n_units, u_begin, u_step;
+  if constexpr (GROUPED) {
+    const int nr = p.M * p.topk;
+    for (int e = tid; e < p.E; e += kThreads) used_flag[e] = 0;
+    __syncthreads();
+    for (int i = tid; i < nr; i += kThreads) {
+      const int e = p.topk_idx[i];
+      topk_s[i] = e;
+      if (e >= 0 && e < p.E) used_flag[e] = 1;
+      else raise(kErrRouting);
+    }
+    __syncthreads();
+    for (int i = tid; i < nr; i += kThreads) {
+      const int row0 = (i / p.topk) * p.topk;
+      for (int j = row0; j < i; ++j)
+        if (topk_s[j] == topk_s[i]) raise(kErrRouting);
+    }
+    if (warp == 0) {
+      int base = 0;
+      for (int e0 = 0; e0 < p.E; e0 += 32) {
+        const int e = e0 + lane;
+        const bool u = (e < p.E) && used_flag[e];
+        const unsigned m = __ballot_sync(0xffffffffu, u);
+        if (u) used_list[base + __popc(m & ((1u << lane) - 1u))] = static_cast<uint16_t>(e);
+        base += __popc(m);
+      }
+      if (lane == 0) misc[1] = base;
+    }
+    __syncthreads();
+    // contiguous blocks of (expert, tile) units so consecutive units share an expert
+    const int total = misc[1] * tiles;
+    u_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * total) / gridDim.x);
+    n_units = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total) / gridDim.x) - u_begin;
+    u_step = 1;
+  } else {
+    // resident activations for this CTA's K range, K-major core-matrix layout:
+    // chunk c (16 k) at c * NTOK * 16, token group j at j * 128, token % 8 at * 16
+    const int kb = kt0 * 128, nchunk = (kt1 - kt0) * 8;
+    for (int i = tid; i < NTOK * nchunk; i += kThreads) {
+      const int tok = i % NTOK, c = i / NTOK;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (tok < p.M) v = __ldg(reinterpret_cast<const uint4*>(p.a + size_t(tok) * p.K + kb + c * 16));
+      *reinterpret_cast<uint4*>(b_s + c * NTOK * 16 + (tok >> 3) * 128 + (tok & 7) * 16) = v;
+    }
+    fence_proxy_async_smem();
+    u_begin = cluster_id;
+    n_units = cluster_id < tiles ? (tiles - 1 - cluster_id) / n_clusters + 1 : 0;
+    u_step = n_clusters;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  // scale factors of B: 2^0 in every byte of 8 columns, all 128 lanes
+  if (warp >= 2 && warp < 6) {
+    const uint32_t q = warp & 3;
+    for (int c = 0; c < 8; c += 4)
+      tmem_st_x4(tbase + ((32 * q) << 16) + kSfbCol + c, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (cs > 1) cluster_sync();
+
+  auto unit_rows = [&](int ui, int& row0, int& row_end, int& e) {
+    const int u = u_begin + ui * u_step;
+    if constexpr (GROUPED) {
+      e = used_list[u / tiles];
+      row0 = e * p.N + (u % tiles) * kRows;
+      row_end = e * p.N + p.N;
+    } else {
+      e = 0;
+      row0 = u * kRows;
+      row_end = p.N;
+    }
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int ui = 0; ui < n_units; ++ui) {
+        int row0, row_end, e;
+        unit_rows(ui, row0, row_end, e);
+        for (int kt = kt0; kt < kt1; ++kt, ++it) {
+          const int slot = it % kCodeStages;
+          wait_bounded(&codes_empty[slot], ((it / kCodeStages) & 1u) ^ 1u);
+          mbar_arrive_expect_tx(&codes_full[slot], kCodeStage);
+          tma_load_2d(codes_s + slot * kCodeStage, &p.tmap_codes, &codes_full[slot], kt * 48, row0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      uint32_t it = 0;
+      const uint32_t a_base = smem_u32(a_s), b_base = smem_u32(b_s);
+      for (int ui = 0; ui < n_units; ++ui) {
+        const int abuf = ui & 1;
+        wait_bounded(b_full, ui & 1);
+        wait_bounded(&acc_empty[abuf], ((ui >> 1) & 1) ^ 1);
+        tc_fence_after();
+        int n_mma = NTOK;
+        if constexpr (GROUPED) n_mma = min(NTOK, (misc[0] + 15) & ~15);
+        const uint32_t idesc = umma_idesc_mxf8(n_mma, 0, 0);
+        for (int kt = kt0; kt < kt1; ++kt, ++it) {
+          const int slot = it % kAStages;
+          wait_bounded(&a_full[slot], (it / kAStages) & 1u);
+          tc_fence_after();
+          const int i = kt - kt0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t ad = umma_desc_kmajor(a_base + slot * kAStage + 2 * j * 2048, 2048, 128);
+            const uint64_t bd = umma_desc_kmajor(b_base + (i * 8 + 2 * j) * NTOK * 16, NTOK * 16, 128);
+            umma_mxf8(tbase + abuf * kAccCols, ad, bd, idesc | (uint32_t(j) << 29),
+                      tbase + kSfaCol + slot * 4, tbase + kSfbCol, (i | j) != 0);
+          }
+          umma_commit(&a_empty[slot]);
+        }
+        umma_commit(&acc_full[abuf]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ decoders --
+    const int dw = warp - 2, dg = dw >> 2, q = warp & 3;
+    const int r = 32 * q + lane;                      // row inside the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+    const uint32_t codes_base = smem_u32(codes_s), a_base = smem_u32(a_s);
+    const uint32_t a_row_off = (r >> 3) * 128 + (r & 7) * 16;
+    uint32_t it = 0;
+    int prev_e = -1;
+    for (int ui = 0; ui < n_units; ++ui) {
+      int row0, row_end, e;
+      unit_rows(ui, row0, row_end, e);
+      int ntok = p.M;
+      if constexpr (GROUPED) {
+        if (e != prev_e) {
+          // token list of expert e, then gather its activation rows into B
+          named_bar_sync(1, kDecWarps * 32);   // previous epilogue is done with the list
+          if (dw == 0) {
+            const int nr = p.M * p.topk;
+            int base = 0;
+            for (int i0 = 0; i0 < nr; i0 += 32) {
+              const int i = i0 + lane;
+              const bool hit = (i < nr) && topk_s[i] == e;
+              const unsigned m = __ballot_sync(0xffffffffu, hit);
+              const int pos = base + __popc(m & ((1u << lane) - 1u));
+              if (hit && pos < 64) list_tok[pos] = (i / p.topk) | ((i % p.topk) << 8);
+              base += __popc(m);
+            }
+            if (lane == 0) misc[0] = min(base, NTOK);
+          }
+          named_bar_sync(1, kDecWarps * 32);
+          const int cnt = misc[0], nz = min(NTOK, (cnt + 15) & ~15);
+          const int nchunk = p.K / 16;
+          for (int i = tid - 64; i < nz * nchunk; i += kDecWarps * 32) {
+            const int tk = i % nz, c = i / nz;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (tk < cnt)
+              v = __ldg(reinterpret_cast<const uint4*>(p.a + size_t(list_tok[tk] & 0xff) * p.K + c * 16));
+            *reinterpret_cast<uint4*>(b_s + c * NTOK * 16 + (tk >> 3) * 128 + (tk & 7) * 16) = v;
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, kDecWarps * 32);
+          prev_e = e;
+        }
+        ntok = misc[0];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_full);
+
+      const int grow = row0 + r;
+      const bool ok = grow < row_end;
+      const uint2 cb = ok ? __ldg(reinterpret_cast<const uint2*>(p.codebooks + size_t(grow) * 8)) : make_uint2(0, 0);
+      const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + size_t(ok ? grow : 0) * (p.K / 32));
+      for (int kt = kt0; kt < kt1; ++kt, ++it) {
+        if (((kt - kt0) & 1) != dg) continue;
+        const int cslot = it % kCodeStages, aslot = it % kAStages;
+        const uint32_t sw = ok ? __ldg(srow + kt) : 0x7F7F7F7Fu;
+        wait_bounded(&codes_full[cslot], (it / kCodeStages) & 1u);
+        const uint32_t crow = codes_base + cslot * kCodeStage + r * 48;
+        const uint4 c0 = lds128(crow), c1 = lds128(crow + 16), c2 = lds128(crow + 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&codes_empty[cslot]);
+        uint4 h[8];
+        decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, h[0], h[1]);
+        decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, h[2], h[3]);
+        decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, h[4], h[5]);
+        decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, h[6], h[7]);
+        wait_bounded(&a_empty[aslot], ((it / kAStages) & 1u) ^ 1u);
+        const uint32_t adst = a_base + aslot * kAStage + a_row_off;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) sts128(adst + c * 2048, h[c].x, h[c].y, h[c].z, h[c].w);
+        // A scale of row m is read from TMEM lane m, column (base + m / 32),
+        // byte = the MMA's a_sf_id: quadrant q writes column base + q
+        tmem_st_x1(tbase + lane_addr + kSfaCol + aslot * 4 + q, sw);
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[aslot]);
+      }
+
+      // ---------------------------------------------------------- epilogue --
+      const int abuf = ui & 1;
+      wait_bounded(&acc_full[abuf], (ui >> 1) & 1);
+      tc_fence_after();
+      constexpr int HALF = NTOK / 2;
+      float v[HALF];
+#pragma unroll
+      for (int c = 0; c < HALF; c += 8) {
+        uint32_t t[8];
+        tmem_ld_x8(tbase + lane_addr + abuf * kAccCols + dg * HALF + c, t);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[c + i] = __uint_as_float(t[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[abuf]);
+
+      if constexpr (!GROUPED) {
+        if (cs > 1) {
+          // split K: partial tiles meet in the leader CTA's shared memory
+          const uint32_t slot_off = ((r * NTOK) + dg * HALF) * 4;
+          if (rank != 0) {
+            wait_bounded<true>(red_free, (ui & 1) ^ 1);
+            const uint32_t dst = mapa_shared(smem_u32(red_s) + (rank - 1) * kRows * NTOK * 4 + slot_off, 0);
+#pragma unroll
+            for (int c = 0; c < HALF; c += 4) st_cluster_v4(dst + c * 4, v[c], v[c + 1], v[c + 2], v[c + 3]);
+            mbar_arrive_remote(mapa_shared(smem_u32(red_full), 0));
+            continue;
+          }
+          wait_bounded<true>(red_full, ui & 1);
+          for (int s = 0; s < cs - 1; ++s) {
+            const float* src = red_s + s * kRows * NTOK + r * NTOK + dg * HALF;
+#pragma unroll
+            for (int c = 0; c < HALF; ++c) v[c] += src[c];
+          }
+          // tell every other CTA of the cluster that its slot may be reused
+          for (int s = 1; s < cs; ++s) mbar_arrive_remote(mapa_shared(smem_u32(red_free), s));
+        }
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < HALF; ++c) {
+            const int tok = dg * HALF + c;
+            if (tok < ntok) p.y[size_t(tok) * p.N + grow] = v[c] * __ldg(p.a_scale + tok);
+          }
+        }
+      } else {
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < HALF; ++c) {
+            const int i = dg * HALF + c;
+            if (i < ntok) {
+              const int tok = list_tok[i] & 0xff, slot = list_tok[i] >> 8;
+              p.y[(size_t(tok) * p.topk + slot) * p.N + (grow - e * p.N)] = v[c] * __ldg(p.a_scale + tok);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown: every tcgen05 op has completed (the epilogue waited on
+  // the last commit); cluster peers may still touch our barriers until all
+  // of them get here.
+  tc_fence_before();
+  __syncthreads();
+  if (cs > 1) cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+template <int NTOK, bool GROUPED>
+int launch_t(const UmmaParams& p, int grid, int cs, int smem, cudaStream_t stream) {
+  auto kern = umma_kernel<NTOK, GROUPED>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return CBQ_ECUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.numAttrs = 0;
+  if (cs > 1) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      return CBQ_ECUDA;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // no more clusters than can be resident at once (the grid is persistent)
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) == cudaSuccess && max_clusters > 0)
+      cfg.gridDim = dim3(std::min(grid / cs, max_clusters) * cs);
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  note_launch();
+  return e == cudaSuccess ? CBQ_OK : CBQ_ECUDA;
+}
+
+template <bool GROUPED>
+int dispatch(const UmmaParams& p, int ntok, int grid, int cs, int smem, cudaStream_t s) {
+  if (ntok <= 16) return launch_t<16, GROUPED>(p, grid, cs, smem, s);
+  if (ntok <= 32) return launch_t<32, GROUPED>(p, grid, cs, smem, s);
+  return launch_t<64, GROUPED>(p, grid, cs, smem, s);
+}
+
+// Token columns of the MMA (its N): 16, 32 or 64.
+int ntok_for(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
+
+}  // namespace
+
+int launch_umma(const UmmaParams& p_in, bool grouped, cudaStream_t stream) {
+  UmmaParams p = p_in;
+  const int sms = device_sm_count();
+  const int ntok = ntok_for(p.M);
+  const int nkt = p.K / 128;
+  const int tiles = (p.N + kRows - 1) / kRows;
+  if (grouped) {
+    p.ksplit = 1;
+    p.b_bytes = ntok * p.K;
+    p.red_bytes = 0;
+    const Layout L(p.b_bytes, 0, true);
+    if (L.total > kMaxSmem) return CBQ_EINVAL;   // K too long for a resident B tile
+    const int units = std::min(p.E, p.M * p.topk) * tiles;
+    const int grid = std::max(1, std::min(units, sms));
+    return dispatch<true>(p, ntok, grid, 1, L.total, stream);
+  }
+  // split K over a cluster when there are too few tiles to fill the GPU:
+  // minimise (rounds of tiles) x (k-tiles per CTA) within the smem budget
+  int best_cs = 0;
+  long long best_cost = 0;
+  for (int cs = 1; cs <= 8 && cs <= nkt; ++cs) {
+    const int per = (nkt + cs - 1) / cs;
+    const Layout L(ntok * per * 128, cs > 1 ? (cs - 1) * kRows * ntok * 4 : 0, false);
+    if (L.total > kMaxSmem) continue;
+    const int clusters = sms / cs;
+    const long long rounds = (tiles + clusters - 1) / clusters;
+    const long long cost = rounds * per * 16 + (cs > 1 ? 4 + cs : 0);
+    if (best_cs == 0 || cost < best_cost) {
+      best_cs = cs;
+      best_cost = cost;
+    }
+  }
+  if (best_cs == 0) return CBQ_EINVAL;
+  const int cs = best_cs;
+  p.ksplit = cs;
+  p.b_bytes = ntok * ((nkt + cs - 1) / cs) * 128;
+  p.red_bytes = cs > 1 ? (cs - 1) * kRows * ntok * 4 : 0;
+  const Layout L(p.b_bytes, p.red_bytes, false);
+  const int grid = std::min(tiles, sms / cs) * cs;
+  return dispatch<false>(p, ntok, grid, cs, L.total, stream);
+}
+
+unsigned take_status_umma(cudaStream_t stream) {
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_status_umma, sizeof(v), 0, cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return kErrTimeout;
+  cudaMemcpyToSymbolAsync(g_status_umma, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
+  cudaStreamSynchronize(stream);
+  return v;
+}
 
 }  // namespace cbq

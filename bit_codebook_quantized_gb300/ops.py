@@ -25,7 +25,8 @@ OK, EINVAL, ECUDA, EDEVICE, ETIMEOUT, EROUTING = 0, -1, -2, -3, -4, -5
 
 # Every symbol include/cbq.h declares.
 EXPORTS = ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path",
-           "cbq_grouped_gemm", "cbq_device_status", "cbq_launch_count", "cbq_status_str")
+           "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_launch_count",
+           "cbq_status_str")
 
 
 class CbqError(RuntimeError):
@@ -60,13 +61,15 @@ def lib() -> ctypes.CDLL:
         L.cbq_gemm_path.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp, i32]
         L.cbq_grouped_gemm.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, vp, i32, i32, i32,
                                        i32, vp, vp]
+        L.cbq_grouped_gemm_path.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, vp, i32, i32,
+                                            i32, i32, vp, vp, i32]
         L.cbq_device_status.argtypes = [vp]
         L.cbq_launch_count.argtypes = []
         L.cbq_launch_count.restype = ctypes.c_uint64
         L.cbq_status_str.argtypes = [ctypes.c_int]
         L.cbq_status_str.restype = ctypes.c_char_p
         for name in ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path",
-                     "cbq_grouped_gemm", "cbq_device_status"):
+                     "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
         return L
@@ -156,15 +159,16 @@ def gemm(a: torch.Tensor, a_scale: torch.Tensor, w: PackedWeights,
 
 def grouped_gemm(a: torch.Tensor, a_scale: torch.Tensor, experts: PackedWeights, E: int,
                  topk_idx: torch.Tensor, out: torch.Tensor | None = None,
-                 stream=None) -> torch.Tensor:
+                 path: int = PATH_AUTO, stream=None) -> torch.Tensor:
     """y[M, topk, N] for stacked experts (experts.N = rows per expert)."""
     M, topk = topk_idx.shape
     if out is None:
         out = torch.empty((M, topk, experts.N), dtype=torch.float32, device=a.device)
     ws = experts.struct()
-    _check(lib().cbq_grouped_gemm(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(ws), E,
-                                  topk_idx.data_ptr(), topk, M, experts.N, experts.K,
-                                  out.data_ptr(), _stream(stream)), "cbq_grouped_gemm")
+    _check(lib().cbq_grouped_gemm_path(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(ws), E,
+                                       topk_idx.data_ptr(), topk, M, experts.N, experts.K,
+                                       out.data_ptr(), _stream(stream), path),
+           "cbq_grouped_gemm")
     return out
 
 

@@ -112,7 +112,7 @@ int cbq_gemm_path(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
  * e*N .. e*N+N-1 of `experts`), topk_idx is DEVICE int32 [M][topk] and
  *   y[t][j][:] = a_scale[t] * a[t] x W_{topk_idx[t][j]}^T   (fp32 [M][topk][N]),
  * with no gate weight and no combine.  Only experts that appear in topk_idx
- * are read from memory.  The routing is read on the device inside the one
+ * are read from memory.  Picks the kernel by M as cbq_gemm does.  The routing is read on the device inside the one
  * kernel launch.  1 <= M <= 64, 1 <= topk <= 8, 1 <= E <= 4096, each row of
  * topk_idx must list distinct experts in [0, E); a violation seen on the
  * device is reported by cbq_device_status as CBQ_EROUTING.
@@ -121,6 +121,13 @@ int cbq_grouped_gemm(const uint8_t *a, const float *a_scale,
                      const cbq_weight_t *experts, int32_t E,
                      const int32_t *topk_idx, int32_t topk, int32_t M,
                      int32_t N, int32_t K, float *y, void *stream);
+
+/* Same as cbq_grouped_gemm with an explicit kernel choice (CBQ_PATH_*). */
+int cbq_grouped_gemm_path(const uint8_t *a, const float *a_scale,
+                          const cbq_weight_t *experts, int32_t E,
+                          const int32_t *topk_idx, int32_t topk, int32_t M,
+                          int32_t N, int32_t K, float *y, void *stream,
+                          int32_t path);
 
 /* Synchronise `stream`, then return and clear the sticky device status of
  * this library on the current device: CBQ_OK, CBQ_ETIMEOUT (a kernel's

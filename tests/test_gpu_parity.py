@@ -13,7 +13,7 @@ from tests.gpu_util import Case, assert_close, ensure_built, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [ops.PATH_GEMV]
+PATHS = [ops.PATH_GEMV, ops.PATH_MMA]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -144,29 +144,31 @@ def _grouped_case(E, N, K, M, budget, topk, seed):
     return pw, a, s, idx
 
 
-def _run_grouped(pw, a, s, idx, E, N, K):
+def _run_grouped(pw, a, s, idx, E, N, K, path=ops.PATH_AUTO):
     w = ops.PackedWeights.from_host(pw.codes, pw.scales, pw.codebooks, N, K)
     y = ops.grouped_gemm(torch.from_numpy(a).cuda(), torch.from_numpy(s).cuda(), w, E,
-                         torch.from_numpy(idx).cuda())
+                         torch.from_numpy(idx).cuda(), path=path)
     torch.cuda.synchronize()
     return y.cpu().numpy()
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("E,N,K,M,budget,topk", [(12, 80, 256, 6, 4, 2), (16, 33, 384, 64, 16, 8),
-                                                  (5, 16, 128, 1, 1, 1)])
-def test_grouped_small(E, N, K, M, budget, topk):
+                                                  (5, 16, 128, 1, 1, 1), (6, 300, 640, 20, 3, 2)])
+def test_grouped_small(path, E, N, K, M, budget, topk):
     pw, a, s, idx = _grouped_case(E, N, K, M, budget, topk, seed=E + N + M)
-    y = _run_grouped(pw, a, s, idx, E, N, K)
+    y = _run_grouped(pw, a, s, idx, E, N, K, path)
     yref, b, reads = oracle.grouped_gemm(a, s, pw.codes, pw.scales, pw.codebooks, E, idx, M, N, K)
     assert_close(y, yref, b, "grouped")
     assert ops.device_status() == ops.OK
 
 
-def test_grouped_full_size_sampled():
+@pytest.mark.parametrize("path", PATHS)
+def test_grouped_full_size_sampled(path):
     wl = synth.workloads()["moe_verify_e128_2048x1536_m64"]
     E, N, K, M = wl.experts, wl.N, wl.K, wl.M
     pw, a, s, idx = _grouped_case(E, N, K, M, wl.budget, wl.topk, seed=321)
-    y = _run_grouped(pw, a, s, idx, E, N, K)
+    y = _run_grouped(pw, a, s, idx, E, N, K, path)
     rows = sample_rows(N, 24, seed=4)
     for t in range(0, M, 7):
         for j in range(wl.topk):
@@ -178,15 +180,16 @@ def test_grouped_full_size_sampled():
     assert ops.device_status() == ops.OK
 
 
-def test_grouped_routing_errors_are_reported():
+@pytest.mark.parametrize("path", PATHS)
+def test_grouped_routing_errors_are_reported(path):
     E, N, K, M = 4, 16, 128, 2
     pw, a, s, idx = _grouped_case(E, N, K, M, 4, 2, seed=8)
     bad = idx.copy()
     bad[1, 0] = 9                              # outside [0, E)
-    _run_grouped(pw, a, s, bad, E, N, K)
+    _run_grouped(pw, a, s, bad, E, N, K, path)
     assert ops.device_status() == ops.EROUTING
     dup = idx.copy()
     dup[0, 1] = dup[0, 0]                      # one token lists an expert twice
-    _run_grouped(pw, a, s, dup, E, N, K)
+    _run_grouped(pw, a, s, dup, E, N, K, path)
     assert ops.device_status() == ops.EROUTING
     assert ops.device_status() == ops.OK       # the status is cleared once read
