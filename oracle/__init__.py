@@ -45,9 +45,14 @@ def build(force: bool = False) -> str:
 def _load():
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        lib = ctypes.CDLL(build())
+        if _lib is None:
+            _lib = configure(ctypes.CDLL(build()))
+        return _lib
+
+
+def configure(lib):
+    """Declare the C signatures on a loaded copy of the oracle library."""
+    if True:
         u8p = ctypes.POINTER(ctypes.c_uint8)
         f32p = ctypes.POINTER(ctypes.c_float)
         f64p = ctypes.POINTER(ctypes.c_double)
@@ -79,8 +84,7 @@ def _load():
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_set_num_threads.argtypes = [ctypes.c_int]
         lib.orc_set_num_threads.restype = None
-        _lib = lib
-        return lib
+    return lib
 
 
 def _p(arr: np.ndarray, ctype):

@@ -331,3 +331,16 @@ def test_pack_is_exact_on_representable_weights():
     codes, scales, cbs = oracle.pack(W)
     back = oracle.unpack(codes, scales, cbs, N, K)
     assert np.array_equal(back, W)
+
+
+def test_pack_ties_go_to_the_lower_index():
+    """A row holding only -1 and +1: the quantile start puts four centroids on
+    each value, every assignment is an exact tie, and ties go to the lowest
+    index, so the codes are exactly 0 (for -1) and 4 (for +1)."""
+    W = np.where(synth.rng_for(3).permutation(256) < 128, -1.0, 1.0).astype(np.float32)
+    W = W.reshape(1, 256)
+    codes, scales, cbs = oracle.pack(W)
+    idx = oracle.indices_from_codes(codes, 1, 256)
+    assert np.all(scales == 127)
+    assert list(cbs[0]) == [0xB8] * 4 + [0x38] * 4
+    assert np.array_equal(idx[0], np.where(W[0] < 0, 0, 4))
