@@ -1,39 +1,45 @@
 // cbq_umma.cu -- verify-round kernel of the codebook-quantised matmul:
-// TMA-staged packed codes, register decode to E4M3, block-scaled FP8 MMA on
-// the 5th-generation tensor cores (tcgen05) with fp32 accumulators in TMEM.
+// TMA-staged packed codes, register decode to E4M3 straight into tensor
+// memory, block-scaled FP8 MMA on the 5th-generation tensor cores (tcgen05)
+// with fp32 accumulators in TMEM.
 //
 // "Hibana: Fast Agentic Inference on Unified-Memory Devices", section "Model
 // surgery / Three-bit weights": the kernel looks the 3-bit codes up in the
 // 8-entry FP8 codebook and feeds FP8 tensor cores; section "Adaptive
 // speculation": a verify round multiplies the drafted tokens of all requests
-// (M = 8..64 rows) by the same weights, and with "Expert sharing" reads only
+// (up to 64 rows) by the same weights, and with "Expert sharing" reads only
 // the experts the round's tokens route to.
 //
 // Mapping to sm_103a (swap-AB: weight rows are the MMA's M = 128, token rows
-// its N = 16..64):
+// its N = 16, 32 or 64):
 //  * warp 0 (one lane) streams the tile's code bytes with 2-D TMA boxes of
-//    [128 rows][48 B] (128 k) into a 6-stage mbarrier ring;
+//    [128 rows][48 B] (one 128-wide k-tile) into an 8-stage mbarrier ring;
 //  * warps 2..9 are two decoder warpgroups taking alternate k-tiles; thread
-//    = weight row.  A thread reads its row's 48 code bytes (3 conflict-free
-//    128-bit shared loads), spreads the codes to nibbles, turns them into
-//    E4M3 bytes with byte-permutes through the row's codebook (two
-//    registers), and writes them as 16-byte rows of 8x16 B core matrices,
-//    the tcgen05 K-major layout.  Its 4 E8M0 group-scale bytes go to TMEM as
-//    the MMA's A scale factors;
+//    = weight row = TMEM lane.  A thread reads its row's 48 code bytes (three
+//    128-bit shared loads at a conflict-free 48-byte pitch), spreads the codes
+//    to nibbles and turns them into E4M3 bytes with byte-permutes through the
+//    row's codebook (two registers), then writes the 128 bytes into its TMEM
+//    lane (tcgen05.st, 32 columns) as the MMA's A operand, and its 4 E8M0
+//    group-scale bytes into TMEM as the A scale factors;
 //  * warp 1 (one lane) issues 4 tcgen05.mma kind::mxf8f6f4.block_scale
-//    (K = 32 each) per k-tile: A = decoded weights (smem), B = E4M3
-//    activations (smem, resident for the CTA's K range), scale A = the group
-//    scales, scale B = 2^0.  The E8M0 group scale is exactly the MX block
-//    scale of a 32-wide K block, so the tensor core applies it;
-//  * the decoder warps read the accumulator (tcgen05.ld), apply a_scale and
-//    store fp32 y.  Two accumulators alternate between tiles;
-//  * narrow problems split K over a thread-block cluster; the partial tiles
-//    are summed in the leader CTA's shared memory through DSMEM stores.
+//    (K = 32 each) per k-tile with A from TMEM and B (the E4M3 activations,
+//    resident in shared memory for the CTA's K range) from a K-major
+//    shared-memory descriptor; B scale factors are 2^0.  The E8M0 group scale
+//    is exactly the MX block scale of a 32-wide K block, so the tensor core
+//    applies it;
+//  * warps 10..13 are the epilogue: tcgen05.ld the accumulator (two
+//    accumulators alternate between tiles so the MMA never waits for the
+//    stores), multiply by a_scale, store fp32 y;
+//  * narrow problems split K over a thread-block cluster; partial tiles are
+//    summed in the leader CTA's shared memory through DSMEM stores.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "cbq_device.cuh"
 #include "cbq_internal.h"
@@ -46,24 +52,29 @@ namespace {
 
 constexpr int kRows = 128;                    // MMA M (weight rows per tile)
 constexpr int kCodeStage = kRows * 48;        // one k-tile of codes: 6 KB
-constexpr int kAStage = kRows * 128;          // one decoded k-tile: 16 KB
-constexpr int kCodeStages = 6;
-constexpr int kAStages = 3;
-constexpr int kDecWarps = 8;
-constexpr int kThreads = 64 + kDecWarps * 32;
-constexpr int kTmemCols = 256;
+constexpr int kCodeStages = 8;
+constexpr int kAStages = 8;                   // decoded k-tiles in TMEM
+constexpr int kDecGroups = 2;
+constexpr int kDecWarps = 4 * kDecGroups;
+constexpr int kEpiWarp0 = 2 + kDecWarps;      // first epilogue warp
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+constexpr int kTmemCols = 512;
 constexpr int kAccCols = 64;                  // accumulator i at column 64 * i
 constexpr int kSfaCol = 128;                  // + 4 * A stage (4-column aligned)
-constexpr int kSfbCol = 160;                  // 8 columns of 2^0
+constexpr int kSfbCol = 192;                  // 8 columns of 2^0
+constexpr int kACol = 256;                    // + 32 * A stage
 constexpr int kMaxExperts = 4096;
 constexpr int kMaxRouting = 64 * 8;
 constexpr int kMaxSmem = 232448;
+constexpr int kMinSmem = 120 * 1024;          // > half an SM: one CTA per SM owns all of TMEM
 
 __device__ __forceinline__ void raise(unsigned bits) { atomicOr(&g_status_umma, bits); }
 __device__ __forceinline__ bool status_set() {
   return *reinterpret_cast<volatile unsigned*>(&g_status_umma) != 0u;
 }
 
+// Spin on an mbarrier phase.  After ~0.5 ms give up at once if another wait
+// already timed out; after kWaitLimitCycles raise kErrTimeout and give up.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
   auto tw = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
@@ -87,17 +98,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
 }
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 
 // Shared-memory carve-up (byte offsets), identical on host and device.
 struct Layout {
-  int codes, a, b, red, bars, route, total;
+  int codes, b, red, bars, route, total;
   __host__ __device__ Layout(int b_bytes, int red_bytes, bool grouped) {
     codes = 0;
-    a = codes + kCodeStages * kCodeStage;
-    b = a + kAStages * kAStage;
+    b = codes + kCodeStages * kCodeStage;
     red = b + b_bytes;
     bars = red + red_bytes;
     route = bars + 256;
@@ -105,22 +112,22 @@ struct Layout {
   }
 };
 
-// Decode one group (three 32-bit words) of a row: 32 E4M3 bytes as two
-// 16-byte halves (codes 0-15 and 16-31).
+// Decode one group (three 32-bit words) of a row into 8 TMEM columns:
+// v[0..7] = E4M3 bytes of codes 0..31, four per column.
 __device__ __forceinline__ void decode_group(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t cb_lo,
-                                             uint32_t cb_hi, uint4& lo, uint4& hi) {
+                                             uint32_t cb_hi, uint32_t* v) {
   const uint32_t s0 = spread_codes8(w0);
   const uint32_t s1 = spread_codes8(__funnelshift_r(w0, w1, 24));
   const uint32_t s2 = spread_codes8(__funnelshift_r(w1, w2, 16));
   const uint32_t s3 = spread_codes8(w2 >> 8);
-  lo.x = lookup4(cb_lo, cb_hi, s0);
-  lo.y = lookup4(cb_lo, cb_hi, s0 >> 16);
-  lo.z = lookup4(cb_lo, cb_hi, s1);
-  lo.w = lookup4(cb_lo, cb_hi, s1 >> 16);
-  hi.x = lookup4(cb_lo, cb_hi, s2);
-  hi.y = lookup4(cb_lo, cb_hi, s2 >> 16);
-  hi.z = lookup4(cb_lo, cb_hi, s3);
-  hi.w = lookup4(cb_lo, cb_hi, s3 >> 16);
+  v[0] = lookup4(cb_lo, cb_hi, s0);
+  v[1] = lookup4(cb_lo, cb_hi, s0 >> 16);
+  v[2] = lookup4(cb_lo, cb_hi, s1);
+  v[3] = lookup4(cb_lo, cb_hi, s1 >> 16);
+  v[4] = lookup4(cb_lo, cb_hi, s2);
+  v[5] = lookup4(cb_lo, cb_hi, s2 >> 16);
+  v[6] = lookup4(cb_lo, cb_hi, s3);
+  v[7] = lookup4(cb_lo, cb_hi, s3 >> 16);
 }
 
 template <int NTOK, bool GROUPED>
@@ -128,7 +135,6 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   extern __shared__ __align__(1024) uint8_t smem[];
   const Layout L(p.b_bytes, p.red_bytes, GROUPED);
   uint8_t* codes_s = smem + L.codes;
-  uint8_t* a_s = smem + L.a;
   uint8_t* b_s = smem + L.b;
   float* red_s = reinterpret_cast<float*>(smem + L.red);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
@@ -167,11 +173,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], kDecWarps);
+      mbar_init(&acc_empty[i], 4);
     }
-    mbar_init(b_full, kDecWarps);
-    mbar_init(red_full, (cs > 1 ? cs - 1 : 1) * kDecWarps * 32);
-    mbar_init(red_free, kDecWarps * 32);
+    mbar_init(b_full, 4);
+    mbar_init(red_full, (cs > 1 ? cs - 1 : 1) * 128);
+    mbar_init(red_free, 128);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) prefetch_tmap(&p.tmap_codes);
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   // scale factors of B: 2^0 in every byte of 8 columns, all 128 lanes
-  if (warp >= 2 && warp < 6) {
+  if (warp >= kEpiWarp0) {
     const uint32_t q = warp & 3;
     for (int c = 0; c < 8; c += 4)
       tmem_st_x4(tbase + ((32 * q) << 16) + kSfbCol + c, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
@@ -278,10 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     // --------------------------------------------------------- MMA issuer --
     if (lane == 0) {
       uint32_t it = 0;
-      const uint32_t a_base = smem_u32(a_s), b_base = smem_u32(b_s);
+      const uint32_t b_base = smem_u32(b_s);
       for (int ui = 0; ui < n_units; ++ui) {
         const int abuf = ui & 1;
-        wait_bounded(b_full, ui & 1);
+        if constexpr (GROUPED) wait_bounded(b_full, ui & 1);   // this unit's gathered B
         wait_bounded(&acc_empty[abuf], ((ui >> 1) & 1) ^ 1);
         tc_fence_after();
         int n_mma = NTOK;
@@ -294,24 +300,65 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
           const int i = kt - kt0;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint64_t ad = umma_desc_kmajor(a_base + slot * kAStage + 2 * j * 2048, 2048, 128);
             const uint64_t bd = umma_desc_kmajor(b_base + (i * 8 + 2 * j) * NTOK * 16, NTOK * 16, 128);
-            umma_mxf8(tbase + abuf * kAccCols, ad, bd, idesc | (uint32_t(j) << 29),
-                      tbase + kSfaCol + slot * 4, tbase + kSfbCol, (i | j) != 0);
+            umma_mxf8_ts(tbase + abuf * kAccCols, tbase + kACol + slot * 32 + j * 8, bd,
+                         idesc | (uint32_t(j) << 29), tbase + kSfaCol + slot * 4, tbase + kSfbCol,
+                         (i | j) != 0);
           }
           umma_commit(&a_empty[slot]);
         }
         umma_commit(&acc_full[abuf]);
       }
     }
-  } else {
+  } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ decoders --
     const int dw = warp - 2, dg = dw >> 2, q = warp & 3;
-    const int r = 32 * q + lane;                      // row inside the tile
+    const int r = 32 * q + lane;                      // row inside the tile == TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t codes_base = smem_u32(codes_s), a_base = smem_u32(a_s);
-    const uint32_t a_row_off = (r >> 3) * 128 + (r & 7) * 16;
-    uint32_t it = 0;
+    const uint32_t codes_base = smem_u32(codes_s);
+    uint32_t it_unit = 0;                             // shared k-tile counter at the unit start
+    for (int ui = 0; ui < n_units; ++ui, it_unit += kt1 - kt0) {
+      int row0, row_end, e;
+      unit_rows(ui, row0, row_end, e);
+      const int grow = row0 + r;
+      const bool ok = grow < row_end;
+      const uint2 cb = ok ? __ldg(reinterpret_cast<const uint2*>(p.codebooks + size_t(grow) * 8)) : make_uint2(0, 0);
+      const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + size_t(ok ? grow : 0) * (p.K / 32));
+      // this group's k-tiles are kt0 + dg, kt0 + dg + kDecGroups, ...; the
+      // scale word is fetched one of them ahead
+      uint32_t sw_next = (ok && kt0 + dg < kt1) ? __ldg(srow + kt0 + dg) : 0x7F7F7F7Fu;
+      for (int kt = kt0 + dg; kt < kt1; kt += kDecGroups) {
+        const uint32_t it = it_unit + (kt - kt0);
+        const int cslot = it % kCodeStages, aslot = it % kAStages;
+        const uint32_t sw = sw_next;
+        if (ok && kt + kDecGroups < kt1) sw_next = __ldg(srow + kt + kDecGroups);
+        wait_bounded(&codes_full[cslot], (it / kCodeStages) & 1u);
+        const uint32_t crow = codes_base + cslot * kCodeStage + r * 48;
+        const uint4 c0 = lds128(crow), c1 = lds128(crow + 16), c2 = lds128(crow + 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&codes_empty[cslot]);
+        uint32_t v[32];
+        decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
+        decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
+        decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, v + 16);
+        decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, v + 24);
+        wait_bounded(&a_empty[aslot], ((it / kAStages) & 1u) ^ 1u);
+        tc_fence_after();
+        tmem_st_x32(tbase + lane_addr + kACol + aslot * 32, v);
+        // A scale of row m is read from TMEM lane m, column (base + m / 32),
+        // byte = the MMA's a_sf_id: quadrant q writes column base + q
+        tmem_st_x1(tbase + lane_addr + kSfaCol + aslot * 4 + q, sw);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[aslot]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue --
+    const int q = warp & 3, ew = warp - kEpiWarp0;
+    const int r = 32 * q + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
     int prev_e = -1;
     for (int ui = 0; ui < n_units; ++ui) {
       int row0, row_end, e;
@@ -320,8 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       if constexpr (GROUPED) {
         if (e != prev_e) {
           // token list of expert e, then gather its activation rows into B
-          named_bar_sync(1, kDecWarps * 32);   // previous epilogue is done with the list
-          if (dw == 0) {
+          // (the MMAs of the previous unit are complete: its epilogue waited)
+          named_bar_sync(2, 128);
+          if (ew == 0) {
             const int nr = p.M * p.topk;
             int base = 0;
             for (int i0 = 0; i0 < nr; i0 += 32) {
@@ -334,10 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
             }
             if (lane == 0) misc[0] = min(base, NTOK);
           }
-          named_bar_sync(1, kDecWarps * 32);
+          named_bar_sync(2, 128);
           const int cnt = misc[0], nz = min(NTOK, (cnt + 15) & ~15);
           const int nchunk = p.K / 16;
-          for (int i = tid - 64; i < nz * nchunk; i += kDecWarps * 32) {
+          for (int i = tid - kEpiWarp0 * 32; i < nz * nchunk; i += 128) {
             const int tk = i % nz, c = i / nz;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (tk < cnt)
@@ -345,59 +393,27 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
             *reinterpret_cast<uint4*>(b_s + c * NTOK * 16 + (tk >> 3) * 128 + (tk & 7) * 16) = v;
           }
           fence_proxy_async_smem();
-          named_bar_sync(1, kDecWarps * 32);
+          named_bar_sync(2, 128);
           prev_e = e;
         }
         ntok = misc[0];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_full);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_full);
 
       const int grow = row0 + r;
       const bool ok = grow < row_end;
-      const uint2 cb = ok ? __ldg(reinterpret_cast<const uint2*>(p.codebooks + size_t(grow) * 8)) : make_uint2(0, 0);
-      const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + size_t(ok ? grow : 0) * (p.K / 32));
-      for (int kt = kt0; kt < kt1; ++kt, ++it) {
-        if (((kt - kt0) & 1) != dg) continue;
-        const int cslot = it % kCodeStages, aslot = it % kAStages;
-        const uint32_t sw = ok ? __ldg(srow + kt) : 0x7F7F7F7Fu;
-        wait_bounded(&codes_full[cslot], (it / kCodeStages) & 1u);
-        const uint32_t crow = codes_base + cslot * kCodeStage + r * 48;
-        const uint4 c0 = lds128(crow), c1 = lds128(crow + 16), c2 = lds128(crow + 32);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&codes_empty[cslot]);
-        uint4 h[8];
-        decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, h[0], h[1]);
-        decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, h[2], h[3]);
-        decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, h[4], h[5]);
-        decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, h[6], h[7]);
-        wait_bounded(&a_empty[aslot], ((it / kAStages) & 1u) ^ 1u);
-        const uint32_t adst = a_base + aslot * kAStage + a_row_off;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) sts128(adst + c * 2048, h[c].x, h[c].y, h[c].z, h[c].w);
-        // A scale of row m is read from TMEM lane m, column (base + m / 32),
-        // byte = the MMA's a_sf_id: quadrant q writes column base + q
-        tmem_st_x1(tbase + lane_addr + kSfaCol + aslot * 4 + q, sw);
-        tmem_st_wait();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[aslot]);
-      }
-
-      // ---------------------------------------------------------- epilogue --
       const int abuf = ui & 1;
       wait_bounded(&acc_full[abuf], (ui >> 1) & 1);
       tc_fence_after();
-      constexpr int HALF = NTOK / 2;
-      float v[HALF];
+      float v[NTOK];
 #pragma unroll
-      for (int c = 0; c < HALF; c += 8) {
-        uint32_t t[8];
-        tmem_ld_x8(tbase + lane_addr + abuf * kAccCols + dg * HALF + c, t);
+      for (int c = 0; c < NTOK; c += 16) {
+        uint32_t t[16];
+        tmem_ld_x16(tbase + lane_addr + abuf * kAccCols + c, t);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[c + i] = __uint_as_float(t[i]);
+        for (int i = 0; i < 16; ++i) v[c + i] = __uint_as_float(t[i]);
       }
       tc_fence_before();
       __syncwarp();
@@ -406,38 +422,41 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       if constexpr (!GROUPED) {
         if (cs > 1) {
           // split K: partial tiles meet in the leader CTA's shared memory
-          const uint32_t slot_off = ((r * NTOK) + dg * HALF) * 4;
+          const uint32_t slot_off = r * NTOK * 4;
           if (rank != 0) {
             wait_bounded<true>(red_free, (ui & 1) ^ 1);
             const uint32_t dst = mapa_shared(smem_u32(red_s) + (rank - 1) * kRows * NTOK * 4 + slot_off, 0);
 #pragma unroll
-            for (int c = 0; c < HALF; c += 4) st_cluster_v4(dst + c * 4, v[c], v[c + 1], v[c + 2], v[c + 3]);
+            for (int c = 0; c < NTOK; c += 4) st_cluster_v4(dst + c * 4, v[c], v[c + 1], v[c + 2], v[c + 3]);
             mbar_arrive_remote(mapa_shared(smem_u32(red_full), 0));
             continue;
           }
           wait_bounded<true>(red_full, ui & 1);
           for (int s = 0; s < cs - 1; ++s) {
-            const float* src = red_s + s * kRows * NTOK + r * NTOK + dg * HALF;
+            const float4* src = reinterpret_cast<const float4*>(red_s + s * kRows * NTOK + r * NTOK);
 #pragma unroll
-            for (int c = 0; c < HALF; ++c) v[c] += src[c];
+            for (int c = 0; c < NTOK / 4; ++c) {
+              const float4 t = src[c];
+              v[4 * c] += t.x;
+              v[4 * c + 1] += t.y;
+              v[4 * c + 2] += t.z;
+              v[4 * c + 3] += t.w;
+            }
           }
           // tell every other CTA of the cluster that its slot may be reused
           for (int s = 1; s < cs; ++s) mbar_arrive_remote(mapa_shared(smem_u32(red_free), s));
         }
         if (ok) {
 #pragma unroll
-          for (int c = 0; c < HALF; ++c) {
-            const int tok = dg * HALF + c;
-            if (tok < ntok) p.y[size_t(tok) * p.N + grow] = v[c] * __ldg(p.a_scale + tok);
-          }
+          for (int c = 0; c < NTOK; ++c)
+            if (c < ntok) p.y[size_t(c) * p.N + grow] = v[c] * __ldg(p.a_scale + c);
         }
       } else {
         if (ok) {
 #pragma unroll
-          for (int c = 0; c < HALF; ++c) {
-            const int i = dg * HALF + c;
-            if (i < ntok) {
-              const int tok = list_tok[i] & 0xff, slot = list_tok[i] >> 8;
+          for (int c = 0; c < NTOK; ++c) {
+            if (c < ntok) {
+              const int tok = list_tok[c] & 0xff, slot = list_tok[c] >> 8;
               p.y[(size_t(tok) * p.topk + slot) * p.N + (grow - e * p.N)] = v[c] * __ldg(p.a_scale + tok);
             }
           }
@@ -459,10 +478,53 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
 }
 
 template <int NTOK, bool GROUPED>
+cudaError_t configure(int smem, int cs) {
+  auto kern = umma_kernel<NTOK, GROUPED>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && cs > 1) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+template <int NTOK, bool GROUPED>
+int max_clusters_t(int cs, int smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, cs, smem);
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (configure<NTOK, GROUPED>(smem, cs) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs * 64);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, umma_kernel<NTOK, GROUPED>, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  cache[key] = n;
+  return n;
+}
+
+int max_clusters(int ntok, int cs, int smem) {
+  if (ntok <= 16) return max_clusters_t<16, false>(cs, smem);
+  if (ntok <= 32) return max_clusters_t<32, false>(cs, smem);
+  return max_clusters_t<64, false>(cs, smem);
+}
+
+template <int NTOK, bool GROUPED>
 int launch_t(const UmmaParams& p, int grid, int cs, int smem, cudaStream_t stream) {
   auto kern = umma_kernel<NTOK, GROUPED>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return CBQ_ECUDA;
+  if (configure<NTOK, GROUPED>(smem, cs) != cudaSuccess) return CBQ_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -471,18 +533,12 @@ int launch_t(const UmmaParams& p, int grid, int cs, int smem, cudaStream_t strea
   cudaLaunchAttribute attr[1];
   cfg.numAttrs = 0;
   if (cs > 1) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-      return CBQ_ECUDA;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // no more clusters than can be resident at once (the grid is persistent)
-    int max_clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) == cudaSuccess && max_clusters > 0)
-      cfg.gridDim = dim3(std::min(grid / cs, max_clusters) * cs);
   }
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
   note_launch();
@@ -515,22 +571,25 @@ int launch_umma(const UmmaParams& p_in, bool grouped, cudaStream_t stream) {
     if (L.total > kMaxSmem) return CBQ_EINVAL;   // K too long for a resident B tile
     const int units = std::min(p.E, p.M * p.topk) * tiles;
     const int grid = std::max(1, std::min(units, sms));
-    return dispatch<true>(p, ntok, grid, 1, L.total, stream);
+    return dispatch<true>(p, ntok, grid, 1, std::max(L.total, kMinSmem), stream);
   }
-  // split K over a cluster when there are too few tiles to fill the GPU:
-  // minimise (rounds of tiles) x (k-tiles per CTA) within the smem budget
-  int best_cs = 0;
+  // Split K over a cluster when there are too few tiles to fill the GPU:
+  // minimise (rounds of tiles over the resident clusters) x (k-tiles per CTA).
+  int best_cs = 0, best_clusters = 0;
   long long best_cost = 0;
   for (int cs = 1; cs <= 8 && cs <= nkt; ++cs) {
     const int per = (nkt + cs - 1) / cs;
     const Layout L(ntok * per * 128, cs > 1 ? (cs - 1) * kRows * ntok * 4 : 0, false);
     if (L.total > kMaxSmem) continue;
-    const int clusters = sms / cs;
+    const int smem = std::max(L.total, kMinSmem);
+    const int clusters = cs == 1 ? sms : max_clusters(ntok, cs, smem);
+    if (clusters <= 0) continue;
     const long long rounds = (tiles + clusters - 1) / clusters;
-    const long long cost = rounds * per * 16 + (cs > 1 ? 4 + cs : 0);
+    const long long cost = rounds * per * 16 + (cs > 1 ? 8 : 0);
     if (best_cs == 0 || cost < best_cost) {
       best_cs = cs;
       best_cost = cost;
+      best_clusters = clusters;
     }
   }
   if (best_cs == 0) return CBQ_EINVAL;
@@ -539,8 +598,8 @@ int launch_umma(const UmmaParams& p_in, bool grouped, cudaStream_t stream) {
   p.b_bytes = ntok * ((nkt + cs - 1) / cs) * 128;
   p.red_bytes = cs > 1 ? (cs - 1) * kRows * ntok * 4 : 0;
   const Layout L(p.b_bytes, p.red_bytes, false);
-  const int grid = std::min(tiles, sms / cs) * cs;
-  return dispatch<false>(p, ntok, grid, cs, L.total, stream);
+  const int grid = std::min(tiles, best_clusters) * cs;
+  return dispatch<false>(p, ntok, grid, cs, std::max(L.total, kMinSmem), stream);
 }
 
 unsigned take_status_umma(cudaStream_t stream) {
