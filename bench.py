@@ -453,7 +453,7 @@ def run_reference(args):
     _oracle_step(o, pw, acts, scs, 16)
     per_row = (time.perf_counter() - t) / 16
     total_steps = max(1, args.steps + args.warmup)
-    rows = int(min(N_DIM, max(1, 60.0 / total_steps / max(per_row, 1e-9))))
+    rows = int(min(N_DIM, max(1, args.ref_seconds / total_steps / max(per_row, 1e-9))))
     for _ in range(args.warmup):
         _oracle_step(o, pw, acts, scs, rows)
     t = time.perf_counter()
@@ -478,6 +478,35 @@ def run_reference(args):
         torch.distributed.destroy_process_group()
 
 
+def run_single(args):
+    """A few back-to-back calls of one named workload on one kernel, for
+    profiler captures (cold cache per profiler pass)."""
+    from bit_codebook_quantized_gb300 import build as _b
+    _b.build()
+    wl = synth.workloads()[args.single]
+    dev = torch.device("cuda", 0)
+    if wl.experts:
+        pw = synth.gen_weights(wl.experts * wl.N, wl.K, seed=1)
+        idx = torch.from_numpy(synth.gen_moe_routing(wl.M, wl.experts, wl.budget, wl.topk, seed=4)).to(dev)
+        y = torch.empty((wl.M, wl.topk, wl.N), device=dev)
+    else:
+        pw = synth.gen_weights(wl.N, wl.K, seed=1)
+        y = torch.empty((wl.M, wl.N), device=dev)
+    w = ops.PackedWeights.from_host(pw.codes, pw.scales, pw.codebooks, wl.N, wl.K, device=dev)
+    a = torch.from_numpy(synth.gen_activations(wl.M, wl.K, seed=2, half_normal=wl.half_normal)).to(dev)
+    s = torch.from_numpy(synth.gen_a_scale(wl.M, seed=3, mode=wl.a_scale)).to(dev)
+    for _ in range(args.calls):
+        if wl.experts:
+            ops.grouped_gemm(a, s, w, wl.experts, idx, out=y, path=args.path)
+        else:
+            ops.gemm(a, s, w, out=y, path=args.path)
+    torch.cuda.synchronize()
+    st = ops.device_status()
+    print(json.dumps({"single": args.single, "path": args.path, "calls": args.calls, "status": st}))
+    if st != ops.OK:
+        sys.exit(1)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -486,7 +515,16 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU-baseline budget on rank 0 (0 disables)")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="--impl reference: CPU seconds the whole run should take")
+    ap.add_argument("--single", default=None,
+                    help="run --calls calls of one workload (see synth.workloads()) and exit")
+    ap.add_argument("--path", type=int, default=0, help="kernel for --single: 0 auto, 1 gemv, 2 mma")
+    ap.add_argument("--calls", type=int, default=3)
     args = ap.parse_args(argv)
+    if args.single:
+        run_single(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -99,6 +99,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+// mbarriers (codes full/empty, A full/empty, 2 accumulators full/empty,
+// B, split-K full/free), then the TMEM base slot and two ints.
+constexpr int kNumBars = 2 * kCodeStages + 2 * kAStages + 4 + 3;
+constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
+static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area too small");
+
 // Shared-memory carve-up (byte offsets), identical on host and device.
 struct Layout {
   int codes, b, red, bars, route, total;
@@ -107,7 +113,7 @@ struct Layout {
     b = codes + kCodeStages * kCodeStage;
     red = b + b_bytes;
     bars = red + red_bytes;
-    route = bars + 256;
+    route = bars + kBarBytes;
     total = route + (grouped ? (kMaxRouting * 4 + 64 * 4 + 16 + kMaxExperts * 2 + kMaxExperts) : 0);
   }
 };
