@@ -7,9 +7,10 @@ more than 4x the 129 MB L2, so weight bytes come from HBM).  Activations,
 a_scale and codebooks are seeded synthetic data of the pages' distributions.
 
 Metric: effective weight GB/s = packed weight bytes (3KN/8 + KN/32 + 8N per
-call) / time.  The timed region is K steps replayed from a CUDA graph, timed
-with CUDA events on the launching stream; per-kernel durations come from
-events between the kernels of the graph.  Prints one JSON line.
+call) / time.  The timed region replays one CUDA graph of S back-to-back
+calls per M, K/S rounds (K steps in all), timed with CUDA events on the
+launching stream; the events around each graph replay give every kernel's
+mean duration inside the same region.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -228,42 +229,41 @@ def run_ours(args):
     if ops.device_status(stream) != ops.OK:
         raise RuntimeError("device status not ok after warm-up")
 
-    # ---- capture a graph of S steps with an event between every kernel -------
+    # ---- one CUDA graph per M: S back-to-back calls on rotating weight copies --
     S = min(args.steps, 250)
     while args.steps % S:
         S -= 1
     reps = args.steps // S
-    try:   # event-record nodes inside the graph time every kernel of the replay
-        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(S * len(MS) + 1)]
-    except TypeError:
-        evs = None
-    g = torch.cuda.CUDAGraph()
+    graphs = {}
     launches_before = ops.launch_count()
-    with torch.cuda.graph(g, stream=stream):
-        e = 0
-        if evs:
-            evs[e].record(stream)
-        for _ in range(S):
-            for M in MS:
+    for M in MS:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(S):
                 w = copies[call[0] % ROTATE]
                 call[0] += 1
                 ops.gemm(acts[M], scs[M], w, out=ys[M], stream=stream)
-                e += 1
-                if evs:
-                    evs[e].record(stream)
-    launches_per_graph = ops.launch_count() - launches_before
-    g.replay()
+        graphs[M] = g
+    launches_per_step = (ops.launch_count() - launches_before) // S
+    for M in MS:
+        graphs[M].replay()
     stream.synchronize()
 
-    # ---- timed region ---------------------------------------------------------
+    # ---- timed region: K steps = reps x (S calls at each M), events between
+    # the graph replays give every kernel's duration inside the same region
+    ev = {M: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)] for M in MS}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):
             t0.record(stream)
-            for _ in range(reps):
-                g.replay()
+            for rep in range(reps):
+                for M in MS:
+                    ev[M][rep][0].record(stream)
+                    graphs[M].replay()
+                    ev[M][rep][1].record(stream)
             t1.record(stream)
         torch.cuda.synchronize()
     barrier(ws)
@@ -271,17 +271,9 @@ def run_ours(args):
     st = ops.device_status(stream)
     if st != ops.OK:
         raise RuntimeError(f"device status {st} after timed region")
-
-    # per-kernel durations from the events of the last replay
-    if evs:
-        per_m_ms = {M: [] for M in MS}
-        for i in range(S * len(MS)):
-            per_m_ms[MS[i % len(MS)]].append(evs[i].elapsed_time(evs[i + 1]))
-        per_m_us = {M: 1e3 * float(np.mean(v)) for M, v in per_m_ms.items()}
-        kernel_timing = "event-record nodes between the kernels of the timed graph"
-    else:
-        per_m_us = time_per_m(stream, copies, acts, scs, ys, call)
-        kernel_timing = "separate graphs per M right after the timed region (no external events)"
+    per_m_us = {M: 1e3 * sum(a.elapsed_time(b) for a, b in ev[M]) / (reps * S) for M in MS}
+    kernel_timing = (f"CUDA events around each of the {reps} replays of every per-M graph of {S} "
+                     f"back-to-back calls, inside the timed region")
 
     units = args.steps * len(MS) * weight_bytes()
     t_max, units_all = reduce_max_sum(ws, elapsed_s, units, dev)
@@ -330,36 +322,16 @@ def run_ours(args):
                        "weight_bytes_per_call": weight_bytes(),
                        "l2": f"inputs larger than L2: {ROTATE} rotating weight copies "
                              f"({ROTATE * weight_bytes() / 1e6:.0f} MB) vs 129 MB L2",
-                       "timing": f"CUDA graph of {S} steps replayed {reps}x, CUDA events; "
-                                 f"per-kernel: {kernel_timing}",
+                       "timing": f"per-M CUDA graphs of {S} calls, {reps} rounds; {kernel_timing}",
                        "parallelism": f"replicas x{ws}"},
             "roofline": roof, "per_call": per_call,
             "e2e": e2e, "cpu_baseline": cpu,
-            "gpu_launches": int(launches_per_graph * reps),
+            "gpu_launches": int(launches_per_step * args.steps),
             "clocks": clk.summary(),
         }
         print(json.dumps(out), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
-
-
-def time_per_m(stream, copies, acts, scs, ys, call, launches=200):
-    out = {}
-    for M in MS:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for _ in range(launches):
-                ops.gemm(acts[M], scs[M], copies[call[0] % ROTATE], out=ys[M], stream=stream)
-                call[0] += 1
-        g.replay()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-        stream.synchronize()
-        out[M] = 1e3 * a.elapsed_time(b) / launches
-    return out
 
 
 def run_e2e(dev, stream, copies, args):

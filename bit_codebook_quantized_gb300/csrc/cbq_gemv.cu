@@ -65,17 +65,19 @@ __device__ __forceinline__ bool status_set() {
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    const long long dt = clock64() - t0;
-    if (dt > (1LL << 20)) {
-      if (status_set()) return false;
-      if (dt > kWaitLimitCycles) {
-        raise(kErrTimeout);
-        return false;
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63u) == 0) {                       // read the clock now and then only
+      const long long dt = clock64() - t0;
+      if (dt > (1LL << 20)) {
+        if (status_set()) return false;
+        if (dt > kWaitLimitCycles) {
+          raise(kErrTimeout);
+          return false;
+        }
       }
     }
   }
-  return true;
 }
 
 struct SmemLayout {

@@ -80,17 +80,19 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
   auto tw = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
   if (tw()) return true;
   const long long t0 = clock64();
-  while (!tw()) {
-    const long long dt = clock64() - t0;
-    if (dt > (1LL << 20)) {
-      if (status_set()) return false;
-      if (dt > kWaitLimitCycles) {
-        raise(kErrTimeout);
-        return false;
+  for (uint32_t n = 1;; ++n) {
+    if (tw()) return true;
+    if ((n & 63u) == 0) {                       // read the clock now and then only
+      const long long dt = clock64() - t0;
+      if (dt > (1LL << 20)) {
+        if (status_set()) return false;
+        if (dt > kWaitLimitCycles) {
+          raise(kErrTimeout);
+          return false;
+        }
       }
     }
   }
-  return true;
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -100,17 +102,20 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 }
 
 // mbarriers (codes full/empty, A full/empty, 2 accumulators full/empty,
-// B, split-K full/free), then the TMEM base slot and two ints.
-constexpr int kNumBars = 2 * kCodeStages + 2 * kAStages + 4 + 3;
+// 2 codebook slots full/empty, B, split-K full/free), then the TMEM base
+// slot and two ints.
+constexpr int kNumBars = 2 * kCodeStages + 2 * kAStages + 4 + 4 + 3;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area too small");
 
 // Shared-memory carve-up (byte offsets), identical on host and device.
 struct Layout {
-  int codes, b, red, bars, route, total;
+  int codes, scales, cbs, b, red, bars, route, total;
   __host__ __device__ Layout(int b_bytes, int red_bytes, bool grouped) {
     codes = 0;
-    b = codes + kCodeStages * kCodeStage;
+    scales = codes + kCodeStages * kCodeStage;     // [stage][128] scale words
+    cbs = scales + kCodeStages * kRows * 4;         // [2][128] codebooks
+    b = cbs + 2 * kRows * 8;
     red = b + b_bytes;
     bars = red + red_bytes;
     route = bars + kBarBytes;
@@ -141,6 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   extern __shared__ __align__(1024) uint8_t smem[];
   const Layout L(p.b_bytes, p.red_bytes, GROUPED);
   uint8_t* codes_s = smem + L.codes;
+  uint32_t* scales_s = reinterpret_cast<uint32_t*>(smem + L.scales);   // [stage][128 rows]
+  uint2* cb_s = reinterpret_cast<uint2*>(smem + L.cbs);                 // [2][128 rows]
   uint8_t* b_s = smem + L.b;
   float* red_s = reinterpret_cast<float*>(smem + L.red);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
@@ -150,7 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   uint64_t* a_empty = a_full + kAStages;
   uint64_t* acc_full = a_empty + kAStages;
   uint64_t* acc_empty = acc_full + 2;
-  uint64_t* b_full = acc_empty + 2;
+  uint64_t* cb_full = acc_empty + 2;
+  uint64_t* cb_empty = cb_full + 2;
+  uint64_t* b_full = cb_empty + 2;
   uint64_t* red_full = b_full + 1;
   uint64_t* red_free = red_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_free + 1);
@@ -167,10 +176,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   const int nkt = p.K / 128;
   const int kt0 = rank * nkt / cs, kt1 = (rank + 1) * nkt / cs;
   const int tiles = (p.N + kRows - 1) / kRows;
+  const int gk = p.K / 32;                                // scale bytes per row
 
   if (tid == 0) {
     for (int i = 0; i < kCodeStages; ++i) {
-      mbar_init(&codes_full[i], 1);
+      mbar_init(&codes_full[i], 1 + 32);                  // TMA bytes + 32 lanes' cp.async
       mbar_init(&codes_empty[i], 4);
     }
     for (int i = 0; i < kAStages; ++i) {
@@ -180,6 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);
+      mbar_init(&cb_full[i], 32);
+      mbar_init(&cb_empty[i], kDecWarps);
     }
     mbar_init(b_full, 4);
     mbar_init(red_full, (cs > 1 ? cs - 1 : 1) * 128);
@@ -191,6 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (cs > 1) cluster_sync();                             // peers' barriers exist before any remote arrive
+  const uint32_t tbase = *tmem_slot;
 
   // ---- which units does this CTA own? ----
   int n_units, u_begin, u_step;
@@ -228,35 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     n_units = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total) / gridDim.x) - u_begin;
     u_step = 1;
   } else {
-    // resident activations for this CTA's K range, K-major core-matrix layout:
-    // chunk c (16 k) at c * NTOK * 16, token group j at j * 128, token % 8 at * 16
-    const int kb = kt0 * 128, nchunk = (kt1 - kt0) * 8;
-    for (int i = tid; i < NTOK * nchunk; i += kThreads) {
-      const int tok = i % NTOK, c = i / NTOK;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (tok < p.M) v = __ldg(reinterpret_cast<const uint4*>(p.a + size_t(tok) * p.K + kb + c * 16));
-      *reinterpret_cast<uint4*>(b_s + c * NTOK * 16 + (tok >> 3) * 128 + (tok & 7) * 16) = v;
-    }
-    fence_proxy_async_smem();
     u_begin = cluster_id;
     n_units = cluster_id < tiles ? (tiles - 1 - cluster_id) / n_clusters + 1 : 0;
     u_step = n_clusters;
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *tmem_slot;
-  // scale factors of B: 2^0 in every byte of 8 columns, all 128 lanes
-  if (warp >= kEpiWarp0) {
-    const uint32_t q = warp & 3;
-    for (int c = 0; c < 8; c += 4)
-      tmem_st_x4(tbase + ((32 * q) << 16) + kSfbCol + c, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-    tmem_st_wait();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (cs > 1) cluster_sync();
 
   auto unit_rows = [&](int ui, int& row0, int& row_end, int& e) {
     const int u = u_begin + ui * u_step;
@@ -272,198 +264,244 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   };
 
   if (warp == 0) {
-    // ------------------------------------------------------ TMA producer --
-    if (lane == 0) {
-      uint32_t it = 0;
-      for (int ui = 0; ui < n_units; ++ui) {
-        int row0, row_end, e;
-        unit_rows(ui, row0, row_end, e);
-        for (int kt = kt0; kt < kt1; ++kt, ++it) {
-          const int slot = it % kCodeStages;
+    // ------------------------------------------------------ producer warp --
+    // Starts at once (the rest of the CTA loads B meanwhile).  Per unit: the
+    // rows' codebooks (cp.async, 8 B a row); per k-tile: the code box (TMA,
+    // lane 0) and the rows' 4 scale bytes (cp.async, 4 rows a lane).
+    uint32_t it = 0;
+    const uint32_t codes_base = smem_u32(codes_s), scales_base = smem_u32(scales_s), cb_base = smem_u32(cb_s);
+    for (int ui = 0; ui < n_units; ++ui) {
+      int row0, row_end, e;
+      unit_rows(ui, row0, row_end, e);
+      const int cbslot = ui & 1;
+      if (lane == 0) wait_bounded(&cb_empty[cbslot], ((ui >> 1) & 1) ^ 1);
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = lane + 32 * i, g = row0 + row;
+        if (g < row_end) cp_async8(cb_base + (cbslot * kRows + row) * 8, p.codebooks + size_t(g) * 8);
+      }
+      cp_async_arrive(&cb_full[cbslot]);
+      for (int kt = kt0; kt < kt1; ++kt, ++it) {
+        const int slot = it % kCodeStages;
+        if (lane == 0) {
           wait_bounded(&codes_empty[slot], ((it / kCodeStages) & 1u) ^ 1u);
           mbar_arrive_expect_tx(&codes_full[slot], kCodeStage);
           tma_load_2d(codes_s + slot * kCodeStage, &p.tmap_codes, &codes_full[slot], kt * 48, row0);
         }
-      }
-    }
-  } else if (warp == 1) {
-    // --------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
-      uint32_t it = 0;
-      const uint32_t b_base = smem_u32(b_s);
-      for (int ui = 0; ui < n_units; ++ui) {
-        const int abuf = ui & 1;
-        if constexpr (GROUPED) wait_bounded(b_full, ui & 1);   // this unit's gathered B
-        wait_bounded(&acc_empty[abuf], ((ui >> 1) & 1) ^ 1);
-        tc_fence_after();
-        int n_mma = NTOK;
-        if constexpr (GROUPED) n_mma = min(NTOK, (misc[0] + 15) & ~15);
-        const uint32_t idesc = umma_idesc_mxf8(n_mma, 0, 0);
-        for (int kt = kt0; kt < kt1; ++kt, ++it) {
-          const int slot = it % kAStages;
-          wait_bounded(&a_full[slot], (it / kAStages) & 1u);
-          tc_fence_after();
-          const int i = kt - kt0;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint64_t bd = umma_desc_kmajor(b_base + (i * 8 + 2 * j) * NTOK * 16, NTOK * 16, 128);
-            umma_mxf8_ts(tbase + abuf * kAccCols, tbase + kACol + slot * 32 + j * 8, bd,
-                         idesc | (uint32_t(j) << 29), tbase + kSfaCol + slot * 4, tbase + kSfbCol,
-                         (i | j) != 0);
-          }
-          umma_commit(&a_empty[slot]);
-        }
-        umma_commit(&acc_full[abuf]);
-      }
-    }
-  } else if (warp < kEpiWarp0) {
-    // ------------------------------------------------------------ decoders --
-    const int dw = warp - 2, dg = dw >> 2, q = warp & 3;
-    const int r = 32 * q + lane;                      // row inside the tile == TMEM lane
-    const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t codes_base = smem_u32(codes_s);
-    uint32_t it_unit = 0;                             // shared k-tile counter at the unit start
-    for (int ui = 0; ui < n_units; ++ui, it_unit += kt1 - kt0) {
-      int row0, row_end, e;
-      unit_rows(ui, row0, row_end, e);
-      const int grow = row0 + r;
-      const bool ok = grow < row_end;
-      const uint2 cb = ok ? __ldg(reinterpret_cast<const uint2*>(p.codebooks + size_t(grow) * 8)) : make_uint2(0, 0);
-      const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + size_t(ok ? grow : 0) * (p.K / 32));
-      // this group's k-tiles are kt0 + dg, kt0 + dg + kDecGroups, ...; the
-      // scale word is fetched one of them ahead
-      uint32_t sw_next = (ok && kt0 + dg < kt1) ? __ldg(srow + kt0 + dg) : 0x7F7F7F7Fu;
-      for (int kt = kt0 + dg; kt < kt1; kt += kDecGroups) {
-        const uint32_t it = it_unit + (kt - kt0);
-        const int cslot = it % kCodeStages, aslot = it % kAStages;
-        const uint32_t sw = sw_next;
-        if (ok && kt + kDecGroups < kt1) sw_next = __ldg(srow + kt + kDecGroups);
-        wait_bounded(&codes_full[cslot], (it / kCodeStages) & 1u);
-        const uint32_t crow = codes_base + cslot * kCodeStage + r * 48;
-        const uint4 c0 = lds128(crow), c1 = lds128(crow + 16), c2 = lds128(crow + 32);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&codes_empty[cslot]);
-        uint32_t v[32];
-        decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
-        decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
-        decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, v + 16);
-        decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, v + 24);
-        wait_bounded(&a_empty[aslot], ((it / kAStages) & 1u) ^ 1u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = lane + 32 * i, g = row0 + row;
+          if (g < row_end) cp_async4(scales_base + (slot * kRows + row) * 4, p.scales + size_t(g) * gk + kt * 4);
+        }
+        cp_async_arrive(&codes_full[slot]);
+      }
+    }
+    (void)codes_base;
+  } else {
+    if constexpr (!GROUPED) {
+      // resident activations for this CTA's K range, K-major core-matrix
+      // layout: chunk c (16 k) at c * NTOK * 16, token group j at j * 128,
+      // token % 8 at * 16
+      const int kb = kt0 * 128, nchunk = (kt1 - kt0) * 8;
+      for (int i = tid - 32; i < NTOK * nchunk; i += kThreads - 32) {
+        const int tok = i % NTOK, c = i / NTOK;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (tok < p.M) v = __ldg(reinterpret_cast<const uint4*>(p.a + size_t(tok) * p.K + kb + c * 16));
+        *reinterpret_cast<uint4*>(b_s + c * NTOK * 16 + (tok >> 3) * 128 + (tok & 7) * 16) = v;
+      }
+      fence_proxy_async_smem();
+    }
+    // scale factors of B: 2^0 in every byte of 8 columns, all 128 lanes
+    if (warp >= kEpiWarp0) {
+      const uint32_t q = warp & 3;
+      for (int c = 0; c < 8; c += 4)
+        tmem_st_x4(tbase + ((32 * q) << 16) + kSfbCol + c, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    named_bar_sync(3, kThreads - 32);                     // everyone but the producer
+    tc_fence_after();
+
+    if (warp == 1) {
+      // --------------------------------------------------------- MMA issuer --
+      if (lane == 0) {
+        uint32_t it = 0;
+        const uint32_t b_base = smem_u32(b_s);
+        for (int ui = 0; ui < n_units; ++ui) {
+          const int abuf = ui & 1;
+          if constexpr (GROUPED) wait_bounded(b_full, ui & 1);   // this unit's gathered B
+          wait_bounded(&acc_empty[abuf], ((ui >> 1) & 1) ^ 1);
+          tc_fence_after();
+          int n_mma = NTOK;
+          if constexpr (GROUPED) n_mma = min(NTOK, (misc[0] + 15) & ~15);
+          const uint32_t idesc = umma_idesc_mxf8(n_mma, 0, 0);
+          for (int kt = kt0; kt < kt1; ++kt, ++it) {
+            const int slot = it % kAStages;
+            wait_bounded(&a_full[slot], (it / kAStages) & 1u);
+            tc_fence_after();
+            const int i = kt - kt0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t bd = umma_desc_kmajor(b_base + (i * 8 + 2 * j) * NTOK * 16, NTOK * 16, 128);
+              umma_mxf8_ts(tbase + abuf * kAccCols, tbase + kACol + slot * 32 + j * 8, bd,
+                           idesc | (uint32_t(j) << 29), tbase + kSfaCol + slot * 4, tbase + kSfbCol,
+                           (i | j) != 0);
+            }
+            umma_commit(&a_empty[slot]);
+          }
+          umma_commit(&acc_full[abuf]);
+        }
+      }
+    } else if (warp < kEpiWarp0) {
+      // ------------------------------------------------------------ decoders --
+      const int dw = warp - 2, dg = dw >> 2, q = warp & 3;
+      const int r = 32 * q + lane;                      // row inside the tile == TMEM lane
+      const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+      const uint32_t codes_base = smem_u32(codes_s);
+      uint32_t it_unit = 0;                             // shared k-tile counter at the unit start
+      for (int ui = 0; ui < n_units; ++ui, it_unit += kt1 - kt0) {
+        int row0, row_end, e;
+        unit_rows(ui, row0, row_end, e);
+        const bool ok = row0 + r < row_end;
+        const int cbslot = ui & 1;
+        wait_bounded(&cb_full[cbslot], (ui >> 1) & 1);
+        const uint2 cb = ok ? cb_s[cbslot * kRows + r] : make_uint2(0, 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cb_empty[cbslot]);
+        // this group's k-tiles are kt0 + dg, kt0 + dg + kDecGroups, ...
+        for (int kt = kt0 + dg; kt < kt1; kt += kDecGroups) {
+          const uint32_t it = it_unit + (kt - kt0);
+          const int cslot = it % kCodeStages, aslot = it % kAStages;
+          wait_bounded(&codes_full[cslot], (it / kCodeStages) & 1u);
+          const uint32_t crow = codes_base + cslot * kCodeStage + r * 48;
+          const uint4 c0 = lds128(crow), c1 = lds128(crow + 16), c2 = lds128(crow + 32);
+          const uint32_t sw = ok ? scales_s[cslot * kRows + r] : 0x7F7F7F7Fu;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&codes_empty[cslot]);
+          uint32_t v[32];
+          decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
+          decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
+          decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, v + 16);
+          decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, v + 24);
+          wait_bounded(&a_empty[aslot], ((it / kAStages) & 1u) ^ 1u);
+          tc_fence_after();
+          tmem_st_x32(tbase + lane_addr + kACol + aslot * 32, v);
+          // A scale of row m is read from TMEM lane m, column (base + m / 32),
+          // byte = the MMA's a_sf_id: quadrant q writes column base + q
+          tmem_st_x1(tbase + lane_addr + kSfaCol + aslot * 4 + q, sw);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[aslot]);
+        }
+      }
+    } else {
+      // ------------------------------------------------------------ epilogue --
+      const int q = warp & 3, ew = warp - kEpiWarp0;
+      const int r = 32 * q + lane;
+      const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+      int prev_e = -1;
+      for (int ui = 0; ui < n_units; ++ui) {
+        int row0, row_end, e;
+        unit_rows(ui, row0, row_end, e);
+        int ntok = p.M;
+        if constexpr (GROUPED) {
+          if (e != prev_e) {
+            // token list of expert e, then gather its activation rows into B
+            // (the MMAs of the previous unit are complete: its epilogue waited)
+            named_bar_sync(2, 128);
+            if (ew == 0) {
+              const int nr = p.M * p.topk;
+              int base = 0;
+              for (int i0 = 0; i0 < nr; i0 += 32) {
+                const int i = i0 + lane;
+                const bool hit = (i < nr) && topk_s[i] == e;
+                const unsigned m = __ballot_sync(0xffffffffu, hit);
+                const int pos = base + __popc(m & ((1u << lane) - 1u));
+                if (hit && pos < 64) list_tok[pos] = (i / p.topk) | ((i % p.topk) << 8);
+                base += __popc(m);
+              }
+              if (lane == 0) misc[0] = min(base, NTOK);
+            }
+            named_bar_sync(2, 128);
+            const int cnt = misc[0], nz = min(NTOK, (cnt + 15) & ~15);
+            const int nchunk = p.K / 16;
+            for (int i = tid - kEpiWarp0 * 32; i < nz * nchunk; i += 128) {
+              const int tk = i % nz, c = i / nz;
+              uint4 v = make_uint4(0, 0, 0, 0);
+              if (tk < cnt)
+                v = __ldg(reinterpret_cast<const uint4*>(p.a + size_t(list_tok[tk] & 0xff) * p.K + c * 16));
+              *reinterpret_cast<uint4*>(b_s + c * NTOK * 16 + (tk >> 3) * 128 + (tk & 7) * 16) = v;
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(2, 128);
+            prev_e = e;
+          }
+          ntok = misc[0];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_full);
+        }
+
+        const int grow = row0 + r;
+        const bool ok = grow < row_end;
+        const int abuf = ui & 1;
+        wait_bounded(&acc_full[abuf], (ui >> 1) & 1);
         tc_fence_after();
-        tmem_st_x32(tbase + lane_addr + kACol + aslot * 32, v);
-        // A scale of row m is read from TMEM lane m, column (base + m / 32),
-        // byte = the MMA's a_sf_id: quadrant q writes column base + q
-        tmem_st_x1(tbase + lane_addr + kSfaCol + aslot * 4 + q, sw);
-        tmem_st_wait();
+        float v[NTOK];
+  #pragma unroll
+        for (int c = 0; c < NTOK; c += 16) {
+          uint32_t t[16];
+          tmem_ld_x16(tbase + lane_addr + abuf * kAccCols + c, t);
+          tmem_ld_wait();
+  #pragma unroll
+          for (int i = 0; i < 16; ++i) v[c + i] = __uint_as_float(t[i]);
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[aslot]);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue --
-    const int q = warp & 3, ew = warp - kEpiWarp0;
-    const int r = 32 * q + lane;
-    const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-    int prev_e = -1;
-    for (int ui = 0; ui < n_units; ++ui) {
-      int row0, row_end, e;
-      unit_rows(ui, row0, row_end, e);
-      int ntok = p.M;
-      if constexpr (GROUPED) {
-        if (e != prev_e) {
-          // token list of expert e, then gather its activation rows into B
-          // (the MMAs of the previous unit are complete: its epilogue waited)
-          named_bar_sync(2, 128);
-          if (ew == 0) {
-            const int nr = p.M * p.topk;
-            int base = 0;
-            for (int i0 = 0; i0 < nr; i0 += 32) {
-              const int i = i0 + lane;
-              const bool hit = (i < nr) && topk_s[i] == e;
-              const unsigned m = __ballot_sync(0xffffffffu, hit);
-              const int pos = base + __popc(m & ((1u << lane) - 1u));
-              if (hit && pos < 64) list_tok[pos] = (i / p.topk) | ((i % p.topk) << 8);
-              base += __popc(m);
-            }
-            if (lane == 0) misc[0] = min(base, NTOK);
-          }
-          named_bar_sync(2, 128);
-          const int cnt = misc[0], nz = min(NTOK, (cnt + 15) & ~15);
-          const int nchunk = p.K / 16;
-          for (int i = tid - kEpiWarp0 * 32; i < nz * nchunk; i += 128) {
-            const int tk = i % nz, c = i / nz;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (tk < cnt)
-              v = __ldg(reinterpret_cast<const uint4*>(p.a + size_t(list_tok[tk] & 0xff) * p.K + c * 16));
-            *reinterpret_cast<uint4*>(b_s + c * NTOK * 16 + (tk >> 3) * 128 + (tk & 7) * 16) = v;
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(2, 128);
-          prev_e = e;
-        }
-        ntok = misc[0];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_full);
-      }
+        if (lane == 0) mbar_arrive(&acc_empty[abuf]);
 
-      const int grow = row0 + r;
-      const bool ok = grow < row_end;
-      const int abuf = ui & 1;
-      wait_bounded(&acc_full[abuf], (ui >> 1) & 1);
-      tc_fence_after();
-      float v[NTOK];
-#pragma unroll
-      for (int c = 0; c < NTOK; c += 16) {
-        uint32_t t[16];
-        tmem_ld_x16(tbase + lane_addr + abuf * kAccCols + c, t);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[c + i] = __uint_as_float(t[i]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[abuf]);
-
-      if constexpr (!GROUPED) {
-        if (cs > 1) {
-          // split K: partial tiles meet in the leader CTA's shared memory
-          const uint32_t slot_off = r * NTOK * 4;
-          if (rank != 0) {
-            wait_bounded<true>(red_free, (ui & 1) ^ 1);
-            const uint32_t dst = mapa_shared(smem_u32(red_s) + (rank - 1) * kRows * NTOK * 4 + slot_off, 0);
-#pragma unroll
-            for (int c = 0; c < NTOK; c += 4) st_cluster_v4(dst + c * 4, v[c], v[c + 1], v[c + 2], v[c + 3]);
-            mbar_arrive_remote(mapa_shared(smem_u32(red_full), 0));
-            continue;
-          }
-          wait_bounded<true>(red_full, ui & 1);
-          for (int s = 0; s < cs - 1; ++s) {
-            const float4* src = reinterpret_cast<const float4*>(red_s + s * kRows * NTOK + r * NTOK);
-#pragma unroll
-            for (int c = 0; c < NTOK / 4; ++c) {
-              const float4 t = src[c];
-              v[4 * c] += t.x;
-              v[4 * c + 1] += t.y;
-              v[4 * c + 2] += t.z;
-              v[4 * c + 3] += t.w;
+        if constexpr (!GROUPED) {
+          if (cs > 1) {
+            // split K: partial tiles meet in the leader CTA's shared memory
+            const uint32_t slot_off = r * NTOK * 4;
+            if (rank != 0) {
+              wait_bounded<true>(red_free, (ui & 1) ^ 1);
+              const uint32_t dst = mapa_shared(smem_u32(red_s) + (rank - 1) * kRows * NTOK * 4 + slot_off, 0);
+  #pragma unroll
+              for (int c = 0; c < NTOK; c += 4) st_cluster_v4(dst + c * 4, v[c], v[c + 1], v[c + 2], v[c + 3]);
+              mbar_arrive_remote(mapa_shared(smem_u32(red_full), 0));
+              continue;
             }
+            wait_bounded<true>(red_full, ui & 1);
+            for (int s = 0; s < cs - 1; ++s) {
+              const float4* src = reinterpret_cast<const float4*>(red_s + s * kRows * NTOK + r * NTOK);
+  #pragma unroll
+              for (int c = 0; c < NTOK / 4; ++c) {
+                const float4 t = src[c];
+                v[4 * c] += t.x;
+                v[4 * c + 1] += t.y;
+                v[4 * c + 2] += t.z;
+                v[4 * c + 3] += t.w;
+              }
+            }
+            // tell every other CTA of the cluster that its slot may be reused
+            for (int s = 1; s < cs; ++s) mbar_arrive_remote(mapa_shared(smem_u32(red_free), s));
           }
-          // tell every other CTA of the cluster that its slot may be reused
-          for (int s = 1; s < cs; ++s) mbar_arrive_remote(mapa_shared(smem_u32(red_free), s));
-        }
-        if (ok) {
-#pragma unroll
-          for (int c = 0; c < NTOK; ++c)
-            if (c < ntok) p.y[size_t(c) * p.N + grow] = v[c] * __ldg(p.a_scale + c);
-        }
-      } else {
-        if (ok) {
-#pragma unroll
-          for (int c = 0; c < NTOK; ++c) {
-            if (c < ntok) {
-              const int tok = list_tok[c] & 0xff, slot = list_tok[c] >> 8;
-              p.y[(size_t(tok) * p.topk + slot) * p.N + (grow - e * p.N)] = v[c] * __ldg(p.a_scale + tok);
+          if (ok) {
+  #pragma unroll
+            for (int c = 0; c < NTOK; ++c)
+              if (c < ntok) p.y[size_t(c) * p.N + grow] = v[c] * __ldg(p.a_scale + c);
+          }
+        } else {
+          if (ok) {
+  #pragma unroll
+            for (int c = 0; c < NTOK; ++c) {
+              if (c < ntok) {
+                const int tok = list_tok[c] & 0xff, slot = list_tok[c] >> 8;
+                p.y[(size_t(tok) * p.topk + slot) * p.N + (grow - e * p.N)] = v[c] * __ldg(p.a_scale + tok);
+              }
             }
           }
         }
