@@ -13,14 +13,18 @@
 // Mapping to sm_103a (swap-AB: weight rows are the MMA's M = 128, token rows
 // its N = 16, 32 or 64):
 //  * warp 0 (one lane) streams the tile's code bytes with 2-D TMA boxes of
-//    [128 rows][48 B] (one 128-wide k-tile) into an 8-stage mbarrier ring;
+//    [128 rows][48 B] (one 128-wide k-tile) into an 8-stage mbarrier ring,
+//    starting right after barrier set-up;
 //  * warps 2..9 are two decoder warpgroups taking alternate k-tiles; thread
 //    = weight row = TMEM lane.  A thread reads its row's 48 code bytes (three
 //    128-bit shared loads at a conflict-free 48-byte pitch), spreads the codes
 //    to nibbles and turns them into E4M3 bytes with byte-permutes through the
 //    row's codebook (two registers), then writes the 128 bytes into its TMEM
 //    lane (tcgen05.st, 32 columns) as the MMA's A operand, and its 4 E8M0
-//    group-scale bytes into TMEM as the A scale factors;
+//    group-scale bytes into TMEM as the A scale factors.  The wait for the
+//    TMEM stores of one k-tile is overlapped with decoding the next; scale
+//    bytes are pulled into L1 16 k-tiles ahead and the next tile's codebook
+//    is loaded during the current one;
 //  * warp 1 (one lane) issues 4 tcgen05.mma kind::mxf8f6f4.block_scale
 //    (K = 32 each) per k-tile with A from TMEM and B (the E4M3 activations,
 //    resident in shared memory for the CTA's K range) from a K-major
@@ -102,20 +106,17 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 }
 
 // mbarriers (codes full/empty, A full/empty, 2 accumulators full/empty,
-// 2 codebook slots full/empty, B, split-K full/free), then the TMEM base
-// slot and two ints.
-constexpr int kNumBars = 2 * kCodeStages + 2 * kAStages + 4 + 4 + 3;
+// B, split-K full/free), then the TMEM base slot and two ints.
+constexpr int kNumBars = 2 * kCodeStages + 2 * kAStages + 4 + 3;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area too small");
 
 // Shared-memory carve-up (byte offsets), identical on host and device.
 struct Layout {
-  int codes, scales, cbs, b, red, bars, route, total;
+  int codes, b, red, bars, route, total;
   __host__ __device__ Layout(int b_bytes, int red_bytes, bool grouped) {
     codes = 0;
-    scales = codes + kCodeStages * kCodeStage;     // [stage][128] scale words
-    cbs = scales + kCodeStages * kRows * 4;         // [2][128] codebooks
-    b = cbs + 2 * kRows * 8;
+    b = codes + kCodeStages * kCodeStage;
     red = b + b_bytes;
     bars = red + red_bytes;
     route = bars + kBarBytes;
@@ -146,8 +147,6 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   extern __shared__ __align__(1024) uint8_t smem[];
   const Layout L(p.b_bytes, p.red_bytes, GROUPED);
   uint8_t* codes_s = smem + L.codes;
-  uint32_t* scales_s = reinterpret_cast<uint32_t*>(smem + L.scales);   // [stage][128 rows]
-  uint2* cb_s = reinterpret_cast<uint2*>(smem + L.cbs);                 // [2][128 rows]
   uint8_t* b_s = smem + L.b;
   float* red_s = reinterpret_cast<float*>(smem + L.red);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
@@ -157,9 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   uint64_t* a_empty = a_full + kAStages;
   uint64_t* acc_full = a_empty + kAStages;
   uint64_t* acc_empty = acc_full + 2;
-  uint64_t* cb_full = acc_empty + 2;
-  uint64_t* cb_empty = cb_full + 2;
-  uint64_t* b_full = cb_empty + 2;
+  uint64_t* b_full = acc_empty + 2;
   uint64_t* red_full = b_full + 1;
   uint64_t* red_free = red_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_free + 1);
@@ -180,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
 
   if (tid == 0) {
     for (int i = 0; i < kCodeStages; ++i) {
-      mbar_init(&codes_full[i], 1 + 32);                  // TMA bytes + 32 lanes' cp.async
+      mbar_init(&codes_full[i], 1);
       mbar_init(&codes_empty[i], 4);
     }
     for (int i = 0; i < kAStages; ++i) {
@@ -190,8 +187,6 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);
-      mbar_init(&cb_full[i], 32);
-      mbar_init(&cb_empty[i], kDecWarps);
     }
     mbar_init(b_full, 4);
     mbar_init(red_full, (cs > 1 ? cs - 1 : 1) * 128);
@@ -199,15 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) prefetch_tmap(&p.tmap_codes);
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  if (cs > 1) cluster_sync();                             // peers' barriers exist before any remote arrive
-  const uint32_t tbase = *tmem_slot;
+  // Cluster peers' barriers must exist before any remote arrive; arrive now,
+  // wait right before the first DSMEM access (epilogue) or at the end.
+  if (cs > 1) cluster_arrive();
 
   // ---- which units does this CTA own? ----
   int n_units, u_begin, u_step;
@@ -263,43 +253,31 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     }
   };
 
+  uint32_t tbase = 0;
   if (warp == 0) {
-    // ------------------------------------------------------ producer warp --
-    // Starts at once (the rest of the CTA loads B meanwhile).  Per unit: the
-    // rows' codebooks (cp.async, 8 B a row); per k-tile: the code box (TMA,
-    // lane 0) and the rows' 4 scale bytes (cp.async, 4 rows a lane).
-    uint32_t it = 0;
-    const uint32_t codes_base = smem_u32(codes_s), scales_base = smem_u32(scales_s), cb_base = smem_u32(cb_s);
-    for (int ui = 0; ui < n_units; ++ui) {
-      int row0, row_end, e;
-      unit_rows(ui, row0, row_end, e);
-      const int cbslot = ui & 1;
-      if (lane == 0) wait_bounded(&cb_empty[cbslot], ((ui >> 1) & 1) ^ 1);
-      __syncwarp();
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int row = lane + 32 * i, g = row0 + row;
-        if (g < row_end) cp_async8(cb_base + (cbslot * kRows + row) * 8, p.codebooks + size_t(g) * 8);
-      }
-      cp_async_arrive(&cb_full[cbslot]);
-      for (int kt = kt0; kt < kt1; ++kt, ++it) {
-        const int slot = it % kCodeStages;
-        if (lane == 0) {
+    // ------------------------------------------------------ TMA producer --
+    // Starts streaming code boxes at once; the rest of the CTA sets up TMEM
+    // and the resident activations meanwhile.
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int ui = 0; ui < n_units; ++ui) {
+        int row0, row_end, e;
+        unit_rows(ui, row0, row_end, e);
+        for (int kt = kt0; kt < kt1; ++kt, ++it) {
+          const int slot = it % kCodeStages;
           wait_bounded(&codes_empty[slot], ((it / kCodeStages) & 1u) ^ 1u);
           mbar_arrive_expect_tx(&codes_full[slot], kCodeStage);
           tma_load_2d(codes_s + slot * kCodeStage, &p.tmap_codes, &codes_full[slot], kt * 48, row0);
         }
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = lane + 32 * i, g = row0 + row;
-          if (g < row_end) cp_async4(scales_base + (slot * kRows + row) * 4, p.scales + size_t(g) * gk + kt * 4);
-        }
-        cp_async_arrive(&codes_full[slot]);
       }
     }
-    (void)codes_base;
+    __syncwarp();
+    if (cs > 1) cluster_wait();
   } else {
+    if (warp == 1) {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
     if constexpr (!GROUPED) {
       // resident activations for this CTA's K range, K-major core-matrix
       // layout: chunk c (16 k) at c * NTOK * 16, token group j at j * 128,
@@ -313,6 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       }
       fence_proxy_async_smem();
     }
+    tc_fence_before();
+    named_bar_sync(3, kThreads - 32);                     // everyone but the producer
+    tc_fence_after();
+    tbase = *tmem_slot;
     // scale factors of B: 2^0 in every byte of 8 columns, all 128 lanes
     if (warp >= kEpiWarp0) {
       const uint32_t q = warp & 3;
@@ -321,10 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       tmem_st_wait();
     }
     tc_fence_before();
-    named_bar_sync(3, kThreads - 32);                     // everyone but the producer
+    named_bar_sync(3, kThreads - 32);
     tc_fence_after();
 
     if (warp == 1) {
+      if (cs > 1) cluster_wait();
       // --------------------------------------------------------- MMA issuer --
       if (lane == 0) {
         uint32_t it = 0;
@@ -354,51 +337,100 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
           umma_commit(&acc_full[abuf]);
         }
       }
+      __syncwarp();
     } else if (warp < kEpiWarp0) {
+      if (cs > 1) cluster_wait();
       // ------------------------------------------------------------ decoders --
       const int dw = warp - 2, dg = dw >> 2, q = warp & 3;
       const int r = 32 * q + lane;                      // row inside the tile == TMEM lane
       const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
       const uint32_t codes_base = smem_u32(codes_s);
+      // Load a k-tile's code row from shared memory, release the stage, and
+      // decode it into 32 TMEM columns worth of E4M3 bytes.
+      auto load_decode = [&](uint32_t it, uint2 cb, uint32_t (&v)[32]) {
+        const int cslot = it % kCodeStages;
+        wait_bounded(&codes_full[cslot], (it / kCodeStages) & 1u);
+        const uint32_t crow = codes_base + cslot * kCodeStage + r * 48;
+        const uint4 c0 = lds128(crow), c1 = lds128(crow + 16), c2 = lds128(crow + 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&codes_empty[cslot]);
+        decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
+        decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
+        decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, v + 16);
+        decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, v + 24);
+      };
+      // Issue the TMEM stores of a decoded k-tile (A operand and its scale
+      // factors); the wait for them comes later, after the next decode.
+      auto store = [&](uint32_t it, uint32_t sw, const uint32_t (&v)[32]) {
+        const int aslot = it % kAStages;
+        wait_bounded(&a_empty[aslot], ((it / kAStages) & 1u) ^ 1u);
+        tc_fence_after();
+        tmem_st_x32(tbase + lane_addr + kACol + aslot * 32, v);
+        // A scale of row m is read from TMEM lane m, column (base + m / 32),
+        // byte = the MMA's a_sf_id: quadrant q writes column base + q
+        tmem_st_x1(tbase + lane_addr + kSfaCol + aslot * 4 + q, sw);
+      };
+      auto publish = [&](uint32_t it) {
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[it % kAStages]);
+      };
       uint32_t it_unit = 0;                             // shared k-tile counter at the unit start
+      int row0n, row_endn, en;
+      if (n_units > 0) unit_rows(0, row0n, row_endn, en);
+      uint2 cb_next = (n_units > 0 && row0n + r < row_endn)
+                          ? __ldg(reinterpret_cast<const uint2*>(p.codebooks + size_t(row0n + r) * 8))
+                          : make_uint2(0, 0);
       for (int ui = 0; ui < n_units; ++ui, it_unit += kt1 - kt0) {
         int row0, row_end, e;
         unit_rows(ui, row0, row_end, e);
         const bool ok = row0 + r < row_end;
-        const int cbslot = ui & 1;
-        wait_bounded(&cb_full[cbslot], (ui >> 1) & 1);
-        const uint2 cb = ok ? cb_s[cbslot * kRows + r] : make_uint2(0, 0);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&cb_empty[cbslot]);
-        // this group's k-tiles are kt0 + dg, kt0 + dg + kDecGroups, ...
-        for (int kt = kt0 + dg; kt < kt1; kt += kDecGroups) {
-          const uint32_t it = it_unit + (kt - kt0);
-          const int cslot = it % kCodeStages, aslot = it % kAStages;
-          wait_bounded(&codes_full[cslot], (it / kCodeStages) & 1u);
-          const uint32_t crow = codes_base + cslot * kCodeStage + r * 48;
-          const uint4 c0 = lds128(crow), c1 = lds128(crow + 16), c2 = lds128(crow + 32);
-          const uint32_t sw = ok ? scales_s[cslot * kRows + r] : 0x7F7F7F7Fu;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&codes_empty[cslot]);
-          uint32_t v[32];
-          decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
-          decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
-          decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, v + 16);
-          decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, v + 24);
-          wait_bounded(&a_empty[aslot], ((it / kAStages) & 1u) ^ 1u);
-          tc_fence_after();
-          tmem_st_x32(tbase + lane_addr + kACol + aslot * 32, v);
-          // A scale of row m is read from TMEM lane m, column (base + m / 32),
-          // byte = the MMA's a_sf_id: quadrant q writes column base + q
-          tmem_st_x1(tbase + lane_addr + kSfaCol + aslot * 4 + q, sw);
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[aslot]);
+        const uint2 cb = cb_next;
+        if (ui + 1 < n_units) {                         // next unit's codebook, in flight meanwhile
+          unit_rows(ui + 1, row0n, row_endn, en);
+          cb_next = row0n + r < row_endn
+                        ? __ldg(reinterpret_cast<const uint2*>(p.codebooks + size_t(row0n + r) * 8))
+                        : make_uint2(0, 0);
+        }
+        const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + size_t(ok ? row0 + r : 0) * gk);
+        // warm L1 with this row's scale bytes: 8 k-tiles per 32-byte sector
+        if (ok)
+          for (int kt = kt0; kt < kt1 && kt < kt0 + 16; kt += 8) prefetch_l1(srow + kt);
+        // this group's k-tiles are kt0 + dg, kt0 + dg + G, ...; software
+        // pipelined: decode k-tile n+1 while the TMEM stores of n land
+        uint32_t va[32], vb[32];
+        int kt = kt0 + dg;
+        uint32_t sa = 0, sb = 0;
+        if (kt < kt1) {
+          sa = ok ? __ldg(srow + kt) : 0x7F7F7F7Fu;
+          load_decode(it_unit + (kt - kt0), cb, va);
+        }
+        while (kt < kt1) {
+          int kn = kt + kDecGroups;
+          store(it_unit + (kt - kt0), sa, va);
+          if (kn < kt1) {
+            if (ok && kn + 16 < kt1 && ((kn + 16) & 7) < kDecGroups) prefetch_l1(srow + kn + 16);
+            sb = ok ? __ldg(srow + kn) : 0x7F7F7F7Fu;
+            load_decode(it_unit + (kn - kt0), cb, vb);
+          }
+          publish(it_unit + (kt - kt0));
+          kt = kn;
+          if (kt >= kt1) break;
+          kn = kt + kDecGroups;
+          store(it_unit + (kt - kt0), sb, vb);
+          if (kn < kt1) {
+            if (ok && kn + 16 < kt1 && ((kn + 16) & 7) < kDecGroups) prefetch_l1(srow + kn + 16);
+            sa = ok ? __ldg(srow + kn) : 0x7F7F7F7Fu;
+            load_decode(it_unit + (kn - kt0), cb, va);
+          }
+          publish(it_unit + (kt - kt0));
+          kt = kn;
         }
       }
     } else {
       // ------------------------------------------------------------ epilogue --
+      if (cs > 1) cluster_wait();
       const int q = warp & 3, ew = warp - kEpiWarp0;
       const int r = 32 * q + lane;
       const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
