@@ -378,7 +378,7 @@ def run_e2e(dev, stream, copies, args):
 def _oracle_step(o, pw, acts, scs, rows):
     sel = np.arange(rows)
     for M in MS:
-        o.gemm(acts[M], scs[M], pw.codes[sel], pw.scales[sel], pw.codebooks[sel], M, rows, K_DIM)
+        o.gemm_rows(acts[M], scs[M], pw.codes, pw.scales, pw.codebooks, M, N_DIM, K_DIM, sel)
 
 
 def cpu_baseline(seconds: float):

@@ -4,7 +4,6 @@
 // caller's stream and never synchronises (except cbq_device_status).
 #include <cuda.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 
 #include <atomic>
 #include <cstdint>
@@ -27,9 +26,6 @@ struct DeviceInfo {
 constexpr int kMaxDevices = 64;
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_dev_mutex;
-
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
 
 int current_device_checked(DeviceInfo** out) {
   int dev = 0;
@@ -64,28 +60,6 @@ int device_sm_count() {
 }
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
-
-int make_tmap_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch,
-                 uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
-  std::call_once(g_encode_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  if (!g_encode) return CBQ_ECUDA;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {pitch};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? CBQ_OK : CBQ_ECUDA;
-}
 
 }  // namespace cbq
 
@@ -141,9 +115,7 @@ int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w,
   if (path == CBQ_PATH_GEMV) {
     GemvParams p;
     std::memset(&p, 0, sizeof(p));
-    st = make_tmap_2d(&p.tmap_codes, w->codes, uint64_t(K) * 3 / 8, uint64_t(N),
-                      uint64_t(K) * 3 / 8, 48, 16, false);
-    if (st != CBQ_OK) return st;
+    p.codes = w->codes;
     p.a = a;
     p.a_scale = a_scale;
     p.scales = w->scales;
@@ -156,6 +128,7 @@ int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w,
   }
   UmmaParams p;
   std::memset(&p, 0, sizeof(p));
+  p.codes = w->codes;
   p.a = a;
   p.a_scale = a_scale;
   p.scales = w->scales;
@@ -164,9 +137,6 @@ int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w,
   p.M = M;
   p.N = N;
   p.K = K;
-  st = make_tmap_2d(&p.tmap_codes, w->codes, uint64_t(K) * 3 / 8, uint64_t(N),
-                    uint64_t(K) * 3 / 8, 48, 128, false);
-  if (st != CBQ_OK) return st;
   return launch_umma(p, false, s);
 }
 
@@ -196,12 +166,10 @@ int cbq_grouped_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weig
   if (!a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(experts))
     return CBQ_EINVAL;
   if (path == CBQ_PATH_AUTO) path = (M <= 4) ? CBQ_PATH_GEMV : CBQ_PATH_MMA;
-  const uint64_t rows = uint64_t(E) * N, pitch = uint64_t(K) * 3 / 8;
   if (path == CBQ_PATH_GEMV) {
     GemvParams p;
     std::memset(&p, 0, sizeof(p));
-    st = make_tmap_2d(&p.tmap_codes, experts->codes, pitch, rows, pitch, 48, 16, false);
-    if (st != CBQ_OK) return st;
+    p.codes = experts->codes;
     p.a = a;
     p.a_scale = a_scale;
     p.scales = experts->scales;
@@ -217,8 +185,7 @@ int cbq_grouped_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weig
   }
   UmmaParams p;
   std::memset(&p, 0, sizeof(p));
-  st = make_tmap_2d(&p.tmap_codes, experts->codes, pitch, rows, pitch, 48, 128, false);
-  if (st != CBQ_OK) return st;
+  p.codes = experts->codes;
   p.a = a;
   p.a_scale = a_scale;
   p.scales = experts->scales;

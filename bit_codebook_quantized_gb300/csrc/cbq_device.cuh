@@ -135,6 +135,27 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, ui
       : "memory");
 }
 
+// 1-D bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0),
+// completing `bytes` transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Code stream layout: rows in tiles of 128 (the last tile holds the
+// remaining rows); tile t starts at byte 128 t (3K/8); inside a tile the
+// 48-byte k-tile pieces (4 groups, 128 weights) of all its rows form one
+// block per k-tile: block c at c * rows_t * 48, row i at i * 48.  K % 128 == 0.
+__host__ __device__ __forceinline__ long long tile_base(int t, int K) {
+  return static_cast<long long>(t) * 128 * (3LL * K / 8);
+}
+__host__ __device__ __forceinline__ int tile_rows(int t, int N) {
+  return N - 128 * t < 128 ? N - 128 * t : 128;
+}
+
 // Named barrier over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

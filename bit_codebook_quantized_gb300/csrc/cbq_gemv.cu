@@ -11,9 +11,9 @@
 // Design (GB300):
 //  * work unit = 16 weight rows ("slab") x the whole K; units are handed out
 //    round-robin to a persistent grid;
-//  * one producer warp streams the slab's code bytes with 2-D TMA boxes of
-//    [16 rows][48 B] (48 B = 4 groups = 128 k), 4 boxes per pipeline stage,
-//    into an S-stage mbarrier ring;
+//  * one producer warp streams the slab's code bytes with 1-D bulk copies of
+//    [16 rows][48 B] (48 B = 4 groups = 128 k; contiguous in the tile-ordered
+//    code stream), 4 copies per pipeline stage, into an S-stage mbarrier ring;
 //  * 4 consumer warps take one box each per stage (a 4-way split of K inside
 //    the CTA).  A lane reads its 24-bit quarter of a group with two 32-bit
 //    shared loads (row pitch 48 B: conflict-free), spreads the 8 codes to
@@ -127,7 +127,6 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
     }
     fence_barrier_init();
   }
-  if (warp == kConsumerWarps && lane == 0) prefetch_tmap(&p.tmap_codes);
 
   int n_units;
   if constexpr (GROUPED) {
@@ -171,23 +170,31 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
     if (lane == 0) {
       uint32_t it = 0;
       for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        int row_base;
+        // the slab's rows inside its 128-row tile; each k-tile piece of the
+        // slab is contiguous (rows x 48 B) in the tile-ordered code stream
+        const uint8_t* mat = p.codes;
+        int slab_row0;
         if constexpr (GROUPED) {
-          int e = used_list[u / slabs];
-          row_base = e * p.N + (u % slabs) * kSlabRows;
+          const int e = used_list[u / slabs];
+          mat += static_cast<long long>(e) * (3LL * p.K / 8) * p.N;
+          slab_row0 = (u % slabs) * kSlabRows;
         } else {
-          row_base = u * kSlabRows;
+          slab_row0 = u * kSlabRows;
         }
+        const int t = slab_row0 / 128, i0 = slab_row0 % 128;
+        const int rows_t = tile_rows(t, p.N);
+        const uint32_t piece = static_cast<uint32_t>(min(kSlabRows, rows_t - i0)) * 48;
+        const uint8_t* tile = mat + tile_base(t, p.K) + static_cast<long long>(i0) * 48;
         for (int st = 0; st < nstages_unit; ++st, ++it) {
           const int slot = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
           wait_bounded(&empty_bar[slot], ph ^ 1u);
           const int c0 = st * kConsumerWarps;
           const int nvalid = min(kConsumerWarps, nchunks - c0);
-          mbar_arrive_expect_tx(&full_bar[slot], nvalid * kBoxBytes);
+          mbar_arrive_expect_tx(&full_bar[slot], nvalid * piece);
           for (int c = 0; c < nvalid; ++c)
-            tma_load_2d(stage_buf + slot * kStageBytes + c * kBoxBytes, &p.tmap_codes,
-                        &full_bar[slot], (c0 + c) * 48, row_base);
+            bulk_g2s(stage_buf + slot * kStageBytes + c * kBoxBytes,
+                     tile + static_cast<long long>(c0 + c) * rows_t * 48, piece, &full_bar[slot]);
         }
       }
     }
@@ -351,7 +358,11 @@ __global__ void unpack_kernel(const uint8_t* __restrict__ codes, const uint8_t* 
   for (long long gi = blockIdx.x * (long long)blockDim.x + threadIdx.x; gi < ngroups;
        gi += (long long)gridDim.x * blockDim.x) {
     const long long n = gi / groups_row;
-    const uint32_t* wp = reinterpret_cast<const uint32_t*>(codes + gi * 12);
+    const int g = static_cast<int>(gi % groups_row);
+    const int t = static_cast<int>(n / 128);
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(
+        codes + tile_base(t, K) + static_cast<long long>(g / 4) * tile_rows(t, N) * 48 + (n % 128) * 48 +
+        (g % 4) * 12);
     const uint32_t w0 = wp[0], w1 = wp[1], w2 = wp[2];
     const uint2 cb = *reinterpret_cast<const uint2*>(codebooks + n * 8);
     const float sc = e8m0_to_f32(scales[gi]);

@@ -12,8 +12,8 @@
 namespace cbq {
 
 // Kernel parameters of the small-M kernel (dense and grouped).
-struct alignas(128) GemvParams {
-  CUtensorMap tmap_codes;     // 2-D map over codes [rows][3K/8], box [16 rows][48 B]
+struct GemvParams {
+  const uint8_t* codes;       // code stream (tile order), expert stack for grouped calls
   const uint8_t* a;           // [M][K] E4M3
   const float* a_scale;       // [M]
   const uint8_t* scales;      // [rows][K/32]
@@ -25,8 +25,8 @@ struct alignas(128) GemvParams {
 };
 
 // Kernel parameters of the tcgen05 kernel (dense and grouped).
-struct alignas(128) UmmaParams {
-  CUtensorMap tmap_codes;     // 2-D map over codes [rows][3K/8], box [128 rows][48 B]
+struct UmmaParams {
+  const uint8_t* codes;       // code stream (tile order), expert stack for grouped calls
   const uint8_t* a;
   const float* a_scale;
   const uint8_t* scales;
@@ -38,14 +38,11 @@ struct alignas(128) UmmaParams {
   int ksplit;                 // K-range split factor (cluster size along K)
   int b_bytes;                // shared bytes of the resident activation tile
   int red_bytes;              // shared bytes of the split-K partial tiles (leader CTA)
+  int code_stages;            // depth of the code-stage ring (<= kMaxCodeStages)
 };
 
 int device_sm_count();
 void note_launch();
-
-// Encode a 2-D uint8 tensor map (rows x cols bytes, row pitch `pitch` bytes).
-int make_tmap_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
-                 uint64_t pitch, uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
 int launch_gemv(const GemvParams& p, bool grouped, cudaStream_t stream);
 int launch_unpack(const uint8_t* codes, const uint8_t* scales, const uint8_t* codebooks, int N,

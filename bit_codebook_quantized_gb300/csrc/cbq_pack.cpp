@@ -141,8 +141,11 @@ int pack_host(const float* W, int N, int K, uint8_t* codes, uint8_t* scales,
     double cbv[8];
     for (int i = 0; i < 8; ++i) cbv[i] = e4m3_to_double(cb[i]);
     for (int k = 0; k < K; ++k) idx[k] = static_cast<uint8_t>(nearest(u[k], cbv));
-    uint8_t* cr = codes + static_cast<size_t>(n) * G * 12;
-    for (int g = 0; g < G; ++g) put_group(cr + 12 * g, idx.data() + 32 * g);
+    // tile order: 128-row tile, then k-tile block of the tile's rows x 48 B
+    const int t = n / 128, rows_t = std::min(128, N - 128 * t), i = n % 128;
+    uint8_t* tile = codes + static_cast<size_t>(t) * 128 * (3 * static_cast<size_t>(K) / 8);
+    for (int g = 0; g < G; ++g)
+      put_group(tile + static_cast<size_t>(g / 4) * rows_t * 48 + i * 48 + (g % 4) * 12, idx.data() + 32 * g);
   }
   return CBQ_OK;
 }

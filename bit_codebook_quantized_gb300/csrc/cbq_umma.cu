@@ -55,8 +55,9 @@ static __device__ unsigned g_status_umma = 0;
 namespace {
 
 constexpr int kRows = 128;                    // MMA M (weight rows per tile)
-constexpr int kCodeStage = kRows * 48;        // one k-tile of codes: 6 KB
-constexpr int kCodeStages = 8;
+constexpr int kKtPerStage = 4;                // k-tiles per code stage (one bulk copy)
+constexpr int kCodeStage = kKtPerStage * kRows * 48;   // 24 KB
+constexpr int kMaxCodeStages = 6;
 constexpr int kAStages = 8;                   // decoded k-tiles in TMEM
 constexpr int kDecGroups = 2;
 constexpr int kDecWarps = 4 * kDecGroups;
@@ -107,16 +108,16 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 
 // mbarriers (codes full/empty, A full/empty, 2 accumulators full/empty,
 // B, split-K full/free), then the TMEM base slot and two ints.
-constexpr int kNumBars = 2 * kCodeStages + 2 * kAStages + 4 + 3;
+constexpr int kNumBars = 2 * kMaxCodeStages + 2 * kAStages + 4 + 3;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area too small");
 
 // Shared-memory carve-up (byte offsets), identical on host and device.
 struct Layout {
   int codes, b, red, bars, route, total;
-  __host__ __device__ Layout(int b_bytes, int red_bytes, bool grouped) {
+  __host__ __device__ Layout(int code_stages, int b_bytes, int red_bytes, bool grouped) {
     codes = 0;
-    b = codes + kCodeStages * kCodeStage;
+    b = codes + code_stages * kCodeStage;
     red = b + b_bytes;
     bars = red + red_bytes;
     route = bars + kBarBytes;
@@ -145,14 +146,15 @@ __device__ __forceinline__ void decode_group(uint32_t w0, uint32_t w1, uint32_t 
 template <int NTOK, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant__ UmmaParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  const Layout L(p.b_bytes, p.red_bytes, GROUPED);
+  const Layout L(p.code_stages, p.b_bytes, p.red_bytes, GROUPED);
+  const int NS = p.code_stages;
   uint8_t* codes_s = smem + L.codes;
   uint8_t* b_s = smem + L.b;
   float* red_s = reinterpret_cast<float*>(smem + L.red);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* codes_full = bars;
-  uint64_t* codes_empty = codes_full + kCodeStages;
-  uint64_t* a_full = codes_empty + kCodeStages;
+  uint64_t* codes_empty = codes_full + kMaxCodeStages;
+  uint64_t* a_full = codes_empty + kMaxCodeStages;
   uint64_t* a_empty = a_full + kAStages;
   uint64_t* acc_full = a_empty + kAStages;
   uint64_t* acc_empty = acc_full + 2;
@@ -174,11 +176,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   const int kt0 = rank * nkt / cs, kt1 = (rank + 1) * nkt / cs;
   const int tiles = (p.N + kRows - 1) / kRows;
   const int gk = p.K / 32;                                // scale bytes per row
+  const int n_stages_u = (kt1 - kt0 + kKtPerStage - 1) / kKtPerStage;   // code stages per unit
 
   if (tid == 0) {
-    for (int i = 0; i < kCodeStages; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(&codes_full[i], 1);
-      mbar_init(&codes_empty[i], 4);
+      mbar_init(&codes_empty[i], kDecWarps);            // every decoder warp, once per stage
     }
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(&a_full[i], 4);
@@ -193,7 +196,6 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     mbar_init(red_free, 128);
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) prefetch_tmap(&p.tmap_codes);
   __syncthreads();
   // Cluster peers' barriers must exist before any remote arrive; arrive now,
   // wait right before the first DSMEM access (epilogue) or at the end.
@@ -240,6 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     u_step = n_clusters;
   }
 
+  // rows of a unit (global row index for scales / codebooks) and where its
+  // 128-row tile starts in the tile-ordered code stream
   auto unit_rows = [&](int ui, int& row0, int& row_end, int& e) {
     const int u = u_begin + ui * u_step;
     if constexpr (GROUPED) {
@@ -252,22 +256,37 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       row_end = p.N;
     }
   };
+  auto unit_tile = [&](int ui, int& rows_t) -> const uint8_t* {
+    const int u = u_begin + ui * u_step;
+    int t = u;
+    const uint8_t* mat = p.codes;
+    if constexpr (GROUPED) {
+      t = u % tiles;
+      mat += static_cast<long long>(used_list[u / tiles]) * (3LL * p.K / 8) * p.N;
+    }
+    rows_t = tile_rows(t, p.N);
+    return mat + tile_base(t, p.K);
+  };
 
   uint32_t tbase = 0;
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
-    // Starts streaming code boxes at once; the rest of the CTA sets up TMEM
-    // and the resident activations meanwhile.
+    // Starts streaming at once; the rest of the CTA sets up TMEM and the
+    // resident activations meanwhile.  One bulk copy per stage: up to 4
+    // consecutive k-tiles of the tile, contiguous in the code stream.
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t sg = 0;
       for (int ui = 0; ui < n_units; ++ui) {
-        int row0, row_end, e;
-        unit_rows(ui, row0, row_end, e);
-        for (int kt = kt0; kt < kt1; ++kt, ++it) {
-          const int slot = it % kCodeStages;
-          wait_bounded(&codes_empty[slot], ((it / kCodeStages) & 1u) ^ 1u);
-          mbar_arrive_expect_tx(&codes_full[slot], kCodeStage);
-          tma_load_2d(codes_s + slot * kCodeStage, &p.tmap_codes, &codes_full[slot], kt * 48, row0);
+        int rows_t;
+        const uint8_t* tile = unit_tile(ui, rows_t);
+        for (int st = 0; st < n_stages_u; ++st, ++sg) {
+          const int slot = sg % NS;
+          const int kb = kt0 + st * kKtPerStage, nk = min(kKtPerStage, kt1 - kb);
+          const uint32_t bytes = static_cast<uint32_t>(nk * rows_t * 48);
+          wait_bounded(&codes_empty[slot], ((sg / NS) & 1u) ^ 1u);
+          mbar_arrive_expect_tx(&codes_full[slot], bytes);
+          bulk_g2s(codes_s + slot * kCodeStage, tile + static_cast<long long>(kb) * rows_t * 48, bytes,
+                   &codes_full[slot]);
         }
       }
     }
@@ -345,15 +364,26 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       const int r = 32 * q + lane;                      // row inside the tile == TMEM lane
       const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
       const uint32_t codes_base = smem_u32(codes_s);
-      // Load a k-tile's code row from shared memory, release the stage, and
-      // decode it into 32 TMEM columns worth of E4M3 bytes.
-      auto load_decode = [&](uint32_t it, uint2 cb, uint32_t (&v)[32]) {
-        const int cslot = it % kCodeStages;
-        wait_bounded(&codes_full[cslot], (it / kCodeStages) & 1u);
-        const uint32_t crow = codes_base + cslot * kCodeStage + r * 48;
+      // Stage bookkeeping: a unit's k-tiles come in stages of kKtPerStage;
+      // each decoder warp releases every stage of the unit exactly once,
+      // after its last read from it.
+      uint32_t sg_unit = 0;                             // global index of the unit's first stage
+      int released = 0, rows_t = kRows;
+      auto release_until = [&](int s_end) {
+        for (; released < s_end; ++released) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&codes_empty[(sg_unit + released) % NS]);
+        }
+      };
+      // Load a k-tile's code row from shared memory and decode it into 32
+      // TMEM columns worth of E4M3 bytes.
+      auto load_decode = [&](int kt, uint2 cb, uint32_t (&v)[32]) {
+        const int s = (kt - kt0) / kKtPerStage, j = (kt - kt0) % kKtPerStage;
+        release_until(s);
+        const uint32_t sgi = sg_unit + s;
+        wait_bounded(&codes_full[sgi % NS], (sgi / NS) & 1u);
+        const uint32_t crow = codes_base + (sgi % NS) * kCodeStage + (j * rows_t + r) * 48;
         const uint4 c0 = lds128(crow), c1 = lds128(crow + 16), c2 = lds128(crow + 32);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&codes_empty[cslot]);
         decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
         decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
         decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, v + 16);
@@ -385,6 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       for (int ui = 0; ui < n_units; ++ui, it_unit += kt1 - kt0) {
         int row0, row_end, e;
         unit_rows(ui, row0, row_end, e);
+        unit_tile(ui, rows_t);
+        sg_unit = static_cast<uint32_t>(ui) * n_stages_u;
+        released = 0;
         const bool ok = row0 + r < row_end;
         const uint2 cb = cb_next;
         if (ui + 1 < n_units) {                         // next unit's codebook, in flight meanwhile
@@ -404,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
         uint32_t sa = 0, sb = 0;
         if (kt < kt1) {
           sa = ok ? __ldg(srow + kt) : 0x7F7F7F7Fu;
-          load_decode(it_unit + (kt - kt0), cb, va);
+          load_decode(kt, cb, va);
         }
         while (kt < kt1) {
           int kn = kt + kDecGroups;
@@ -412,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
           if (kn < kt1) {
             if (ok && kn + 16 < kt1 && ((kn + 16) & 7) < kDecGroups) prefetch_l1(srow + kn + 16);
             sb = ok ? __ldg(srow + kn) : 0x7F7F7F7Fu;
-            load_decode(it_unit + (kn - kt0), cb, vb);
+            load_decode(kn, cb, vb);
           }
           publish(it_unit + (kt - kt0));
           kt = kn;
@@ -422,11 +455,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
           if (kn < kt1) {
             if (ok && kn + 16 < kt1 && ((kn + 16) & 7) < kDecGroups) prefetch_l1(srow + kn + 16);
             sa = ok ? __ldg(srow + kn) : 0x7F7F7F7Fu;
-            load_decode(it_unit + (kn - kt0), cb, va);
+            load_decode(kn, cb, va);
           }
           publish(it_unit + (kt - kt0));
           kt = kn;
         }
+        release_until(n_stages_u);
       }
     } else {
       // ------------------------------------------------------------ epilogue --
@@ -628,6 +662,13 @@ int dispatch(const UmmaParams& p, int ntok, int grid, int cs, int smem, cudaStre
   return launch_t<64, GROUPED>(p, grid, cs, smem, s);
 }
 
+// Deepest code-stage ring that fits next to the other shared-memory areas.
+int code_stages_for(int b_bytes, int red_bytes, bool grouped) {
+  for (int st = kMaxCodeStages; st >= 2; --st)
+    if (Layout(st, b_bytes, red_bytes, grouped).total <= kMaxSmem) return st;
+  return 0;
+}
+
 // Token columns of the MMA (its N): 16, 32 or 64.
 int ntok_for(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
@@ -643,8 +684,9 @@ int launch_umma(const UmmaParams& p_in, bool grouped, cudaStream_t stream) {
     p.ksplit = 1;
     p.b_bytes = ntok * p.K;
     p.red_bytes = 0;
-    const Layout L(p.b_bytes, 0, true);
-    if (L.total > kMaxSmem) return CBQ_EINVAL;   // K too long for a resident B tile
+    p.code_stages = code_stages_for(p.b_bytes, 0, true);
+    if (p.code_stages < 2) return CBQ_EINVAL;    // K too long for a resident B tile
+    const Layout L(p.code_stages, p.b_bytes, 0, true);
     const int units = std::min(p.E, p.M * p.topk) * tiles;
     const int grid = std::max(1, std::min(units, sms));
     return dispatch<true>(p, ntok, grid, 1, std::max(L.total, kMinSmem), stream);
@@ -655,8 +697,10 @@ int launch_umma(const UmmaParams& p_in, bool grouped, cudaStream_t stream) {
   long long best_cost = 0;
   for (int cs = 1; cs <= 8 && cs <= nkt; ++cs) {
     const int per = (nkt + cs - 1) / cs;
-    const Layout L(ntok * per * 128, cs > 1 ? (cs - 1) * kRows * ntok * 4 : 0, false);
-    if (L.total > kMaxSmem) continue;
+    const int b_bytes = ntok * per * 128, red_bytes = cs > 1 ? (cs - 1) * kRows * ntok * 4 : 0;
+    const int stages = code_stages_for(b_bytes, red_bytes, false);
+    if (stages < 2) continue;
+    const Layout L(stages, b_bytes, red_bytes, false);
     const int smem = std::max(L.total, kMinSmem);
     const int clusters = cs == 1 ? sms : max_clusters(ntok, cs, smem);
     if (clusters <= 0) continue;
@@ -673,7 +717,8 @@ int launch_umma(const UmmaParams& p_in, bool grouped, cudaStream_t stream) {
   p.ksplit = cs;
   p.b_bytes = ntok * ((nkt + cs - 1) / cs) * 128;
   p.red_bytes = cs > 1 ? (cs - 1) * kRows * ntok * 4 : 0;
-  const Layout L(p.b_bytes, p.red_bytes, false);
+  p.code_stages = code_stages_for(p.b_bytes, p.red_bytes, false);
+  const Layout L(p.code_stages, p.b_bytes, p.red_bytes, false);
   const int grid = std::min(tiles, best_clusters) * cs;
   return dispatch<false>(p, ntok, grid, cs, std::max(L.total, kMinSmem), stream);
 }

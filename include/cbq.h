@@ -10,9 +10,14 @@
  * experts its tokens route to.
  *
  * Packed format (fixed by this library; the pages leave it open):
- *   codes     uint8 [rows][3K/8]  row-major over K; group g = k/32 of row n is
- *             the 12 bytes at offset (n*K/32 + g)*12, read as a 96-bit
- *             little-endian number with code j = k%32 at bits 3j..3j+2.
+ *   codes     uint8 [3KN/8]  one group (row n, g = k/32) is 12 bytes, a
+ *             96-bit little-endian number with code j = k%32 at bits
+ *             3j..3j+2.  Groups are ordered in tiles of 128 rows (the last
+ *             tile holds the remaining R rows): tile t starts at byte
+ *             128*t*(3K/8); inside it, k-tile c (four groups, k in
+ *             [128c, 128c+128)) is a block of R rows x 48 bytes at c*R*48,
+ *             row n%128 at (n%128)*48, group g%4 at (g%4)*12.  A tile's
+ *             consecutive k-tiles are therefore contiguous bytes.
  *   scales    uint8 [rows][K/32]  E8M0: value 2^(s-127); 255 (NaN) not allowed.
  *   codebooks uint8 [rows][8]     OCP FP8 E4M3 ("fn"), one codebook per row.
  *   w[n,k] = E4M3(codebooks[n][code(n,k)]) * 2^(scales[n][k/32] - 127)
@@ -56,7 +61,7 @@ extern "C" {
 
 /* One packed matrix in device memory (all three arrays 16-byte aligned). */
 typedef struct cbq_weight {
-    const uint8_t *codes;      /* [rows][3K/8]  */
+    const uint8_t *codes;      /* [3K*rows/8], tile order */
     const uint8_t *scales;     /* [rows][K/32]  */
     const uint8_t *codebooks;  /* [rows][8]     */
 } cbq_weight_t;
@@ -108,8 +113,9 @@ int cbq_gemm_path(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
                   int32_t path);
 
 /* Mixture-of-experts verify round ("Adaptive speculation / Expert sharing"):
- * the E experts are stacked in one packed matrix (expert e owns rows
- * e*N .. e*N+N-1 of `experts`), topk_idx is DEVICE int32 [M][topk] and
+ * the E experts' packed matrices are stacked (expert e: codes from byte
+ * e*3KN/8, scales and codebooks from row e*N), topk_idx is DEVICE int32
+ * [M][topk] and
  *   y[t][j][:] = a_scale[t] * a[t] x W_{topk_idx[t][j]}^T   (fp32 [M][topk][N]),
  * with no gate weight and no combine.  Only experts that appear in topk_idx
  * are read from memory.  Picks the kernel by M as cbq_gemm does.  The routing is read on the device inside the one

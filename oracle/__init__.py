@@ -65,10 +65,15 @@ def configure(lib):
         lib.orc_e8m0_value.restype = ctypes.c_double
         lib.orc_e4m3_round.argtypes = [ctypes.c_double]
         lib.orc_e4m3_round.restype = ctypes.c_uint8
-        lib.orc_code.argtypes = [u8p, i64, i64, i64]
+        lib.orc_group_offset.argtypes = [i64, i64, i64, i64]
+        lib.orc_group_offset.restype = i64
+        lib.orc_code.argtypes = [u8p, i64, i64, i64, i64]
         lib.orc_code.restype = ctypes.c_int
-        lib.orc_set_code.argtypes = [u8p, i64, i64, i64, ctypes.c_int]
+        lib.orc_set_code.argtypes = [u8p, i64, i64, i64, i64, ctypes.c_int]
         lib.orc_set_code.restype = None
+        lib.orc_gemm_rows.argtypes = [u8p, f32p, u8p, u8p, u8p, i64, i64, i64, i64p, i64, f32p,
+                                      f64p]
+        lib.orc_gemm_rows.restype = None
         lib.orc_group_scale.argtypes = [f32p]
         lib.orc_group_scale.restype = ctypes.c_uint8
         lib.orc_unpack.argtypes = [u8p, u8p, u8p, i64, i64, f32p]
@@ -117,13 +122,21 @@ def e4m3_table() -> np.ndarray:
 
 # ---- bitstream ---------------------------------------------------------------
 
-def code_at(codes: np.ndarray, K: int, n: int, k: int) -> int:
+def group_offset(N: int, K: int, n: int, g: int) -> int:
+    """Byte offset of group (n, g) in the code stream (128-row tiles,
+    k-tile-major inside a tile; see cbq_oracle.c)."""
+    return int(_load().orc_group_offset(N, K, n, g))
+
+
+def code_at(codes: np.ndarray, N: int, K: int, n: int, k: int) -> int:
     codes = _u8(codes)
-    return int(_load().orc_code(_p(codes, ctypes.c_uint8), K, n, k))
+    return int(_load().orc_code(_p(codes, ctypes.c_uint8), N, K, n, k))
 
 
 def codes_from_indices(idx: np.ndarray) -> np.ndarray:
-    """Pack an [N, K] array of codes 0..7 into the 96-bit-per-group stream."""
+    """Pack an [N, K] array of codes 0..7 into the code stream (3KN/8 bytes,
+    returned with shape [N, 3K/8] for convenience; the bytes are in tile
+    order, not row order)."""
     idx = np.ascontiguousarray(idx, dtype=np.int64)
     N, K = idx.shape
     out = np.zeros(N * (K // 32) * 12, dtype=np.uint8)
@@ -131,7 +144,7 @@ def codes_from_indices(idx: np.ndarray) -> np.ndarray:
     p = _p(out, ctypes.c_uint8)
     for n in range(N):
         for k in range(K):
-            lib.orc_set_code(p, K, n, k, int(idx[n, k]))
+            lib.orc_set_code(p, N, K, n, k, int(idx[n, k]))
     return out.reshape(N, K // 32 * 12)
 
 
@@ -142,7 +155,7 @@ def indices_from_codes(codes: np.ndarray, N: int, K: int) -> np.ndarray:
     out = np.empty((N, K), dtype=np.int64)
     for n in range(N):
         for k in range(K):
-            out[n, k] = lib.orc_code(p, K, n, k)
+            out[n, k] = lib.orc_code(p, N, K, n, k)
     return out
 
 
@@ -167,6 +180,28 @@ def gemm(a, a_scale, codes, scales, codebooks, M: int, N: int, K: int):
                      _p(codebooks, ctypes.c_uint8), M, N, K,
                      _p(y, ctypes.c_float), _p(bound, ctypes.c_double))
     return y, bound
+
+
+def gemm_rows(a, a_scale, codes, scales, codebooks, M: int, N: int, K: int, rows):
+    """y and bound [M, len(rows)] for the listed output rows of the N-row matrix."""
+    a, codes, scales, codebooks = _u8(a), _u8(codes), _u8(scales), _u8(codebooks)
+    a_scale = np.ascontiguousarray(a_scale, dtype=np.float32)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    y = np.empty((M, len(rows)), dtype=np.float32)
+    bound = np.empty((M, len(rows)), dtype=np.float64)
+    _load().orc_gemm_rows(_p(a, ctypes.c_uint8), _p(a_scale, ctypes.c_float),
+                          _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8),
+                          _p(codebooks, ctypes.c_uint8), M, N, K, _p(rows, ctypes.c_int64),
+                          len(rows), _p(y, ctypes.c_float), _p(bound, ctypes.c_double))
+    return y, bound
+
+
+def expert(codes, scales, codebooks, e: int, N: int, K: int):
+    """(codes, scales, codebooks) of expert e in a stack of packed experts."""
+    cb = 3 * K * N // 8
+    flat = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1)
+    return (flat[e * cb:(e + 1) * cb], np.ascontiguousarray(scales)[e * N:(e + 1) * N],
+            np.ascontiguousarray(codebooks)[e * N:(e + 1) * N])
 
 
 def grouped_gemm(a, a_scale, codes, scales, codebooks, E: int, topk_idx,

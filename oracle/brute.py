@@ -8,7 +8,8 @@ all: the C oracle is pinned against it on shapes from 1x32x1 to 4x64x8.
 Format (from "Hibana: Fast Agentic Inference on Unified-Memory Devices",
 section "Model surgery / Three-bit weights": 8-entry FP8 codebook, 3-bit
 codes, one 8-bit scale per 32 weights): the 12 bytes of a group form one
-little-endian 96-bit integer and code j is ``(G >> 3j) & 7``.
+little-endian 96-bit integer and code j is ``(G >> 3j) & 7``; groups sit in
+128-row tiles, k-tile-major inside a tile (``group_offset``).
 """
 from __future__ import annotations
 
@@ -34,21 +35,36 @@ def e8m0(s: int) -> Fraction:
     return Fraction(2) ** (s - 127)
 
 
-def group_int(codes_row: bytes, g: int) -> int:
-    return int.from_bytes(bytes(codes_row[12 * g: 12 * g + 12]), "little")
+def group_offset(N: int, K: int, n: int, g: int) -> int:
+    """Byte offset of group (n, g): 128-row tiles (the last one holding the
+    remaining R rows) starting at 128t * 3K/8; inside a tile, k-tile
+    c = g // 4 is a block of R rows x W bytes, W = 12 x (its groups, 4 but
+    in a last partial k-tile)."""
+    t, i = divmod(n, 128)
+    R = min(128, N - 128 * t)
+    c = g // 4
+    W = 12 * min(4, K // 32 - 4 * c)
+    return 128 * t * (3 * K // 8) + c * R * 48 + i * W + (g % 4) * 12
 
 
-def code(codes_row: bytes, k: int) -> int:
-    return (group_int(codes_row, k // 32) >> (3 * (k % 32))) & 7
+def group_int(codes, N: int, K: int, n: int, g: int) -> int:
+    flat = bytes(bytearray(codes.reshape(-1) if hasattr(codes, "reshape") else codes))
+    o = group_offset(N, K, n, g)
+    return int.from_bytes(flat[o:o + 12], "little")
 
 
-def weight(codes_row, scales_row, cb_row, k: int) -> Fraction:
-    return e4m3(int(cb_row[code(codes_row, k)])) * e8m0(int(scales_row[k // 32]))
+def code(codes, N: int, K: int, n: int, k: int) -> int:
+    return (group_int(codes, N, K, n, k // 32) >> (3 * (k % 32))) & 7
+
+
+def weight(codes, scales, codebooks, N: int, K: int, n: int, k: int) -> Fraction:
+    return e4m3(int(codebooks[n][code(codes, N, K, n, k)])) * e8m0(int(scales[n][k // 32]))
 
 
 def gemm_exact(a, a_scale, codes, scales, codebooks, M: int, N: int, K: int):
     """Exact y[m][n] as Fractions.  ``a`` is [M][K] E4M3 bytes, ``a_scale``
-    a list of floats (taken exactly), the packed arrays are per-row byte rows."""
+    a list of floats (taken exactly), ``codes`` the packed stream."""
+    flat = bytes(bytearray(codes.reshape(-1) if hasattr(codes, "reshape") else codes))
     out = []
     for m in range(M):
         row = []
@@ -56,7 +72,10 @@ def gemm_exact(a, a_scale, codes, scales, codebooks, M: int, N: int, K: int):
         for n in range(N):
             acc = Fraction(0)
             for k in range(K):
-                acc += e4m3(int(a[m][k])) * weight(codes[n], scales[n], codebooks[n], k)
+                o = group_offset(N, K, n, k // 32)
+                c = (int.from_bytes(flat[o:o + 12], "little") >> (3 * (k % 32))) & 7
+                w = e4m3(int(codebooks[n][c])) * e8m0(int(scales[n][k // 32]))
+                acc += e4m3(int(a[m][k])) * w
             row.append(s * acc)
         out.append(row)
     return out

@@ -11,9 +11,14 @@
  * weights is a 3-bit index into an 8-entry FP8 codebook, plus one 8-bit scale
  * per group, i.e. 3 + 8/32 = 3.25 bits per weight.  The storage format fixed
  * for this library (the pages leave it open):
- *   codes     : row-major over K; group (n, g = k/32) is 12 bytes at byte
- *               offset (n*K/32 + g)*12, read as a 96-bit little-endian number
- *               with code j = k%32 at bits 3j..3j+2.
+ *   codes     : one group (n, g = k/32) is 12 bytes, read as a 96-bit
+ *               little-endian number with code j = k%32 at bits 3j..3j+2.
+ *               Groups are ordered in 128-row tiles: tile t = n/128 holds
+ *               rows 128t .. 128t+R-1 (R = min(128, N-128t)) and starts at
+ *               byte 128t * 3K/8; inside it, k-tile c = k/128 (four groups,
+ *               fewer in a last partial k-tile) is a block of R rows x W
+ *               bytes (W = 12 x its groups) at c*R*48, row n%128 at
+ *               (n%128)*W, group g%4 at (g%4)*12.  Total 3KN/8 bytes.
  *   scales    : uint8 [N][K/32], E8M0, value 2^(s-127).
  *   codebooks : uint8 [N][8], OCP FP8 E4M3 ("fn") per output row.
  *   a         : uint8 E4M3 [M][K], a_scale fp32 [M]; y fp32 [M][N].
@@ -100,11 +105,23 @@ uint8_t orc_e4m3_round(double x)
 
 /* ---- bitstream --------------------------------------------------------- */
 
+/* Byte offset of group (n, g) in the code stream (layout in the header). */
+int64_t orc_group_offset(int64_t N, int64_t K, int64_t n, int64_t g)
+{
+    int64_t t = n / 128;                          /* row tile */
+    int64_t R = (N - 128 * t < 128) ? N - 128 * t : 128;  /* rows in it */
+    int64_t tile_base = 128 * t * (3 * K / 8);
+    int64_t c = g / 4;                            /* k-tile of 128 weights */
+    int64_t G = K / 32;                           /* groups per row */
+    int64_t W = (G - 4 * c < 4) ? 12 * (G - 4 * c) : 48;  /* block row bytes */
+    return tile_base + c * R * 48 + (n % 128) * W + (g % 4) * 12;
+}
+
 /* Code of weight (n, k): bits 3j..3j+2 of the 96-bit little-endian group,
  * read one bit at a time. */
-int orc_code(const uint8_t *codes, int64_t K, int64_t n, int64_t k)
+int orc_code(const uint8_t *codes, int64_t N, int64_t K, int64_t n, int64_t k)
 {
-    int64_t base = (n * (K / 32) + k / 32) * 12;
+    int64_t base = orc_group_offset(N, K, n, k / 32);
     int j = (int)(k % 32);
     int code = 0;
     for (int i = 0; i < 3; i++) {
@@ -117,9 +134,9 @@ int orc_code(const uint8_t *codes, int64_t K, int64_t n, int64_t k)
 
 /* Write code c for weight (n, k) one bit at a time (codes must start zeroed
  * or hold the old value; bits are overwritten). */
-void orc_set_code(uint8_t *codes, int64_t K, int64_t n, int64_t k, int c)
+void orc_set_code(uint8_t *codes, int64_t N, int64_t K, int64_t n, int64_t k, int c)
 {
-    int64_t base = (n * (K / 32) + k / 32) * 12;
+    int64_t base = orc_group_offset(N, K, n, k / 32);
     int j = (int)(k % 32);
     for (int i = 0; i < 3; i++) {
         int pos = 3 * j + i;
@@ -133,9 +150,9 @@ void orc_set_code(uint8_t *codes, int64_t K, int64_t n, int64_t k, int c)
 
 /* Dequantised weight w[n,k] = E4M3(cb[n][code]) * 2^(s[n,g]-127), exact. */
 double orc_weight(const uint8_t *codes, const uint8_t *scales,
-                  const uint8_t *codebooks, int64_t K, int64_t n, int64_t k)
+                  const uint8_t *codebooks, int64_t N, int64_t K, int64_t n, int64_t k)
 {
-    int c = orc_code(codes, K, n, k);
+    int c = orc_code(codes, N, K, n, k);
     return orc_e4m3_value(codebooks[n * 8 + c]) *
            orc_e8m0_value(scales[n * (K / 32) + k / 32]);
 }
@@ -147,7 +164,7 @@ void orc_unpack(const uint8_t *codes, const uint8_t *scales,
 {
     for (int64_t n = 0; n < N; n++)
         for (int64_t k = 0; k < K; k++)
-            W[n * K + k] = (float)orc_weight(codes, scales, codebooks, K, n, k);
+            W[n * K + k] = (float)orc_weight(codes, scales, codebooks, N, K, n, k);
 }
 
 /* y[m,n] and the error-bound base B[m,n] = |a_scale[m]| * sum_k |a*w|.
@@ -164,13 +181,38 @@ void orc_gemm(const uint8_t *a, const float *a_scale,
             double acc = 0.0, accabs = 0.0;
             for (int64_t k = 0; k < K; k++) {
                 double p = orc_e4m3_value(a[m * K + k]) *
-                           orc_weight(codes, scales, codebooks, K, n, k);
+                           orc_weight(codes, scales, codebooks, N, K, n, k);
                 acc += p;
                 accabs += fabs(p);
             }
             y[m * N + n] = (float)((double)a_scale[m] * acc);
             if (bound)
                 bound[m * N + n] = fabs((double)a_scale[m]) * accabs;
+        }
+    }
+}
+
+/* y for a subset of output rows: y[m][i] for row rows[i] of the N-row
+ * matrix (same arithmetic as orc_gemm, row by row). */
+void orc_gemm_rows(const uint8_t *a, const float *a_scale,
+                   const uint8_t *codes, const uint8_t *scales,
+                   const uint8_t *codebooks, int64_t M, int64_t N, int64_t K,
+                   const int64_t *rows, int64_t nrows, float *y, double *bound)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < nrows; i++) {
+        int64_t n = rows[i];
+        for (int64_t m = 0; m < M; m++) {
+            double acc = 0.0, accabs = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                double p = orc_e4m3_value(a[m * K + k]) *
+                           orc_weight(codes, scales, codebooks, N, K, n, k);
+                acc += p;
+                accabs += fabs(p);
+            }
+            y[m * nrows + i] = (float)((double)a_scale[m] * acc);
+            if (bound)
+                bound[m * nrows + i] = fabs((double)a_scale[m]) * accabs;
         }
     }
 }
@@ -191,7 +233,7 @@ void orc_grouped_gemm(const uint8_t *a, const float *a_scale,
     for (int64_t t = 0; t < M; t++) {
         for (int64_t j = 0; j < topk; j++) {
             int64_t e = topk_idx[t * topk + j];
-            const uint8_t *ce = codes + e * N * gk * 12;
+            const uint8_t *ce = codes + e * (3 * K * N / 8);
             const uint8_t *se = scales + e * N * gk;
             const uint8_t *be = codebooks + e * N * 8;
             touched[e] = 1;
@@ -317,7 +359,7 @@ void orc_pack(const float *W, int64_t N, int64_t K,
                 if (fabs(u[k] - orc_e4m3_value(cb[c])) <
                     fabs(u[k] - orc_e4m3_value(cb[best])))
                     best = c;
-            orc_set_code(codes, K, n, k, best);
+            orc_set_code(codes, N, K, n, k, best);
         }
     }
     free(u);

@@ -173,9 +173,8 @@ def test_grouped_full_size_sampled(path):
     for t in range(0, M, 7):
         for j in range(wl.topk):
             e = int(idx[t, j])
-            sel = e * N + rows
-            yr, b = oracle.gemm(a[t:t + 1], s[t:t + 1], pw.codes[sel], pw.scales[sel],
-                                pw.codebooks[sel], 1, len(rows), K)
+            ce, se, be = oracle.expert(pw.codes, pw.scales, pw.codebooks, e, N, K)
+            yr, b = oracle.gemm_rows(a[t:t + 1], s[t:t + 1], ce, se, be, 1, N, K, rows)
             assert_close(y[t, j, rows][None], yr, b, f"token {t} slot {j}")
     assert ops.device_status() == ops.OK
 

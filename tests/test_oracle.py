@@ -23,10 +23,11 @@ def _lib_weights(pw):
     N, K = pw.N, pw.K
     W = np.empty((N, K), dtype=np.float64)
     cbv = _torch_e4m3(pw.codebooks)
+    flat = bytes(pw.codes.reshape(-1))
     for n in range(N):
-        row = bytes(pw.codes[n])
         for g in range(K // 32):
-            G = int.from_bytes(row[12 * g:12 * g + 12], "little")
+            o = brute.group_offset(N, K, n, g)
+            G = int.from_bytes(flat[o:o + 12], "little")
             sc = math.ldexp(1.0, int(pw.scales[n, g]) - 127)
             for j in range(32):
                 W[n, 32 * g + j] = cbv[n, (G >> (3 * j)) & 7] * sc
@@ -114,22 +115,38 @@ def test_bit_layout_golden(golden_dir):
         got = oracle.codes_from_indices(idx)
         assert bytes(got.ravel()) == want, name
         for k in range(32):
-            assert oracle.code_at(np.frombuffer(want, dtype=np.uint8), 32, 0, k) == idx[0, k]
+            assert oracle.code_at(np.frombuffer(want, dtype=np.uint8), 1, 32, 0, k) == idx[0, k]
         n += 1
     assert n == 6
 
 
 def test_bitstream_roundtrip_vs_bigint():
     rng = synth.rng_for(11)
-    N, K = 5, 128
-    idx = rng.integers(0, 8, size=(N, K))
-    packed = oracle.codes_from_indices(idx)
-    assert packed.shape == (N, 3 * K // 8)
-    for n in range(N):
-        for g in range(K // 32):
-            G = sum(int(idx[n, 32 * g + j]) << (3 * j) for j in range(32))
-            assert bytes(packed[n, 12 * g:12 * g + 12]) == G.to_bytes(12, "little")
-    assert np.array_equal(oracle.indices_from_codes(packed, N, K), idx)
+    for N, K in [(5, 128), (130, 256)]:
+        idx = rng.integers(0, 8, size=(N, K))
+        packed = oracle.codes_from_indices(idx).reshape(-1)
+        assert packed.size == 3 * K * N // 8
+        seen = set()
+        for n in range(N):
+            for g in range(K // 32):
+                G = sum(int(idx[n, 32 * g + j]) << (3 * j) for j in range(32))
+                o = brute.group_offset(N, K, n, g)
+                assert bytes(packed[o:o + 12]) == G.to_bytes(12, "little")
+                seen.add(o)
+        assert len(seen) == N * K // 32            # every group has its own 12 bytes
+        assert np.array_equal(oracle.indices_from_codes(packed, N, K), idx)
+
+
+def test_tile_layout_golden(golden_dir):
+    n = 0
+    for line in open(os.path.join(golden_dir, "tile_layout.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        N, K, row, g, off = map(int, line.split()[:5])
+        assert oracle.group_offset(N, K, row, g) == off, line
+        assert brute.group_offset(N, K, row, g) == off, line
+        n += 1
+    assert n == 12
 
 
 # ---- footprint -----------------------------------------------------------------
@@ -181,8 +198,8 @@ def test_gemm_vs_exact_rationals(M, N, K):
             # one fp32 rounding (the oracle rounds a_scale*sum in double first)
             assert abs(float(y[m, n]) - float(ref32)) <= float(np.spacing(np.abs(ref32))), (m, n)
             absum = abs(float(a_scale[m])) * sum(
-                abs(float(brute.e4m3(int(a[m][k])) * brute.weight(pw.codes[n], pw.scales[n],
-                                                                  pw.codebooks[n], k)))
+                abs(float(brute.e4m3(int(a[m][k])) * brute.weight(pw.codes, pw.scales,
+                                                                  pw.codebooks, N, K, n, k)))
                 for k in range(K))
             assert bound[m, n] == pytest.approx(absum, rel=1e-12, abs=0)
 
@@ -253,12 +270,10 @@ def test_grouped_equals_per_expert_gemm_and_reads_only_budget():
     for t in range(M):
         for j in range(topk):
             e = int(idx[t, j])
-            rows = slice(e * N, (e + 1) * N)
-            ye, be = oracle.gemm(a[t:t + 1], s[t:t + 1], pw.codes[rows], pw.scales[rows],
-                                 pw.codebooks[rows], 1, N, K)
+            ce, se, be = oracle.expert(pw.codes, pw.scales, pw.codebooks, e, N, K)
+            ye, _ = oracle.gemm(a[t:t + 1], s[t:t + 1], ce, se, be, 1, N, K)
             assert np.array_equal(y[t, j], ye[0])
-            ex = brute.gemm_exact(a[t:t + 1], s[t:t + 1], pw.codes[rows], pw.scales[rows],
-                                  pw.codebooks[rows], 1, 3, K)[0]
+            ex = brute.gemm_exact(a[t:t + 1], s[t:t + 1], ce, se, be, 1, N, K)[0]
             for n in range(3):
                 assert abs(float(y[t, j, n]) - float(np.float32(float(ex[n])))) <= \
                     float(np.spacing(np.float32(abs(float(ex[n])))))
@@ -344,3 +359,14 @@ def test_pack_ties_go_to_the_lower_index():
     assert np.all(scales == 127)
     assert list(cbs[0]) == [0xB8] * 4 + [0x38] * 4
     assert np.array_equal(idx[0], np.where(W[0] < 0, 0, 4))
+
+
+def test_gemm_rows_equals_full_gemm_rows():
+    M, N, K = 3, 300, 256
+    pw = synth.gen_weights(N, K, seed=51)
+    a = synth.gen_activations(M, K, seed=52)
+    s = synth.gen_a_scale(M, seed=53, mode="uniform")
+    y, b = oracle.gemm(a, s, pw.codes, pw.scales, pw.codebooks, M, N, K)
+    rows = np.array([0, 1, 127, 128, 255, 256, 299])
+    yr, br = oracle.gemm_rows(a, s, pw.codes, pw.scales, pw.codebooks, M, N, K, rows)
+    assert np.array_equal(yr, y[:, rows]) and np.array_equal(br, b[:, rows])

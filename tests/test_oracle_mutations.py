@@ -21,8 +21,12 @@ MUTANTS = {
     "e4m3_subnormal": ("ldexp((double)m, -9)", "ldexp((double)m, -8)"),
     "e4m3_sign": ("return sign ? -v : v;", "return v;"),
     "code_bit_order": ("code |= bit << i;", "code |= bit << (2 - i);"),
-    "code_group_offset": ("int64_t base = (n * (K / 32) + k / 32) * 12;\n    int j = (int)(k % 32);\n    int code",
-                          "int64_t base = (n * (K / 32) + k / 32) * 12 + 1;\n    int j = (int)(k % 32);\n    int code"),
+    "code_group_offset": ("return tile_base + c * R * 48 + (n % 128) * W + (g % 4) * 12;",
+                          "return tile_base + c * 128 * 48 + (n % 128) * W + (g % 4) * 12;"),
+    "row_major_groups": ("return tile_base + c * R * 48 + (n % 128) * W + (g % 4) * 12;",
+                         "return (n * (K / 32) + g) * 12;"),
+    "partial_ktile_width": ("int64_t W = (G - 4 * c < 4) ? 12 * (G - 4 * c) : 48;",
+                            "int64_t W = 48;"),
     "e8m0_bias": ("return ldexp(1.0, (int)s - 127);", "return ldexp(1.0, (int)s - 128);"),
     "dropped_abs_sign": ("acc += p;", "acc += fabs(p);"),
     "no_a_scale": ("y[m * N + n] = (float)((double)a_scale[m] * acc);", "y[m * N + n] = (float)acc;"),
@@ -65,8 +69,13 @@ def _pins_pass() -> bool:
     if bytes(oracle.codes_from_indices(idx).ravel()) != bytes.fromhex("88c6fa" * 4):
         return False
     g = np.frombuffer(bytes.fromhex("000000c0010000000000000000"[:24]), dtype=np.uint8)
-    if oracle.code_at(g, 32, 0, 10) != 7:
+    if oracle.code_at(g, 1, 32, 0, 10) != 7:
         return False
+    # tile order of groups (hand-worked golden offsets)
+    for N_, K_, n_, g_, off in [(130, 256, 129, 5, 12444), (130, 256, 5, 4, 6384),
+                                (300, 384, 299, 5, 41052), (2, 96, 1, 2, 60)]:
+        if oracle.group_offset(N_, K_, n_, g_) != off:
+            return False
     # exact rationals on a tiny gemm
     M, N, K = 2, 3, 64
     pw = synth.gen_weights(N, K, 5, 100, 140)
@@ -116,7 +125,8 @@ def test_pins_pass_on_the_real_oracle():
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_mutant(name):
     old, new = MUTANTS[name]
-    assert SRC.count(old) == 1, f"mutation anchor for {name} not unique"
+    # the anchor may appear in both gemm loops (all rows / listed rows): mutate every copy
+    assert SRC.count(old) >= 1, f"mutation anchor for {name} missing"
     lib = _build(SRC.replace(old, new), name)
     saved = oracle._lib
     oracle._lib = lib
