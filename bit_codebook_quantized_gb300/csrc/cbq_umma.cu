@@ -59,7 +59,7 @@ constexpr int kKtPerStage = 4;                // k-tiles per code stage (one bul
 constexpr int kCodeStage = kKtPerStage * kRows * 48;   // 24 KB
 constexpr int kMaxCodeStages = 6;
 constexpr int kAStages = 8;                   // decoded k-tiles in TMEM
-constexpr int kDecGroups = 2;
+constexpr int kDecGroups = 4;
 constexpr int kDecWarps = 4 * kDecGroups;
 constexpr int kEpiWarp0 = 2 + kDecWarps;      // first epilogue warp
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
@@ -430,35 +430,16 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
         // warm L1 with this row's scale bytes: 8 k-tiles per 32-byte sector
         if (ok)
           for (int kt = kt0; kt < kt1 && kt < kt0 + 16; kt += 8) prefetch_l1(srow + kt);
-        // this group's k-tiles are kt0 + dg, kt0 + dg + G, ...; software
-        // pipelined: decode k-tile n+1 while the TMEM stores of n land
-        uint32_t va[32], vb[32];
-        int kt = kt0 + dg;
-        uint32_t sa = 0, sb = 0;
-        if (kt < kt1) {
-          sa = ok ? __ldg(srow + kt) : 0x7F7F7F7Fu;
-          load_decode(kt, cb, va);
-        }
-        while (kt < kt1) {
-          int kn = kt + kDecGroups;
-          store(it_unit + (kt - kt0), sa, va);
-          if (kn < kt1) {
-            if (ok && kn + 16 < kt1 && ((kn + 16) & 7) < kDecGroups) prefetch_l1(srow + kn + 16);
-            sb = ok ? __ldg(srow + kn) : 0x7F7F7F7Fu;
-            load_decode(kn, cb, vb);
-          }
-          publish(it_unit + (kt - kt0));
-          kt = kn;
-          if (kt >= kt1) break;
-          kn = kt + kDecGroups;
-          store(it_unit + (kt - kt0), sb, vb);
-          if (kn < kt1) {
-            if (ok && kn + 16 < kt1 && ((kn + 16) & 7) < kDecGroups) prefetch_l1(srow + kn + 16);
-            sa = ok ? __ldg(srow + kn) : 0x7F7F7F7Fu;
-            load_decode(kn, cb, va);
-          }
-          publish(it_unit + (kt - kt0));
-          kt = kn;
+        // this group's k-tiles are kt0 + dg, kt0 + dg + G, ...; the other
+        // groups' warps fill the issue slots while this one waits on TMEM
+        for (int kt = kt0 + dg; kt < kt1; kt += kDecGroups) {
+          const uint32_t it = it_unit + (kt - kt0);
+          if (ok && kt + 16 < kt1 && ((kt + 16) & 7) < kDecGroups) prefetch_l1(srow + kt + 16);
+          const uint32_t sw = ok ? __ldg(srow + kt) : 0x7F7F7F7Fu;
+          uint32_t v[32];
+          load_decode(kt, cb, v);
+          store(it, sw, v);
+          publish(it);
         }
         release_until(n_stages_u);
       }
@@ -515,60 +496,63 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
         const int abuf = ui & 1;
         wait_bounded(&acc_full[abuf], (ui >> 1) & 1);
         tc_fence_after();
-        float v[NTOK];
-  #pragma unroll
-        for (int c = 0; c < NTOK; c += 16) {
+        const bool split = !GROUPED && cs > 1;
+        if (split && rank != 0) wait_bounded<true>(red_free, (ui & 1) ^ 1);
+        if (split && rank == 0) wait_bounded<true>(red_full, ui & 1);
+        // 16 accumulator columns (token rows) at a time: load, reduce, store
+#pragma unroll 1
+        for (int c0 = 0; c0 < NTOK; c0 += 16) {
           uint32_t t[16];
-          tmem_ld_x16(tbase + lane_addr + abuf * kAccCols + c, t);
+          tmem_ld_x16(tbase + lane_addr + abuf * kAccCols + c0, t);
           tmem_ld_wait();
-  #pragma unroll
-          for (int i = 0; i < 16; ++i) v[c + i] = __uint_as_float(t[i]);
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(t[i]);
+          if (split) {
+            if (rank != 0) {
+              // split K: partial tiles meet in the leader CTA's shared memory
+              const uint32_t dst = mapa_shared(
+                  smem_u32(red_s) + ((rank - 1) * kRows * NTOK + r * NTOK + c0) * 4, 0);
+#pragma unroll
+              for (int i = 0; i < 16; i += 4) st_cluster_v4(dst + i * 4, v[i], v[i + 1], v[i + 2], v[i + 3]);
+              continue;
+            }
+            for (int sidx = 0; sidx < cs - 1; ++sidx) {
+              const float4* src = reinterpret_cast<const float4*>(red_s + sidx * kRows * NTOK + r * NTOK + c0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float4 f = src[i];
+                v[4 * i] += f.x;
+                v[4 * i + 1] += f.y;
+                v[4 * i + 2] += f.z;
+                v[4 * i + 3] += f.w;
+              }
+            }
+          }
+          if (ok) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int c = c0 + i;
+              if (c < ntok) {
+                if constexpr (GROUPED) {
+                  const int tok = list_tok[c] & 0xff, slot = list_tok[c] >> 8;
+                  p.y[(size_t(tok) * p.topk + slot) * p.N + (grow - e * p.N)] = v[i] * __ldg(p.a_scale + tok);
+                } else {
+                  p.y[size_t(c) * p.N + grow] = v[i] * __ldg(p.a_scale + c);
+                }
+              }
+            }
+          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[abuf]);
-
-        if constexpr (!GROUPED) {
-          if (cs > 1) {
-            // split K: partial tiles meet in the leader CTA's shared memory
-            const uint32_t slot_off = r * NTOK * 4;
-            if (rank != 0) {
-              wait_bounded<true>(red_free, (ui & 1) ^ 1);
-              const uint32_t dst = mapa_shared(smem_u32(red_s) + (rank - 1) * kRows * NTOK * 4 + slot_off, 0);
-  #pragma unroll
-              for (int c = 0; c < NTOK; c += 4) st_cluster_v4(dst + c * 4, v[c], v[c + 1], v[c + 2], v[c + 3]);
-              mbar_arrive_remote(mapa_shared(smem_u32(red_full), 0));
-              continue;
-            }
-            wait_bounded<true>(red_full, ui & 1);
-            for (int s = 0; s < cs - 1; ++s) {
-              const float4* src = reinterpret_cast<const float4*>(red_s + s * kRows * NTOK + r * NTOK);
-  #pragma unroll
-              for (int c = 0; c < NTOK / 4; ++c) {
-                const float4 t = src[c];
-                v[4 * c] += t.x;
-                v[4 * c + 1] += t.y;
-                v[4 * c + 2] += t.z;
-                v[4 * c + 3] += t.w;
-              }
-            }
+        if (split) {
+          if (rank != 0) {
+            mbar_arrive_remote(mapa_shared(smem_u32(red_full), 0));
+          } else {
             // tell every other CTA of the cluster that its slot may be reused
-            for (int s = 1; s < cs; ++s) mbar_arrive_remote(mapa_shared(smem_u32(red_free), s));
-          }
-          if (ok) {
-  #pragma unroll
-            for (int c = 0; c < NTOK; ++c)
-              if (c < ntok) p.y[size_t(c) * p.N + grow] = v[c] * __ldg(p.a_scale + c);
-          }
-        } else {
-          if (ok) {
-  #pragma unroll
-            for (int c = 0; c < NTOK; ++c) {
-              if (c < ntok) {
-                const int tok = list_tok[c] & 0xff, slot = list_tok[c] >> 8;
-                p.y[(size_t(tok) * p.topk + slot) * p.N + (grow - e * p.N)] = v[c] * __ldg(p.a_scale + tok);
-              }
-            }
+            for (int sidx = 1; sidx < cs; ++sidx) mbar_arrive_remote(mapa_shared(smem_u32(red_free), sidx));
           }
         }
       }
