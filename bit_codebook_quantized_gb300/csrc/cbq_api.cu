@@ -1,6 +1,6 @@
 // cbq_api.cu -- the C entry points declared in include/cbq.h: argument
-// checks, tensor-map encoding, kernel selection.  All device work is done by
-// the kernels in cbq_gemv.cu and cbq_umma.cu; this file launches them on the
+// checks and kernel selection.  All device work is done by the kernels in
+// cbq_sk.cu, cbq_gemv.cu and cbq_umma.cu; this file launches them on the
 // caller's stream and never synchronises (except cbq_device_status).
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -98,7 +98,7 @@ int cbq_unpack(const cbq_weight_t* w, int32_t N, int32_t K, float* W_out, void* 
 int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w, int32_t M,
                   int32_t N, int32_t K, float* y, void* stream, int32_t path) {
   if (M < 0 || M > 64 || N < 0 || K < 0 || K % 128 != 0) return CBQ_EINVAL;
-  if (path < CBQ_PATH_AUTO || path > CBQ_PATH_MMA) return CBQ_EINVAL;
+  if (path < CBQ_PATH_AUTO || path > CBQ_PATH_STREAMK) return CBQ_EINVAL;
   if (M == 0 || N == 0) return CBQ_OK;
   if (!y || !aligned(y, 4)) return CBQ_EINVAL;
   int st = current_device_checked(nullptr);
@@ -111,7 +111,23 @@ int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w,
   }
   if (!a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(w))
     return CBQ_EINVAL;
-  if (path == CBQ_PATH_AUTO) path = (M <= 4) ? CBQ_PATH_GEMV : CBQ_PATH_MMA;
+  const bool automatic = path == CBQ_PATH_AUTO;
+  if (automatic) path = sk_applicable(M, N, K) ? CBQ_PATH_STREAMK : CBQ_PATH_MMA;
+  if (path == CBQ_PATH_STREAMK) {
+    if (!sk_applicable(M, N, K)) return CBQ_EINVAL;
+    SkParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.codes = w->codes;
+    p.a = a;
+    p.a_scale = a_scale;
+    p.scales = w->scales;
+    p.codebooks = w->codebooks;
+    p.y = y;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    return launch_sk(p, s);
+  }
   if (path == CBQ_PATH_GEMV) {
     GemvParams p;
     std::memset(&p, 0, sizeof(p));
@@ -137,7 +153,21 @@ int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w,
   p.M = M;
   p.N = N;
   p.K = K;
-  return launch_umma(p, false, s);
+  const int r = launch_umma(p, false, s);
+  if (r != CBQ_EINVAL || !automatic) return r;
+  // the tile kernel's resident activations do not fit either: GEMV kernel
+  GemvParams g;
+  std::memset(&g, 0, sizeof(g));
+  g.codes = w->codes;
+  g.a = a;
+  g.a_scale = a_scale;
+  g.scales = w->scales;
+  g.codebooks = w->codebooks;
+  g.y = y;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  return launch_gemv(g, false, s);
 }
 
 int cbq_gemm(const uint8_t* a, const float* a_scale, const cbq_weight_t* w, int32_t M, int32_t N,
@@ -210,7 +240,7 @@ int cbq_grouped_gemm(const uint8_t* a, const float* a_scale, const cbq_weight_t*
 int cbq_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return CBQ_ECUDA;
-  unsigned v = take_status_gemv(s) | take_status_umma(s);
+  unsigned v = take_status_gemv(s) | take_status_umma(s) | take_status_sk(s);
   if (v & 1u) return CBQ_ETIMEOUT;
   if (v & 2u) return CBQ_EROUTING;
   return CBQ_OK;

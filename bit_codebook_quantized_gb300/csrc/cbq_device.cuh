@@ -28,19 +28,35 @@ constexpr long long kWaitLimitCycles = 4000000000LL;
 // are ignored) so that code j lands in nibble j.  The result, and the result
 // shifted right by 16, are byte-permute selectors for codes 0-3 and 4-7.
 __device__ __forceinline__ uint32_t spread_codes8(uint32_t f) {
-  uint32_t lo = f & 0x00000FFFu;                  // codes 0-3
-  uint32_t hi = f & 0x00FFF000u;                  // codes 4-7
-  uint32_t h = lo + (hi << 4);                    // codes 4-7 -> bits 16..27
-  uint32_t t = h & 0x0FC00FC0u;                   // codes 2,3 and 6,7
-  h = h + t * 3u;                                 // move them up by 2 bits
-  t = h & 0x38383838u;                            // odd codes
-  return h + t;                                   // move them up by 1 bit
+  uint32_t h = f & 0x00FFFFFFu;                   // the 8 codes, bits 0..23
+  h += (h & 0x00FFF000u) * 15u;                   // codes 4-7 up by 4 bits
+  h += (h & 0x0FC00FC0u) * 3u;                    // codes 2,3 and 6,7 up by 2
+  return h + (h & 0x38383838u);                   // odd codes up by 1
 }
 
 // Four E4M3 codebook bytes for the four codes held in nibbles 0..3 of `sel`
 // (each 0..7; nibble bit 3 clear).  cb_lo holds entries 0-3, cb_hi 4-7.
 __device__ __forceinline__ uint32_t lookup4(uint32_t cb_lo, uint32_t cb_hi, uint32_t sel) {
   return __byte_perm(cb_lo, cb_hi, sel);
+}
+
+// Decode one group (three 32-bit words) of a row into 32 E4M3 bytes
+// (8 TMEM columns):
+// v[0..7] = E4M3 bytes of codes 0..31, four per column.
+__device__ __forceinline__ void decode_group(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t cb_lo,
+                                             uint32_t cb_hi, uint32_t* v) {
+  const uint32_t s0 = spread_codes8(w0);
+  const uint32_t s1 = spread_codes8(__funnelshift_r(w0, w1, 24));
+  const uint32_t s2 = spread_codes8(__funnelshift_r(w1, w2, 16));
+  const uint32_t s3 = spread_codes8(w2 >> 8);
+  v[0] = lookup4(cb_lo, cb_hi, s0);
+  v[1] = lookup4(cb_lo, cb_hi, s0 >> 16);
+  v[2] = lookup4(cb_lo, cb_hi, s1);
+  v[3] = lookup4(cb_lo, cb_hi, s1 >> 16);
+  v[4] = lookup4(cb_lo, cb_hi, s2);
+  v[5] = lookup4(cb_lo, cb_hi, s2 >> 16);
+  v[6] = lookup4(cb_lo, cb_hi, s3);
+  v[7] = lookup4(cb_lo, cb_hi, s3 >> 16);
 }
 
 // E8M0 byte -> fp32 2^(s-127) (s = 0 gives the subnormal 2^-127).

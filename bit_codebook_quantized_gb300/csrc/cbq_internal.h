@@ -41,6 +41,21 @@ struct UmmaParams {
   int code_stages;            // depth of the code-stage ring (<= kMaxCodeStages)
 };
 
+// Kernel parameters of the stream-K kernel (dense calls, cbq_sk.cu).
+struct SkParams {
+  const uint8_t* codes;       // code stream (tile order)
+  const uint8_t* a;           // [M][K] E4M3
+  const float* a_scale;       // [M]
+  const uint8_t* scales;      // [N][K/32]
+  const uint8_t* codebooks;   // [N][8]
+  float* y;                   // [M][N]
+  float* partial;             // scratch: 2 x grid partial tiles of 128 x NTOK fp32
+  unsigned* counters;         // scratch: one arrival counter per 128-row tile, zero between calls
+  int M, N, K;
+  int stages;                 // depth of the code-stage ring
+  int b_ktiles;               // k-tiles of resident activations
+};
+
 int device_sm_count();
 void note_launch();
 
@@ -51,6 +66,10 @@ unsigned take_status_gemv(cudaStream_t stream);
 
 int launch_umma(const UmmaParams& p, bool grouped, cudaStream_t stream);
 unsigned take_status_umma(cudaStream_t stream);
+
+bool sk_applicable(int M, int N, int K);
+int launch_sk(const SkParams& p, cudaStream_t stream);
+unsigned take_status_sk(cudaStream_t stream);
 
 // Host quantiser (cbq_pack.cpp).
 int pack_host(const float* W, int N, int K, uint8_t* codes, uint8_t* scales,

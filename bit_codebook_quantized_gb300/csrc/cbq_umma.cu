@@ -125,24 +125,6 @@ struct Layout {
   }
 };
 
-// Decode one group (three 32-bit words) of a row into 8 TMEM columns:
-// v[0..7] = E4M3 bytes of codes 0..31, four per column.
-__device__ __forceinline__ void decode_group(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t cb_lo,
-                                             uint32_t cb_hi, uint32_t* v) {
-  const uint32_t s0 = spread_codes8(w0);
-  const uint32_t s1 = spread_codes8(__funnelshift_r(w0, w1, 24));
-  const uint32_t s2 = spread_codes8(__funnelshift_r(w1, w2, 16));
-  const uint32_t s3 = spread_codes8(w2 >> 8);
-  v[0] = lookup4(cb_lo, cb_hi, s0);
-  v[1] = lookup4(cb_lo, cb_hi, s0 >> 16);
-  v[2] = lookup4(cb_lo, cb_hi, s1);
-  v[3] = lookup4(cb_lo, cb_hi, s1 >> 16);
-  v[4] = lookup4(cb_lo, cb_hi, s2);
-  v[5] = lookup4(cb_lo, cb_hi, s2 >> 16);
-  v[6] = lookup4(cb_lo, cb_hi, s3);
-  v[7] = lookup4(cb_lo, cb_hi, s3 >> 16);
-}
-
 template <int NTOK, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant__ UmmaParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];

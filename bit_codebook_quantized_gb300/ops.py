@@ -20,7 +20,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libcbq.so")
 
-PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
+PATH_AUTO, PATH_GEMV, PATH_MMA, PATH_STREAMK = 0, 1, 2, 3
 OK, EINVAL, ECUDA, EDEVICE, ETIMEOUT, EROUTING = 0, -1, -2, -3, -4, -5
 
 # Every symbol include/cbq.h declares.
@@ -41,7 +41,7 @@ class _Weight(ctypes.Structure):
 
 
 _lib = None
-_lock = threading.Lock()
+_lock = threading.RLock()
 
 
 def lib() -> ctypes.CDLL:
@@ -76,10 +76,9 @@ def lib() -> ctypes.CDLL:
 
 
 def status_str(status: int) -> str:
-    try:
-        return lib().cbq_status_str(int(status)).decode()
-    except CbqError:
+    if _lib is None:                      # never load (or wait on the loader) from an error path
         return "library not loaded"
+    return _lib.cbq_status_str(int(status)).decode()
 
 
 def _check(status: int, what: str) -> None:

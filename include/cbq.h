@@ -54,10 +54,22 @@ extern "C" {
 #define CBQ_EROUTING (-5)    /* grouped call: an expert id outside [0,E) or a
                                 token listing one expert twice was seen */
 
-/* Which kernel cbq_gemm_path runs. */
-#define CBQ_PATH_AUTO 0      /* M <= 4: GEMV kernel; M >= 5: tcgen05 kernel */
+/* Which kernel cbq_gemm_path / cbq_grouped_gemm_path runs. */
+#define CBQ_PATH_AUTO 0      /* dense: stream-K kernel when its resident
+                                activations fit in shared memory, else the
+                                tcgen05 tile kernel when its do, else GEMV;
+                                grouped: M <= 4 GEMV, else the tile kernel */
 #define CBQ_PATH_GEMV 1      /* register-decode + warp MMA kernel, any M <= 64 */
-#define CBQ_PATH_MMA 2       /* TMA + tcgen05 block-scaled FP8 kernel, any M <= 64 */
+#define CBQ_PATH_MMA 2       /* tcgen05 block-scaled FP8 tile kernel (K split
+                                over a cluster), any M <= 64 */
+#define CBQ_PATH_STREAMK 3   /* dense only: tcgen05 kernel with an equal
+                                contiguous share of the weights per SM; needs
+                                ntok(M) * min(K/128, share) * 128 bytes of
+                                activations to fit next to a 3-stage ring
+                                (ntok = 16/32/64), else CBQ_EINVAL.  Uses a
+                                per-(device, stream) scratch buffer allocated
+                                on first use; calls on one stream must not
+                                run concurrently (graph replays included) */
 
 /* One packed matrix in device memory (all three arrays 16-byte aligned). */
 typedef struct cbq_weight {
@@ -101,7 +113,10 @@ int cbq_unpack(const cbq_weight_t *w, int32_t N, int32_t K, float *W_out,
 /* y[M][N] = a_scale * (a[M][K] x W^T): the decode-step / verify-round matmul
  * against packed weights.  a, a_scale, y and w's arrays are DEVICE pointers.
  * 1 <= M <= 64 (M == 0 or N == 0 is a no-op); N >= 0; K % 128 == 0 (K == 0
- * writes y = 0).  Picks the kernel by M (CBQ_PATH_AUTO); one launch.
+ * writes y = 0).  Picks the kernel as CBQ_PATH_AUTO says; one launch (plus
+ * a scratch allocation and zeroing on the stream's first stream-K call).
+ * The result is deterministic: a tile shared by several SMs is summed in a
+ * fixed order.
  * Errors: CBQ_EINVAL, CBQ_EDEVICE, CBQ_ECUDA. */
 int cbq_gemm(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
              int32_t M, int32_t N, int32_t K, float *y, void *stream);

@@ -112,3 +112,17 @@ def test_host_pack_matches_oracle_on_few_valued_rows(L):
     ocodes, oscales, ocbs = oracle.pack(W)
     assert np.array_equal(codes, ocodes) and np.array_equal(scales, oscales)
     assert np.array_equal(cbs, ocbs)
+
+
+def test_missing_library_fails_loudly():
+    # the binding raises at once when the shared library is absent (no
+    # fallback, no hang in the error path)
+    import subprocess
+    import sys
+    code = ("from bit_codebook_quantized_gb300 import ops\n"
+            "ops.LIB_PATH = '/nonexistent/libcbq.so'\n"
+            "try:\n    ops.lib()\nexcept ops.CbqError as e:\n    print('raised', e.status)\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120,
+                       cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert r.returncode == 0, r.stderr
+    assert "raised -2" in r.stdout

@@ -13,7 +13,8 @@ from tests.gpu_util import Case, assert_close, ensure_built, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [ops.PATH_GEMV, ops.PATH_MMA]
+PATHS = [ops.PATH_GEMV, ops.PATH_MMA, ops.PATH_STREAMK]
+GROUPED_PATHS = [ops.PATH_GEMV, ops.PATH_MMA]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -93,6 +94,38 @@ def test_a_scale_linearity(path):
     assert np.array_equal(y2, 2 * y1)
 
 
+def test_streamk_many_parts_deterministic():
+    # K = 25600 over one 40-row tile: ~150 SMs share the tile's 200 k-tiles,
+    # the last to arrive sums every part; two runs agree bit for bit
+    c = Case(5, 40, 25600, seed=77)
+    y1 = c.run(ops.PATH_STREAMK)
+    y2 = c.run(ops.PATH_STREAMK)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    yref, b = c.oracle()
+    assert_close(y1, yref, b, "many parts")
+    assert ops.device_status() == ops.OK
+
+
+def test_streamk_shape_sequence_on_one_stream():
+    # tile counters are back to zero after every call, whatever the shape
+    cases = [Case(1, 300, 1024, seed=81), Case(16, 1000, 384, seed=82), Case(64, 129, 2048, seed=83)]
+    for c in cases + cases[::-1]:
+        yref, b = c.oracle()
+        assert_close(c.run(ops.PATH_STREAMK), yref, b, f"M {c.M} N {c.N} K {c.K}")
+    assert ops.device_status() == ops.OK
+
+
+def test_streamk_rejects_what_does_not_fit():
+    # 64 token columns x 53 k-tiles of resident activations per SM do not fit
+    c = Case(64, 5120, 25600, seed=5)
+    a, s, w = c.device()
+    with pytest.raises(ops.CbqError):
+        ops.gemm(a, s, w, path=ops.PATH_STREAMK)
+    rows = sample_rows(c.N, 24, seed=6)
+    yref, b = c.oracle_rows(rows)
+    assert_close(c.run(ops.PATH_AUTO)[:, rows], yref, b, "auto falls back to the tile kernel")
+
+
 def test_auto_path_matches_both_kernels():
     for M in (1, 4, 5, 8, 16):
         c = Case(M, 96, 256, seed=40 + M)
@@ -134,6 +167,19 @@ def test_full_size_sampled(name):
     assert ops.device_status() == ops.OK
 
 
+@pytest.mark.parametrize("name", ["decode_4096x12288_m8", "verify_down_25600x5120_m16",
+                                  "vocab_head_2048x151936_m64"])
+def test_full_size_sampled_tile_kernel(name):
+    wl = synth.workloads()[name]
+    c = Case(wl.M, wl.N, wl.K, seed=zlib.crc32(name.encode()) % 1000, a_scale=wl.a_scale,
+             half_normal=wl.half_normal)
+    y = c.run(ops.PATH_MMA)
+    rows = sample_rows(wl.N, 48, seed=4)
+    yref, b = c.oracle_rows(rows)
+    assert_close(y[:, rows], yref, b, name)
+    assert ops.device_status() == ops.OK
+
+
 # ---- grouped (MoE verify round) ---------------------------------------------------
 
 def _grouped_case(E, N, K, M, budget, topk, seed):
@@ -152,7 +198,7 @@ def _run_grouped(pw, a, s, idx, E, N, K, path=ops.PATH_AUTO):
     return y.cpu().numpy()
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", GROUPED_PATHS)
 @pytest.mark.parametrize("E,N,K,M,budget,topk", [(12, 80, 256, 6, 4, 2), (16, 33, 384, 64, 16, 8),
                                                   (5, 16, 128, 1, 1, 1), (6, 300, 640, 20, 3, 2)])
 def test_grouped_small(path, E, N, K, M, budget, topk):
@@ -163,7 +209,7 @@ def test_grouped_small(path, E, N, K, M, budget, topk):
     assert ops.device_status() == ops.OK
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", GROUPED_PATHS)
 def test_grouped_full_size_sampled(path):
     wl = synth.workloads()["moe_verify_e128_2048x1536_m64"]
     E, N, K, M = wl.experts, wl.N, wl.K, wl.M
@@ -179,7 +225,7 @@ def test_grouped_full_size_sampled(path):
     assert ops.device_status() == ops.OK
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", GROUPED_PATHS)
 def test_grouped_routing_errors_are_reported(path):
     E, N, K, M = 4, 16, 128, 2
     pw, a, s, idx = _grouped_case(E, N, K, M, 4, 2, seed=8)
