@@ -47,9 +47,12 @@ METRIC = "effective weight GB/s and % of GB300 HBM roofline per cbq_gemm call (M
 WORKLOAD = "decode_4096x12288: cbq_gemm at M=1,2,4,8, K=4096, N=12288 (fused gate+up)"
 
 
+KERNEL_NAMES = {ops.PATH_GEMV: "gemv_kernel", ops.PATH_MMA: "umma_kernel", ops.PATH_STREAMK: "sk_kernel"}
+
+
 def kernel_of(M: int) -> str:
-    """Kernel the library's automatic choice runs at M rows."""
-    return "gemv_kernel" if M <= 4 else "umma_kernel"
+    """Kernel the library's automatic choice runs at M rows on the step's matrix."""
+    return KERNEL_NAMES[ops.auto_path(M, N_DIM, K_DIM)]
 
 
 def weight_bytes(N=N_DIM, K=K_DIM) -> int:

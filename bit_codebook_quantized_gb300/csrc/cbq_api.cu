@@ -53,6 +53,21 @@ bool weight_ok(const cbq_weight_t* w) {
 
 }  // namespace
 
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
 int device_sm_count() {
   DeviceInfo* d = nullptr;
   if (current_device_checked(&d) != CBQ_OK) return 1;
@@ -95,6 +110,19 @@ int cbq_unpack(const cbq_weight_t* w, int32_t N, int32_t K, float* W_out, void* 
                        static_cast<cudaStream_t>(stream));
 }
 
+int cbq_gemm_auto_path(int32_t M, int32_t N, int32_t K) {
+  if (M < 1 || M > 64 || N < 1 || K < 128 || K % 128 != 0) return CBQ_EINVAL;
+  // Measured on GB300 (CUDA graphs of back-to-back calls, weights beyond L2):
+  // up to 8 token rows the GEMV kernel wins on matrices up to ~64 M weights
+  // and the tile kernel beyond; from 9 rows the stream-K kernel wins up to
+  // ~128 M weights.  The tile kernel needs its activations resident; where
+  // they do not fit, the GEMV kernel runs (see cbq_gemm_path).
+  const long long weights = static_cast<long long>(N) * K;
+  if (M <= 8) return weights <= (1LL << 26) ? CBQ_PATH_GEMV : CBQ_PATH_MMA;
+  if (weights <= (1LL << 27) && sk_applicable(M, N, K)) return CBQ_PATH_STREAMK;
+  return CBQ_PATH_MMA;
+}
+
 int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w, int32_t M,
                   int32_t N, int32_t K, float* y, void* stream, int32_t path) {
   if (M < 0 || M > 64 || N < 0 || K < 0 || K % 128 != 0) return CBQ_EINVAL;
@@ -112,7 +140,7 @@ int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w,
   if (!a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(w))
     return CBQ_EINVAL;
   const bool automatic = path == CBQ_PATH_AUTO;
-  if (automatic) path = sk_applicable(M, N, K) ? CBQ_PATH_STREAMK : CBQ_PATH_MMA;
+  if (automatic) path = cbq_gemm_auto_path(M, N, K);
   if (path == CBQ_PATH_STREAMK) {
     if (!sk_applicable(M, N, K)) return CBQ_EINVAL;
     SkParams p;

@@ -17,8 +17,17 @@ namespace cbq {
 // word; cbq_device_status() collects and clears them).
 enum : unsigned { kErrTimeout = 1u, kErrRouting = 2u };
 
-// Bounded waits give up after this many SM clock cycles (~2 s at 2 GHz).
+// Bounded waits give up after this many SM clock cycles (~2 s at 2 GHz), or
+// (waits that may be suspended, when the SM clock may not advance for the
+// waiting warp) after this many nanoseconds of the global timer.
 constexpr long long kWaitLimitCycles = 4000000000LL;
+constexpr long long kWaitLimitNs = 2000000000LL;
+
+__device__ __forceinline__ long long global_ns() {
+  long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 // ---------------------------------------------------------------------------
 // Decode: 8 codes (a 24-bit field) -> 8 E4M3 bytes through the codebook.
@@ -123,6 +132,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same, but the thread may be suspended (up to `hint_ns`) until the phase
+// completes instead of returning at once: a waiting warp then takes no issue
+// slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // 4- or 8-byte asynchronous global -> shared copies (cp.async), tracked by an
 // mbarrier: cp_async_arrive makes `bar` receive one arrival (not counted in
 // advance: the barrier's expected count must include it) once every
@@ -149,6 +173,30 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, ui
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
+}
+
+// 3-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar,
+                                            int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// 32-bit load with acquire semantics at GPU scope.
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their writes are visible / let dependent grids start.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // 1-D bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0),
@@ -210,6 +258,16 @@ __device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint3
 __device__ __forceinline__ uint64_t umma_desc_kmajor(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+
+// Same for a K-major operand stored with the 128-byte swizzle (what a TMA
+// load with CU_TENSOR_MAP_SWIZZLE_128B writes): rows of 128 bytes, the 16-byte
+// chunk j of row r at chunk j ^ (r % 8), 8-row atoms of 1024 bytes (1024-byte
+// aligned); sbo = 1024, layout type 2 at [61,64).  An MMA reading K bytes
+// [32 i, 32 i + 32) of the atom starts at atom + 32 i.
+__device__ __forceinline__ uint64_t umma_desc_kmajor_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
 // Instruction descriptor of a block-scaled kind::mxf8f6f4 MMA with E4M3 A

@@ -43,6 +43,8 @@ struct UmmaParams {
 
 // Kernel parameters of the stream-K kernel (dense calls, cbq_sk.cu).
 struct SkParams {
+  CUtensorMap a_map;          // activations a[M][K]: box of ntok rows x 128 B, 128-byte swizzle
+                              // (b_layout 0), or the [K/16][M][16] view, box [8][ntok][16] (1)
   const uint8_t* codes;       // code stream (tile order)
   const uint8_t* a;           // [M][K] E4M3
   const float* a_scale;       // [M]
@@ -54,7 +56,14 @@ struct SkParams {
   int M, N, K;
   int stages;                 // depth of the code-stage ring
   int b_ktiles;               // k-tiles of resident activations
+  int b_layout;               // 0: 128-byte swizzled rows, 1: core-matrix chunks (no swizzle)
 };
+
+// cuTensorMapEncodeTiled from the driver (nullptr if unavailable).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
 
 int device_sm_count();
 void note_launch();

@@ -59,44 +59,55 @@ constexpr int kRows = 128;                            // MMA M: weight rows per 
 constexpr int kUnitsPerStage = 4;
 constexpr int kStageBytes = kUnitsPerStage * kRows * 48;   // 24 KB
 constexpr int kMaxStages = 8;
-constexpr int kASlots = 8;                            // decoded units in TMEM
+constexpr int kMaxASlots = 16;                        // decoded units in TMEM (see TmemMap)
 constexpr int kDecGroups = 4;
 constexpr int kDecWarps = 4 * kDecGroups;
 constexpr int kEpiWarp0 = 2 + kDecWarps;
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kTmemCols = 512;
-constexpr int kAccCols = 64;                          // accumulator i at column 64 i
-constexpr int kSfaCol = 128;                          // + 4 * A slot (4-column aligned)
-constexpr int kSfbCol = 192;                          // 8 columns of 2^0
-constexpr int kACol = 256;                            // + 32 * A slot
 constexpr int kMaxSmem = 232448;
 constexpr int kMinSmem = 120 * 1024;                  // one CTA per SM: it owns all of TMEM
-constexpr int kNumBars = 2 * kMaxStages + 2 * kASlots + 4;
+constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxASlots + 5;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
-static_assert(kACol + 32 * kASlots <= kTmemCols, "A slots exceed the allocation");
-static_assert(kSfaCol + 4 * kASlots <= kSfbCol && kSfbCol + 8 <= kACol, "TMEM areas overlap");
-static_assert(2 * kAccCols <= kSfaCol, "accumulators overlap the scale factors");
+
+// Tensor-memory columns for NTOK token columns: two fp32 accumulators of NTOK
+// columns (32-column aligned), 8 columns of B scale factors (2^0), then S A
+// slots, each with 4 scale-factor columns (4-column aligned) and 32 columns
+// of E4M3 A (128 k), as many slots as fit in the 512 columns.
+template <int NTOK>
+struct TmemMap {
+  static constexpr int kAccStride = NTOK < 32 ? 32 : NTOK;
+  static constexpr int kAcc = 0;                              // + kAccStride * buffer
+  static constexpr int kSfb = 2 * kAccStride;
+  static constexpr int kSfa = kSfb + 8;                       // + 4 * slot
+  static constexpr int slots_fit(int s) { return ((kSfa + 4 * s + 31) / 32) * 32 + 32 * s <= kTmemCols; }
+  static constexpr int kSlots = slots_fit(16) ? 16 : slots_fit(13) ? 13 : slots_fit(12) ? 12 : 10;
+  static constexpr int kA = ((kSfa + 4 * kSlots + 31) / 32) * 32;   // + 32 * slot
+  static_assert(kA + 32 * kSlots <= kTmemCols, "A slots exceed the allocation");
+  static_assert(kSlots <= kMaxASlots, "barrier arrays too small");
+};
 
 __device__ __forceinline__ void raise(unsigned bits) { atomicOr(&g_status_sk, bits); }
 __device__ __forceinline__ bool status_set() {
   return *reinterpret_cast<volatile unsigned*>(&g_status_sk) != 0u;
 }
 
-// Spin on an mbarrier phase.  After ~0.5 ms give up at once if another wait
-// already timed out; after kWaitLimitCycles raise kErrTimeout and give up.
+// Wait for an mbarrier phase, suspended in the barrier rather than spinning
+// (spinning warps would steal issue slots from the decoders and the MMA
+// issuer on the same sub-partition).  After ~0.5 ms give up at once if
+// another wait already timed out; after kWaitLimitNs raise kErrTimeout and
+// give up.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 63u) == 0) {
-      const long long dt = clock64() - t0;
-      if (dt > (1LL << 20)) {
-        if (status_set()) return false;
-        if (dt > kWaitLimitCycles) {
-          raise(kErrTimeout);
-          return false;
-        }
+  const long long t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+    const long long dt = global_ns() - t0;
+    if (dt > 500000LL) {
+      if (status_set()) return false;
+      if (dt > kWaitLimitNs) {
+        raise(kErrTimeout);
+        return false;
       }
     }
   }
@@ -135,6 +146,7 @@ struct Geo {
 
 template <int NTOK>
 __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__ SkParams p) {
+  using TM = TmemMap<NTOK>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int NS = p.stages;
   uint8_t* codes_s = smem;
@@ -143,10 +155,11 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   uint64_t* full = bars;
   uint64_t* empty = full + kMaxStages;
   uint64_t* a_full = empty + kMaxStages;
-  uint64_t* a_empty = a_full + kASlots;
-  uint64_t* acc_full = a_empty + kASlots;
+  uint64_t* a_empty = a_full + kMaxASlots;
+  uint64_t* acc_full = a_empty + kMaxASlots;
   uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* b_full = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -167,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kDecWarps);                 // every decoder warp, once per stage
     }
-    for (int i = 0; i < kASlots; ++i) {
+    for (int i = 0; i < kMaxASlots; ++i) {
       mbar_init(&a_full[i], 4);
       mbar_init(&a_empty[i], 1);
     }
@@ -175,9 +188,14 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);
     }
+    mbar_init(b_full, 1);
     fence_barrier_init();
   }
   __syncthreads();
+  // The next kernel on the stream may start its prologue (and, if it is this
+  // one, its weight stream) as soon as SMs free up; whatever this grid reads
+  // from or writes for earlier kernels waits on grid_dependency_wait below.
+  grid_launch_dependents();
 
   uint32_t tbase = 0;
   if (warp == 0) {
@@ -205,42 +223,34 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       tmem_alloc(tmem_slot, kTmemCols);
       tmem_relinquish();
     }
-    // Resident activations: k-tile c of this CTA's share sits in slot
-    // (c - c_first) mod KT, K-major core-matrix layout inside a slot: chunk
-    // (16 k) cc at cc * NTOK * 16, token group at * 128, token % 8 at * 16.
-    {
-      const int nb = min(KT, n_units);
-      const int total = nb * 8 * NTOK;
-      for (int i = tid - 32; i < total; i += kThreads - 32) {
-        const int tok = i % NTOK, ch = i / NTOK;        // ch = slot * 8 + chunk
-        int c = c_first + (ch >> 3);
-        if (c >= KT) c -= KT;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (tok < p.M)
-          v = __ldg(reinterpret_cast<const uint4*>(p.a + static_cast<size_t>(tok) * p.K + c * 128 + (ch & 7) * 16));
-        *reinterpret_cast<uint4*>(b_s + ch * NTOK * 16 + (tok >> 3) * 128 + (tok & 7) * 16) = v;
-      }
-      fence_proxy_async_smem();
-    }
     tc_fence_before();
     named_bar_sync(1, kThreads - 32);                  // everyone but the producer
     tc_fence_after();
     tbase = *tmem_slot;
-    if (warp >= kEpiWarp0) {                            // B scale factors: 2^0
-      const uint32_t q = warp & 3;
-      for (int c = 0; c < 8; c += 4)
-        tmem_st_x4(tbase + ((32 * q) << 16) + kSfbCol + c, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-      tmem_st_wait();
-    }
-    tc_fence_before();
-    named_bar_sync(1, kThreads - 32);
-    tc_fence_after();
 
     if (warp == 1) {
       // --------------------------------------------------------- MMA issuer --
+      named_bar_sync(3, 160);                          // B scale factors are in TMEM
+      tc_fence_after();
       if (lane == 0) {
+        // Resident activations (written by an earlier kernel, so after the
+        // grid dependency): k-tile c of this CTA's share lands in slot
+        // (c - c_first) mod KT as ntok rows of 128 bytes in the 128-byte
+        // swizzled K-major layout (one TMA box); token rows >= M are outside
+        // the tensor and arrive as zeros.
+        grid_dependency_wait();
+        const int nb = min(KT, n_units);
+        mbar_arrive_expect_tx(b_full, static_cast<uint32_t>(nb * NTOK * 128));
+        for (int sl = 0; sl < nb; ++sl) {
+          int c = c_first + sl;
+          if (c >= KT) c -= KT;
+          uint8_t* dst = b_s + sl * NTOK * 128;
+          if (p.b_layout == 0) tma_load_2d(dst, &p.a_map, b_full, c * 128, 0);
+          else tma_load_3d(dst, &p.a_map, b_full, 0, 0, 8 * c);
+        }
         const uint32_t b_base = smem_u32(b_s);
         const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
+        wait_bounded(b_full, 0);
         int seg = 0, c = c_first;
         for (int i = 0; i < n_units; ++i, c = (c + 1 == KT) ? 0 : c + 1) {
           const bool seg_first = (i == 0) || (c == 0);
@@ -249,16 +259,19 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
             wait_bounded(&acc_empty[abuf], ((seg >> 1) & 1u) ^ 1u);
             tc_fence_after();
           }
-          const int as = i % kASlots;
-          wait_bounded(&a_full[as], (i / kASlots) & 1u);
+          const int as = i % TM::kSlots;
+          wait_bounded(&a_full[as], (i / TM::kSlots) & 1u);
           tc_fence_after();
           int bsl = c - c_first;
           if (bsl < 0) bsl += KT;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint64_t bd = umma_desc_kmajor(b_base + (bsl * 8 + 2 * j) * NTOK * 16, NTOK * 16, 128);
-            umma_mxf8_ts(tbase + abuf * kAccCols, tbase + kACol + as * 32 + j * 8, bd, idesc | (uint32_t(j) << 29),
-                         tbase + kSfaCol + as * 4, tbase + kSfbCol, (seg_first && j == 0) ? 0u : 1u);
+            const uint32_t slot_addr = b_base + bsl * NTOK * 128;
+            const uint64_t bd = p.b_layout == 0 ? umma_desc_kmajor_sw128(slot_addr + 32 * j)
+                                                : umma_desc_kmajor(slot_addr + 2 * j * NTOK * 16, NTOK * 16, 128);
+            umma_mxf8_ts(tbase + TM::kAcc + abuf * TM::kAccStride, tbase + TM::kA + as * 32 + j * 8, bd,
+                         idesc | (uint32_t(j) << 29), tbase + TM::kSfa + as * 4, tbase + TM::kSfb,
+                         (seg_first && j == 0) ? 0u : 1u);
           }
           umma_commit(&a_empty[as]);
           if (c == KT - 1 || i == n_units - 1) {
@@ -275,30 +288,56 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
       const uint32_t codes_base = smem_u32(codes_s);
       const int gk = p.K / 32;
-      // scale word and codebook of this row for unit (t, c) (loaded one of
-      // this group's units ahead)
-      auto unit_inputs = [&](bool valid, int t, int c, uint32_t& sw, uint2& cb) {
-        sw = 0x7F7F7F7Fu;
-        cb = make_uint2(0, 0);
-        const int n = t * kRows + r;
-        if (valid && n < p.N) {
-          sw = __ldg(reinterpret_cast<const uint32_t*>(p.scales + static_cast<size_t>(n) * gk + 4 * c));
-          cb = __ldg(reinterpret_cast<const uint2*>(p.codebooks + static_cast<size_t>(n) * 8));
-        }
+      // Scale word and codebook of this row for a unit: pulled into L1 two of
+      // this group's units ahead (no register waits on the prefetch), then
+      // loaded at the top of the unit's iteration and first used after its
+      // decode.  Rows past N: 2^0 and an all-zero codebook.
+      auto scale_ptr = [&](int t, int c) {
+        return reinterpret_cast<const uint32_t*>(p.scales + static_cast<size_t>(t * kRows + r) * gk + 4 * c);
       };
+      auto cb_ptr = [&](int t) { return reinterpret_cast<const uint2*>(p.codebooks + static_cast<size_t>(t * kRows + r) * 8); };
       int tu = t_first, cu = c_first;                   // this group's unit in the current stage
       geo.advance(tu, cu, g);
-      int tn = tu, cn = cu;                             // and in the next stage
-      geo.advance(tn, cn, kDecGroups);
-      uint32_t sw_next;
-      uint2 cb_next;
-      unit_inputs(g < n_units, tu, cu, sw_next, cb_next);
+      int tn = tu, cn = cu;                             // and two stages ahead
+      geo.advance(tn, cn, 2 * kDecGroups);
+      if (tu * kRows + r < p.N && g < n_units) {
+        prefetch_l1(scale_ptr(tu, cu));
+        prefetch_l1(cb_ptr(tu));
+      }
+      {
+        int t1 = tu, c1 = cu;
+        geo.advance(t1, c1, kDecGroups);
+        if (t1 * kRows + r < p.N && g + kDecGroups < n_units) {
+          prefetch_l1(scale_ptr(t1, c1));
+          prefetch_l1(cb_ptr(t1));
+        }
+      }
+      // The TMEM stores of a unit complete while the next unit is loaded and
+      // decoded; only then does the warp wait for them and publish the unit.
+      int pending = -1;                                 // A slot stored, not yet published
+      auto publish = [&]() {
+        if (pending >= 0) {
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[pending]);
+          pending = -1;
+        }
+      };
       for (int j = 0; j < n_stages; ++j) {
         const int i = j * kUnitsPerStage + g;
         const int slot = j % NS;
-        const uint32_t sw = sw_next;
-        const uint2 cb = cb_next;
-        unit_inputs(i + kDecGroups < n_units, tn, cn, sw_next, cb_next);
+        const bool row_ok = i < n_units && tu * kRows + r < p.N;
+        uint32_t sw = 0x7F7F7F7Fu;
+        uint2 cb = make_uint2(0, 0);
+        if (row_ok) {
+          sw = __ldg(scale_ptr(tu, cu));
+          cb = __ldg(cb_ptr(tu));
+        }
+        if (i + 2 * kDecGroups < n_units && tn * kRows + r < p.N) {
+          prefetch_l1(scale_ptr(tn, cn));
+          prefetch_l1(cb_ptr(tn));
+        }
         // every decoder warp waits for every stage before releasing it, so an
         // early release can never count towards an older phase
         wait_bounded(&full[slot], (j / NS) & 1u);
@@ -322,8 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
-        tu = tn;
-        cu = cn;
+        geo.advance(tu, cu, kDecGroups);
         geo.advance(tn, cn, kDecGroups);
         if (has) {
           uint32_t v[32];
@@ -331,24 +369,30 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
           decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, v + 16);
           decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, v + 24);
-          const int as = i % kASlots;
-          wait_bounded(&a_empty[as], ((i / kASlots) & 1u) ^ 1u);
+          publish();
+          const int as = i % TM::kSlots;
+          wait_bounded(&a_empty[as], ((i / TM::kSlots) & 1u) ^ 1u);
           tc_fence_after();
-          tmem_st_x32(tbase + lane_addr + kACol + as * 32, v);
+          tmem_st_x32(tbase + lane_addr + TM::kA + as * 32, v);
           // A scale of row m: TMEM lane m, column base + m / 32, byte = a_sf_id
-          tmem_st_x1(tbase + lane_addr + kSfaCol + as * 4 + q, sw);
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[as]);
+          tmem_st_x1(tbase + lane_addr + TM::kSfa + as * 4 + q, sw);
+          pending = as;
         }
       }
+      publish();
     } else {
       // ------------------------------------------------------------ epilogue --
       const int q = warp & 3;
       const int r = 32 * q + lane;
       const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
       const bool leader = tid == kEpiWarp0 * 32;
+      // scale factors of B: 2^0 in every byte of 8 columns, all 128 lanes
+      for (int cc = 0; cc < 8; cc += 4)
+        tmem_st_x4(tbase + lane_addr + TM::kSfb + cc, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      tmem_st_wait();
+      tc_fence_before();
+      named_bar_sync(3, 160);
+      grid_dependency_wait();                           // y and the scratch may still be in use
       int seg = 0, t = t_first, c = c_first, seg_c = c_first;   // seg_c: k-tile the segment starts at
       for (int i = 0; i < n_units; ++i, geo.advance(t, c, 1)) {
         if (c != KT - 1 && i != n_units - 1) continue;
@@ -356,50 +400,78 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         const int n = t * kRows + r;
         const bool ok = n < p.N;
         const int abuf = seg & 1;
+        const uint32_t acc_addr = tbase + lane_addr + TM::kAcc + abuf * TM::kAccStride;
         wait_bounded(&acc_full[abuf], (seg >> 1) & 1u);
         tc_fence_after();
-        float* part = p.partial + (static_cast<size_t>(2 * blockIdx.x + (seg > 0 ? 1 : 0)) * kRows + r) * NTOK;
+        if (complete) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < NTOK; c0 += 16) {
-          uint32_t tv[16];
-          tmem_ld_x16(tbase + lane_addr + abuf * kAccCols + c0, tv);
-          tmem_ld_wait();
-          if (complete) {
+          for (int c0 = 0; c0 < NTOK; c0 += 16) {
+            uint32_t tv[16];
+            tmem_ld_x16(acc_addr + c0, tv);
+            tmem_ld_wait();
             if (ok) {
 #pragma unroll
               for (int k = 0; k < 16; ++k)
                 if (c0 + k < p.M)
                   p.y[static_cast<size_t>(c0 + k) * p.N + n] = __uint_as_float(tv[k]) * __ldg(p.a_scale + c0 + k);
             }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(part + c0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              dst[k] = make_float4(__uint_as_float(tv[4 * k]), __uint_as_float(tv[4 * k + 1]),
-                                   __uint_as_float(tv[4 * k + 2]), __uint_as_float(tv[4 * k + 3]));
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[abuf]);
-        if (!complete) {
-          // partial tile: publish, count, and the last part sums them all
+        } else {
+          // Partial tile.  Each part's fp32 tile goes to its scratch slot and
+          // bumps the tile's counter; the part that finds every other part
+          // published sums all parts in part order and writes y.  A CTA's
+          // last segment usually arrives after the other parts (first segments
+          // of later CTAs, finished early), so it first just reads the counter.
           const long long tu = static_cast<long long>(t) * KT;
           const long long b_first = geo.owner(tu);
           const int nparts = static_cast<int>(geo.owner(tu + KT - 1) - b_first + 1);
-          __threadfence();
-          named_bar_sync(2, 128);
-          if (leader) *last_flag = atomicAdd(p.counters + t, 1u) == static_cast<unsigned>(nparts - 1);
-          named_bar_sync(2, 128);
-          if (*last_flag) {
+          const int pme = static_cast<int>(blockIdx.x - b_first);
+          bool own_published = false, last = false;
+          if (i == n_units - 1) {                         // this CTA's last segment
+            if (leader) *last_flag = ld_acquire_gpu(p.counters + t) == static_cast<unsigned>(nparts - 1);
+            named_bar_sync(2, 128);
+            last = *last_flag;
+            named_bar_sync(2, 128);
+          }
+          if (!last) {
+            float* part = p.partial + (static_cast<size_t>(2 * blockIdx.x + (seg > 0 ? 1 : 0)) * kRows + r) * NTOK;
+#pragma unroll 1
+            for (int c0 = 0; c0 < NTOK; c0 += 16) {
+              uint32_t tv[16];
+              tmem_ld_x16(acc_addr + c0, tv);
+              tmem_ld_wait();
+              float4* dst = reinterpret_cast<float4*>(part + c0);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                dst[k] = make_float4(__uint_as_float(tv[4 * k]), __uint_as_float(tv[4 * k + 1]),
+                                     __uint_as_float(tv[4 * k + 2]), __uint_as_float(tv[4 * k + 3]));
+            }
+            own_published = true;
+            __threadfence();
+            named_bar_sync(2, 128);
+            if (leader) *last_flag = atomicAdd(p.counters + t, 1u) == static_cast<unsigned>(nparts - 1);
+            named_bar_sync(2, 128);
+            last = *last_flag;
+          }
+          if (last) {
             __threadfence();
 #pragma unroll 1
             for (int c0 = 0; c0 < NTOK; c0 += 16) {
+              uint32_t tv[16];
+              if (!own_published) {
+                tmem_ld_x16(acc_addr + c0, tv);
+                tmem_ld_wait();
+              }
               float acc[16];
 #pragma unroll
               for (int k = 0; k < 16; ++k) acc[k] = 0.f;
 #pragma unroll 1
               for (int pi = 0; pi < nparts; ++pi) {
+                if (pi == pme && !own_published) {
+#pragma unroll
+                  for (int k = 0; k < 16; ++k) acc[k] += __uint_as_float(tv[k]);
+                  continue;
+                }
                 // part 0's CTA reaches this tile as its last segment if its
                 // share started in an earlier tile; every later part as its first
                 const long long b = b_first + pi;
@@ -423,8 +495,11 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
             }
             if (leader) p.counters[t] = 0u;              // ready for the next call
           }
-          named_bar_sync(2, 128);
+          named_bar_sync(2, 128);                        // last_flag is reused by the next segment
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[abuf]);
         seg_c = c + 1 == KT ? 0 : c + 1;
         ++seg;
       }
@@ -524,9 +599,52 @@ int launch_t(const SkParams& p, const Plan& pl, cudaStream_t stream) {
   auto kern = sk_kernel<NTOK>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem) != cudaSuccess)
     return CBQ_ECUDA;
-  kern<<<pl.grid, kThreads, pl.smem, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
   note_launch();
-  return cudaGetLastError() == cudaSuccess ? CBQ_OK : CBQ_ECUDA;
+  return e == cudaSuccess ? CBQ_OK : CBQ_ECUDA;
+}
+
+// Activations a[M][K] as a TMA tensor whose box is one k-tile of `ntok`
+// token rows: a 2-D view with a (128 B, ntok) box and the 128-byte swizzle;
+// rows past M read as zeros.  If the driver refuses it, a 3-D view (16 bytes,
+// M rows of stride K, K/16 chunks of stride 16) with a (16, ntok, 8) box that
+// lands in the unswizzled core-matrix layout.
+int encode_a_map(SkParams& p, int ntok) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return CBQ_ECUDA;
+  void* base = const_cast<uint8_t*>(p.a);
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K)};
+    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(ntok)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&p.a_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+      p.b_layout = 0;
+      return CBQ_OK;
+    }
+  }
+  const cuuint64_t dims[3] = {16, static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(p.K / 16)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.K), 16};
+  const cuuint32_t box[3] = {16, static_cast<cuuint32_t>(ntok), 8};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&p.a_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return CBQ_ECUDA;
+  p.b_layout = 1;
+  return CBQ_OK;
 }
 
 }  // namespace
@@ -547,6 +665,8 @@ int launch_sk(const SkParams& p_in, cudaStream_t stream) {
   p.counters = sc.counters;
   p.stages = pl.stages;
   p.b_ktiles = pl.b_ktiles;
+  const int em = encode_a_map(p, pl.ntok);
+  if (em != CBQ_OK) return em;
   if (pl.ntok == 16) return launch_t<16>(p, pl, stream);
   if (pl.ntok == 32) return launch_t<32>(p, pl, stream);
   return launch_t<64>(p, pl, stream);

@@ -24,7 +24,7 @@ PATH_AUTO, PATH_GEMV, PATH_MMA, PATH_STREAMK = 0, 1, 2, 3
 OK, EINVAL, ECUDA, EDEVICE, ETIMEOUT, EROUTING = 0, -1, -2, -3, -4, -5
 
 # Every symbol include/cbq.h declares.
-EXPORTS = ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path",
+EXPORTS = ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path", "cbq_gemm_auto_path",
            "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_launch_count",
            "cbq_status_str")
 
@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
         L.cbq_unpack.argtypes = [ctypes.POINTER(_Weight), i32, i32, vp, vp]
         L.cbq_gemm.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp]
         L.cbq_gemm_path.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp, i32]
+        L.cbq_gemm_auto_path.argtypes = [i32, i32, i32]
         L.cbq_grouped_gemm.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, vp, i32, i32, i32,
                                        i32, vp, vp]
         L.cbq_grouped_gemm_path.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, vp, i32, i32,
@@ -68,11 +69,18 @@ def lib() -> ctypes.CDLL:
         L.cbq_launch_count.restype = ctypes.c_uint64
         L.cbq_status_str.argtypes = [ctypes.c_int]
         L.cbq_status_str.restype = ctypes.c_char_p
-        for name in ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path",
+        for name in ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path", "cbq_gemm_auto_path",
                      "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
         return L
+
+
+def auto_path(M: int, N: int, K: int) -> int:
+    """The kernel cbq_gemm picks for an M x N x K call (PATH_GEMV/_MMA/_STREAMK)."""
+    p = lib().cbq_gemm_auto_path(M, N, K)
+    _check(p if p < 0 else OK, "cbq_gemm_auto_path")
+    return p
 
 
 def status_str(status: int) -> str:

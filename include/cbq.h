@@ -55,10 +55,8 @@ extern "C" {
                                 token listing one expert twice was seen */
 
 /* Which kernel cbq_gemm_path / cbq_grouped_gemm_path runs. */
-#define CBQ_PATH_AUTO 0      /* dense: stream-K kernel when its resident
-                                activations fit in shared memory, else the
-                                tcgen05 tile kernel when its do, else GEMV;
-                                grouped: M <= 4 GEMV, else the tile kernel */
+#define CBQ_PATH_AUTO 0      /* dense: see cbq_gemm_auto_path; grouped:
+                                M <= 4 GEMV, else the tile kernel */
 #define CBQ_PATH_GEMV 1      /* register-decode + warp MMA kernel, any M <= 64 */
 #define CBQ_PATH_MMA 2       /* tcgen05 block-scaled FP8 tile kernel (K split
                                 over a cluster), any M <= 64 */
@@ -116,10 +114,21 @@ int cbq_unpack(const cbq_weight_t *w, int32_t N, int32_t K, float *W_out,
  * writes y = 0).  Picks the kernel as CBQ_PATH_AUTO says; one launch (plus
  * a scratch allocation and zeroing on the stream's first stream-K call).
  * The result is deterministic: a tile shared by several SMs is summed in a
- * fixed order.
+ * fixed order.  The stream-K kernel is launched as a programmatic dependent
+ * of the previous kernel on `stream`: it may start streaming the packed
+ * weights before that kernel has finished (a, a_scale and y are touched only
+ * after it has), so the weights must not be written by the kernel launched
+ * just before it on the same stream (copies and host writes are fine).
  * Errors: CBQ_EINVAL, CBQ_EDEVICE, CBQ_ECUDA. */
 int cbq_gemm(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
              int32_t M, int32_t N, int32_t K, float *y, void *stream);
+
+/* The kernel (CBQ_PATH_GEMV / _MMA / _STREAMK) that cbq_gemm picks for an
+ * M x N x K call, chosen by measured speed on GB300; CBQ_EINVAL for sizes
+ * cbq_gemm rejects.  (If the tile kernel's activations do not fit in shared
+ * memory, cbq_gemm then runs the GEMV kernel instead of CBQ_PATH_MMA.)
+ * Host only: no device access. */
+int cbq_gemm_auto_path(int32_t M, int32_t N, int32_t K);
 
 /* Same as cbq_gemm with an explicit kernel choice (CBQ_PATH_*); used by the
  * tests and the benchmark to exercise each kernel at every M. */

@@ -126,3 +126,13 @@ def test_missing_library_fails_loudly():
                        cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     assert r.returncode == 0, r.stderr
     assert "raised -2" in r.stdout
+
+
+def test_auto_path_choice(L):
+    # host-only decision table of cbq_gemm (no device access)
+    assert L.cbq_gemm_auto_path(1, 12288, 4096) == ops.PATH_GEMV
+    assert L.cbq_gemm_auto_path(8, 12288, 4096) == ops.PATH_GEMV
+    assert L.cbq_gemm_auto_path(1, 151936, 2048) == ops.PATH_MMA
+    assert L.cbq_gemm_auto_path(0, 16, 128) == ops.EINVAL
+    assert L.cbq_gemm_auto_path(4, 16, 100) == ops.EINVAL
+    assert L.cbq_gemm_auto_path(65, 16, 128) == ops.EINVAL
