@@ -61,13 +61,31 @@ constexpr int kStageBytes = kUnitsPerStage * kRows * 48;   // 24 KB
 constexpr int kMaxStages = 8;
 constexpr int kMaxASlots = 16;                        // decoded units in TMEM (see TmemMap)
 constexpr int kDecGroups = 4;
-constexpr int kDecWarps = 4 * kDecGroups;
-constexpr int kEpiWarp0 = 2 + kDecWarps;
-constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+// Warp roles.  A warp's sub-partition (SMSP) is warp % 4, and a warp may only
+// touch the TMEM lanes of quadrant warp % 4.  Sub-partition 1 hosts the MMA
+// issuer, so it gets no decode work: the rows of quadrant 1 are decoded by
+// three helper warps on sub-partitions 0, 2, 3 into a shared-memory staging
+// ring, and one light warp on sub-partition 1 moves them into TMEM.
+//   warps 0..15 with warp % 4 != 1: decoders of their own quadrant, group
+//     warp / 4 (12 warps); warp 1: TMEM allocation + MMA issuer; warp 5:
+//     bulk producer; warp 9: quadrant-1 storer; warps 16..19: epilogue of
+//     quadrants 0..3; warps 20, 22, 23: quadrant-1 helpers; 13, 21: idle.
+constexpr int kMmaWarp = 1;
+constexpr int kProdWarp = 5;
+constexpr int kStoreWarp = 9;
+constexpr int kEpiWarp0 = 16;
+constexpr int kNumWarps = 24;
+constexpr int kThreads = kNumWarps * 32;
+constexpr int kOwnDecWarps = 12;                      // decoders of quadrants 0, 2, 3
+constexpr int kHelpers = 3;
+constexpr int kStageArrivals = kOwnDecWarps + kHelpers;
+constexpr int kStgEntries = 6;                        // quadrant-1 staging ring
+constexpr int kStgBytes = 32 * 128 + 32 * 4 + 128;    // 32 rows x 128 B, 32 scale words, pad
+__device__ __forceinline__ int helper_index(int warp) { return warp == 20 ? 0 : warp == 22 ? 1 : warp == 23 ? 2 : -1; }
 constexpr int kTmemCols = 512;
 constexpr int kMaxSmem = 232448;
 constexpr int kMinSmem = 120 * 1024;                  // one CTA per SM: it owns all of TMEM
-constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxASlots + 5;
+constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxASlots + 5 + 2 * kStgEntries;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
 
 // Tensor-memory columns for NTOK token columns: two fp32 accumulators of NTOK
@@ -151,7 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   const int NS = p.stages;
   uint8_t* codes_s = smem;
   uint8_t* b_s = smem + NS * kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(b_s + p.b_ktiles * NTOK * 128);
+  uint8_t* stg_s = b_s + p.b_ktiles * NTOK * 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_s + kStgEntries * kStgBytes);
   uint64_t* full = bars;
   uint64_t* empty = full + kMaxStages;
   uint64_t* a_full = empty + kMaxStages;
@@ -159,7 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   uint64_t* acc_full = a_empty + kMaxASlots;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* b_full = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 1);
+  uint64_t* stg_full = b_full + 1;
+  uint64_t* stg_empty = stg_full + kStgEntries;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stg_empty + kStgEntries);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -178,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kDecWarps);                 // every decoder warp, once per stage
+      mbar_init(&empty[i], kStageArrivals);            // every decoder and helper warp, once per stage
     }
     for (int i = 0; i < kMaxASlots; ++i) {
       mbar_init(&a_full[i], 4);
@@ -189,6 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       mbar_init(&acc_empty[i], 4);
     }
     mbar_init(b_full, 1);
+    for (int i = 0; i < kStgEntries; ++i) {
+      mbar_init(&stg_full[i], 1);
+      mbar_init(&stg_empty[i], 1);
+    }
     fence_barrier_init();
   }
   __syncthreads();
@@ -198,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   grid_launch_dependents();
 
   uint32_t tbase = 0;
-  if (warp == 0) {
+  if (warp == kProdWarp) {
     // -------------------------------------------------------- bulk producer --
     if (lane == 0) {
       int ta = t_first, ca = c_first;                 // first unit of stage j
@@ -219,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     }
     __syncwarp();
   } else {
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
       tmem_alloc(tmem_slot, kTmemCols);
       tmem_relinquish();
     }
@@ -228,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     tc_fence_after();
     tbase = *tmem_slot;
 
-    if (warp == 1) {
+    const int helper = helper_index(warp);
+    if (warp == kMmaWarp) {
       // --------------------------------------------------------- MMA issuer --
       named_bar_sync(3, 160);                          // B scale factors are in TMEM
       tc_fence_after();
@@ -281,9 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         }
       }
       __syncwarp();
-    } else if (warp < kEpiWarp0) {
-      // ------------------------------------------------------------ decoders --
-      const int g = (warp - 2) >> 2, q = warp & 3;
+    } else if (warp < kEpiWarp0 && (warp & 3) != 1) {
+      // ---------------------------------------------- decoders (own quadrant) --
+      const int g = warp >> 2, q = warp & 3;
       const int r = 32 * q + lane;                      // row inside the tile == TMEM lane
       const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
       const uint32_t codes_base = smem_u32(codes_s);
@@ -380,7 +406,92 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         }
       }
       publish();
-    } else {
+    } else if (helper >= 0) {
+      // ---------------------------------- quadrant-1 helpers: decode to smem --
+      // Helper h decodes rows 32..63 of the units i with i % 3 == h into the
+      // staging ring (entry i % kStgEntries): row lane's 128 E4M3 bytes as 8
+      // chunks of 16, chunk x of lane l at (x ^ (l & 7)) * 16 (conflict-free),
+      // then the row's scale word.
+      const int r = 32 + lane;
+      const uint32_t codes_base = smem_u32(codes_s);
+      const int gk = p.K / 32;
+      int ta = t_first, ca = c_first;                   // first unit of stage j
+      for (int j = 0; j < n_stages; ++j) {
+        const int slot = j % NS;
+        wait_bounded(&full[slot], (j / NS) & 1u);
+        int tk = ta, ck = ca, rel = 0;                  // unit k of the stage, its offset
+        for (int k = 0; k < kUnitsPerStage; ++k) {
+          const int i = j * kUnitsPerStage + k;
+          if (i >= n_units) break;
+          const int rows = geo.rows(tk);
+          if (i % kHelpers == helper) {
+            const int e = i % kStgEntries;
+            uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, c2 = c0;
+            if (r < rows) {
+              const uint32_t at = codes_base + slot * kStageBytes + rel + r * 48;
+              c0 = lds128(at);
+              c1 = lds128(at + 16);
+              c2 = lds128(at + 32);
+            }
+            const int n = tk * kRows + r;
+            uint32_t sw = 0x7F7F7F7Fu;
+            uint2 cb = make_uint2(0, 0);
+            if (n < p.N) {
+              sw = __ldg(reinterpret_cast<const uint32_t*>(p.scales + static_cast<size_t>(n) * gk + 4 * ck));
+              cb = __ldg(reinterpret_cast<const uint2*>(p.codebooks + static_cast<size_t>(n) * 8));
+            }
+            uint32_t v[32];
+            decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
+            decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
+            decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, v + 16);
+            decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, v + 24);
+            wait_bounded(&stg_empty[e], ((i / kStgEntries) & 1u) ^ 1u);
+            uint8_t* ent = stg_s + e * kStgBytes;
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              *reinterpret_cast<uint4*>(ent + lane * 128 + ((x ^ (lane & 7)) * 16)) =
+                  make_uint4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+            reinterpret_cast<uint32_t*>(ent + 32 * 128)[lane] = sw;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&stg_full[e]);
+          }
+          rel += rows * 48;
+          geo.advance(tk, ck, 1);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        geo.advance(ta, ca, kUnitsPerStage);
+      }
+    } else if (warp == kStoreWarp) {
+      // ------------------------------------- quadrant-1 storer: smem -> TMEM --
+      const uint32_t lane_addr = 32u << 16;
+      for (int i = 0; i < n_units; ++i) {
+        const int e = i % kStgEntries;
+        wait_bounded(&stg_full[e], (i / kStgEntries) & 1u);
+        const uint8_t* ent = stg_s + e * kStgBytes;
+        uint32_t v[32];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          const uint4 w = *reinterpret_cast<const uint4*>(ent + lane * 128 + ((x ^ (lane & 7)) * 16));
+          v[4 * x] = w.x;
+          v[4 * x + 1] = w.y;
+          v[4 * x + 2] = w.z;
+          v[4 * x + 3] = w.w;
+        }
+        const uint32_t sw = reinterpret_cast<const uint32_t*>(ent + 32 * 128)[lane];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&stg_empty[e]);
+        const int as = i % TM::kSlots;
+        wait_bounded(&a_empty[as], ((i / TM::kSlots) & 1u) ^ 1u);
+        tc_fence_after();
+        tmem_st_x32(tbase + lane_addr + TM::kA + as * 32, v);
+        tmem_st_x1(tbase + lane_addr + TM::kSfa + as * 4 + 1, sw);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[as]);
+      }
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
       // ------------------------------------------------------------ epilogue --
       const int q = warp & 3;
       const int r = 32 * q + lane;
@@ -532,10 +643,10 @@ bool plan_for(int M, int N, int K, Plan& pl) {
   pl.ntok = ntok_for(M);
   pl.b_ktiles = static_cast<int>(std::min<long long>(KT, per));
   const int b_bytes = pl.b_ktiles * pl.ntok * 128;
-  const int room = kMaxSmem - b_bytes - kBarBytes;
+  const int room = kMaxSmem - b_bytes - kStgEntries * kStgBytes - kBarBytes;
   pl.stages = std::min(kMaxStages, room / kStageBytes);
   if (pl.stages < 3) return false;
-  pl.smem = std::max(pl.stages * kStageBytes + b_bytes + kBarBytes, kMinSmem);
+  pl.smem = std::max(pl.stages * kStageBytes + b_bytes + kStgEntries * kStgBytes + kBarBytes, kMinSmem);
   pl.grid = static_cast<int>(G);
   pl.tiles = static_cast<int>(tiles);
   return true;
