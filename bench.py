@@ -261,6 +261,10 @@ def run_ours(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):
+            # untimed primer: keeps the GPU busy while the host enqueues the
+            # timed replays, so the first one does not include host launch
+            # latency (its weight copies are not the first timed graph's)
+            graphs[MS[-1]].replay()
             t0.record(stream)
             for rep in range(reps):
                 for M in MS:
