@@ -198,6 +198,29 @@ int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w,
   return launch_gemv(g, false, s);
 }
 
+int cbq_gemm_noalloc(const uint8_t* a, const float* a_scale, const cbq_weight_t* w, int32_t M,
+                     int32_t N, int32_t K, float* y, void* stream) {
+  if (M < 0 || M > 64 || N < 0 || K < 0 || K % 128 != 0) return CBQ_EINVAL;
+  if (M == 0 || N == 0) return CBQ_OK;
+  if (K == 0 || !sk_applicable(M, N, K)) return CBQ_EINVAL;
+  if (!y || !aligned(y, 4) || !a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(w))
+    return CBQ_EINVAL;
+  int st = current_device_checked(nullptr);
+  if (st != CBQ_OK) return st;
+  SkParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.codes = w->codes;
+  p.a = a;
+  p.a_scale = a_scale;
+  p.scales = w->scales;
+  p.codebooks = w->codebooks;
+  p.y = y;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  return launch_sk_static(p, static_cast<cudaStream_t>(stream));
+}
+
 int cbq_gemm(const uint8_t* a, const float* a_scale, const cbq_weight_t* w, int32_t M, int32_t N,
              int32_t K, float* y, void* stream) {
   return cbq_gemm_path(a, a_scale, w, M, N, K, y, stream, CBQ_PATH_AUTO);

@@ -78,6 +78,7 @@ unsigned take_status_umma(cudaStream_t stream);
 
 bool sk_applicable(int M, int N, int K);
 int launch_sk(const SkParams& p, cudaStream_t stream);
+int launch_sk_static(const SkParams& p, cudaStream_t stream);
 unsigned take_status_sk(cudaStream_t stream);
 
 // Host quantiser (cbq_pack.cpp).

@@ -765,15 +765,12 @@ bool sk_applicable(int M, int N, int K) {
   return plan_for(M, N, K, pl);
 }
 
-int launch_sk(const SkParams& p_in, cudaStream_t stream) {
-  Plan pl;
-  if (!plan_for(p_in.M, p_in.N, p_in.K, pl)) return CBQ_EINVAL;
-  Scratch sc;
-  const int st = scratch_for(stream, size_t(2) * pl.grid * kRows * pl.ntok, size_t(pl.tiles), sc);
-  if (st != CBQ_OK) return st;
+namespace {
+
+int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigned* counters, cudaStream_t stream) {
   SkParams p = p_in;
-  p.partial = sc.partial;
-  p.counters = sc.counters;
+  p.partial = partial;
+  p.counters = counters;
   p.stages = pl.stages;
   p.b_ktiles = pl.b_ktiles;
   const int em = encode_a_map(p, pl.ntok);
@@ -781,6 +778,57 @@ int launch_sk(const SkParams& p_in, cudaStream_t stream) {
   if (pl.ntok == 16) return launch_t<16>(p, pl, stream);
   if (pl.ntok == 32) return launch_t<32>(p, pl, stream);
   return launch_t<64>(p, pl, stream);
+}
+
+// Static scratch of the allocation-free entry point: partial tiles for up to
+// kStaticCtas CTAs at 64 token columns, and counters for kStaticTiles tiles.
+// Zero at module load; each kernel returns the counters it used to zero.
+constexpr int kStaticCtas = 160;
+constexpr int kStaticTiles = 1 << 16;
+__device__ __align__(256) float g_static_partial[2 * kStaticCtas * kRows * 64];
+__device__ __align__(256) unsigned g_static_counters[kStaticTiles];
+
+}  // namespace
+
+int launch_sk(const SkParams& p_in, cudaStream_t stream) {
+  Plan pl;
+  if (!plan_for(p_in.M, p_in.N, p_in.K, pl)) return CBQ_EINVAL;
+  Scratch sc;
+  const int st = scratch_for(stream, size_t(2) * pl.grid * kRows * pl.ntok, size_t(pl.tiles), sc);
+  if (st != CBQ_OK) return st;
+  return launch_planned(p_in, pl, sc.partial, sc.counters, stream);
+}
+
+int launch_sk_static(const SkParams& p_in, cudaStream_t stream) {
+  Plan pl;
+  if (!plan_for(p_in.M, p_in.N, p_in.K, pl)) return CBQ_EINVAL;
+  if (pl.grid > kStaticCtas || pl.tiles > kStaticTiles) return CBQ_EINVAL;
+  // the static buffers' addresses on the current device
+  static std::mutex mu;
+  static void* partial_at[64] = {};
+  static void* counters_at[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CBQ_EDEVICE;
+  void *partial = nullptr, *counters = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!partial_at[dev] || !counters_at[dev]) {
+      void *a = nullptr, *b = nullptr;
+      if (cudaGetSymbolAddress(&a, g_static_partial) != cudaSuccess ||
+          cudaGetSymbolAddress(&b, g_static_counters) != cudaSuccess) {
+        cudaGetLastError();
+        return CBQ_ECUDA;
+      }
+      partial_at[dev] = a;
+      counters_at[dev] = b;
+    }
+    partial = partial_at[dev];
+    counters = counters_at[dev];
+  }
+  // the counters of the tiles this call uses start at zero even if an
+  // earlier call gave up part-way
+  if (cudaMemsetAsync(counters, 0, sizeof(unsigned) * pl.tiles, stream) != cudaSuccess) return CBQ_ECUDA;
+  return launch_planned(p_in, pl, static_cast<float*>(partial), static_cast<unsigned*>(counters), stream);
 }
 
 unsigned take_status_sk(cudaStream_t stream) {

@@ -25,6 +25,7 @@ OK, EINVAL, ECUDA, EDEVICE, ETIMEOUT, EROUTING = 0, -1, -2, -3, -4, -5
 
 # Every symbol include/cbq.h declares.
 EXPORTS = ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path", "cbq_gemm_auto_path",
+           "cbq_gemm_noalloc",
            "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_launch_count",
            "cbq_status_str")
 
@@ -60,6 +61,7 @@ def lib() -> ctypes.CDLL:
         L.cbq_gemm.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp]
         L.cbq_gemm_path.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp, i32]
         L.cbq_gemm_auto_path.argtypes = [i32, i32, i32]
+        L.cbq_gemm_noalloc.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp]
         L.cbq_grouped_gemm.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, vp, i32, i32, i32,
                                        i32, vp, vp]
         L.cbq_grouped_gemm_path.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, vp, i32, i32,
@@ -70,6 +72,7 @@ def lib() -> ctypes.CDLL:
         L.cbq_status_str.argtypes = [ctypes.c_int]
         L.cbq_status_str.restype = ctypes.c_char_p
         for name in ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path", "cbq_gemm_auto_path",
+                     "cbq_gemm_noalloc",
                      "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -161,6 +164,16 @@ def gemm(a: torch.Tensor, a_scale: torch.Tensor, w: PackedWeights,
     ws = w.struct()
     _check(lib().cbq_gemm_path(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(ws), M, w.N, w.K,
                                out.data_ptr(), _stream(stream), path), "cbq_gemm")
+    return out
+
+
+def gemm_noalloc(a: torch.Tensor, a_scale: torch.Tensor, w: PackedWeights,
+                 out: torch.Tensor, stream=None) -> torch.Tensor:
+    """cbq_gemm_noalloc: the stream-K matmul on the library's static scratch
+    (no allocation; concurrent calls on one device race)."""
+    ws = w.struct()
+    _check(lib().cbq_gemm_noalloc(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(ws), a.shape[0], w.N,
+                                  w.K, out.data_ptr(), _stream(stream)), "cbq_gemm_noalloc")
     return out
 
 

@@ -136,6 +136,22 @@ int cbq_gemm_path(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
                   int32_t M, int32_t N, int32_t K, float *y, void *stream,
                   int32_t path);
 
+/* The stream-K matmul of cbq_gemm (CBQ_PATH_STREAMK) with no allocation at
+ * all: its scratch (fp32 partial tiles and per-tile arrival counters) is a
+ * fixed static device buffer of the library (10.5 MB of partials for up to
+ * 160 SMs at 64 token columns, 65536 tile counters, i.e. N <= 8388608), so
+ * the call works where the caller forbids allocations.  The pages have no
+ * counterpart: this is a deployment variant of the same kernel.
+ * Each call first clears the counters of the tiles it uses (one
+ * cudaMemsetAsync on `stream`, no allocation), then launches the kernel.
+ * The buffer is shared by every caller on the device: two calls that may run
+ * at the same time (different streams, overlapping graph replays) race on it
+ * and give wrong results; serialise them.
+ * Errors: CBQ_EINVAL (bad argument, K == 0, or a problem the stream-K kernel
+ * or the static buffer cannot take), CBQ_EDEVICE, CBQ_ECUDA. */
+int cbq_gemm_noalloc(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
+                     int32_t M, int32_t N, int32_t K, float *y, void *stream);
+
 /* Mixture-of-experts verify round ("Adaptive speculation / Expert sharing"):
  * the E experts' packed matrices are stacked (expert e: codes from byte
  * e*3KN/8, scales and codebooks from row e*N), topk_idx is DEVICE int32
