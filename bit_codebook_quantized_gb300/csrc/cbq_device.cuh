@@ -321,6 +321,13 @@ __device__ __forceinline__ void umma_mxf8_ts(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// Copy a 128-row x 16-byte matrix from shared memory (described like an MMA
+// operand: 8-row x 16-byte core matrices, `sdesc`) into 4 TMEM columns of all
+// 128 lanes (row r -> lane r).  Asynchronous, in order with this thread's MMAs.
+__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

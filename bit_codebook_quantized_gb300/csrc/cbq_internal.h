@@ -55,6 +55,7 @@ struct SkParams {
   unsigned* counters;         // scratch: one arrival counter per 128-row tile, zero between calls
   int M, N, K;
   int stages;                 // depth of the code-stage ring
+  int a_slots;                // decoded-unit slots in shared memory
   int b_ktiles;               // k-tiles of resident activations
   int b_layout;               // 0: 128-byte swizzled rows, 1: core-matrix chunks (no swizzle)
 };

@@ -1,8 +1,7 @@
 // cbq_sk.cu -- stream-K kernel of the codebook-quantised matmul for dense
 // calls: every SM streams an equal, contiguous share of the packed weights,
-// decodes the 3-bit codes to E4M3 straight into tensor memory and multiplies
-// them with the block-scaled FP8 tensor cores (tcgen05), fp32 accumulators in
-// TMEM.
+// decodes the 3-bit codes to E4M3 in shared memory and multiplies them with
+// the block-scaled FP8 tensor cores (tcgen05), fp32 accumulators in TMEM.
 //
 // "Hibana: Fast Agentic Inference on Unified-Memory Devices", section "Model
 // surgery / Three-bit weights": codes look up an 8-entry FP8 codebook per
@@ -20,21 +19,24 @@
 // to scratch, the last one sums the parts in part order (deterministic) and
 // writes y.
 //
-// Roles (one CTA per SM, 704 threads):
-//  * warp 0 (one lane): 1-D bulk copies of 4 consecutive units (24 KB, one
-//    contiguous piece of the stream) into a ring of shared-memory stages;
-//  * warps 2..17: four decoder warpgroups, group g takes unit g of every
-//    stage; thread = weight row = TMEM lane.  A thread loads its row's 48
-//    code bytes (three 128-bit loads at a conflict-free 48-byte pitch),
-//    releases the stage, spreads the codes to nibbles and turns them into
-//    E4M3 bytes with byte-permutes through the row's codebook (two
-//    registers), writes the 128 bytes into its TMEM lane as the MMA's A
-//    operand (32 columns) and its 4 E8M0 group scales as the A scale factors;
-//  * warp 1 (one lane): 4 tcgen05.mma kind::mxf8f6f4.block_scale (K = 32)
-//    per unit, A from TMEM, B (the activations, resident in shared memory
-//    for the CTA's k-tiles) from a K-major descriptor; the E8M0 group scale
-//    is the MX block scale of its 32-wide K block;
-//  * warps 18..21: epilogue -- tcgen05.ld the accumulator (two alternate, one
+// Roles (one CTA per SM, 768 threads; a warp's sub-partition is warp % 4):
+//  * warp 5: 1-D bulk copies of 4 consecutive units (24 KB, one contiguous
+//    piece of the stream) into a ring of shared-memory stages;
+//  * 12 decoder warps, all on sub-partitions 0, 2, 3 (so the MMA issuer on
+//    sub-partition 1 has its issue slots to itself), in 3 groups of 4: group
+//    g decodes the units i = g mod 3, one warp per 32 rows; a thread (one
+//    row) loads its 48 code bytes, releases the stage,
+//    spreads the codes to nibbles and turns them into E4M3 bytes with
+//    byte-permutes through the row's codebook (two registers), and stores
+//    the 128 bytes into the unit's A slot in shared memory (K-major
+//    core-matrix layout, conflict-free 16-byte stores) with the row's 4 E8M0
+//    group scales beside them;
+//  * warp 1 (one lane): per unit one tcgen05.cp of the scales into TMEM and
+//    4 tcgen05.mma kind::mxf8f6f4.block_scale (K = 32) with A and B (the
+//    activations, resident in shared memory for the CTA's k-tiles, landed by
+//    TMA) from shared-memory descriptors; the E8M0 group scale is the MX
+//    block scale of its 32-wide K block;
+//  * warps 16..19: epilogue -- tcgen05.ld the accumulator (two alternate, one
 //    per tile segment), then either y = a_scale * acc or the partial-tile
 //    protocol above.
 #include <cuda.h>
@@ -59,50 +61,41 @@ constexpr int kRows = 128;                            // MMA M: weight rows per 
 constexpr int kUnitsPerStage = 4;
 constexpr int kStageBytes = kUnitsPerStage * kRows * 48;   // 24 KB
 constexpr int kMaxStages = 8;
-constexpr int kMaxASlots = 16;                        // decoded units in TMEM (see TmemMap)
-constexpr int kDecGroups = 4;
-// Warp roles.  A warp's sub-partition (SMSP) is warp % 4, and a warp may only
-// touch the TMEM lanes of quadrant warp % 4.  Sub-partition 1 hosts the MMA
-// issuer, so it gets no decode work: the rows of quadrant 1 are decoded by
-// three helper warps on sub-partitions 0, 2, 3 into a shared-memory staging
-// ring, and one light warp on sub-partition 1 moves them into TMEM.
-//   warps 0..15 with warp % 4 != 1: decoders of their own quadrant, group
-//     warp / 4 (12 warps); warp 1: TMEM allocation + MMA issuer; warp 5:
-//     bulk producer; warp 9: quadrant-1 storer; warps 16..19: epilogue of
-//     quadrants 0..3; warps 20, 22, 23: quadrant-1 helpers; 13, 21: idle.
+constexpr int kMaxASlots = 8;
+constexpr int kASlotA = kRows * 128;                  // decoded E4M3 A of one unit
+constexpr int kASlotBytes = kASlotA + kRows * 16;     // + one 16-byte scale row per weight row
+constexpr int kTasksPerUnit = 4;                      // 32 rows each
+constexpr int kDecGroups = 3;                         // unit i goes to group i % 3
+constexpr int kDecoders = kDecGroups * kTasksPerUnit; // 12
 constexpr int kMmaWarp = 1;
 constexpr int kProdWarp = 5;
-constexpr int kStoreWarp = 9;
-constexpr int kEpiWarp0 = 16;
+constexpr int kEpiWarp0 = 16;                         // warps 16..19: quadrants 0..3
 constexpr int kNumWarps = 24;
 constexpr int kThreads = kNumWarps * 32;
-constexpr int kOwnDecWarps = 12;                      // decoders of quadrants 0, 2, 3
-constexpr int kHelpers = 3;
-constexpr int kStageArrivals = kOwnDecWarps + kHelpers;
-constexpr int kStgEntries = 6;                        // quadrant-1 staging ring
-constexpr int kStgBytes = 32 * 128 + 32 * 4 + 128;    // 32 rows x 128 B, 32 scale words, pad
-__device__ __forceinline__ int helper_index(int warp) { return warp == 20 ? 0 : warp == 22 ? 1 : warp == 23 ? 2 : -1; }
-constexpr int kTmemCols = 512;
+constexpr int kTmemCols = 256;
 constexpr int kMaxSmem = 232448;
-constexpr int kMinSmem = 120 * 1024;                  // one CTA per SM: it owns all of TMEM
-constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxASlots + 5 + 2 * kStgEntries;
+constexpr int kMinSmem = 120 * 1024;                  // one CTA per SM
+constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxASlots + 5;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
 
-// Tensor-memory columns for NTOK token columns: two fp32 accumulators of NTOK
-// columns (32-column aligned), 8 columns of B scale factors (2^0), then S A
-// slots, each with 4 scale-factor columns (4-column aligned) and 32 columns
-// of E4M3 A (128 k), as many slots as fit in the 512 columns.
+// Decoder index of a warp (0..11), or -1: warps 0..15 off sub-partition 1
+// (sub-partition 1 belongs to the MMA issuer).  Warps 9, 13, 20..23 idle.
+__device__ __forceinline__ int decoder_index(int warp) {
+  if (warp >= 16) return -1;
+  const int q = warp & 3;
+  return q == 1 ? -1 : (warp >> 2) * 3 + (q == 0 ? 0 : q - 1);
+}
+
+// Tensor-memory columns for NTOK token columns: two fp32 accumulators (32-column
+// aligned), 8 columns of B scale factors (2^0), then 4 scale-factor columns per
+// A slot (4-column aligned).
 template <int NTOK>
 struct TmemMap {
   static constexpr int kAccStride = NTOK < 32 ? 32 : NTOK;
   static constexpr int kAcc = 0;                              // + kAccStride * buffer
   static constexpr int kSfb = 2 * kAccStride;
   static constexpr int kSfa = kSfb + 8;                       // + 4 * slot
-  static constexpr int slots_fit(int s) { return ((kSfa + 4 * s + 31) / 32) * 32 + 32 * s <= kTmemCols; }
-  static constexpr int kSlots = slots_fit(16) ? 16 : slots_fit(13) ? 13 : slots_fit(12) ? 12 : 10;
-  static constexpr int kA = ((kSfa + 4 * kSlots + 31) / 32) * 32;   // + 32 * slot
-  static_assert(kA + 32 * kSlots <= kTmemCols, "A slots exceed the allocation");
-  static_assert(kSlots <= kMaxASlots, "barrier arrays too small");
+  static_assert(kSfa + 4 * kMaxASlots <= kTmemCols, "TMEM map exceeds the allocation");
 };
 
 __device__ __forceinline__ void raise(unsigned bits) { atomicOr(&g_status_sk, bits); }
@@ -111,10 +104,9 @@ __device__ __forceinline__ bool status_set() {
 }
 
 // Wait for an mbarrier phase, suspended in the barrier rather than spinning
-// (spinning warps would steal issue slots from the decoders and the MMA
-// issuer on the same sub-partition).  After ~0.5 ms give up at once if
-// another wait already timed out; after kWaitLimitNs raise kErrTimeout and
-// give up.
+// (spinning warps would steal issue slots from the warps that work).  After
+// ~0.5 ms give up at once if another wait already timed out; after
+// kWaitLimitNs raise kErrTimeout and give up.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = global_ns();
@@ -137,6 +129,10 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr));
   return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // Unit geometry of an N x K weight in the tile-ordered code stream.  Unit
@@ -166,11 +162,11 @@ template <int NTOK>
 __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__ SkParams p) {
   using TM = TmemMap<NTOK>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  const int NS = p.stages;
+  const int NS = p.stages, S = p.a_slots;
   uint8_t* codes_s = smem;
   uint8_t* b_s = smem + NS * kStageBytes;
-  uint8_t* stg_s = b_s + p.b_ktiles * NTOK * 128;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_s + kStgEntries * kStgBytes);
+  uint8_t* a_s = b_s + p.b_ktiles * NTOK * 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(a_s + S * kASlotBytes);
   uint64_t* full = bars;
   uint64_t* empty = full + kMaxStages;
   uint64_t* a_full = empty + kMaxStages;
@@ -178,9 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   uint64_t* acc_full = a_empty + kMaxASlots;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* b_full = acc_empty + 2;
-  uint64_t* stg_full = b_full + 1;
-  uint64_t* stg_empty = stg_full + kStgEntries;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stg_empty + kStgEntries);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -199,10 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kStageArrivals);            // every decoder and helper warp, once per stage
+      mbar_init(&empty[i], kUnitsPerStage * kTasksPerUnit);   // every task of the stage, once
     }
-    for (int i = 0; i < kMaxASlots; ++i) {
-      mbar_init(&a_full[i], 4);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&a_full[i], kTasksPerUnit);
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -210,10 +204,6 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       mbar_init(&acc_empty[i], 4);
     }
     mbar_init(b_full, 1);
-    for (int i = 0; i < kStgEntries; ++i) {
-      mbar_init(&stg_full[i], 1);
-      mbar_init(&stg_empty[i], 1);
-    }
     fence_barrier_init();
   }
   __syncthreads();
@@ -253,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     tc_fence_after();
     tbase = *tmem_slot;
 
-    const int helper = helper_index(warp);
+    const int dec = decoder_index(warp);
     if (warp == kMmaWarp) {
       // --------------------------------------------------------- MMA issuer --
       named_bar_sync(3, 160);                          // B scale factors are in TMEM
@@ -275,9 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           else tma_load_3d(dst, &p.a_map, b_full, 0, 0, 8 * c);
         }
         const uint32_t b_base = smem_u32(b_s);
+        const uint32_t a_base = smem_u32(a_s);
         const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
         wait_bounded(b_full, 0);
-        int seg = 0, c = c_first;
+        int seg = 0, c = c_first, as = 0;
+        uint32_t a_phase = 0;
         for (int i = 0; i < n_units; ++i, c = (c + 1 == KT) ? 0 : c + 1) {
           const bool seg_first = (i == 0) || (c == 0);
           const int abuf = seg & 1;
@@ -285,21 +277,29 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
             wait_bounded(&acc_empty[abuf], ((seg >> 1) & 1u) ^ 1u);
             tc_fence_after();
           }
-          const int as = i % TM::kSlots;
-          wait_bounded(&a_full[as], (i / TM::kSlots) & 1u);
+          wait_bounded(&a_full[as], a_phase);
           tc_fence_after();
+          const uint32_t slot_addr = a_base + as * kASlotBytes;
+          // the unit's scale rows -> 4 TMEM columns (row r's scale word sits
+          // in every 32-bit word of its 16-byte row, whichever column the MMA
+          // reads for it)
+          tmem_cp_128x128b(tbase + TM::kSfa + 4 * as, umma_desc_kmajor(slot_addr + kASlotA, 128, 128));
           int bsl = c - c_first;
           if (bsl < 0) bsl += KT;
+          const uint32_t b_slot = b_base + bsl * NTOK * 128;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint32_t slot_addr = b_base + bsl * NTOK * 128;
-            const uint64_t bd = p.b_layout == 0 ? umma_desc_kmajor_sw128(slot_addr + 32 * j)
-                                                : umma_desc_kmajor(slot_addr + 2 * j * NTOK * 16, NTOK * 16, 128);
-            umma_mxf8_ts(tbase + TM::kAcc + abuf * TM::kAccStride, tbase + TM::kA + as * 32 + j * 8, bd,
-                         idesc | (uint32_t(j) << 29), tbase + TM::kSfa + as * 4, tbase + TM::kSfb,
-                         (seg_first && j == 0) ? 0u : 1u);
+            const uint64_t ad = umma_desc_kmajor(slot_addr + 2 * j * (kRows * 16), kRows * 16, 128);
+            const uint64_t bd = p.b_layout == 0 ? umma_desc_kmajor_sw128(b_slot + 32 * j)
+                                                : umma_desc_kmajor(b_slot + 2 * j * NTOK * 16, NTOK * 16, 128);
+            umma_mxf8(tbase + TM::kAcc + abuf * TM::kAccStride, ad, bd, idesc | (uint32_t(j) << 29),
+                      tbase + TM::kSfa + 4 * as, tbase + TM::kSfb, (seg_first && j == 0) ? 0u : 1u);
           }
           umma_commit(&a_empty[as]);
+          if (++as == S) {
+            as = 0;
+            a_phase ^= 1u;
+          }
           if (c == KT - 1 || i == n_units - 1) {
             umma_commit(&acc_full[abuf]);
             ++seg;
@@ -307,72 +307,42 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         }
       }
       __syncwarp();
-    } else if (warp < kEpiWarp0 && (warp & 3) != 1) {
-      // ---------------------------------------------- decoders (own quadrant) --
-      const int g = warp >> 2, q = warp & 3;
-      const int r = 32 * q + lane;                      // row inside the tile == TMEM lane
-      const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+    } else if (dec >= 0) {
+      // ------------------------------------------------------------ decoders --
+      // Decoder d = 4 g + q takes rows 32 q .. 32 q + 31 of the units
+      // i = g, g + 3, ... (group g = i % 3).  A group walks its units in
+      // order and the A-slot count is a multiple of 3, so a slot always goes
+      // back to the same group: the slot's parity wait can never be a phase
+      // (two uses) early.  Row r's 128 bytes go to the A slot as 8 chunks of
+      // 16 (chunk x at x * 2048 + r * 16: core matrices of 8 rows x 16 bytes,
+      // 128 bytes apart along M, 2048 apart along K), its scale word to the
+      // slot's scale row r (4 copies).
       const uint32_t codes_base = smem_u32(codes_s);
+      const uint32_t a_base = smem_u32(a_s);
       const int gk = p.K / 32;
-      // Scale word and codebook of this row for a unit: pulled into L1 two of
-      // this group's units ahead (no register waits on the prefetch), then
-      // loaded at the top of the unit's iteration and first used after its
-      // decode.  Rows past N: 2^0 and an all-zero codebook.
-      auto scale_ptr = [&](int t, int c) {
-        return reinterpret_cast<const uint32_t*>(p.scales + static_cast<size_t>(t * kRows + r) * gk + 4 * c);
-      };
-      auto cb_ptr = [&](int t) { return reinterpret_cast<const uint2*>(p.codebooks + static_cast<size_t>(t * kRows + r) * 8); };
-      int tu = t_first, cu = c_first;                   // this group's unit in the current stage
-      geo.advance(tu, cu, g);
-      int tn = tu, cn = cu;                             // and two stages ahead
-      geo.advance(tn, cn, 2 * kDecGroups);
-      if (tu * kRows + r < p.N && g < n_units) {
-        prefetch_l1(scale_ptr(tu, cu));
-        prefetch_l1(cb_ptr(tu));
-      }
-      {
-        int t1 = tu, c1 = cu;
-        geo.advance(t1, c1, kDecGroups);
-        if (t1 * kRows + r < p.N && g + kDecGroups < n_units) {
-          prefetch_l1(scale_ptr(t1, c1));
-          prefetch_l1(cb_ptr(t1));
-        }
-      }
-      // The TMEM stores of a unit complete while the next unit is loaded and
-      // decoded; only then does the warp wait for them and publish the unit.
-      int pending = -1;                                 // A slot stored, not yet published
-      auto publish = [&]() {
-        if (pending >= 0) {
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[pending]);
-          pending = -1;
-        }
-      };
-      for (int j = 0; j < n_stages; ++j) {
-        const int i = j * kUnitsPerStage + g;
+      const int grp = dec / kTasksPerUnit, q = dec % kTasksPerUnit;
+      int tu = t_first, cu = c_first, iu = 0;           // position of unit iu
+      for (int i = grp; i < n_units; i += kDecGroups) {
+        geo.advance(tu, cu, i - iu);
+        iu = i;
+        const int j = i / kUnitsPerStage, k = i % kUnitsPerStage;
         const int slot = j % NS;
-        const bool row_ok = i < n_units && tu * kRows + r < p.N;
+        const int r = 32 * q + lane;                    // row inside the tile
+        const int n = tu * kRows + r;
         uint32_t sw = 0x7F7F7F7Fu;
         uint2 cb = make_uint2(0, 0);
-        if (row_ok) {
-          sw = __ldg(scale_ptr(tu, cu));
-          cb = __ldg(cb_ptr(tu));
+        if (n < p.N) {
+          sw = __ldg(reinterpret_cast<const uint32_t*>(p.scales + static_cast<size_t>(n) * gk + 4 * cu));
+          cb = __ldg(reinterpret_cast<const uint2*>(p.codebooks + static_cast<size_t>(n) * 8));
         }
-        if (i + 2 * kDecGroups < n_units && tn * kRows + r < p.N) {
-          prefetch_l1(scale_ptr(tn, cn));
-          prefetch_l1(cb_ptr(tn));
-        }
-        // every decoder warp waits for every stage before releasing it, so an
-        // early release can never count towards an older phase
+        // every task waits for its stage before releasing it, so an early
+        // release can never count towards an older phase
         wait_bounded(&full[slot], (j / NS) & 1u);
-        const bool has = i < n_units;
         uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, c2 = c0;
-        if (has && r < geo.rows(tu)) {
-          // units before this one in the stage: g of them, each rows * 48 bytes
+        if (r < geo.rows(tu)) {
+          // units before this one in the stage: k of them, each rows * 48 bytes
           int tb = tu, cb0 = cu, rel = 0;
-          for (int k = 0; k < g; ++k) {
+          for (int kk = 0; kk < k; ++kk) {
             if (cb0 == 0) {
               --tb;
               cb0 = KT;
@@ -387,112 +357,23 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
-        geo.advance(tu, cu, kDecGroups);
-        geo.advance(tn, cn, kDecGroups);
-        if (has) {
-          uint32_t v[32];
-          decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
-          decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
-          decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, v + 16);
-          decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, v + 24);
-          publish();
-          const int as = i % TM::kSlots;
-          wait_bounded(&a_empty[as], ((i / TM::kSlots) & 1u) ^ 1u);
-          tc_fence_after();
-          tmem_st_x32(tbase + lane_addr + TM::kA + as * 32, v);
-          // A scale of row m: TMEM lane m, column base + m / 32, byte = a_sf_id
-          tmem_st_x1(tbase + lane_addr + TM::kSfa + as * 4 + q, sw);
-          pending = as;
-        }
-      }
-      publish();
-    } else if (helper >= 0) {
-      // ---------------------------------- quadrant-1 helpers: decode to smem --
-      // Helper h decodes rows 32..63 of the units i with i % 3 == h into the
-      // staging ring (entry i % kStgEntries): row lane's 128 E4M3 bytes as 8
-      // chunks of 16, chunk x of lane l at (x ^ (l & 7)) * 16 (conflict-free),
-      // then the row's scale word.
-      const int r = 32 + lane;
-      const uint32_t codes_base = smem_u32(codes_s);
-      const int gk = p.K / 32;
-      int ta = t_first, ca = c_first;                   // first unit of stage j
-      for (int j = 0; j < n_stages; ++j) {
-        const int slot = j % NS;
-        wait_bounded(&full[slot], (j / NS) & 1u);
-        int tk = ta, ck = ca, rel = 0;                  // unit k of the stage, its offset
-        for (int k = 0; k < kUnitsPerStage; ++k) {
-          const int i = j * kUnitsPerStage + k;
-          if (i >= n_units) break;
-          const int rows = geo.rows(tk);
-          if (i % kHelpers == helper) {
-            const int e = i % kStgEntries;
-            uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, c2 = c0;
-            if (r < rows) {
-              const uint32_t at = codes_base + slot * kStageBytes + rel + r * 48;
-              c0 = lds128(at);
-              c1 = lds128(at + 16);
-              c2 = lds128(at + 32);
-            }
-            const int n = tk * kRows + r;
-            uint32_t sw = 0x7F7F7F7Fu;
-            uint2 cb = make_uint2(0, 0);
-            if (n < p.N) {
-              sw = __ldg(reinterpret_cast<const uint32_t*>(p.scales + static_cast<size_t>(n) * gk + 4 * ck));
-              cb = __ldg(reinterpret_cast<const uint2*>(p.codebooks + static_cast<size_t>(n) * 8));
-            }
-            uint32_t v[32];
-            decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
-            decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
-            decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, v + 16);
-            decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, v + 24);
-            wait_bounded(&stg_empty[e], ((i / kStgEntries) & 1u) ^ 1u);
-            uint8_t* ent = stg_s + e * kStgBytes;
-#pragma unroll
-            for (int x = 0; x < 8; ++x)
-              *reinterpret_cast<uint4*>(ent + lane * 128 + ((x ^ (lane & 7)) * 16)) =
-                  make_uint4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
-            reinterpret_cast<uint32_t*>(ent + 32 * 128)[lane] = sw;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&stg_full[e]);
-          }
-          rel += rows * 48;
-          geo.advance(tk, ck, 1);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        geo.advance(ta, ca, kUnitsPerStage);
-      }
-    } else if (warp == kStoreWarp) {
-      // ------------------------------------- quadrant-1 storer: smem -> TMEM --
-      const uint32_t lane_addr = 32u << 16;
-      for (int i = 0; i < n_units; ++i) {
-        const int e = i % kStgEntries;
-        wait_bounded(&stg_full[e], (i / kStgEntries) & 1u);
-        const uint8_t* ent = stg_s + e * kStgBytes;
         uint32_t v[32];
+        decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
+        decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
+        decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, v + 16);
+        decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, v + 24);
+        const int as = i % S;
+        wait_bounded(&a_empty[as], ((i / S) & 1u) ^ 1u);
+        const uint32_t slot_addr = a_base + as * kASlotBytes;
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          const uint4 w = *reinterpret_cast<const uint4*>(ent + lane * 128 + ((x ^ (lane & 7)) * 16));
-          v[4 * x] = w.x;
-          v[4 * x + 1] = w.y;
-          v[4 * x + 2] = w.z;
-          v[4 * x + 3] = w.w;
-        }
-        const uint32_t sw = reinterpret_cast<const uint32_t*>(ent + 32 * 128)[lane];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&stg_empty[e]);
-        const int as = i % TM::kSlots;
-        wait_bounded(&a_empty[as], ((i / TM::kSlots) & 1u) ^ 1u);
-        tc_fence_after();
-        tmem_st_x32(tbase + lane_addr + TM::kA + as * 32, v);
-        tmem_st_x1(tbase + lane_addr + TM::kSfa + as * 4 + 1, sw);
-        tmem_st_wait();
-        tc_fence_before();
+        for (int x = 0; x < 8; ++x)
+          sts128(slot_addr + x * (kRows * 16) + r * 16, v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+        sts128(slot_addr + kASlotA + r * 16, sw, sw, sw, sw);
+        fence_proxy_async_smem();                       // visible to the tensor core
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[as]);
       }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
-      // ------------------------------------------------------------ epilogue --
       const int q = warp & 3;
       const int r = 32 * q + lane;
       const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
@@ -621,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   // op has completed; the producer saw its last copies land.
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
@@ -630,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
 int ntok_for(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
 struct Plan {
-  int ntok = 0, grid = 0, stages = 0, b_ktiles = 0, smem = 0, tiles = 0;
+  int ntok = 0, grid = 0, stages = 0, a_slots = 0, b_ktiles = 0, smem = 0, tiles = 0;
 };
 
 bool plan_for(int M, int N, int K, Plan& pl) {
@@ -643,10 +524,13 @@ bool plan_for(int M, int N, int K, Plan& pl) {
   pl.ntok = ntok_for(M);
   pl.b_ktiles = static_cast<int>(std::min<long long>(KT, per));
   const int b_bytes = pl.b_ktiles * pl.ntok * 128;
-  const int room = kMaxSmem - b_bytes - kStgEntries * kStgBytes - kBarBytes;
-  pl.stages = std::min(kMaxStages, room / kStageBytes);
+  // A slots first (6 or 3: a multiple of the decoder groups), then as many
+  // code stages as fit (3..8)
+  const int room = kMaxSmem - b_bytes - kBarBytes;
+  pl.a_slots = room - 6 * kASlotBytes >= 3 * kStageBytes ? 6 : 3;
+  pl.stages = std::min(kMaxStages, (room - pl.a_slots * kASlotBytes) / kStageBytes);
   if (pl.stages < 3) return false;
-  pl.smem = std::max(pl.stages * kStageBytes + b_bytes + kStgEntries * kStgBytes + kBarBytes, kMinSmem);
+  pl.smem = std::max(pl.stages * kStageBytes + b_bytes + pl.a_slots * kASlotBytes + kBarBytes, kMinSmem);
   pl.grid = static_cast<int>(G);
   pl.tiles = static_cast<int>(tiles);
   return true;
@@ -772,6 +656,7 @@ int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigne
   p.partial = partial;
   p.counters = counters;
   p.stages = pl.stages;
+  p.a_slots = pl.a_slots;
   p.b_ktiles = pl.b_ktiles;
   const int em = encode_a_map(p, pl.ntok);
   if (em != CBQ_OK) return em;
