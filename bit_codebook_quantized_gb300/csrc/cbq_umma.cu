@@ -61,6 +61,7 @@ constexpr int kMaxCodeStages = 6;
 constexpr int kAStages = 8;                   // decoded k-tiles in TMEM
 constexpr int kDecGroups = 4;
 constexpr int kDecWarps = 4 * kDecGroups;
+static_assert(kAStages == 2 * kDecGroups, "each decoder group owns two A slots");
 constexpr int kEpiWarp0 = 2 + kDecWarps;      // first epilogue warp
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kTmemCols = 512;
@@ -311,7 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       if (cs > 1) cluster_wait();
       // --------------------------------------------------------- MMA issuer --
       if (lane == 0) {
-        uint32_t it = 0;
+        // k-tile kt of a unit belongs to decoder group (kt - kt0) % kDecGroups,
+        // which owns A slots g and g + kDecGroups and uses them alternately:
+        // use n of group g -> slot (n & 1) * kDecGroups + g, phase n >> 1,
+        // with n = unit * (k-tiles of g per unit) + (kt - kt0) / kDecGroups
+        const int nk = kt1 - kt0;
         const uint32_t b_base = smem_u32(b_s);
         for (int ui = 0; ui < n_units; ++ui) {
           const int abuf = ui & 1;
@@ -321,11 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
           int n_mma = NTOK;
           if constexpr (GROUPED) n_mma = min(NTOK, (misc[0] + 15) & ~15);
           const uint32_t idesc = umma_idesc_mxf8(n_mma, 0, 0);
-          for (int kt = kt0; kt < kt1; ++kt, ++it) {
-            const int slot = it % kAStages;
-            wait_bounded(&a_full[slot], (it / kAStages) & 1u);
+          for (int kt = kt0; kt < kt1; ++kt) {
+            const int i = kt - kt0, grp = i % kDecGroups;
+            const uint32_t n = static_cast<uint32_t>(ui * ((nk + kDecGroups - 1 - grp) / kDecGroups) + i / kDecGroups);
+            const int slot = static_cast<int>(n & 1u) * kDecGroups + grp;
+            wait_bounded(&a_full[slot], (n >> 1) & 1u);
             tc_fence_after();
-            const int i = kt - kt0;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint64_t bd = umma_desc_kmajor(b_base + (i * 8 + 2 * j) * NTOK * 16, NTOK * 16, 128);
@@ -351,10 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       // after its last read from it.
       uint32_t sg_unit = 0;                             // global index of the unit's first stage
       int released = 0, rows_t = kRows;
+      // Every release is preceded by a wait for that stage, so an early
+      // release can never count towards an older phase of its slot.
       auto release_until = [&](int s_end) {
         for (; released < s_end; ++released) {
+          const uint32_t sg = sg_unit + released;
+          wait_bounded(&codes_full[sg % NS], (sg / NS) & 1u);
           __syncwarp();
-          if (lane == 0) mbar_arrive(&codes_empty[(sg_unit + released) % NS]);
+          if (lane == 0) mbar_arrive(&codes_empty[sg % NS]);
         }
       };
       // Load a k-tile's code row from shared memory and decode it into 32
@@ -373,28 +383,31 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       };
       // Issue the TMEM stores of a decoded k-tile (A operand and its scale
       // factors); the wait for them comes later, after the next decode.
-      auto store = [&](uint32_t it, uint32_t sw, const uint32_t (&v)[32]) {
-        const int aslot = it % kAStages;
-        wait_bounded(&a_empty[aslot], ((it / kAStages) & 1u) ^ 1u);
+      // This group's A slots are dg and dg + kDecGroups, used alternately in
+      // the group's own k-tile order (so a slot's parity wait cannot be two
+      // uses early): use n -> slot (n & 1) * kDecGroups + dg, phase n >> 1.
+      uint32_t uses = 0;
+      auto store = [&](uint32_t n, uint32_t sw, const uint32_t (&v)[32]) {
+        const int aslot = static_cast<int>(n & 1u) * kDecGroups + dg;
+        wait_bounded(&a_empty[aslot], ((n >> 1) & 1u) ^ 1u);
         tc_fence_after();
         tmem_st_x32(tbase + lane_addr + kACol + aslot * 32, v);
         // A scale of row m is read from TMEM lane m, column (base + m / 32),
         // byte = the MMA's a_sf_id: quadrant q writes column base + q
         tmem_st_x1(tbase + lane_addr + kSfaCol + aslot * 4 + q, sw);
       };
-      auto publish = [&](uint32_t it) {
+      auto publish = [&](uint32_t n) {
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[it % kAStages]);
+        if (lane == 0) mbar_arrive(&a_full[static_cast<int>(n & 1u) * kDecGroups + dg]);
       };
-      uint32_t it_unit = 0;                             // shared k-tile counter at the unit start
       int row0n, row_endn, en;
       if (n_units > 0) unit_rows(0, row0n, row_endn, en);
       uint2 cb_next = (n_units > 0 && row0n + r < row_endn)
                           ? __ldg(reinterpret_cast<const uint2*>(p.codebooks + size_t(row0n + r) * 8))
                           : make_uint2(0, 0);
-      for (int ui = 0; ui < n_units; ++ui, it_unit += kt1 - kt0) {
+      for (int ui = 0; ui < n_units; ++ui) {
         int row0, row_end, e;
         unit_rows(ui, row0, row_end, e);
         unit_tile(ui, rows_t);
@@ -415,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
         // this group's k-tiles are kt0 + dg, kt0 + dg + G, ...; the other
         // groups' warps fill the issue slots while this one waits on TMEM
         for (int kt = kt0 + dg; kt < kt1; kt += kDecGroups) {
-          const uint32_t it = it_unit + (kt - kt0);
+          const uint32_t it = uses++;
           if (ok && kt + 16 < kt1 && ((kt + 16) & 7) < kDecGroups) prefetch_l1(srow + kt + 16);
           const uint32_t sw = ok ? __ldg(srow + kt) : 0x7F7F7F7Fu;
           uint32_t v[32];
