@@ -66,7 +66,7 @@ constexpr int kASlotA = kRows * 128;                  // decoded E4M3 A of one u
 constexpr int kASlotBytes = kASlotA + kRows * 16;     // + one 16-byte scale row per weight row
 constexpr int kTasksPerUnit = 4;                      // 32 rows each
 constexpr int kDecGroups = 3;                         // unit i goes to group i % 3
-constexpr int kDecoders = kDecGroups * kTasksPerUnit; // 12
+static_assert(kDecGroups * kTasksPerUnit == 12, "12 decoder warps");
 constexpr int kMmaWarp = 1;
 constexpr int kProdWarp = 5;
 constexpr int kEpiWarp0 = 16;                         // warps 16..19: quadrants 0..3
@@ -321,23 +321,38 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       const uint32_t a_base = smem_u32(a_s);
       const int gk = p.K / 32;
       const int grp = dec / kTasksPerUnit, q = dec % kTasksPerUnit;
-      int tu = t_first, cu = c_first, iu = 0;           // position of unit iu
-      for (int i = grp; i < n_units; i += kDecGroups) {
-        geo.advance(tu, cu, i - iu);
-        iu = i;
-        const int j = i / kUnitsPerStage, k = i % kUnitsPerStage;
-        const int slot = j % NS;
-        const int r = 32 * q + lane;                    // row inside the tile
-        const int n = tu * kRows + r;
-        uint32_t sw = 0x7F7F7F7Fu;
-        uint2 cb = make_uint2(0, 0);
-        if (n < p.N) {
-          sw = __ldg(reinterpret_cast<const uint32_t*>(p.scales + static_cast<size_t>(n) * gk + 4 * cu));
+      const int r = 32 * q + lane;                      // row inside the tile
+      // scale word and codebook of row r for the unit at (t, c)
+      auto load_sc = [&](int t, int c, bool valid, uint32_t& sw, uint2& cb) {
+        sw = 0x7F7F7F7Fu;
+        cb = make_uint2(0, 0);
+        const int n = t * kRows + r;
+        if (valid && n < p.N) {
+          sw = __ldg(reinterpret_cast<const uint32_t*>(p.scales + static_cast<size_t>(n) * gk + 4 * c));
           cb = __ldg(reinterpret_cast<const uint2*>(p.codebooks + static_cast<size_t>(n) * 8));
         }
+      };
+      // Stage slot / phase and A slot / phase of the current unit, advanced
+      // incrementally (no division by the runtime ring sizes per unit).
+      int st_j = 0, st_slot = 0, a_slot = 0;
+      uint32_t st_phase = 0, a_phase = 0;
+      auto seek = [&](int i) {                          // i only grows, by 3 at most 1 stage
+        const int j = i / kUnitsPerStage;
+        while (st_j < j) {
+          ++st_j;
+          if (++st_slot == NS) {
+            st_slot = 0;
+            st_phase ^= 1u;
+          }
+        }
+      };
+      auto process = [&](int i, int tu, int cu, uint32_t sw, uint2 cb) {
+        const int k = i % kUnitsPerStage;
+        seek(i);
+        const int slot = st_slot;
         // every task waits for its stage before releasing it, so an early
         // release can never count towards an older phase
-        wait_bounded(&full[slot], (j / NS) & 1u);
+        wait_bounded(&full[slot], st_phase);
         uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, c2 = c0;
         if (r < geo.rows(tu)) {
           // units before this one in the stage: k of them, each rows * 48 bytes
@@ -362,8 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
         decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, v + 16);
         decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, v + 24);
-        const int as = i % S;
-        wait_bounded(&a_empty[as], ((i / S) & 1u) ^ 1u);
+        const int as = a_slot;
+        wait_bounded(&a_empty[as], a_phase ^ 1u);
         const uint32_t slot_addr = a_base + as * kASlotBytes;
 #pragma unroll
         for (int x = 0; x < 8; ++x)
@@ -372,6 +387,32 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         fence_proxy_async_smem();                       // visible to the tensor core
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[as]);
+        a_slot += kDecGroups;                           // this group's next slot
+        if (a_slot >= S) {
+          a_slot -= S;
+          a_phase ^= 1u;
+        }
+      };
+      // Two register sets for the scale word and codebook, so the loads for
+      // the group's next unit are in flight during the current one (unrolled
+      // by two: no register copy has to wait for a load).
+      int ta = t_first, ca = c_first;                   // unit i (set A)
+      geo.advance(ta, ca, grp);
+      a_slot = grp;                                     // unit grp's A slot (S is a multiple of 3)
+      uint32_t swA, swB;
+      uint2 cbA, cbB;
+      load_sc(ta, ca, grp < n_units, swA, cbA);
+      for (int i = grp; i < n_units; i += 2 * kDecGroups) {
+        int tb = ta, cbb = ca;                          // unit i + 3 (set B)
+        geo.advance(tb, cbb, kDecGroups);
+        load_sc(tb, cbb, i + kDecGroups < n_units, swB, cbB);
+        process(i, ta, ca, swA, cbA);
+        if (i + kDecGroups >= n_units) break;
+        ta = tb;                                        // unit i + 6 (set A)
+        ca = cbb;
+        geo.advance(ta, ca, kDecGroups);
+        load_sc(ta, ca, i + 2 * kDecGroups < n_units, swA, cbA);
+        process(i + kDecGroups, tb, cbb, swB, cbB);
       }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
       const int q = warp & 3;
