@@ -284,12 +284,25 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       // resident activations for this CTA's K range, K-major core-matrix
       // layout: chunk c (16 k) at c * NTOK * 16, token group j at j * 128,
       // token % 8 at * 16
-      const int kb = kt0 * 128, nchunk = (kt1 - kt0) * 8;
-      for (int i = tid - 32; i < NTOK * nchunk; i += kThreads - 32) {
-        const int tok = i % NTOK, c = i / NTOK;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (tok < p.M) v = __ldg(reinterpret_cast<const uint4*>(p.a + size_t(tok) * p.K + kb + c * 16));
-        *reinterpret_cast<uint4*>(b_s + c * NTOK * 16 + (tok >> 3) * 128 + (tok & 7) * 16) = v;
+      const int kb = kt0 * 128, nchunk = (kt1 - kt0) * 8, total = NTOK * nchunk;
+      // 4 loads in flight per thread before their stores
+      for (int i0 = tid - 32; i0 < total; i0 += (kThreads - 32) * 4) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * (kThreads - 32);
+          v[u] = make_uint4(0, 0, 0, 0);
+          if (i < total && i % NTOK < p.M)
+            v[u] = __ldg(reinterpret_cast<const uint4*>(p.a + size_t(i % NTOK) * p.K + kb + (i / NTOK) * 16));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * (kThreads - 32);
+          if (i < total) {
+            const int tok = i % NTOK, c = i / NTOK;
+            *reinterpret_cast<uint4*>(b_s + c * NTOK * 16 + (tok >> 3) * 128 + (tok & 7) * 16) = v[u];
+          }
+        }
       }
       fence_proxy_async_smem();
     }
@@ -469,13 +482,25 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
             }
             named_bar_sync(2, 128);
             const int cnt = misc[0], nz = min(NTOK, (cnt + 15) & ~15);
-            const int nchunk = p.K / 16;
-            for (int i = tid - kEpiWarp0 * 32; i < nz * nchunk; i += 128) {
-              const int tk = i % nz, c = i / nz;
-              uint4 v = make_uint4(0, 0, 0, 0);
-              if (tk < cnt)
-                v = __ldg(reinterpret_cast<const uint4*>(p.a + size_t(list_tok[tk] & 0xff) * p.K + c * 16));
-              *reinterpret_cast<uint4*>(b_s + c * NTOK * 16 + (tk >> 3) * 128 + (tk & 7) * 16) = v;
+            const int nchunk = p.K / 16, total = nz * nchunk;
+            // 8 loads in flight per thread before their stores
+            for (int i0 = tid - kEpiWarp0 * 32; i0 < total; i0 += 128 * 8) {
+              uint4 v[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * 128;
+                v[u] = make_uint4(0, 0, 0, 0);
+                if (i < total && i % nz < cnt)
+                  v[u] = __ldg(reinterpret_cast<const uint4*>(p.a + size_t(list_tok[i % nz] & 0xff) * p.K + (i / nz) * 16));
+              }
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * 128;
+                if (i < total) {
+                  const int tk = i % nz, c = i / nz;
+                  *reinterpret_cast<uint4*>(b_s + c * NTOK * 16 + (tk >> 3) * 128 + (tk & 7) * 16) = v[u];
+                }
+              }
             }
             fence_proxy_async_smem();
             named_bar_sync(2, 128);
