@@ -73,6 +73,15 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
   return s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
 }
 
+// Byte q (0..3, a compile-time constant after unrolling) of a word of four
+// E8M0 scales -> fp32 2^(s-127): the byte is moved into the exponent field;
+// s = 0 leaves the field empty and the unsigned max turns it into the
+// subnormal 2^-127 (every other s gives a larger bit pattern).
+__device__ __forceinline__ float e8m0_word_byte_to_f32(uint32_t word, int q) {
+  const uint32_t e = (q < 3 ? (word << (23 - 8 * q)) : (word >> 1)) & 0x7F800000u;
+  return __uint_as_float(max(e, 0x00400000u));
+}
+
 // Twenty-four bits of a group starting at bit 24*t: codes 8t..8t+7.  The
 // group's three 32-bit words are w0, w1, w2.
 __device__ __forceinline__ uint32_t group_field(uint32_t w0, uint32_t w1, uint32_t w2, int t) {

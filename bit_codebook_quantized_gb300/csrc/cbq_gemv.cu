@@ -59,22 +59,20 @@ __device__ __forceinline__ bool status_set() {
   return *reinterpret_cast<volatile unsigned*>(&g_status_gemv) != 0u;
 }
 
-// Spin on an mbarrier phase.  After ~0.5 ms of waiting, give up at once if
-// another wait of this kernel already timed out; after kWaitLimitCycles,
-// raise kErrTimeout and give up.
+// Wait for an mbarrier phase, suspended in the barrier between polls.  After
+// ~0.5 ms give up at once if another wait of this kernel already timed out;
+// after kWaitLimitNs raise kErrTimeout and give up.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 63u) == 0) {                       // read the clock now and then only
-      const long long dt = clock64() - t0;
-      if (dt > (1LL << 20)) {
-        if (status_set()) return false;
-        if (dt > kWaitLimitCycles) {
-          raise(kErrTimeout);
-          return false;
-        }
+  const long long t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+    const long long dt = global_ns() - t0;
+    if (dt > 500000LL) {
+      if (status_set()) return false;
+      if (dt > kWaitLimitNs) {
+        raise(kErrTimeout);
+        return false;
       }
     }
   }
@@ -301,8 +299,8 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
           uint32_t a2 = lookup4(cbA.x, cbA.y, selA >> 16);
           uint32_t a1 = lookup4(cbB.x, cbB.y, selB);
           uint32_t a3 = lookup4(cbB.x, cbB.y, selB >> 16);
-          const float fsA = e8m0_to_f32((sA >> (8 * q)) & 0xffu);
-          const float fsB = e8m0_to_f32((sB >> (8 * q)) & 0xffu);
+          const float fsA = e8m0_word_byte_to_f32(sA, q);
+          const float fsB = e8m0_word_byte_to_f32(sB, q);
 #pragma unroll
           for (int tc = 0; tc < TOKC; ++tc) {
             if (tc * 8 < ntok) {

@@ -59,9 +59,11 @@ def test_gemm_shapes(path, N, K):
 
 
 @pytest.mark.parametrize("path", PATHS)
-def test_one_hot_is_bit_exact(path):
+@pytest.mark.parametrize("lo,hi", [(100, 150), (0, 3)])
+def test_one_hot_is_bit_exact(path, lo, hi):
+    # (0, 3): E8M0 0 (2^-127) and weights that are fp32 subnormals
     N, K = 150, 512
-    c = Case(8, N, K, seed=5, scale_lo=100, scale_hi=150)
+    c = Case(8, N, K, seed=5, scale_lo=lo, scale_hi=hi)
     ks = [0, 1, 31, 32, 100, 255, 256, 511]
     c.a[:] = 0
     for m, k in enumerate(ks):
