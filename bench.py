@@ -165,10 +165,19 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sms)}
 
 
-def kernel_source_hash() -> str:
+# the sources each kernel is compiled from (its translation unit and the
+# headers it includes)
+KERNEL_SOURCES = {
+    "gemv_kernel": ["cbq_gemv.cu", "cbq_device.cuh", "cbq_internal.h"],
+    "umma_kernel": ["cbq_umma.cu", "cbq_device.cuh", "cbq_internal.h"],
+    "sk_kernel": ["cbq_sk.cu", "cbq_device.cuh", "cbq_internal.h"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_codebook_quantized_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -181,12 +190,12 @@ def profiled_traffic(kernel: str):
         return None
     src, per_m = None, {}
     for line in open(p):
-        if line.startswith("kernel_source_sha256:"):
+        if line.startswith(f"kernel_source_sha256[{kernel}]:"):
             src = line.split(":", 1)[1].strip()
         if line.startswith(f"dram_bytes_per_launch[{kernel}]"):
             k, v = line.split(":", 1)
             per_m[k.split("M=")[1].rstrip("]").strip()] = float(v)
-    if src != kernel_source_hash() or not per_m:
+    if kernel not in KERNEL_SOURCES or src != kernel_source_hash(kernel) or not per_m:
         return None
     return per_m
 

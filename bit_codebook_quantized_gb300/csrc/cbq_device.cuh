@@ -169,6 +169,14 @@ __device__ __forceinline__ void cp_async8(uint32_t smem_addr, const void* gptr) 
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// 16-byte asynchronous copy that reads `src_bytes` (16 or 0) bytes from
+// global memory and fills the rest of the 16 with zeros; both addresses
+// 16-byte aligned.  cp_async_wait_all waits for every copy this thread issued.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t smem_addr, const void* gptr, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr), "l"(gptr), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

@@ -483,25 +483,15 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
             named_bar_sync(2, 128);
             const int cnt = misc[0], nz = min(NTOK, (cnt + 15) & ~15);
             const int nchunk = p.K / 16, total = nz * nchunk;
-            // 8 loads in flight per thread before their stores
-            for (int i0 = tid - kEpiWarp0 * 32; i0 < total; i0 += 128 * 8) {
-              uint4 v[8];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const int i = i0 + u * 128;
-                v[u] = make_uint4(0, 0, 0, 0);
-                if (i < total && i % nz < cnt)
-                  v[u] = __ldg(reinterpret_cast<const uint4*>(p.a + size_t(list_tok[i % nz] & 0xff) * p.K + (i / nz) * 16));
-              }
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const int i = i0 + u * 128;
-                if (i < total) {
-                  const int tk = i % nz, c = i / nz;
-                  *reinterpret_cast<uint4*>(b_s + c * NTOK * 16 + (tk >> 3) * 128 + (tk & 7) * 16) = v[u];
-                }
-              }
+            // asynchronous 16-byte copies, all in flight at once (rows past
+            // the expert's token count are zero-filled)
+            for (int i = tid - kEpiWarp0 * 32; i < total; i += 128) {
+              const int tk = i % nz, c = i / nz;
+              const bool real = tk < cnt;
+              const uint8_t* src = real ? p.a + size_t(list_tok[tk] & 0xff) * p.K + c * 16 : p.a;
+              cp_async16_zfill(smem_u32(b_s + c * NTOK * 16 + (tk >> 3) * 128 + (tk & 7) * 16), src, real ? 16u : 0u);
             }
+            cp_async_wait_all();
             fence_proxy_async_smem();
             named_bar_sync(2, 128);
             prev_e = e;
