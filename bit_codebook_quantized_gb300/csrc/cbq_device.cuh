@@ -17,10 +17,9 @@ namespace cbq {
 // word; cbq_device_status() collects and clears them).
 enum : unsigned { kErrTimeout = 1u, kErrRouting = 2u };
 
-// Bounded waits give up after this many SM clock cycles (~2 s at 2 GHz), or
-// (waits that may be suspended, when the SM clock may not advance for the
-// waiting warp) after this many nanoseconds of the global timer.
-constexpr long long kWaitLimitCycles = 4000000000LL;
+// Bounded waits give up after this many nanoseconds of the global timer
+// (~2 s; the SM clock may not advance for a suspended warp, the global timer
+// does).
 constexpr long long kWaitLimitNs = 2000000000LL;
 
 __device__ __forceinline__ long long global_ns() {
@@ -415,6 +414,19 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// The same with a suspend-time hint (ns): the waiting thread may sleep in the
+// barrier instead of polling.
+__device__ __forceinline__ bool mbar_try_wait_cluster_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }

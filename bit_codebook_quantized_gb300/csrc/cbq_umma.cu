@@ -79,23 +79,25 @@ __device__ __forceinline__ bool status_set() {
   return *reinterpret_cast<volatile unsigned*>(&g_status_umma) != 0u;
 }
 
-// Spin on an mbarrier phase.  After ~0.5 ms give up at once if another wait
-// already timed out; after kWaitLimitCycles raise kErrTimeout and give up.
+// Wait for an mbarrier phase, suspended in the barrier between polls: warps
+// that poll in a loop take issue slots and shared-memory bandwidth from the
+// warps they wait for (at the start of a grouped call, polling decoder warps
+// slowed the activation gather several-fold).  After ~0.5 ms give up at once
+// if another wait already timed out; after kWaitLimitNs raise kErrTimeout
+// and give up.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
-  auto tw = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-  if (tw()) return true;
-  const long long t0 = clock64();
-  for (uint32_t n = 1;; ++n) {
-    if (tw()) return true;
-    if ((n & 63u) == 0) {                       // read the clock now and then only
-      const long long dt = clock64() - t0;
-      if (dt > (1LL << 20)) {
-        if (status_set()) return false;
-        if (dt > kWaitLimitCycles) {
-          raise(kErrTimeout);
-          return false;
-        }
+  if (CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  const long long t0 = global_ns();
+  for (;;) {
+    if (CLUSTER ? mbar_try_wait_cluster_suspend(bar, parity, 20000u) : mbar_try_wait_suspend(bar, parity, 20000u))
+      return true;
+    const long long dt = global_ns() - t0;
+    if (dt > 500000LL) {
+      if (status_set()) return false;
+      if (dt > kWaitLimitNs) {
+        raise(kErrTimeout);
+        return false;
       }
     }
   }
