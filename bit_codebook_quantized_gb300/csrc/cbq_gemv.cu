@@ -167,6 +167,7 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
   if (warp == kConsumerWarps) {
     if (lane == 0) {
       uint32_t it = 0;
+      const uint64_t pol = l2_evict_first_policy();
       for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         // the slab's rows inside its 128-row tile; each k-tile piece of the
         // slab is contiguous (rows x 48 B) in the tile-ordered code stream
@@ -192,7 +193,7 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
           mbar_arrive_expect_tx(&full_bar[slot], nvalid * piece);
           for (int c = 0; c < nvalid; ++c)
             bulk_g2s(stage_buf + slot * kStageBytes + c * kBoxBytes,
-                     tile + static_cast<long long>(c0 + c) * rows_t * 48, piece, &full_bar[slot]);
+                     tile + static_cast<long long>(c0 + c) * rows_t * 48, piece, &full_bar[slot], pol);
         }
       }
     }

@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     // -------------------------------------------------------- bulk producer --
     if (lane == 0) {
       int ta = t_first, ca = c_first;                 // first unit of stage j
+      const uint64_t pol = l2_evict_first_policy();
       for (int j = 0; j < n_stages; ++j) {
         const int slot = j % NS;
         const int nu = min(kUnitsPerStage, n_units - j * kUnitsPerStage);
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         geo.advance(ta, ca, kUnitsPerStage);
         wait_bounded(&empty[slot], ((j / NS) & 1u) ^ 1u);
         mbar_arrive_expect_tx(&full[slot], bytes);
-        bulk_g2s(codes_s + slot * kStageBytes, p.codes + oa, bytes, &full[slot]);
+        bulk_g2s(codes_s + slot * kStageBytes, p.codes + oa, bytes, &full[slot], pol);
       }
       // every copy has landed before the CTA can leave
       for (int j = max(0, n_stages - NS); j < n_stages; ++j) wait_bounded(&full[j % NS], (j / NS) & 1u);

@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     // consecutive k-tiles of the tile, contiguous in the code stream.
     if (lane == 0) {
       uint32_t sg = 0;
+      const uint64_t pol = l2_evict_first_policy();
       for (int ui = 0; ui < n_units; ++ui) {
         int rows_t;
         const uint8_t* tile = unit_tile(ui, rows_t);
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
           wait_bounded(&codes_empty[slot], ((sg / NS) & 1u) ^ 1u);
           mbar_arrive_expect_tx(&codes_full[slot], bytes);
           bulk_g2s(codes_s + slot * kCodeStage, tile + static_cast<long long>(kb) * rows_t * 48, bytes,
-                   &codes_full[slot]);
+                   &codes_full[slot], pol);
         }
       }
     }
