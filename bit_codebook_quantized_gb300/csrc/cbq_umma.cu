@@ -12,30 +12,36 @@
 //
 // Mapping to sm_103a (swap-AB: weight rows are the MMA's M = 128, token rows
 // its N = 16, 32 or 64):
-//  * warp 0 (one lane) streams the tile's code bytes with 2-D TMA boxes of
-//    [128 rows][48 B] (one 128-wide k-tile) into an 8-stage mbarrier ring,
-//    starting right after barrier set-up;
-//  * warps 2..9 are two decoder warpgroups taking alternate k-tiles; thread
-//    = weight row = TMEM lane.  A thread reads its row's 48 code bytes (three
-//    128-bit shared loads at a conflict-free 48-byte pitch), spreads the codes
-//    to nibbles and turns them into E4M3 bytes with byte-permutes through the
-//    row's codebook (two registers), then writes the 128 bytes into its TMEM
-//    lane (tcgen05.st, 32 columns) as the MMA's A operand, and its 4 E8M0
-//    group-scale bytes into TMEM as the A scale factors.  The wait for the
-//    TMEM stores of one k-tile is overlapped with decoding the next; scale
-//    bytes are pulled into L1 16 k-tiles ahead and the next tile's codebook
-//    is loaded during the current one;
+//  * warp 0 (one lane) streams the tile's code bytes with 1-D bulk copies of
+//    4 k-tiles (24 KB, contiguous in the tile-ordered stream) into a ring of
+//    up to 6 stages, starting right after barrier set-up;
+//  * warps 2..17 are four decoder groups of 4 warps taking k-tiles round
+//    robin; thread = weight row = TMEM lane.  A thread reads its row's 48
+//    code bytes (three 128-bit shared loads at a conflict-free 48-byte
+//    pitch), spreads the codes to nibbles and turns them into E4M3 bytes with
+//    byte-permutes through the row's codebook (two registers), then writes the
+//    128 bytes into its TMEM lane (tcgen05.st, 32 columns) as the MMA's A
+//    operand, and its 4 E8M0 group-scale bytes into TMEM as the A scale
+//    factors.  Each group owns two A slots; the wait for the TMEM stores of
+//    one k-tile is overlapped with decoding the next; scale bytes are pulled
+//    into L1 16 k-tiles ahead and the next tile's codebook is loaded during
+//    the current one;
 //  * warp 1 (one lane) issues 4 tcgen05.mma kind::mxf8f6f4.block_scale
 //    (K = 32 each) per k-tile with A from TMEM and B (the E4M3 activations,
-//    resident in shared memory for the CTA's K range) from a K-major
-//    shared-memory descriptor; B scale factors are 2^0.  The E8M0 group scale
-//    is exactly the MX block scale of a 32-wide K block, so the tensor core
-//    applies it;
-//  * warps 10..13 are the epilogue: tcgen05.ld the accumulator (two
+//    resident in shared memory for the CTA's K range, landed by 16-byte
+//    asynchronous copies at the start) from a K-major shared-memory
+//    descriptor; B scale factors are 2^0.  The E8M0 group scale is exactly the
+//    MX block scale of a 32-wide K block, so the tensor core applies it;
+//  * warps 18..21 are the epilogue: tcgen05.ld the accumulator (two
 //    accumulators alternate between tiles so the MMA never waits for the
 //    stores), multiply by a_scale, store fp32 y;
 //  * narrow problems split K over a thread-block cluster; partial tiles are
-//    summed in the leader CTA's shared memory through DSMEM stores.
+//    summed in the leader CTA's shared memory through DSMEM stores;
+//  * grouped calls (one MoE verify round): every CTA derives the ascending
+//    list of the experts the round routes to from topk_idx, and takes a
+//    contiguous block of (expert, tile) units; all tokens stay resident, the
+//    MMAs run over every token column, and the epilogue stores the columns of
+//    the tokens routed to the unit's expert into their y slots.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -110,8 +116,8 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 }
 
 // mbarriers (codes full/empty, A full/empty, 2 accumulators full/empty,
-// B, split-K full/free), then the TMEM base slot and two ints.
-constexpr int kNumBars = 2 * kMaxCodeStages + 2 * kAStages + 4 + 3;
+// split-K full/free), then the TMEM base slot and two ints.
+constexpr int kNumBars = 2 * kMaxCodeStages + 2 * kAStages + 4 + 2;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area too small");
 
@@ -143,14 +149,13 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   uint64_t* a_empty = a_full + kAStages;
   uint64_t* acc_full = a_empty + kAStages;
   uint64_t* acc_empty = acc_full + 2;
-  uint64_t* b_full = acc_empty + 2;
-  uint64_t* red_full = b_full + 1;
+  uint64_t* red_full = acc_empty + 2;
   uint64_t* red_free = red_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_free + 1);
-  int* misc = reinterpret_cast<int*>(tmem_slot + 2);     // [0] list count, [1] experts used
+  int* misc = reinterpret_cast<int*>(tmem_slot + 2);     // [1] experts used (grouped)
   int32_t* topk_s = reinterpret_cast<int32_t*>(smem + L.route);
-  int32_t* list_tok = topk_s + kMaxRouting;              // token | slot << 8
-  uint16_t* used_list = reinterpret_cast<uint16_t*>(list_tok + 64 + 4);
+  int32_t* slot_of = topk_s + kMaxRouting;               // grouped: y slot of each token for the current expert, or -1
+  uint16_t* used_list = reinterpret_cast<uint16_t*>(slot_of + 64 + 4);
   uint8_t* used_flag = reinterpret_cast<uint8_t*>(used_list + kMaxExperts);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -176,7 +181,6 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);
     }
-    mbar_init(b_full, 4);
     mbar_init(red_full, (cs > 1 ? cs - 1 : 1) * 128);
     mbar_init(red_free, 128);
     fence_barrier_init();
@@ -283,30 +287,21 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       tmem_alloc(tmem_slot, kTmemCols);
       tmem_relinquish();
     }
-    if constexpr (!GROUPED) {
+    {
       // resident activations for this CTA's K range, K-major core-matrix
       // layout: chunk c (16 k) at c * NTOK * 16, token group j at j * 128,
-      // token % 8 at * 16
+      // token % 8 at * 16; token rows >= M are zero-filled.  A grouped call
+      // keeps every token resident: the MMAs run over all token columns and
+      // the epilogue keeps the columns of the tokens routed to the unit's
+      // expert.  One 16-byte asynchronous copy per chunk, all in flight.
       const int kb = kt0 * 128, nchunk = (kt1 - kt0) * 8, total = NTOK * nchunk;
-      // 4 loads in flight per thread before their stores
-      for (int i0 = tid - 32; i0 < total; i0 += (kThreads - 32) * 4) {
-        uint4 v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = i0 + u * (kThreads - 32);
-          v[u] = make_uint4(0, 0, 0, 0);
-          if (i < total && i % NTOK < p.M)
-            v[u] = __ldg(reinterpret_cast<const uint4*>(p.a + size_t(i % NTOK) * p.K + kb + (i / NTOK) * 16));
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = i0 + u * (kThreads - 32);
-          if (i < total) {
-            const int tok = i % NTOK, c = i / NTOK;
-            *reinterpret_cast<uint4*>(b_s + c * NTOK * 16 + (tok >> 3) * 128 + (tok & 7) * 16) = v[u];
-          }
-        }
+      for (int i = tid - 32; i < total; i += kThreads - 32) {
+        const int tok = i % NTOK, c = i / NTOK;
+        const bool real = tok < p.M;
+        cp_async16_zfill(smem_u32(b_s + c * NTOK * 16 + (tok >> 3) * 128 + (tok & 7) * 16),
+                         real ? p.a + size_t(tok) * p.K + kb + c * 16 : p.a, real ? 16u : 0u);
       }
+      cp_async_wait_all();
       fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -336,12 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
         const uint32_t b_base = smem_u32(b_s);
         for (int ui = 0; ui < n_units; ++ui) {
           const int abuf = ui & 1;
-          if constexpr (GROUPED) wait_bounded(b_full, ui & 1);   // this unit's gathered B
           wait_bounded(&acc_empty[abuf], ((ui >> 1) & 1) ^ 1);
           tc_fence_after();
-          int n_mma = NTOK;
-          if constexpr (GROUPED) n_mma = min(NTOK, (misc[0] + 15) & ~15);
-          const uint32_t idesc = umma_idesc_mxf8(n_mma, 0, 0);
+          const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
           for (int kt = kt0; kt < kt1; ++kt) {
             const int i = kt - kt0, grp = i % kDecGroups;
             const uint32_t n = static_cast<uint32_t>(ui * ((nk + kDecGroups - 1 - grp) / kDecGroups) + i / kDecGroups);
@@ -464,44 +456,19 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       for (int ui = 0; ui < n_units; ++ui) {
         int row0, row_end, e;
         unit_rows(ui, row0, row_end, e);
-        int ntok = p.M;
         if constexpr (GROUPED) {
           if (e != prev_e) {
-            // token list of expert e, then gather its activation rows into B
-            // (the MMAs of the previous unit are complete: its epilogue waited)
+            // y slot of every token routed to expert e (a token lists an
+            // expert at most once; the routing check above raised otherwise)
             named_bar_sync(2, 128);
-            if (ew == 0) {
-              const int nr = p.M * p.topk;
-              int base = 0;
-              for (int i0 = 0; i0 < nr; i0 += 32) {
-                const int i = i0 + lane;
-                const bool hit = (i < nr) && topk_s[i] == e;
-                const unsigned m = __ballot_sync(0xffffffffu, hit);
-                const int pos = base + __popc(m & ((1u << lane) - 1u));
-                if (hit && pos < 64) list_tok[pos] = (i / p.topk) | ((i % p.topk) << 8);
-                base += __popc(m);
-              }
-              if (lane == 0) misc[0] = min(base, NTOK);
-            }
+            for (int t = tid - kEpiWarp0 * 32; t < 64; t += 128) slot_of[t] = -1;
             named_bar_sync(2, 128);
-            const int cnt = misc[0], nz = min(NTOK, (cnt + 15) & ~15);
-            const int nchunk = p.K / 16, total = nz * nchunk;
-            // asynchronous 16-byte copies, all in flight at once (rows past
-            // the expert's token count are zero-filled)
-            for (int i = tid - kEpiWarp0 * 32; i < total; i += 128) {
-              const int tk = i % nz, c = i / nz;
-              const bool real = tk < cnt;
-              const uint8_t* src = real ? p.a + size_t(list_tok[tk] & 0xff) * p.K + c * 16 : p.a;
-              cp_async16_zfill(smem_u32(b_s + c * NTOK * 16 + (tk >> 3) * 128 + (tk & 7) * 16), src, real ? 16u : 0u);
-            }
-            cp_async_wait_all();
-            fence_proxy_async_smem();
+            const int nr = p.M * p.topk;
+            for (int i = tid - kEpiWarp0 * 32; i < nr; i += 128)
+              if (topk_s[i] == e) slot_of[i / p.topk] = i % p.topk;
             named_bar_sync(2, 128);
             prev_e = e;
           }
-          ntok = misc[0];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(b_full);
         }
 
         const int grow = row0 + r;
@@ -546,10 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int c = c0 + i;
-              if (c < ntok) {
+              if (c < p.M) {
                 if constexpr (GROUPED) {
-                  const int tok = list_tok[c] & 0xff, slot = list_tok[c] >> 8;
-                  p.y[(size_t(tok) * p.topk + slot) * p.N + (grow - e * p.N)] = v[i] * __ldg(p.a_scale + tok);
+                  const int slot = slot_of[c];
+                  if (slot >= 0) p.y[(size_t(c) * p.topk + slot) * p.N + (grow - e * p.N)] = v[i] * __ldg(p.a_scale + c);
                 } else {
                   p.y[size_t(c) * p.N + grow] = v[i] * __ldg(p.a_scale + c);
                 }
