@@ -28,9 +28,9 @@
 //    the current one;
 //  * warp 1 (one lane) issues 4 tcgen05.mma kind::mxf8f6f4.block_scale
 //    (K = 32 each) per k-tile with A from TMEM and B (the E4M3 activations,
-//    resident in shared memory for the CTA's K range, landed by 16-byte
-//    asynchronous copies at the start) from a K-major shared-memory
-//    descriptor; B scale factors are 2^0.  The E8M0 group scale is exactly the
+//    resident in shared memory for the CTA's K range, landed by the epilogue
+//    warps' 16-byte asynchronous copies while the decoders start) from a
+//    K-major shared-memory descriptor; B scale factors are 2^0.  The E8M0 group scale is exactly the
 //    MX block scale of a 32-wide K block, so the tensor core applies it;
 //  * warps 18..21 are the epilogue: tcgen05.ld the accumulator (two
 //    accumulators alternate between tiles so the MMA never waits for the
@@ -116,8 +116,8 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 }
 
 // mbarriers (codes full/empty, A full/empty, 2 accumulators full/empty,
-// split-K full/free), then the TMEM base slot and two ints.
-constexpr int kNumBars = 2 * kMaxCodeStages + 2 * kAStages + 4 + 2;
+// B, split-K full/free), then the TMEM base slot and two ints.
+constexpr int kNumBars = 2 * kMaxCodeStages + 2 * kAStages + 4 + 3;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area too small");
 
@@ -149,7 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   uint64_t* a_empty = a_full + kAStages;
   uint64_t* acc_full = a_empty + kAStages;
   uint64_t* acc_empty = acc_full + 2;
-  uint64_t* red_full = acc_empty + 2;
+  uint64_t* b_full = acc_empty + 2;                      // resident activations landed
+  uint64_t* red_full = b_full + 1;
   uint64_t* red_free = red_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_free + 1);
   int* misc = reinterpret_cast<int*>(tmem_slot + 2);     // [1] experts used (grouped)
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);
     }
+    mbar_init(b_full, 128);
     mbar_init(red_full, (cs > 1 ? cs - 1 : 1) * 128);
     mbar_init(red_free, 128);
     fence_barrier_init();
@@ -287,23 +289,6 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       tmem_alloc(tmem_slot, kTmemCols);
       tmem_relinquish();
     }
-    {
-      // resident activations for this CTA's K range, K-major core-matrix
-      // layout: chunk c (16 k) at c * NTOK * 16, token group j at j * 128,
-      // token % 8 at * 16; token rows >= M are zero-filled.  A grouped call
-      // keeps every token resident: the MMAs run over all token columns and
-      // the epilogue keeps the columns of the tokens routed to the unit's
-      // expert.  One 16-byte asynchronous copy per chunk, all in flight.
-      const int kb = kt0 * 128, nchunk = (kt1 - kt0) * 8, total = NTOK * nchunk;
-      for (int i = tid - 32; i < total; i += kThreads - 32) {
-        const int tok = i % NTOK, c = i / NTOK;
-        const bool real = tok < p.M;
-        cp_async16_zfill(smem_u32(b_s + c * NTOK * 16 + (tok >> 3) * 128 + (tok & 7) * 16),
-                         real ? p.a + size_t(tok) * p.K + kb + c * 16 : p.a, real ? 16u : 0u);
-      }
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-    }
     tc_fence_before();
     named_bar_sync(3, kThreads - 32);                     // everyone but the producer
     tc_fence_after();
@@ -329,6 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
         // with n = unit * (k-tiles of g per unit) + (kt - kt0) / kDecGroups
         const int nk = kt1 - kt0;
         const uint32_t b_base = smem_u32(b_s);
+        wait_bounded(b_full, 0);                        // resident activations landed
+        tc_fence_after();
         for (int ui = 0; ui < n_units; ++ui) {
           const int abuf = ui & 1;
           wait_bounded(&acc_empty[abuf], ((ui >> 1) & 1) ^ 1);
@@ -448,6 +435,26 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       }
     } else {
       // ------------------------------------------------------------ epilogue --
+      {
+        // Resident activations for this CTA's K range (the epilogue warps
+        // have nothing else to do before the first accumulator; the decoders
+        // start at once), K-major core-matrix layout: chunk c (16 k) at
+        // c * NTOK * 16, token group j at j * 128, token % 8 at * 16; token
+        // rows >= M are zero-filled.  A grouped call keeps every token
+        // resident: the MMAs run over all token columns and the epilogue keeps
+        // the columns of the tokens routed to the unit's expert.  16-byte
+        // asynchronous copies, all in flight; the MMA issuer waits on b_full.
+        const int kb = kt0 * 128, nchunk = (kt1 - kt0) * 8, total = NTOK * nchunk;
+        for (int i = tid - kEpiWarp0 * 32; i < total; i += 128) {
+          const int tok = i % NTOK, c = i / NTOK;
+          const bool real = tok < p.M;
+          cp_async16_zfill(smem_u32(b_s + c * NTOK * 16 + (tok >> 3) * 128 + (tok & 7) * 16),
+                           real ? p.a + size_t(tok) * p.K + kb + c * 16 : p.a, real ? 16u : 0u);
+        }
+        cp_async_wait_all();
+        fence_proxy_async_smem();                       // visible to the tensor core
+        mbar_arrive(b_full);
+      }
       if (cs > 1) cluster_wait();
       const int q = warp & 3, ew = warp - kEpiWarp0;
       const int r = 32 * q + lane;
