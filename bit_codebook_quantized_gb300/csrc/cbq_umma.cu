@@ -308,34 +308,49 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       if (cs > 1) cluster_wait();
       // --------------------------------------------------------- MMA issuer --
       if (lane == 0) {
-        // k-tile kt of a unit belongs to decoder group (kt - kt0) % kDecGroups,
+        // k-tile i (from kt0) of a unit belongs to decoder group i % kDecGroups,
         // which owns A slots g and g + kDecGroups and uses them alternately:
         // use n of group g -> slot (n & 1) * kDecGroups + g, phase n >> 1,
-        // with n = unit * (k-tiles of g per unit) + (kt - kt0) / kDecGroups
+        // with n = (its uses in earlier units) + i / kDecGroups.  The loop is
+        // unrolled over the groups so each group's use count is a register,
+        // and descriptors advance by adding offsets: this thread shares its
+        // sub-partition with decoder warps, so every instruction here counts.
         const int nk = kt1 - kt0;
-        const uint32_t b_base = smem_u32(b_s);
+        const uint64_t bd0 = umma_desc_kmajor(smem_u32(b_s), NTOK * 16, 128);
+        const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
+        const uint32_t a_col = tbase + kACol, sfa_col = tbase + kSfaCol, sfb_col = tbase + kSfbCol;
+        uint32_t nbase[kDecGroups];
+#pragma unroll
+        for (int g = 0; g < kDecGroups; ++g) nbase[g] = 0;
         wait_bounded(b_full, 0);                        // resident activations landed
         tc_fence_after();
         for (int ui = 0; ui < n_units; ++ui) {
           const int abuf = ui & 1;
           wait_bounded(&acc_empty[abuf], ((ui >> 1) & 1) ^ 1);
           tc_fence_after();
-          const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
-          for (int kt = kt0; kt < kt1; ++kt) {
-            const int i = kt - kt0, grp = i % kDecGroups;
-            const uint32_t n = static_cast<uint32_t>(ui * ((nk + kDecGroups - 1 - grp) / kDecGroups) + i / kDecGroups);
-            const int slot = static_cast<int>(n & 1u) * kDecGroups + grp;
-            wait_bounded(&a_full[slot], (n >> 1) & 1u);
-            tc_fence_after();
+          const uint32_t d_col = tbase + abuf * kAccCols;
+          for (int i0 = 0; i0 < nk; i0 += kDecGroups) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint64_t bd = umma_desc_kmajor(b_base + (i * 8 + 2 * j) * NTOK * 16, NTOK * 16, 128);
-              umma_mxf8_ts(tbase + abuf * kAccCols, tbase + kACol + slot * 32 + j * 8, bd,
-                           idesc | (uint32_t(j) << 29), tbase + kSfaCol + slot * 4, tbase + kSfbCol,
-                           (i | j) != 0);
+            for (int g = 0; g < kDecGroups; ++g) {
+              const int i = i0 + g;
+              if (i < nk) {
+                const uint32_t n = nbase[g] + static_cast<uint32_t>(i0 / kDecGroups);
+                const uint32_t slot = (n & 1u) * kDecGroups + g;
+                wait_bounded(&a_full[slot], (n >> 1) & 1u);
+                tc_fence_after();
+                // B of k-tile i: chunks 8 i .. 8 i + 7 at (chunk * NTOK * 16) bytes,
+                // i.e. (chunk * NTOK) in the descriptor's 16-byte address units
+                const uint64_t bdi = bd0 + static_cast<uint64_t>(i * 8 * NTOK);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  umma_mxf8_ts(d_col, a_col + slot * 32 + j * 8, bdi + static_cast<uint64_t>(2 * j * NTOK),
+                               idesc | (uint32_t(j) << 29), sfa_col + slot * 4, sfb_col, (i | j) != 0);
+                umma_commit(&a_empty[slot]);
+              }
             }
-            umma_commit(&a_empty[slot]);
           }
+#pragma unroll
+          for (int g = 0; g < kDecGroups; ++g) nbase[g] += static_cast<uint32_t>((nk + kDecGroups - 1 - g) / kDecGroups);
           umma_commit(&acc_full[abuf]);
         }
       }
