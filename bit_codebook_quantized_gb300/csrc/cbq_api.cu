@@ -114,14 +114,13 @@ int cbq_gemm_auto_path(int32_t M, int32_t N, int32_t K) {
   if (M < 1 || M > 64 || N < 1 || K < 128 || K % 128 != 0) return CBQ_EINVAL;
   // Measured on GB300 (CUDA graphs of back-to-back calls, weights beyond L2):
   // up to 8 token rows the GEMV kernel wins on matrices up to ~64 M weights
-  // and the stream-K kernel beyond; from 9 rows the stream-K kernel wins up
-  // to ~128 M weights; elsewhere, or where the stream-K kernel's resident
-  // activations do not fit, the tile kernel.  The tile kernel needs its
-  // activations resident too; where they do not fit, the GEMV kernel runs
-  // (see cbq_gemm_path).
+  // and the tile kernel beyond; from 9 rows the stream-K kernel wins up to
+  // ~128 M weights if its resident activations fit, the tile kernel
+  // elsewhere.  The tile kernel needs its activations resident too; where
+  // they do not fit, the GEMV kernel runs (see cbq_gemm_path).
   const long long weights = static_cast<long long>(N) * K;
-  if (M <= 8 && weights <= (1LL << 26)) return CBQ_PATH_GEMV;
-  if ((M <= 8 || weights <= (1LL << 27)) && sk_applicable(M, N, K)) return CBQ_PATH_STREAMK;
+  if (M <= 8) return weights <= (1LL << 26) ? CBQ_PATH_GEMV : CBQ_PATH_MMA;
+  if (weights <= (1LL << 27) && sk_applicable(M, N, K)) return CBQ_PATH_STREAMK;
   return CBQ_PATH_MMA;
 }
 

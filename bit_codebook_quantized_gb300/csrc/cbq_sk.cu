@@ -265,13 +265,23 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           if (p.b_layout == 0) tma_load_2d(dst, &p.a_map, b_full, c * 128, 0);
           else tma_load_3d(dst, &p.a_map, b_full, 0, 0, 8 * c);
         }
-        const uint32_t b_base = smem_u32(b_s);
+        // Descriptors advance by adding offsets in their 16-byte address
+        // units (every shared address here is below 256 KB, so the 14-bit
+        // address field never carries): A slot as at as * kASlotBytes, its
+        // K chunk pair j at 2 j * 2048; B slot at bsl * NTOK * 128, its MMA j
+        // at 32 j (swizzled) or 2 j * NTOK * 16 bytes (core matrices).
         const uint32_t a_base = smem_u32(a_s);
+        const uint64_t ad0 = umma_desc_kmajor(a_base, kRows * 16, 128);
+        const uint64_t sd0 = umma_desc_kmajor(a_base + kASlotA, 128, 128);
+        const uint64_t bd0 = p.b_layout == 0 ? umma_desc_kmajor_sw128(smem_u32(b_s))
+                                             : umma_desc_kmajor(smem_u32(b_s), NTOK * 16, 128);
+        const uint32_t b_step_j = p.b_layout == 0 ? 2u : 2u * NTOK;
         const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
+        const uint32_t sfa0 = tbase + TM::kSfa, sfb = tbase + TM::kSfb;
         wait_bounded(b_full, 0);
-        int seg = 0, c = c_first, as = 0;
+        int seg = 0, c = c_first, as = 0, bsl = 0;
         uint32_t a_phase = 0;
-        for (int i = 0; i < n_units; ++i, c = (c + 1 == KT) ? 0 : c + 1) {
+        for (int i = 0; i < n_units; ++i) {
           const bool seg_first = (i == 0) || (c == 0);
           const int abuf = seg & 1;
           if (seg_first) {
@@ -280,22 +290,18 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           }
           wait_bounded(&a_full[as], a_phase);
           tc_fence_after();
-          const uint32_t slot_addr = a_base + as * kASlotBytes;
+          const uint64_t a_off = static_cast<uint64_t>(as * (kASlotBytes >> 4));
           // the unit's scale rows -> 4 TMEM columns (row r's scale word sits
           // in every 32-bit word of its 16-byte row, whichever column the MMA
           // reads for it)
-          tmem_cp_128x128b(tbase + TM::kSfa + 4 * as, umma_desc_kmajor(slot_addr + kASlotA, 128, 128));
-          int bsl = c - c_first;
-          if (bsl < 0) bsl += KT;
-          const uint32_t b_slot = b_base + bsl * NTOK * 128;
+          tmem_cp_128x128b(sfa0 + 4 * as, sd0 + a_off);
+          const uint64_t adu = ad0 + a_off;
+          const uint64_t bdu = bd0 + static_cast<uint64_t>(bsl * NTOK * 8);
+          const uint32_t d_col = tbase + TM::kAcc + abuf * TM::kAccStride;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint64_t ad = umma_desc_kmajor(slot_addr + 2 * j * (kRows * 16), kRows * 16, 128);
-            const uint64_t bd = p.b_layout == 0 ? umma_desc_kmajor_sw128(b_slot + 32 * j)
-                                                : umma_desc_kmajor(b_slot + 2 * j * NTOK * 16, NTOK * 16, 128);
-            umma_mxf8(tbase + TM::kAcc + abuf * TM::kAccStride, ad, bd, idesc | (uint32_t(j) << 29),
-                      tbase + TM::kSfa + 4 * as, tbase + TM::kSfb, (seg_first && j == 0) ? 0u : 1u);
-          }
+          for (int j = 0; j < 4; ++j)
+            umma_mxf8(d_col, adu + static_cast<uint64_t>(j * 256), bdu + static_cast<uint64_t>(j * b_step_j),
+                      idesc | (uint32_t(j) << 29), sfa0 + 4 * as, sfb, (seg_first && j == 0) ? 0u : 1u);
           umma_commit(&a_empty[as]);
           if (++as == S) {
             as = 0;
@@ -305,6 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
             umma_commit(&acc_full[abuf]);
             ++seg;
           }
+          c = (c + 1 == KT) ? 0 : c + 1;
+          bsl = (bsl + 1 == KT) ? 0 : bsl + 1;        // (c - c_first) mod KT
         }
       }
       __syncwarp();

@@ -132,10 +132,11 @@ def test_auto_path_choice(L):
     # host-only decision table of cbq_gemm (no device access)
     assert L.cbq_gemm_auto_path(1, 12288, 4096) == ops.PATH_GEMV
     assert L.cbq_gemm_auto_path(8, 12288, 4096) == ops.PATH_GEMV
-    # large matrices at small M: the stream-K kernel (its plan needs no device
-    # for these shapes); at M = 64 its resident activations do not fit
-    assert L.cbq_gemm_auto_path(1, 151936, 2048) == ops.PATH_STREAMK
-    assert L.cbq_gemm_auto_path(8, 151936, 2048) == ops.PATH_STREAMK
+    assert L.cbq_gemm_auto_path(1, 151936, 2048) == ops.PATH_MMA
+    assert L.cbq_gemm_auto_path(8, 151936, 2048) == ops.PATH_MMA
+    # the stream-K plan needs no device for these shapes; at M = 64 on the
+    # vocabulary head its resident activations do not fit
+    assert L.cbq_gemm_auto_path(16, 25600, 5120) == ops.PATH_STREAMK
     assert L.cbq_gemm_auto_path(64, 151936, 2048) == ops.PATH_MMA
     assert L.cbq_gemm_auto_path(0, 16, 128) == ops.EINVAL
     assert L.cbq_gemm_auto_path(4, 16, 100) == ops.EINVAL
