@@ -363,18 +363,13 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         // release can never count towards an older phase
         wait_bounded(&full[slot], st_phase);
         uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, c2 = c0;
-        if (r < geo.rows(tu)) {
-          // units before this one in the stage: k of them, each rows * 48 bytes
-          int tb = tu, cb0 = cu, rel = 0;
-          for (int kk = 0; kk < k; ++kk) {
-            if (cb0 == 0) {
-              --tb;
-              cb0 = KT;
-            }
-            --cb0;
-            rel += geo.rows(tb) * 48;
-          }
-          const uint32_t at = codes_base + slot * kStageBytes + rel + r * 48;
+        const int rows_u = geo.rows(tu);
+        if (r < rows_u) {
+          // units before this one in the stage: k of them, min(k, cu) in tile
+          // tu (rows_u rows each; tu may be the ragged last tile) and the
+          // rest in full tiles before it
+          const int kin = min(k, cu);
+          const uint32_t at = codes_base + slot * kStageBytes + (kin * rows_u + (k - kin) * kRows + r) * 48;
           c0 = lds128(at);
           c1 = lds128(at + 16);
           c2 = lds128(at + 32);
