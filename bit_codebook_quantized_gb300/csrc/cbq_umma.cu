@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
         mbar_arrive(b_full);
       }
       if (cs > 1) cluster_wait();
-      const int q = warp & 3, ew = warp - kEpiWarp0;
+      const int q = warp & 3;
       const int r = 32 * q + lane;
       const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
       int prev_e = -1;
