@@ -22,10 +22,11 @@
 //    byte-permutes through the row's codebook (two registers), then writes the
 //    128 bytes into its TMEM lane (tcgen05.st, 32 columns) as the MMA's A
 //    operand, and its 4 E8M0 group-scale bytes into TMEM as the A scale
-//    factors.  Each group owns two A slots; the wait for the TMEM stores of
-//    one k-tile is overlapped with decoding the next; scale bytes are pulled
-//    into L1 16 k-tiles ahead and the next tile's codebook is loaded during
-//    the current one;
+//    factors.  Each group owns two A slots; while one warp waits for its
+//    TMEM stores the other groups' warps decode (deferring that wait past the
+//    warp's next decode measured no different); scale bytes are pulled into
+//    L1 16 k-tiles ahead and the next tile's codebook is loaded during the
+//    current one;
 //  * warp 1 (one lane) issues 4 tcgen05.mma kind::mxf8f6f4.block_scale
 //    (K = 32 each) per k-tile with A from TMEM and B (the E4M3 activations,
 //    resident in shared memory for the CTA's K range, landed by the epilogue
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
         decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, v + 24);
       };
       // Issue the TMEM stores of a decoded k-tile (A operand and its scale
-      // factors); the wait for them comes later, after the next decode.
+      // factors); publish() waits for them and hands the slot to the MMA.
       // This group's A slots are dg and dg + kDecGroups, used alternately in
       // the group's own k-tile order (so a slot's parity wait cannot be two
       // uses early): use n -> slot (n & 1) * kDecGroups + dg, phase n >> 1.
