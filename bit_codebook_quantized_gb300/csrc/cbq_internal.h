@@ -26,6 +26,7 @@ struct GemvParams {
 
 // Kernel parameters of the tcgen05 kernel (dense and grouped).
 struct UmmaParams {
+  CUtensorMap a_map;          // activations a[M][K]: box of ntok rows x 128 B (one k-tile), 128-byte swizzle
   const uint8_t* codes;       // code stream (tile order), expert stack for grouped calls
   const uint8_t* a;
   const float* a_scale;

@@ -29,9 +29,10 @@
 //    current one;
 //  * warp 1 (one lane) issues 4 tcgen05.mma kind::mxf8f6f4.block_scale
 //    (K = 32 each) per k-tile with A from TMEM and B (the E4M3 activations,
-//    resident in shared memory for the CTA's K range, landed by the epilogue
-//    warps' 16-byte asynchronous copies while the decoders start) from a
-//    K-major shared-memory descriptor; B scale factors are 2^0.  The E8M0 group scale is exactly the
+//    resident in shared memory for the CTA's K range: one TMA box of ntok
+//    rows x 128 B per k-tile with the 128-byte swizzle, issued by an epilogue
+//    thread while the decoders start) from a K-major swizzled shared-memory
+//    descriptor; B scale factors are 2^0.  The E8M0 group scale is exactly the
 //    MX block scale of a 32-wide K block, so the tensor core applies it;
 //  * warps 18..21 are the epilogue: tcgen05.ld the accumulator (two
 //    accumulators alternate between tiles so the MMA never waits for the
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);
     }
-    mbar_init(b_full, 128);
+    mbar_init(b_full, 1);
     mbar_init(red_full, (cs > 1 ? cs - 1 : 1) * 128);
     mbar_init(red_free, 128);
     fence_barrier_init();
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
         // and descriptors advance by adding offsets: this thread shares its
         // sub-partition with decoder warps, so every instruction here counts.
         const int nk = kt1 - kt0;
-        const uint64_t bd0 = umma_desc_kmajor(smem_u32(b_s), NTOK * 16, 128);
+        const uint64_t bd0 = umma_desc_kmajor_sw128(smem_u32(b_s));
         const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
         const uint32_t a_col = tbase + kACol, sfa_col = tbase + kSfaCol, sfb_col = tbase + kSfbCol;
         uint32_t nbase[kDecGroups];
@@ -339,12 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
                 const uint32_t slot = (n & 1u) * kDecGroups + g;
                 wait_bounded(&a_full[slot], (n >> 1) & 1u);
                 tc_fence_after();
-                // B of k-tile i: chunks 8 i .. 8 i + 7 at (chunk * NTOK * 16) bytes,
-                // i.e. (chunk * NTOK) in the descriptor's 16-byte address units
-                const uint64_t bdi = bd0 + static_cast<uint64_t>(i * 8 * NTOK);
+                // B of k-tile i: NTOK swizzled rows of 128 bytes at i * NTOK * 128,
+                // i.e. i * NTOK * 8 in the descriptor's 16-byte address units;
+                // MMA j reads K bytes [32 j, 32 j + 32) of the rows (+2 j)
+                const uint64_t bdi = bd0 + static_cast<uint64_t>(i * NTOK * 8);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                  umma_mxf8_ts(d_col, a_col + slot * 32 + j * 8, bdi + static_cast<uint64_t>(2 * j * NTOK),
+                  umma_mxf8_ts(d_col, a_col + slot * 32 + j * 8, bdi + static_cast<uint64_t>(2 * j),
                                idesc | (uint32_t(j) << 29), sfa_col + slot * 4, sfb_col, (i | j) != 0);
                 umma_commit(&a_empty[slot]);
               }
@@ -451,25 +453,17 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       }
     } else {
       // ------------------------------------------------------------ epilogue --
-      {
-        // Resident activations for this CTA's K range (the epilogue warps
-        // have nothing else to do before the first accumulator; the decoders
-        // start at once), K-major core-matrix layout: chunk c (16 k) at
-        // c * NTOK * 16, token group j at j * 128, token % 8 at * 16; token
-        // rows >= M are zero-filled.  A grouped call keeps every token
-        // resident: the MMAs run over all token columns and the epilogue keeps
-        // the columns of the tokens routed to the unit's expert.  16-byte
-        // asynchronous copies, all in flight; the MMA issuer waits on b_full.
-        const int kb = kt0 * 128, nchunk = (kt1 - kt0) * 8, total = NTOK * nchunk;
-        for (int i = tid - kEpiWarp0 * 32; i < total; i += 128) {
-          const int tok = i % NTOK, c = i / NTOK;
-          const bool real = tok < p.M;
-          cp_async16_zfill(smem_u32(b_s + c * NTOK * 16 + (tok >> 3) * 128 + (tok & 7) * 16),
-                           real ? p.a + size_t(tok) * p.K + kb + c * 16 : p.a, real ? 16u : 0u);
-        }
-        cp_async_wait_all();
-        fence_proxy_async_smem();                       // visible to the tensor core
-        mbar_arrive(b_full);
+      if (tid == kEpiWarp0 * 32) {
+        // Resident activations for this CTA's K range, issued by one thread
+        // of the epilogue (nothing else to do before the first accumulator;
+        // the decoders start at once): one TMA box per k-tile, NTOK token
+        // rows of 128 bytes in the 128-byte swizzled K-major layout at
+        // (kt - kt0) * NTOK * 128; token rows >= M are outside the tensor and
+        // arrive as zeros.  A grouped call keeps every token resident: the
+        // MMAs run over all token columns and the epilogue keeps the columns
+        // of the tokens routed to the unit's expert.
+        mbar_arrive_expect_tx(b_full, static_cast<uint32_t>((kt1 - kt0) * NTOK * 128));
+        for (int c = kt0; c < kt1; ++c) tma_load_2d(b_s + (c - kt0) * NTOK * 128, &p.a_map, b_full, c * 128, 0);
       }
       if (cs > 1) cluster_wait();
       const int q = warp & 3;
@@ -659,12 +653,29 @@ int code_stages_for(int b_bytes, int red_bytes, bool grouped) {
 // Token columns of the MMA (its N): 16, 32 or 64.
 int ntok_for(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
+// Activations a[M][K] as a TMA tensor whose box is one k-tile (128 bytes) of
+// ntok token rows, landed with the 128-byte swizzle; rows past M read as zeros.
+int encode_a_map(UmmaParams& p, int ntok) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return CBQ_ECUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K)};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(ntok)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(&p.a_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.a), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? CBQ_OK
+             : CBQ_ECUDA;
+}
+
 }  // namespace
 
 int launch_umma(const UmmaParams& p_in, bool grouped, cudaStream_t stream) {
   UmmaParams p = p_in;
   const int sms = device_sm_count();
   const int ntok = ntok_for(p.M);
+  if (const int em = encode_a_map(p, ntok); em != CBQ_OK) return em;
   const int nkt = p.K / 128;
   const int tiles = (p.N + kRows - 1) / kRows;
   if (grouped) {
