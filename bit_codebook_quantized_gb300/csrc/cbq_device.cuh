@@ -155,14 +155,6 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
-// 16-byte asynchronous copy that reads `src_bytes` (16 or 0) bytes from
-// global memory and fills the rest of the 16 with zeros; both addresses
-// 16-byte aligned.  cp_async_wait_all waits for every copy this thread issued.
-__device__ __forceinline__ void cp_async16_zfill(uint32_t smem_addr, const void* gptr, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr), "l"(gptr), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // 2-D tiled TMA load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar,
