@@ -87,12 +87,10 @@ __device__ __forceinline__ bool status_set() {
   return *reinterpret_cast<volatile unsigned*>(&g_status_umma) != 0u;
 }
 
-// Wait for an mbarrier phase, suspended in the barrier between polls: warps
-// that poll in a loop take issue slots and shared-memory bandwidth from the
-// warps they wait for (at the start of a grouped call, polling decoder warps
-// slowed the activation gather several-fold).  After ~0.5 ms give up at once
-// if another wait already timed out; after kWaitLimitNs raise kErrTimeout
-// and give up.
+// Wait for an mbarrier phase, suspended in the barrier between polls (a
+// polling warp takes issue slots from the warps it waits for).  After ~0.5 ms
+// give up at once if another wait already timed out; after kWaitLimitNs
+// raise kErrTimeout and give up.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
   if (CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
