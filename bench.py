@@ -175,10 +175,15 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(kernel: str) -> str:
+    """Hash of the kernel's code: its sources with // comments and blank lines
+    removed, so a comment-only edit keeps the recorded counters."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_codebook_quantized_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel]:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        for line in open(os.path.join(csrc, f), encoding="utf-8"):
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 
