@@ -60,3 +60,46 @@ def test_reference_arm_under_torchrun_prints_once():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 2
     assert d["cpu_baseline"]["kind"] == "oracle" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def _load_bench(root):
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    b.ROOT = root
+    return b
+
+
+def test_kernel_hash_ignores_comments_and_sees_code(tmp_path):
+    # the recorded DRAM counters stay valid across comment edits, not code edits
+    import shutil
+    src = os.path.join(ROOT, "bit_codebook_quantized_gb300", "csrc")
+    dst = tmp_path / "bit_codebook_quantized_gb300" / "csrc"
+    shutil.copytree(src, dst)
+    b = _load_bench(str(tmp_path))
+    h0 = b.kernel_source_hash("gemv_kernel")
+    f = dst / "cbq_gemv.cu"
+    text = f.read_text()
+    f.write_text(text.replace("namespace cbq {", "namespace cbq {  // an added comment\n// and a comment line", 1))
+    assert b.kernel_source_hash("gemv_kernel") == h0
+    f.write_text(text.replace("constexpr int kStages = 4;", "constexpr int kStages = 5;", 1))
+    assert b.kernel_source_hash("gemv_kernel") != h0
+    assert b.kernel_source_hash("sk_kernel") != b.kernel_source_hash("umma_kernel")
+
+
+def test_profiled_traffic_needs_a_matching_hash(tmp_path):
+    import shutil
+    shutil.copytree(os.path.join(ROOT, "bit_codebook_quantized_gb300", "csrc"),
+                    tmp_path / "bit_codebook_quantized_gb300" / "csrc")
+    (tmp_path / "profiles").mkdir()
+    b = _load_bench(str(tmp_path))
+    h = b.kernel_source_hash("gemv_kernel")
+    prof = tmp_path / "profiles" / "cbq_gemm_decode_4096x12288.md"
+    prof.write_text(f"kernel_source_sha256[gemv_kernel]: {h}\n"
+                    "dram_bytes_per_launch[gemv_kernel] M=1: 100\n"
+                    "dram_bytes_per_launch[gemv_kernel] M=8: 200\n")
+    assert b.profiled_traffic("gemv_kernel") == {"1": 100.0, "8": 200.0}
+    assert b.profiled_traffic("sk_kernel") is None                 # no counters recorded for it
+    prof.write_text(prof.read_text().replace(h, "0" * 16))
+    assert b.profiled_traffic("gemv_kernel") is None                # sources changed since
