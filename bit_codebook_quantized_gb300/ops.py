@@ -27,7 +27,7 @@ OK, EINVAL, ECUDA, EDEVICE, ETIMEOUT, EROUTING = 0, -1, -2, -3, -4, -5
 EXPORTS = ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path", "cbq_gemm_auto_path",
            "cbq_gemm_noalloc",
            "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_launch_count",
-           "cbq_status_str")
+           "cbq_status_str", "cbq_draft_length")
 
 
 class CbqError(RuntimeError):
@@ -71,9 +71,11 @@ def lib() -> ctypes.CDLL:
         L.cbq_launch_count.restype = ctypes.c_uint64
         L.cbq_status_str.argtypes = [ctypes.c_int]
         L.cbq_status_str.restype = ctypes.c_char_p
+        dp = ctypes.POINTER(ctypes.c_double)
+        L.cbq_draft_length.argtypes = [ctypes.c_double, ctypes.c_double, i32, ctypes.POINTER(i32), dp, dp]
         for name in ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path", "cbq_gemm_auto_path",
                      "cbq_gemm_noalloc",
-                     "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status"):
+                     "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_draft_length"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
         return L
@@ -84,6 +86,16 @@ def auto_path(M: int, N: int, K: int) -> int:
     p = lib().cbq_gemm_auto_path(M, N, K)
     _check(p if p < 0 else OK, "cbq_gemm_auto_path")
     return p
+
+
+def draft_length(q: float, c: float, dmax: int) -> tuple[int, float, float]:
+    """(d*, E[N_d*], E[N_d*] / T(d*)) of cbq_draft_length: the draft length
+    that maximises expected tokens per unit of round time."""
+    d = ctypes.c_int32(0)
+    e, r = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    _check(lib().cbq_draft_length(float(q), float(c), int(dmax), ctypes.byref(d), ctypes.byref(e),
+                                  ctypes.byref(r)), "cbq_draft_length")
+    return d.value, e.value, r.value
 
 
 def status_str(status: int) -> str:

@@ -187,6 +187,23 @@ uint64_t cbq_launch_count(void);
 /* Human-readable text for a status code (static storage). */
 const char *cbq_status_str(int status);
 
+/* Draft length of the next speculative round ("Hibana: Fast Agentic
+ * Inference on Unified-Memory Devices", section "Adaptive speculation /
+ * Adaptive draft length"): d* = argmax over 1 <= d <= dmax of
+ * E[N_d] / T(d), with E[N_d] = sum_{j=0..d} q^j the expected tokens a round
+ * emits (accepted prefix + the target's own token) and T(d) = 1 + c (d - 1)
+ * its time relative to d = 1.  The verify round that follows multiplies
+ * d* + 1 token rows per request.
+ *   q      acceptance probability of a drafted token, in [0, 1]
+ *   c      added relative cost of one more draft token, finite and >= 0
+ *   dmax   longest draft allowed, >= 1
+ *   d_star out: the chosen length (ties go to the shorter draft)
+ *   expected_tokens, tokens_per_time: out, may be NULL: E[N_d*] and
+ *          E[N_d*] / T(d*)
+ * Host only (no device work); CBQ_EINVAL on arguments out of range. */
+int cbq_draft_length(double q, double c, int32_t dmax, int32_t *d_star,
+                     double *expected_tokens, double *tokens_per_time);
+
 #ifdef __cplusplus
 }
 #endif
