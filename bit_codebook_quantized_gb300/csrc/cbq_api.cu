@@ -1,6 +1,6 @@
 // cbq_api.cu -- the C entry points declared in include/cbq.h: argument
 // checks and kernel selection.  All device work is done by the kernels in
-// cbq_sk.cu, cbq_gemv.cu and cbq_umma.cu; this file launches them on the
+// cbq_sk.cu, cbq_gemv.cu, cbq_umma.cu and cbq_budget.cu; this file launches them on the
 // caller's stream and never synchronises (except cbq_device_status).
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -296,6 +296,16 @@ int cbq_device_status(void* stream) {
   if (v & 1u) return CBQ_ETIMEOUT;
   if (v & 2u) return CBQ_EROUTING;
   return CBQ_OK;
+}
+
+int cbq_select_budget(const float* logits, int32_t T, int32_t E, int32_t k, int32_t B, int32_t* budget,
+                      int32_t* topk_idx, void* stream) {
+  if (T < 1 || E < 1 || E > kMaxBudgetExperts || k < 1 || B < k || B > E) return CBQ_EINVAL;
+  if (!logits || !aligned(logits, 4) || !budget || !aligned(budget, 4) || !topk_idx || !aligned(topk_idx, 4))
+    return CBQ_EINVAL;
+  const int st = current_device_checked(nullptr);
+  if (st != CBQ_OK) return st;
+  return launch_budget(logits, T, E, k, B, budget, topk_idx, static_cast<cudaStream_t>(stream));
 }
 
 uint64_t cbq_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

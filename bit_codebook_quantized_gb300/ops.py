@@ -27,7 +27,7 @@ OK, EINVAL, ECUDA, EDEVICE, ETIMEOUT, EROUTING = 0, -1, -2, -3, -4, -5
 EXPORTS = ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path", "cbq_gemm_auto_path",
            "cbq_gemm_noalloc",
            "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_launch_count",
-           "cbq_status_str", "cbq_draft_length")
+           "cbq_status_str", "cbq_draft_length", "cbq_select_budget")
 
 
 class CbqError(RuntimeError):
@@ -73,9 +73,11 @@ def lib() -> ctypes.CDLL:
         L.cbq_status_str.restype = ctypes.c_char_p
         dp = ctypes.POINTER(ctypes.c_double)
         L.cbq_draft_length.argtypes = [ctypes.c_double, ctypes.c_double, i32, ctypes.POINTER(i32), dp, dp]
+        L.cbq_select_budget.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
         for name in ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path", "cbq_gemm_auto_path",
                      "cbq_gemm_noalloc",
-                     "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_draft_length"):
+                     "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_draft_length",
+                     "cbq_select_budget"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
         return L
@@ -86,6 +88,20 @@ def auto_path(M: int, N: int, K: int) -> int:
     p = lib().cbq_gemm_auto_path(M, N, K)
     _check(p if p < 0 else OK, "cbq_gemm_auto_path")
     return p
+
+
+def select_budget(logits: torch.Tensor, k: int, B: int, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """(budget [B] ascending expert ids, topk_idx [T, k]) of cbq_select_budget
+    for router logits [T, E] (fp32, on the GPU)."""
+    if logits.dtype != torch.float32 or logits.dim() != 2 or not logits.is_cuda:
+        raise CbqError(EINVAL, "select_budget: logits must be a CUDA float32 [T, E] tensor")
+    logits = logits.contiguous()
+    T, E = logits.shape
+    budget = torch.empty(max(B, 0), dtype=torch.int32, device=logits.device)
+    topk = torch.empty((T, max(k, 0)), dtype=torch.int32, device=logits.device)
+    _check(lib().cbq_select_budget(logits.data_ptr(), T, E, int(k), int(B), budget.data_ptr(),
+                                   topk.data_ptr(), _stream(stream)), "cbq_select_budget")
+    return budget, topk
 
 
 def draft_length(q: float, c: float, dmax: int) -> tuple[int, float, float]:

@@ -187,6 +187,27 @@ uint64_t cbq_launch_count(void);
 /* Human-readable text for a status code (static storage). */
 const char *cbq_status_str(int status);
 
+/* Shared expert budget of one MoE verify round ("Hibana: Fast Agentic
+ * Inference on Unified-Memory Devices", section "Adaptive speculation /
+ * Expert sharing"): the round reads only B experts, and a token's choice
+ * outside them is replaced by one inside.  Rule (the page gives a toy only):
+ * each token ranks experts by its logit (higher first, ties -> lower id) and
+ * takes its own top-k; expert e scores sum_t (k - rank of e in t's top-k);
+ * the budget is the B best-scoring experts (ties -> lower id); each token
+ * then takes its top-k among the budget.
+ *   logits   device fp32 [T][E] router logits, finite
+ *   T        tokens of the round, >= 1
+ *   E        experts, 1 <= E <= 4096
+ *   k        choices per token, 1 <= k <= B
+ *   B        budget, k <= B <= E
+ *   budget   device int32 [B] out: the budget's expert ids, ascending
+ *   topk_idx device int32 [T][k] out: each token's choices in rank order
+ *            (the routing cbq_grouped_gemm takes)
+ * One kernel launch on `stream`; CBQ_EINVAL on bad arguments (no launch). */
+int cbq_select_budget(const float *logits, int32_t T, int32_t E, int32_t k,
+                      int32_t B, int32_t *budget, int32_t *topk_idx,
+                      void *stream);
+
 /* Draft length of the next speculative round ("Hibana: Fast Agentic
  * Inference on Unified-Memory Devices", section "Adaptive speculation /
  * Adaptive draft length"): d* = argmax over 1 <= d <= dmax of

@@ -1,0 +1,51 @@
+"""Oracle for the shared expert budget of a verify round -- TEST INFRASTRUCTURE
+ONLY (tests may import it; the library never does; no code is shared).
+
+"Hibana: Fast Agentic Inference on Unified-Memory Devices", section
+"Adaptive speculation / Expert sharing": verifying drafted tokens loads every
+expert any of them picked; the round gets a shared expert budget so it reads
+fewer weights, and a token's choice outside the budget is replaced by one
+inside it.  The page shows only a toy, so the rule here is a proposal, each
+step the plainest reading and every decision a comparison or an integer sum
+(so two implementations agree exactly):
+
+1. each token ranks the experts by its router logit (higher first, equal
+   logits -> lower expert id) and takes its own top-k;
+2. expert e scores sum over tokens of (k - r) where r is e's rank (0-based)
+   in that token's own top-k (a first choice counts k, a k-th choice 1);
+3. the budget is the B experts with the highest score (ties -> lower id);
+4. each token's final choices are its top-k among the budget experts, in
+   its own rank order (the same comparison as step 1).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _ranked(row, experts):
+    # higher logit first, equal logits -> lower id (compares float32 values exactly)
+    return sorted(experts, key=lambda e: (-float(row[e]), e))
+
+
+def own_topk(logits: np.ndarray, k: int) -> list[list[int]]:
+    T, E = logits.shape
+    return [_ranked(logits[t], range(E))[:k] for t in range(T)]
+
+
+def scores(logits: np.ndarray, k: int) -> list[int]:
+    E = logits.shape[1]
+    s = [0] * E
+    for choices in own_topk(logits, k):
+        for r, e in enumerate(choices):
+            s[e] += k - r
+    return s
+
+
+def select_budget(logits: np.ndarray, k: int, B: int):
+    """(budget as ascending expert ids [B], topk_idx [T][k] in rank order)."""
+    T, E = logits.shape
+    assert 1 <= k <= B <= E and T >= 1
+    s = scores(logits, k)
+    budget = sorted(sorted(range(E), key=lambda e: (-s[e], e))[:B])
+    topk = [_ranked(logits[t], budget)[:k] for t in range(T)]
+    return budget, topk
