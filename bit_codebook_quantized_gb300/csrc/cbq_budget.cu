@@ -14,10 +14,11 @@
 //  4. each token takes its top-k among the budget experts, in rank order.
 // The result (topk_idx, [T][k]) is what cbq_grouped_gemm reads.
 //
-// One CTA of 8 warps (a round has at most a few dozen tokens): a warp finds a
-// token's next choice as the best (logit, id) that ranks after the previous
-// one, so no per-token state beyond the previous pick is kept; expert scores
-// are shared-memory integers.
+// One CTA of 8 warps (a round has at most a few dozen tokens): a warp copies a
+// token's logits into its own shared-memory row once, then finds each next
+// choice as the best (logit, id) that ranks after the previous one, so no
+// per-token state beyond the previous pick is kept; expert scores are
+// shared-memory integers.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -59,7 +60,7 @@ __device__ __forceinline__ void warp_best(V& bv, int& be) {
 // (pv, pe) (pe < 0: the first choice), among the experts `allowed` marks (all
 // if null).  Every lane of the warp returns it.
 __device__ __forceinline__ int next_choice(const float* row, int E, float pv, int pe, const uint8_t* allowed,
-                                           float& bv) {
+                                           float& bv) {   // row: the warp's shared-memory copy
   const int lane = threadIdx.x & 31;
   int be = -1;
   bv = 0.f;
@@ -80,7 +81,15 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_kernel(const float* __r
   __shared__ uint8_t in_budget[kMaxBudgetExperts];
   __shared__ int red_s[kBudgetWarps], red_e[kBudgetWarps];
   __shared__ int pick;
+  extern __shared__ float rows[];                       // [kBudgetWarps][E]: one token row per warp
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* my_row = rows + static_cast<size_t>(warp) * E;
+  auto stage_row = [&](int t) {                         // the token's logits, coalesced, once
+    __syncwarp();
+    const float* g = logits + static_cast<size_t>(t) * E;
+    for (int e = lane; e < E; e += 32) my_row[e] = g[e];
+    __syncwarp();
+  };
   for (int e = tid; e < E; e += kBudgetThreads) {
     score[e] = 0;
     in_budget[e] = 0;
@@ -88,12 +97,12 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_kernel(const float* __r
   __syncthreads();
   // 1, 2: own top-k of every token, scores
   for (int t = warp; t < T; t += kBudgetWarps) {
-    const float* row = logits + static_cast<size_t>(t) * E;
+    stage_row(t);
     float pv = 0.f;
     int pe = -1;
     for (int r = 0; r < k; ++r) {
       float bv;
-      const int be = next_choice(row, E, pv, pe, nullptr, bv);
+      const int be = next_choice(my_row, E, pv, pe, nullptr, bv);
       if (lane == 0) atomicAdd(&score[be], k - r);
       pv = bv;
       pe = be;
@@ -142,12 +151,12 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_kernel(const float* __r
   }
   // 4: every token's top-k inside the budget
   for (int t = warp; t < T; t += kBudgetWarps) {
-    const float* row = logits + static_cast<size_t>(t) * E;
+    stage_row(t);
     float pv = 0.f;
     int pe = -1;
     for (int r = 0; r < k; ++r) {
       float bv;
-      const int be = next_choice(row, E, pv, pe, in_budget, bv);
+      const int be = next_choice(my_row, E, pv, pe, in_budget, bv);
       if (lane == 0) topk_out[static_cast<size_t>(t) * k + r] = be;
       pv = bv;
       pe = be;
@@ -159,7 +168,11 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_kernel(const float* __r
 
 int launch_budget(const float* logits, int T, int E, int k, int B, int32_t* budget, int32_t* topk,
                   cudaStream_t stream) {
-  budget_kernel<<<1, kBudgetThreads, 0, stream>>>(logits, T, E, k, B, budget, topk);
+  const int smem = kBudgetWarps * E * static_cast<int>(sizeof(float));
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(budget_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return CBQ_ECUDA;
+  budget_kernel<<<1, kBudgetThreads, smem, stream>>>(logits, T, E, k, B, budget, topk);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? CBQ_OK : CBQ_ECUDA;
 }
