@@ -63,6 +63,15 @@ def test_argument_errors_before_device(L):
     assert L.cbq_grouped_gemm(16, 16, p, 4, 16, 9, 1, 8, 128, 16, None) == ops.EINVAL
     assert L.cbq_grouped_gemm(16, 16, p, 4, 16, 5, 1, 8, 128, 16, None) == ops.EINVAL
     assert L.cbq_unpack(p, 8, 100, 16, None) == ops.EINVAL
+    # expert budget: k in [1, B], B <= E <= 4096, T >= 1, outputs present and aligned
+    assert L.cbq_select_budget(16, 4, 12, 0, 4, 16, 16, None) == ops.EINVAL
+    assert L.cbq_select_budget(16, 4, 12, 5, 4, 16, 16, None) == ops.EINVAL
+    assert L.cbq_select_budget(16, 4, 12, 2, 13, 16, 16, None) == ops.EINVAL
+    assert L.cbq_select_budget(16, 4, 4097, 2, 4, 16, 16, None) == ops.EINVAL
+    assert L.cbq_select_budget(16, 0, 12, 2, 4, 16, 16, None) == ops.EINVAL
+    assert L.cbq_select_budget(None, 4, 12, 2, 4, 16, 16, None) == ops.EINVAL
+    assert L.cbq_select_budget(16, 4, 12, 2, 4, None, 16, None) == ops.EINVAL
+    assert L.cbq_select_budget(18, 4, 12, 2, 4, 16, 16, None) == ops.EINVAL   # logits not 4-byte aligned
     # empty problems are no-ops that succeed without a device
     assert L.cbq_gemm(0, 0, None, 0, 8, 128, 0, None) == ops.OK
     assert L.cbq_gemm(0, 0, None, 4, 0, 128, 0, None) == ops.OK
