@@ -1,11 +1,12 @@
 // cbq_budget.cu -- the shared expert budget of one verify round.
 //
 // "Hibana: Fast Agentic Inference on Unified-Memory Devices", section
-// "Adaptive speculation / Expert sharing": verifying drafted tokens loads
-// every expert any of them picked; the round gets a shared expert budget so it
-// reads fewer weights, and a choice outside the budget is replaced by one
-// inside it.  The page shows a toy only; the rule (every decision a comparison
-// or an integer sum, so it is reproducible exactly):
+// "Adaptive speculation / Expert sharing": checking a round of drafted tokens
+// has to read every expert chosen by at least one of them; limiting the whole
+// round to one common set of experts cuts the bytes read, and a token whose
+// choice falls outside the set takes its best expert inside it instead.  The
+// page illustrates this on a small example only; the rule (every decision a
+// comparison or an integer sum, so it is reproducible exactly):
 //  1. each token ranks the experts by its router logit (higher first, equal
 //     logits -> lower id) and takes its own top-k;
 //  2. expert e scores sum over tokens of (k - r), r its 0-based rank in that

@@ -3,8 +3,9 @@
 // "Hibana: Fast Agentic Inference on Unified-Memory Devices", section
 // "Adaptive speculation / Adaptive draft length": with acceptance probability
 // q per drafted token and c the added cost of one more draft token, a round
-// of d drafted tokens emits E[N_d] = sum_{j=0..d} q^j tokens on average (the
-// accepted prefix plus the target model's own next token) in time
+// of d drafted tokens yields E[N_d] = sum_{j=0..d} q^j tokens on average (the
+// drafted tokens accepted before the first rejection, plus one token the
+// target model produces itself) in time
 // T(d) = 1 + c (d - 1) relative to d = 1; the round drafts
 // d* = argmax_{1 <= d <= dmax} E[N_d] / T(d) tokens, so the verify round that
 // follows multiplies d* + 1 token rows per request by the weights.

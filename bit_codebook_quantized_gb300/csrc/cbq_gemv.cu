@@ -4,8 +4,8 @@
 // "Hibana: Fast Agentic Inference on Unified-Memory Devices", section "Model
 // surgery / Three-bit weights": decode is bound by memory bandwidth, so the
 // kernel streams only the packed bytes (3 bits per weight + 8 bits per group
-// of 32), looks the codes up in the row's 8-entry E4M3 codebook and feeds FP8
-// tensor cores.  Section "Adaptive speculation / Expert sharing": the grouped
+// of 32), turns each code into its value in the row's 8-entry E4M3 codebook
+// on the fly and multiplies on FP8 tensor cores.  Section "Adaptive speculation / Expert sharing": the grouped
 // variant reads only the experts that the round's tokens route to.
 //
 // Design (GB300):

@@ -2,9 +2,10 @@
 // E8M0 group scales and one E4M3 codebook per row.
 //
 // "Hibana: Fast Agentic Inference on Unified-Memory Devices", section "Model
-// surgery / Three-bit weights": each group of 32 weights snaps to an 8-entry
-// FP8 codebook (3-bit codes) with one 8-bit scale per group.  The pages do not
-// say how the codebook is fitted; the rule fixed here (and in include/cbq.h)
+// surgery / Three-bit weights": every weight of a 32-weight group is stored
+// as a 3-bit index into an 8-entry FP8 codebook, with one 8-bit scale per
+// group.  The pages give no rule for choosing the codebook; the one fixed here
+// (and in include/cbq.h)
 // is: power-of-two group scale from the group maximum, 8-centroid 1-D Lloyd
 // per row over the scaled values, centroids rounded to E4M3 and sorted,
 // nearest-centroid codes.  The result is deterministic and independent of the

@@ -4,8 +4,9 @@
 // with fp32 accumulators in TMEM.
 //
 // "Hibana: Fast Agentic Inference on Unified-Memory Devices", section "Model
-// surgery / Three-bit weights": the kernel looks the 3-bit codes up in the
-// 8-entry FP8 codebook and feeds FP8 tensor cores; section "Adaptive
+// surgery / Three-bit weights": each 3-bit code becomes its value in the
+// row's 8-entry FP8 codebook on the fly, and the products run on the FP8
+// tensor cores; section "Adaptive
 // speculation": a verify round multiplies the drafted tokens of all requests
 // (up to 64 rows) by the same weights, and with "Expert sharing" reads only
 // the experts the round's tokens route to.

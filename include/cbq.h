@@ -4,8 +4,8 @@
  * Method: "Hibana: Fast Agentic Inference on Unified-Memory Devices",
  * section "Model surgery / Three-bit weights": every group of 32 weights is a
  * 3-bit index into an 8-entry FP8 codebook plus one 8-bit scale per group,
- * 3 + 8/32 = 3.25 bits per weight, and the kernel looks the codes up and feeds
- * FP8 tensor cores.  Section "Adaptive speculation / Expert sharing": a
+ * 3 + 8/32 = 3.25 bits per weight; the matmul turns each code into its FP8
+ * codebook value on the fly and multiplies on the FP8 tensor cores.  Section "Adaptive speculation / Expert sharing": a
  * speculative-verify round of a mixture-of-experts layer reads only the
  * experts its tokens route to.
  *
@@ -85,8 +85,8 @@ int cbq_packed_sizes(int32_t N, int32_t K, size_t *codes_bytes,
 
 /* Quantise fp32 weights W (HOST, [N][K] row-major) into the packed format
  * (HOST outputs, sized by cbq_packed_sizes).  Runs on the calling thread, is
- * deterministic, and implements the fitting rule this library fixes for the
- * pages' "snap each group to a fitted 8-entry FP8 codebook":
+ * deterministic, and implements the rule this library fixes for choosing the
+ * codebooks and codes (the pages do not give one):
  *   1. per group of 32: s = clamp(127 + ceil(log2 max|w|), 0, 254), 127 if all
  *      zero, so |w| / 2^(s-127) <= 1;
  *   2. u = w / 2^(s-127);
@@ -190,7 +190,8 @@ const char *cbq_status_str(int status);
 /* Shared expert budget of one MoE verify round ("Hibana: Fast Agentic
  * Inference on Unified-Memory Devices", section "Adaptive speculation /
  * Expert sharing"): the round reads only B experts, and a token's choice
- * outside them is replaced by one inside.  Rule (the page gives a toy only):
+ * outside them gives way to the token's best expert inside.  Rule (the page
+ * illustrates the idea on a small example only):
  * each token ranks experts by its logit (higher first, ties -> lower id) and
  * takes its own top-k; expert e scores sum_t (k - rank of e in t's top-k);
  * the budget is the B best-scoring experts (ties -> lower id); each token
@@ -212,7 +213,8 @@ int cbq_select_budget(const float *logits, int32_t T, int32_t E, int32_t k,
  * Inference on Unified-Memory Devices", section "Adaptive speculation /
  * Adaptive draft length"): d* = argmax over 1 <= d <= dmax of
  * E[N_d] / T(d), with E[N_d] = sum_{j=0..d} q^j the expected tokens a round
- * emits (accepted prefix + the target's own token) and T(d) = 1 + c (d - 1)
+ * yields (the drafted tokens accepted before the first rejection, plus the
+ * token the target model produces itself) and T(d) = 1 + c (d - 1)
  * its time relative to d = 1.  The verify round that follows multiplies
  * d* + 1 token rows per request.
  *   q      acceptance probability of a drafted token, in [0, 1]

@@ -2,10 +2,11 @@
 ONLY (tests may import it; the library never does; no code is shared).
 
 "Hibana: Fast Agentic Inference on Unified-Memory Devices", section
-"Adaptive speculation / Expert sharing": verifying drafted tokens loads every
-expert any of them picked; the round gets a shared expert budget so it reads
-fewer weights, and a token's choice outside the budget is replaced by one
-inside it.  The page shows only a toy, so the rule here is a proposal, each
+"Adaptive speculation / Expert sharing": checking a round of drafted tokens has
+to read every expert chosen by at least one of them; limiting the whole round
+to one common set of experts cuts the bytes read, and a token whose choice
+falls outside the set takes its best expert inside it instead.  The page
+illustrates this on a small example only, so the rule here is a proposal, each
 step the plainest reading and every decision a comparison or an integer sum
 (so two implementations agree exactly):
 

@@ -250,9 +250,10 @@ void orc_grouped_gemm(const uint8_t *a, const float *a_scale,
 
 /* ---- pack (quantiser) -------------------------------------------------- */
 /*
- * The pages say only that a group "snaps" to an 8-entry FP8 codebook that is
- * "fitted"; the format puts one codebook on each output row and one E8M0
- * scale on each group of 32.  The fitting rule taken here, step by step:
+ * The pages state only that each 32-weight group is mapped onto an 8-entry
+ * FP8 codebook derived from the weights; the format puts one codebook on each
+ * output row and one E8M0 scale on each group of 32.  The rule taken here,
+ * step by step:
  *  1. group scale s = clamp(127 + ceil(log2(max|w|)), 0, 254), s = 127 for
  *     an all-zero group, so that |w| / 2^(s-127) <= 1;
  *  2. u = w / 2^(s-127) for every weight of the row;

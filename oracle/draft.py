@@ -4,7 +4,8 @@ import it; the library never does; no code is shared with it).
 "Hibana: Fast Agentic Inference on Unified-Memory Devices", section
 "Adaptive speculation / Adaptive draft length": a round drafts d tokens; each
 drafted token is accepted with probability q (tracked per request); the round
-emits the accepted prefix plus the target model's own next token, so the
+yields the drafted tokens accepted before the first rejection plus one token
+the target model produces itself, so the
 expected tokens per round are E[N_d] = sum_{j=0..d} q^j = (1 - q^(d+1)) / (1 - q);
 a round takes T(d) = 1 + c (d - 1) relative to a round with d = 1, c being the
 added cost of one more draft token; the chosen length is

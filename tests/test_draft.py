@@ -69,8 +69,9 @@ def test_double_rule_equals_the_exact_rule():
 
 
 def test_higher_acceptance_never_shortens_the_draft():
-    # "High acceptance earns long drafts": E[N_(d+1)] / E[N_d] grows with q,
-    # so d* is non-decreasing in q (exact rationals, no rounding)
+    # the page's point that frequent acceptance warrants longer drafts:
+    # E[N_(d+1)] / E[N_d] grows with q, so d* is non-decreasing in q (exact
+    # rationals, no rounding)
     for c in CS:
         for dmax in DMAX:
             ds = [draft.draft_length_exact(Fraction(i, 40), Fraction(c), dmax)[0] for i in range(41)]
@@ -139,7 +140,7 @@ def _mutant(**over):
 def test_pins_catch_planted_mistakes():
     assert _pins_pass(_mutant())                                   # the oracle as it is
     mutants = {
-        "the target's own token left out": _mutant(expected_tokens=lambda q, d: draft.expected_tokens(q, d) - 1.0),
+        "the target-produced token left out": _mutant(expected_tokens=lambda q, d: draft.expected_tokens(q, d) - 1.0),
         "one term too few": _mutant(expected_tokens=lambda q, d: draft.expected_tokens(q, d - 1) if d > 0 else 0.0),
         "round time 1 + c d": _mutant(round_time=lambda c, d: 1.0 + c * d),
         "ties to the longer draft": _mutant(_ties_longer=True),
