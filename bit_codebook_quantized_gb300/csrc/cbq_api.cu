@@ -10,6 +10,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "cbq_budget.h"
 #include "cbq_internal.h"
 
 namespace cbq {

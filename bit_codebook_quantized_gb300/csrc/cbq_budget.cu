@@ -24,6 +24,7 @@
 
 #include <cstdint>
 
+#include "cbq_budget.h"
 #include "cbq_internal.h"
 
 namespace cbq {

@@ -83,12 +83,6 @@ int launch_sk(const SkParams& p, cudaStream_t stream);
 int launch_sk_static(const SkParams& p, cudaStream_t stream);
 unsigned take_status_sk(cudaStream_t stream);
 
-// Shared expert budget of a verify round (cbq_budget.cu); at most
-// kMaxBudgetExperts experts.
-constexpr int kMaxBudgetExperts = 4096;
-int launch_budget(const float* logits, int T, int E, int k, int B, int32_t* budget, int32_t* topk,
-                  cudaStream_t stream);
-
 // Host quantiser (cbq_pack.cpp).
 int pack_host(const float* W, int N, int K, uint8_t* codes, uint8_t* scales,
               uint8_t* codebooks);
