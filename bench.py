@@ -303,6 +303,7 @@ def run_ours(args):
 
     # ---- e2e through the public API with host buffers --------------------------
     e2e = run_e2e(dev, stream, copies, args)
+    e2e["eager"] = run_e2e_eager(dev, stream, copies, steps=max(20, min(args.steps, 1000)))
 
     peak, peak_src = measured_peak()
     per_call = []
@@ -328,6 +329,19 @@ def run_ours(args):
             "algorithmic_bytes_per_launch": int(dom_bytes), "peak_source": peak_src,
             "share_of_step": round(sum(per_m_us[M] for M in fam[dom]) / sum(per_m_us.values()), 3)}
 
+    # ---- every workload of the specification, >= 200 graphed calls each ------
+    per_config = None
+    if args.per_config_calls > 0:
+        del copies, graphs
+        torch.cuda.empty_cache()
+        with ClockSampler(local) as clk_pc:
+            per_config = run_per_config(dev, stream, peak, calls=args.per_config_calls)
+        per_config = {"points": per_config, "clocks": clk_pc.summary(),
+                      "timing": f"per point: one CUDA graph of {args.per_config_calls} back-to-back "
+                                f"calls on rotating weight copies (>= 4x L2 in all), replayed "
+                                f"{PC_REPS} times after one untimed replay; CUDA events on the "
+                                f"launching stream"}
+
     cpu = None
     if rank == 0 and ws == 1 and args.cpu_seconds > 0:
         cpu = cpu_baseline(seconds=args.cpu_seconds)
@@ -347,7 +361,7 @@ def run_ours(args):
                        "timing": f"per-M CUDA graphs of {S} calls, {reps} rounds; {kernel_timing}",
                        "parallelism": f"replicas x{ws}"},
             "roofline": roof, "per_call": per_call,
-            "e2e": e2e, "cpu_baseline": cpu,
+            "e2e": e2e, "cpu_baseline": cpu, "per_config": per_config,
             "gpu_launches": int(launches_per_step * args.steps),
             "clocks": clk.summary(),
         }
@@ -417,6 +431,119 @@ def run_e2e(dev, stream, copies, args):
             "ms_per_step": round(dt * 1e3 / steps, 4),
             "mode": "one CUDA graph per step (one H2D copy of all inputs, 4 cbq_gemm calls, one D2H "
                     "copy of all outputs), host waits every step"}
+
+
+PC_REPS = 4
+L2_FALLBACK = 129 * 10**6
+
+
+def workload_bytes(wl) -> tuple[int, int]:
+    """(packed weight bytes read, algorithmic bytes) of one call of a workload.
+    A grouped call reads only the budgeted experts; its output holds one row
+    per (token, chosen expert) and it also reads the routing indices."""
+    wb = weight_bytes(wl.N, wl.K)
+    if wl.experts:
+        w_read = wl.budget * wb
+        return w_read, w_read + wl.M * wl.K + 4 * wl.M + 4 * wl.M * wl.topk * wl.N + 4 * wl.M * wl.topk
+    return wb, wb + wl.M * wl.K + 4 * wl.M + 4 * wl.M * wl.N
+
+
+def run_per_config(dev, stream, peak, calls=250):
+    """Every workload of the specification timed the same way: one CUDA graph
+    of `calls` back-to-back calls through the public API, each call on the next
+    of R weight copies (R chosen so the copies fill at least 4x L2), one
+    untimed replay, then PC_REPS timed replays between CUDA events on the
+    launching stream."""
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", L2_FALLBACK) or L2_FALLBACK
+    points = []
+    for name, wl in synth.workloads().items():
+        rows = wl.experts * wl.N if wl.experts else wl.N
+        pw = synth.gen_weights(rows, wl.K, seed=1)
+        w0 = ops.PackedWeights.from_host(pw.codes, pw.scales, pw.codebooks, wl.N, wl.K, device=dev)
+        copy_bytes = w0.nbytes
+        R = int(min(512, max(2, -(-4 * l2 // copy_bytes))))
+        copies = [w0] + [ops.PackedWeights(w0.codes.clone(), w0.scales.clone(), w0.codebooks.clone(),
+                                           wl.N, wl.K) for _ in range(R - 1)]
+        a = torch.from_numpy(synth.gen_activations(wl.M, wl.K, seed=2, half_normal=wl.half_normal)).to(dev)
+        s = torch.from_numpy(synth.gen_a_scale(wl.M, seed=3, mode=wl.a_scale)).to(dev)
+        if wl.experts:
+            idx = torch.from_numpy(synth.gen_moe_routing(wl.M, wl.experts, wl.budget, wl.topk, seed=4)).to(dev)
+            y = torch.empty((wl.M, wl.topk, wl.N), dtype=torch.float32, device=dev)
+            run = lambda w: ops.grouped_gemm(a, s, w, wl.experts, idx, out=y, stream=stream)  # noqa: E731
+            kernel = KERNEL_NAMES[ops.PATH_GEMV if wl.M <= 4 else ops.PATH_MMA]
+        else:
+            y = torch.empty((wl.M, wl.N), dtype=torch.float32, device=dev)
+            run = lambda w: ops.gemm(a, s, w, out=y, stream=stream)  # noqa: E731
+            kernel = KERNEL_NAMES[ops.auto_path(wl.M, wl.N, wl.K)]
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                run(copies[i % R])
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(calls):
+                run(copies[i % R])
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(PC_REPS + 1)]
+        with torch.cuda.stream(stream):
+            g.replay()
+            ev[0].record(stream)
+            for r in range(PC_REPS):
+                g.replay()
+                ev[r + 1].record(stream)
+        stream.synchronize()
+        if ops.device_status(stream) != ops.OK:
+            raise RuntimeError(f"device status not ok after {name}")
+        us = ev[0].elapsed_time(ev[-1]) * 1e3 / (PC_REPS * calls)
+        w_read, alg = workload_bytes(wl)
+        points.append({"workload": name, "M": wl.M, "N": wl.N, "K": wl.K,
+                       **({"experts": wl.experts, "budget": wl.budget, "topk": wl.topk} if wl.experts else {}),
+                       "kernel": kernel, "us": round(us, 3),
+                       "weight_GBps": round(w_read / us / 1e3, 1),
+                       "roofline_frac": round(alg / us / 1e3 / peak, 4),
+                       "tokens_per_s": round(wl.M / us * 1e6, 1),
+                       "weight_copies": R})
+        del g, copies, w0, y
+        torch.cuda.empty_cache()
+    return points
+
+
+def run_e2e_eager(dev, stream, copies, steps):
+    """The e2e step without CUDA graphs: every step copies the inputs from
+    pinned host memory, calls cbq_gemm for M = 1, 2, 4, 8 from the host (one
+    library call per matmul, as an eager caller would), reads every y back
+    and waits."""
+    a_host = {M: torch.from_numpy(synth.gen_activations(M, K_DIM, seed=10 + M)).pin_memory() for M in MS}
+    s_host = {M: torch.from_numpy(synth.gen_a_scale(M, seed=20 + M, mode="uniform")).pin_memory() for M in MS}
+    a_dev = {M: torch.empty_like(a_host[M], device=dev) for M in MS}
+    s_dev = {M: torch.empty_like(s_host[M], device=dev) for M in MS}
+    y_dev = {M: torch.empty((M, N_DIM), dtype=torch.float32, device=dev) for M in MS}
+    y_host = {M: torch.empty((M, N_DIM), dtype=torch.float32).pin_memory() for M in MS}
+    call = [0]
+
+    def step():
+        with torch.cuda.stream(stream):
+            for M in MS:
+                a_dev[M].copy_(a_host[M], non_blocking=True)
+                s_dev[M].copy_(s_host[M], non_blocking=True)
+            for M in MS:
+                ops.gemm(a_dev[M], s_dev[M], copies[call[0] % len(copies)], out=y_dev[M], stream=stream)
+                call[0] += 1
+            for M in MS:
+                y_host[M].copy_(y_dev[M], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(5):
+        step()
+    t = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = time.perf_counter() - t
+    return {"value": round(steps * len(MS) * weight_bytes() / dt / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": sum(M * K_DIM + 4 * M for M in MS),
+            "d2h_bytes_per_step": sum(4 * M * N_DIM for M in MS), "steps": steps,
+            "ms_per_step": round(dt * 1e3 / steps, 4),
+            "mode": "eager: per step 8 H2D copies, 4 cbq_gemm calls from the host, 4 D2H copies, "
+                    "host waits every step"}
 
 
 # ------------------------------------------------------- oracle (CPU) arm --
@@ -539,6 +666,8 @@ def main(argv=None):
                     help="run --calls calls of one workload (see synth.workloads()) and exit")
     ap.add_argument("--path", type=int, default=0, help="kernel for --single: 0 auto, 1 gemv, 2 mma")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--per-config-calls", type=int, default=250,
+                    help="graphed calls per point of the all-workload leg (0 disables)")
     args = ap.parse_args(argv)
     if args.single:
         run_single(args)
