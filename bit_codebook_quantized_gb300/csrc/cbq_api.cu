@@ -301,7 +301,7 @@ int cbq_device_status(void* stream) {
 
 int cbq_select_budget(const float* logits, int32_t T, int32_t E, int32_t k, int32_t B, int32_t* budget,
                       int32_t* topk_idx, void* stream) {
-  if (T < 1 || E < 1 || E > kMaxBudgetExperts || k < 1 || B < k || B > E) return CBQ_EINVAL;
+  if (T < 1 || E < 1 || E > kMaxBudgetExperts || k < 1 || k > kMaxBudgetK || B < k || B > E) return CBQ_EINVAL;
   if (!logits || !aligned(logits, 4) || !budget || !aligned(budget, 4) || !topk_idx || !aligned(topk_idx, 4))
     return CBQ_EINVAL;
   const int st = current_device_checked(nullptr);

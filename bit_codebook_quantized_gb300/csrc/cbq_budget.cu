@@ -15,11 +15,17 @@
 //  4. each token takes its top-k among the budget experts, in rank order.
 // The result (topk_idx, [T][k]) is what cbq_grouped_gemm reads.
 //
-// One CTA of 8 warps (a round has at most a few dozen tokens): a warp copies a
-// token's logits into its own shared-memory row once, then finds each next
-// choice as the best (logit, id) that ranks after the previous one, so no
-// per-token state beyond the previous pick is kept; expert scores are
-// shared-memory integers.
+// Logits are compared through a 32-bit key that orders floats as numbers
+// (-0 and +0 equal) and puts NaN below every other value, so the kernel is
+// total: any input gives k valid, distinct expert ids per token.
+//
+// One CTA of 32 warps.  A (key, id) pair is one 64-bit word, key in the high
+// half and (2^32 - 1 - id) in the low half, so "ranks before" is plain
+// unsigned ">".  Steps 1 and 4: one warp per token; every lane keeps the
+// best 8 words of its experts (a branch-free insertion chain, taken only when
+// a word beats the lane's 8th), then k rounds of a warp-wide maximum merge the
+// 32 lists.  Step 2: shared-memory atomic adds of (k - r) into the high half
+// of each expert's word.  Step 3: one bitonic sort of those words.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -30,115 +36,105 @@
 namespace cbq {
 namespace {
 
-constexpr int kBudgetWarps = 8;
+constexpr int kBudgetWarps = 32;
 constexpr int kBudgetThreads = kBudgetWarps * 32;
+constexpr int kListLen = kMaxBudgetK;                  // per-lane candidate list
 
-// (v, e) ranks before (w, f): larger value first, equal values -> lower id.
-template <typename V>
-__device__ __forceinline__ bool ranks_before(V v, int e, V w, int f) {
-  return v > w || (v == w && e < f);
+// Order-preserving key of a logit: larger logit -> larger key; -0 == +0;
+// NaN -> 0, below every other value (no other float maps to 0).
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  if (v != v) return 0u;
+  if (v == 0.f) v = 0.f;
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Keep (ov, oe) in (bv, be) if it ranks before it (id -1 = nothing yet).
-template <typename V>
-__device__ __forceinline__ void keep_better(V& bv, int& be, V ov, int oe) {
-  if (oe >= 0 && (be < 0 || ranks_before(ov, oe, bv, be))) {
-    bv = ov;
-    be = oe;
-  }
+__device__ __forceinline__ uint64_t rank_word(uint32_t key, int e) {
+  return (static_cast<uint64_t>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(e));
 }
+__device__ __forceinline__ int word_id(uint64_t w) { return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(w)); }
 
-template <typename V>
-__device__ __forceinline__ void warp_best(V& bv, int& be) {
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
-    const V ov = __shfl_xor_sync(0xffffffffu, bv, off);
-    const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-    keep_better(bv, be, ov, oe);
+    const uint64_t o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = o > v ? o : v;
+  }
+  return v;
+}
+
+// Insert w into the lane's descending list (only called when w beats its last).
+__device__ __forceinline__ void insert(uint64_t (&list)[kListLen], uint64_t w) {
+#pragma unroll
+  for (int i = 0; i < kListLen; ++i) {
+    const uint64_t hi = list[i] > w ? list[i] : w;
+    w = list[i] > w ? w : list[i];
+    list[i] = hi;
   }
 }
 
-// A token's next choice: the best (logit, id) of its row that ranks after
-// (pv, pe) (pe < 0: the first choice), among the experts `allowed` marks (all
-// if null).  Every lane of the warp returns it.
-__device__ __forceinline__ int next_choice(const float* row, int E, float pv, int pe, const uint8_t* allowed,
-                                           float& bv) {   // row: the warp's shared-memory copy
+// The token's top-k among `count` experts (expert of candidate j: ids ? ids[j]
+// : j), merged over the warp; calls emit(r, e) on lane 0 for rank r = 0..k-1.
+template <typename Emit>
+__device__ __forceinline__ void token_topk(const float* __restrict__ row, const int16_t* ids, int count, int k,
+                                           Emit emit) {
   const int lane = threadIdx.x & 31;
-  int be = -1;
-  bv = 0.f;
-  for (int e = lane; e < E; e += 32) {
-    if (allowed && !allowed[e]) continue;
-    const float v = row[e];
-    if (pe >= 0 && !ranks_before(pv, pe, v, e)) continue;
-    keep_better(bv, be, v, e);
+  uint64_t list[kListLen];
+#pragma unroll
+  for (int i = 0; i < kListLen; ++i) list[i] = 0;     // below every real word
+  for (int j = lane; j < count; j += 32) {
+    const int e = ids ? ids[j] : j;
+    const uint64_t w = rank_word(logit_key(__ldg(row + e)), e);
+    if (w > list[kListLen - 1]) insert(list, w);
   }
-  warp_best(bv, be);
-  return be;
+  for (int r = 0; r < k; ++r) {
+    const uint64_t m = warp_max_u64(list[0]);
+    if (list[0] == m) {                                // the one lane that held it pops it
+#pragma unroll
+      for (int i = 0; i + 1 < kListLen; ++i) list[i] = list[i + 1];
+      list[kListLen - 1] = 0;
+    }
+    if (lane == 0) emit(r, word_id(m));
+  }
 }
 
 __global__ void __launch_bounds__(kBudgetThreads) budget_kernel(const float* __restrict__ logits, int T, int E,
                                                                  int k, int B, int32_t* __restrict__ budget_out,
                                                                  int32_t* __restrict__ topk_out) {
-  __shared__ int score[kMaxBudgetExperts];
+  __shared__ unsigned long long words[kMaxBudgetExperts];   // (score, id) of every expert
   __shared__ uint8_t in_budget[kMaxBudgetExperts];
-  __shared__ int red_s[kBudgetWarps], red_e[kBudgetWarps];
-  __shared__ int pick;
-  extern __shared__ float rows[];                       // [kBudgetWarps][E]: one token row per warp
+  __shared__ int16_t blist[kMaxBudgetExperts];              // budget ids, ascending
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  float* my_row = rows + static_cast<size_t>(warp) * E;
-  auto stage_row = [&](int t) {                         // the token's logits, coalesced, once
-    __syncwarp();
-    const float* g = logits + static_cast<size_t>(t) * E;
-    for (int e = lane; e < E; e += 32) my_row[e] = g[e];
-    __syncwarp();
-  };
-  for (int e = tid; e < E; e += kBudgetThreads) {
-    score[e] = 0;
+  int P = 32;                                               // sort width: power of two >= E
+  while (P < E) P <<= 1;
+  for (int e = tid; e < P; e += kBudgetThreads) {
+    words[e] = e < E ? rank_word(0u, e) : 0ull;             // padding sorts last
     in_budget[e] = 0;
   }
   __syncthreads();
-  // 1, 2: own top-k of every token, scores
-  for (int t = warp; t < T; t += kBudgetWarps) {
-    stage_row(t);
-    float pv = 0.f;
-    int pe = -1;
-    for (int r = 0; r < k; ++r) {
-      float bv;
-      const int be = next_choice(my_row, E, pv, pe, nullptr, bv);
-      if (lane == 0) atomicAdd(&score[be], k - r);
-      pv = bv;
-      pe = be;
-    }
-  }
+  // 1, 2: own top-k of every token; score (k - r) into the expert's high half
+  for (int t = warp; t < T; t += kBudgetWarps)
+    token_topk(logits + static_cast<size_t>(t) * E, nullptr, E, k, [&](int r, int e) {
+      atomicAdd(&words[e], static_cast<unsigned long long>(k - r) << 32);
+    });
   __syncthreads();
-  // 3: the budget, one expert per pass: the best (score, id) after the last pick
-  int ps = 0, pid = -1;
-  for (int j = 0; j < B; ++j) {
-    int bs = 0, be = -1;
-    for (int e = tid; e < E; e += kBudgetThreads) {
-      const int s = score[e];
-      if (pid >= 0 && !ranks_before(ps, pid, s, e)) continue;
-      keep_better(bs, be, s, e);
-    }
-    warp_best(bs, be);
-    if (lane == 0) {
-      red_s[warp] = bs;
-      red_e[warp] = be;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      bs = lane < kBudgetWarps ? red_s[lane] : 0;
-      be = lane < kBudgetWarps ? red_e[lane] : -1;
-      warp_best(bs, be);
-      if (lane == 0) {
-        pick = be;
-        in_budget[be] = 1;
+  // 3: bitonic sort, descending: words[0..B) are the budget
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < P / 2; i += kBudgetThreads) {
+        const int lo = 2 * i - (i & (stride - 1));          // first of the pair
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const unsigned long long a = words[lo], b = words[hi];
+        if ((a < b) == desc) {
+          words[lo] = b;
+          words[hi] = a;
+        }
       }
+      __syncthreads();
     }
-    __syncthreads();
-    pid = pick;
-    ps = score[pid];
   }
+  for (int j = tid; j < B; j += kBudgetThreads) in_budget[word_id(words[j])] = 1;
   __syncthreads();
   // the budget in ascending expert order
   if (warp == 0) {
@@ -147,34 +143,26 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_kernel(const float* __r
       const int e = e0 + lane;
       const bool f = e < E && in_budget[e];
       const unsigned m = __ballot_sync(0xffffffffu, f);
-      if (f) budget_out[base + __popc(m & ((1u << lane) - 1u))] = e;
+      if (f) {
+        const int at = base + __popc(m & ((1u << lane) - 1u));
+        budget_out[at] = e;
+        blist[at] = static_cast<int16_t>(e);
+      }
       base += __popc(m);
     }
   }
+  __syncthreads();
   // 4: every token's top-k inside the budget
-  for (int t = warp; t < T; t += kBudgetWarps) {
-    stage_row(t);
-    float pv = 0.f;
-    int pe = -1;
-    for (int r = 0; r < k; ++r) {
-      float bv;
-      const int be = next_choice(my_row, E, pv, pe, in_budget, bv);
-      if (lane == 0) topk_out[static_cast<size_t>(t) * k + r] = be;
-      pv = bv;
-      pe = be;
-    }
-  }
+  for (int t = warp; t < T; t += kBudgetWarps)
+    token_topk(logits + static_cast<size_t>(t) * E, blist, B, k,
+               [&](int r, int e) { topk_out[static_cast<size_t>(t) * k + r] = e; });
 }
 
 }  // namespace
 
 int launch_budget(const float* logits, int T, int E, int k, int B, int32_t* budget, int32_t* topk,
                   cudaStream_t stream) {
-  const int smem = kBudgetWarps * E * static_cast<int>(sizeof(float));
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(budget_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return CBQ_ECUDA;
-  budget_kernel<<<1, kBudgetThreads, smem, stream>>>(logits, T, E, k, B, budget, topk);
+  budget_kernel<<<1, kBudgetThreads, 0, stream>>>(logits, T, E, k, B, budget, topk);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? CBQ_OK : CBQ_ECUDA;
 }

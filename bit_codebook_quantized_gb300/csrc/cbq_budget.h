@@ -8,8 +8,10 @@
 
 namespace cbq {
 
-// At most this many experts (one shared-memory score per expert).
+// At most this many experts (one shared-memory word per expert) and at most
+// this many choices per token (the routing cbq_grouped_gemm takes has at most 8).
 constexpr int kMaxBudgetExperts = 4096;
+constexpr int kMaxBudgetK = 8;
 
 int launch_budget(const float* logits, int T, int E, int k, int B, int32_t* budget, int32_t* topk,
                   cudaStream_t stream);

@@ -17,9 +17,16 @@
 
 #include "cbq_internal.h"
 
+namespace {
+constexpr int32_t kMaxDraft = 63;
+}
+
 extern "C" int cbq_draft_length(double q, double c, int32_t dmax, int32_t* d_star, double* expected_tokens,
                                 double* tokens_per_time) {
-  if (!d_star || dmax < 1 || !(q >= 0.0 && q <= 1.0) || !(c >= 0.0) || !std::isfinite(c)) return CBQ_EINVAL;
+  // dmax <= 63: a verify round multiplies d* + 1 token rows per request and
+  // cbq_gemm takes at most 64 rows, so a longer draft could not be verified.
+  if (!d_star || dmax < 1 || dmax > kMaxDraft || !(q >= 0.0 && q <= 1.0) || !(c >= 0.0) || !std::isfinite(c))
+    return CBQ_EINVAL;
   double sum = 1.0, power = 1.0;                  // E[N_0] = q^0
   int32_t best_d = 0;
   double best_e = 0.0, best_r = 0.0;

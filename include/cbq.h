@@ -195,11 +195,14 @@ const char *cbq_status_str(int status);
  * each token ranks experts by its logit (higher first, ties -> lower id) and
  * takes its own top-k; expert e scores sum_t (k - rank of e in t's top-k);
  * the budget is the B best-scoring experts (ties -> lower id); each token
- * then takes its top-k among the budget.
- *   logits   device fp32 [T][E] router logits, finite
+ * then takes its top-k among the budget.  Logits compare as numbers (-0 and
+ * +0 are equal); a NaN logit ranks below every other value, so any input
+ * gives k distinct in-budget ids per token.
+ *   logits   device fp32 [T][E] router logits
  *   T        tokens of the round, >= 1
  *   E        experts, 1 <= E <= 4096
- *   k        choices per token, 1 <= k <= B
+ *   k        choices per token, 1 <= k <= min(B, 8) (cbq_grouped_gemm takes
+ *            at most 8 choices per token)
  *   B        budget, k <= B <= E
  *   budget   device int32 [B] out: the budget's expert ids, ascending
  *   topk_idx device int32 [T][k] out: each token's choices in rank order
@@ -219,7 +222,8 @@ int cbq_select_budget(const float *logits, int32_t T, int32_t E, int32_t k,
  * d* + 1 token rows per request.
  *   q      acceptance probability of a drafted token, in [0, 1]
  *   c      added relative cost of one more draft token, finite and >= 0
- *   dmax   longest draft allowed, >= 1
+ *   dmax   longest draft allowed, 1 <= dmax <= 63 (the verify round of one
+ *          request then has at most 64 token rows, the most cbq_gemm takes)
  *   d_star out: the chosen length (ties go to the shorter draft)
  *   expected_tokens, tokens_per_time: out, may be NULL: E[N_d*] and
  *          E[N_d*] / T(d*)

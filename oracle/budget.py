@@ -20,12 +20,22 @@ step the plainest reading and every decision a comparison or an integer sum
 """
 from __future__ import annotations
 
+import math
+
 import numpy as np
 
 
+def _rank_key(row, e):
+    """Sort key of expert e in a token's ranking: higher logit first, equal
+    logits -> lower id (float32 values compared exactly, -0 equal to +0).  The
+    page says nothing of non-finite logits; the reading taken here is that a
+    NaN logit ranks below every other value, NaNs among themselves by id."""
+    v = float(row[e])
+    return (1, 0.0, e) if math.isnan(v) else (0, -v, e)
+
+
 def _ranked(row, experts):
-    # higher logit first, equal logits -> lower id (compares float32 values exactly)
-    return sorted(experts, key=lambda e: (-float(row[e]), e))
+    return sorted(experts, key=lambda e: _rank_key(row, e))
 
 
 def own_topk(logits: np.ndarray, k: int) -> list[list[int]]:

@@ -150,3 +150,12 @@ def test_auto_path_choice(L):
     assert L.cbq_gemm_auto_path(0, 16, 128) == ops.EINVAL
     assert L.cbq_gemm_auto_path(4, 16, 100) == ops.EINVAL
     assert L.cbq_gemm_auto_path(65, 16, 128) == ops.EINVAL
+
+
+def test_library_pack_matches_the_hand_worked_lloyd_row(golden_dir):
+    # the library's quantiser (its own code) on the hand-worked Lloyd row
+    from tests.test_oracle import lloyd_golden_row
+    W, cb, sc = lloyd_golden_row(golden_dir)
+    codes, scales, cbs = ops.pack(W)
+    assert bytes(cbs.ravel()) == cb
+    assert scales.ravel().tolist() == sc

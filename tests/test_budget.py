@@ -96,3 +96,18 @@ def test_pins_catch_planted_mistakes():
     assert run(score_fn=lambda r: 1) != budget                     # plain votes
     assert run(score_fn=lambda r: k - r + 1) != budget             # rank weight off by one
     assert run(tie_high=True) != budget                            # ties to the higher id
+
+
+def test_non_finite_and_signed_zero_logits():
+    # Worked by hand, k = 3: row [1, NaN, 3, NaN, -inf, -0.0, +0.0]; NaN ranks
+    # below every value (NaNs by id), -0 equals +0 (lower id first):
+    # order 2 (3), 0 (1), 5 (-0), 6 (+0), 4 (-inf), 1 (NaN), 3 (NaN).
+    row = np.array([[1, np.nan, 3, np.nan, -np.inf, -0.0, 0.0]], dtype=np.float32)
+    assert ob.own_topk(row, 7) == [[2, 0, 5, 6, 4, 1, 3]]
+    # the numpy restatement agrees: lexsort puts NaN last and keeps id order in ties
+    assert list(np.lexsort((np.arange(7), -row[0].astype(np.float64)))) == [2, 0, 5, 6, 4, 1, 3]
+    # a token whose logits are all NaN still gets k distinct in-budget choices
+    x = _random_logits(8, 20, 3)
+    x[2, :] = np.nan
+    budget, topk = ob.select_budget(x, 4, 6)
+    assert len(topk[2]) == 4 and len(set(topk[2])) == 4 and set(topk[2]) <= set(budget)

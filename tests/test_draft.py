@@ -13,7 +13,7 @@ from oracle import draft
 
 QS = [i / 20 for i in range(21)]
 CS = [0.0, 0.01, 0.05, 0.1, 0.2, 0.3, 0.45, 0.5, 0.55, 0.7, 1.0, 2.0]
-DMAX = [1, 2, 3, 4, 8, 16, 32]
+DMAX = [1, 2, 3, 4, 8, 16, 32, 63]
 
 
 # ---- the oracle against the page ---------------------------------------------
@@ -89,7 +89,8 @@ def test_library_matches_the_oracle(dmax):
 
 def test_library_rejects_bad_arguments():
     for q, c, dmax in [(-0.1, 0.1, 8), (1.1, 0.1, 8), (math.nan, 0.1, 8), (0.5, -0.1, 8),
-                       (0.5, math.inf, 8), (0.5, math.nan, 8), (0.5, 0.1, 0)]:
+                       (0.5, math.inf, 8), (0.5, math.nan, 8), (0.5, 0.1, 0), (0.5, 0.1, 64),
+                       (0.5, 0.1, 2**31 - 1)]:
         with pytest.raises(ops.CbqError):
             ops.draft_length(q, c, dmax)
     assert ops.lib().cbq_draft_length(0.5, 0.1, 8, None, None, None) == ops.EINVAL

@@ -40,9 +40,26 @@ def test_budget_matches_the_oracle(T, E, k, B, ties):
     assert ops.device_status() == ops.OK
 
 
+def test_budget_non_finite_logits_match_the_oracle():
+    # NaN ranks below every value, -0 equals +0, infinities order normally;
+    # a row of NaNs still yields k distinct budget experts
+    logits = _logits(40, 96, 9, True)
+    logits[0, [3, 7, 50]] = np.nan
+    logits[1, :] = np.nan
+    logits[2, [0, 1]] = [np.inf, -np.inf]
+    logits[3, :] = 0.0
+    logits[3, ::2] = -0.0
+    budget, topk = ops.select_budget(torch.from_numpy(logits).cuda(), 8, 20)
+    torch.cuda.synchronize()
+    want_budget, want_topk = ob.select_budget(logits, 8, 20)
+    assert budget.cpu().tolist() == want_budget
+    assert topk.cpu().tolist() == want_topk
+    assert ops.device_status() == ops.OK
+
+
 def test_budget_rejects_bad_arguments():
     x = torch.zeros((4, 16), dtype=torch.float32, device="cuda")
-    for k, B in [(0, 4), (5, 4), (2, 17)]:
+    for k, B in [(0, 4), (5, 4), (2, 17), (9, 12)]:
         with pytest.raises(ops.CbqError):
             ops.select_budget(x, k, B)
     with pytest.raises(ops.CbqError):

@@ -370,3 +370,41 @@ def test_gemm_rows_equals_full_gemm_rows():
     rows = np.array([0, 1, 127, 128, 255, 256, 299])
     yr, br = oracle.gemm_rows(a, s, pw.codes, pw.scales, pw.codebooks, M, N, K, rows)
     assert np.array_equal(yr, y[:, rows]) and np.array_equal(br, b[:, rows])
+
+
+def lloyd_golden_row(golden_dir):
+    """The hand-worked Lloyd row of tests/golden/lloyd_row.txt: (W [1, 128],
+    codebook bytes, scale bytes)."""
+    from fractions import Fraction
+    vals, cb, sc, inside = [], None, None, False
+    for line in open(os.path.join(golden_dir, "lloyd_row.txt")):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        if line == "values":
+            inside = True
+        elif line == "end":
+            inside = False
+        elif inside:
+            v, n = line.split()
+            vals += [Fraction(v)] * int(n)
+        elif line.startswith("codebook"):
+            cb = bytes(int(x, 16) for x in line.split()[1:])
+        elif line.startswith("scales"):
+            sc = [int(x) for x in line.split()[1:]]
+    S = sorted(vals)
+    assert len(S) == 128
+    row = [S[4 * j + g] for g in range(4) for j in range(32)]
+    W = np.array([float(v) for v in row], np.float32).reshape(1, 128)
+    assert all(Fraction(float(w)) == v for w, v in zip(W[0], row))   # exact in fp32
+    return W, cb, sc
+
+
+def test_pack_lloyd_fit_hand_worked_row(golden_dir):
+    """Step 3 of the packer (quantile start, 16 rounds, empty cluster kept):
+    a row whose fit still moves one point per round through round 16; the
+    sorted E4M3 codebook and the scale bytes equal the hand-worked ones."""
+    W, cb, sc = lloyd_golden_row(golden_dir)
+    codes, scales, cbs = oracle.pack(W)
+    assert bytes(cbs.ravel()) == cb
+    assert scales.ravel().tolist() == sc

@@ -36,6 +36,13 @@ MUTANTS = {
     "pack_tie_upper": ("if (fabs(u[k] - orc_e4m3_value(cb[c])) <\n                    fabs",
                        "if (fabs(u[k] - orc_e4m3_value(cb[c])) <=\n                    fabs"),
     "round_half_away": ("double r = nearbyint(sig);", "double r = floor(sig + 0.5);"),
+    "lloyd_15_rounds": ("for (int it = 0; it < 16; it++)", "for (int it = 0; it < 15; it++)"),
+    "lloyd_one_round": ("for (int it = 0; it < 16; it++)", "for (int it = 0; it < 1; it++)"),
+    "lloyd_start_floor": ("cen[i] = sorted[(int64_t)((i + 0.5) * (double)K / 8.0)];",
+                          "cen[i] = sorted[(int64_t)(i * (double)K / 8.0)];"),
+    "lloyd_empty_reset": ("if (cnt[c] > 0)\n                    cen[c] = sum[c] / (double)cnt[c];",
+                          "if (cnt[c] > 0)\n                    cen[c] = sum[c] / (double)cnt[c];\n"
+                          "                else\n                    cen[c] = 0.0;"),
 }
 
 
@@ -114,6 +121,12 @@ def _pins_pass() -> bool:
             return False
     # E4M3 rounding ties go to the even mantissa
     if oracle.e4m3_round(1.0625) != 0x38 or oracle.e4m3_round(1.1875) != 0x3A:
+        return False
+    # the hand-worked Lloyd row (quantile start, 16 rounds, empty cluster kept)
+    from tests.test_oracle import lloyd_golden_row
+    Wl, cbl, scl = lloyd_golden_row(os.path.join(os.path.dirname(os.path.dirname(__file__)), "tests", "golden"))
+    _, sl, bl = oracle.pack(Wl)
+    if bytes(bl.ravel()) != cbl or sl.ravel().tolist() != scl:
         return False
     return True
 
