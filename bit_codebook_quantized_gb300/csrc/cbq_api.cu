@@ -18,6 +18,8 @@ namespace cbq {
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
+constexpr long long kDefaultWaitNs = 2000000000LL;   // 2 s
+std::atomic<long long> g_wait_ns{kDefaultWaitNs};
 
 struct DeviceInfo {
   int sm_count = 0;
@@ -77,6 +79,8 @@ int device_sm_count() {
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
 }  // namespace cbq
 
 using namespace cbq;
@@ -111,22 +115,34 @@ int cbq_unpack(const cbq_weight_t* w, int32_t N, int32_t K, float* W_out, void* 
                        static_cast<cudaStream_t>(stream));
 }
 
-int cbq_gemm_auto_path(int32_t M, int32_t N, int32_t K) {
+int cbq_gemm_auto_path(int32_t M, int32_t N, int32_t K, int32_t with_workspace) {
   if (M < 1 || M > 64 || N < 1 || K < 128 || K % 128 != 0) return CBQ_EINVAL;
-  // Measured on GB300 (CUDA graphs of back-to-back calls, weights beyond L2):
-  // up to 8 token rows the GEMV kernel wins on matrices up to ~64 M weights
-  // and the tile kernel beyond; from 9 rows the stream-K kernel wins up to
-  // ~128 M weights if its resident activations fit, the tile kernel
-  // elsewhere.  The tile kernel needs its activations resident too; where
-  // they do not fit, the GEMV kernel runs (see cbq_gemm_path).
+  // Measured on GB300 (CUDA graphs of back-to-back calls, weights beyond L2).
+  // With a workspace the stream-K kernel (equal contiguous weight share per
+  // SM) takes every shape it fits.  Without one: up to 8 token rows the GEMV
+  // kernel on matrices up to ~64 M weights and the tile kernel beyond; from 9
+  // rows the tile kernel.  The tile kernel needs its activations resident;
+  // where they do not fit, the GEMV kernel runs (see cbq_gemm_path).
+  if (with_workspace && sk_applicable(M, N, K)) return CBQ_PATH_STREAMK;
   const long long weights = static_cast<long long>(N) * K;
   if (M <= 8) return weights <= (1LL << 26) ? CBQ_PATH_GEMV : CBQ_PATH_MMA;
-  if (weights <= (1LL << 27) && sk_applicable(M, N, K)) return CBQ_PATH_STREAMK;
   return CBQ_PATH_MMA;
 }
 
+int cbq_gemm_workspace_size(int32_t M, int32_t N, int32_t K, size_t* bytes) {
+  if (!bytes || M < 0 || M > 64 || N < 0 || K < 0 || K % 128 != 0) return CBQ_EINVAL;
+  *bytes = (M == 0 || N == 0 || K == 0) ? 0 : sk_workspace_bytes(M, N, K);
+  return CBQ_OK;
+}
+
+int cbq_set_wait_limit(int64_t ns) {
+  g_wait_ns.store(ns > 0 ? static_cast<long long>(ns) : kDefaultWaitNs, std::memory_order_relaxed);
+  return CBQ_OK;
+}
+
 int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w, int32_t M,
-                  int32_t N, int32_t K, float* y, void* stream, int32_t path) {
+                  int32_t N, int32_t K, float* y, void* workspace, size_t workspace_bytes, void* stream,
+                  int32_t path) {
   if (M < 0 || M > 64 || N < 0 || K < 0 || K % 128 != 0) return CBQ_EINVAL;
   if (path < CBQ_PATH_AUTO || path > CBQ_PATH_STREAMK) return CBQ_EINVAL;
   if (M == 0 || N == 0) return CBQ_OK;
@@ -142,7 +158,7 @@ int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w,
   if (!a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(w))
     return CBQ_EINVAL;
   const bool automatic = path == CBQ_PATH_AUTO;
-  if (automatic) path = cbq_gemm_auto_path(M, N, K);
+  if (automatic) path = cbq_gemm_auto_path(M, N, K, workspace != nullptr);
   if (path == CBQ_PATH_STREAMK) {
     if (!sk_applicable(M, N, K)) return CBQ_EINVAL;
     SkParams p;
@@ -156,7 +172,8 @@ int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w,
     p.M = M;
     p.N = N;
     p.K = K;
-    return launch_sk(p, s);
+    p.wait_ns = wait_limit_ns();
+    return launch_sk(p, workspace, workspace_bytes, s);
   }
   if (path == CBQ_PATH_GEMV) {
     GemvParams p;
@@ -170,6 +187,7 @@ int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w,
     p.M = M;
     p.N = N;
     p.K = K;
+    p.wait_ns = wait_limit_ns();
     return launch_gemv(p, false, s);
   }
   UmmaParams p;
@@ -183,6 +201,7 @@ int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w,
   p.M = M;
   p.N = N;
   p.K = K;
+  p.wait_ns = wait_limit_ns();
   const int r = launch_umma(p, false, s);
   if (r != CBQ_EINVAL || !automatic) return r;
   // the tile kernel's resident activations do not fit either: GEMV kernel
@@ -197,6 +216,7 @@ int cbq_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* w,
   g.M = M;
   g.N = N;
   g.K = K;
+  g.wait_ns = wait_limit_ns();
   return launch_gemv(g, false, s);
 }
 
@@ -220,12 +240,18 @@ int cbq_gemm_noalloc(const uint8_t* a, const float* a_scale, const cbq_weight_t*
   p.M = M;
   p.N = N;
   p.K = K;
+  p.wait_ns = wait_limit_ns();
   return launch_sk_static(p, static_cast<cudaStream_t>(stream));
+}
+
+int cbq_gemm_ws(const uint8_t* a, const float* a_scale, const cbq_weight_t* w, int32_t M, int32_t N,
+                int32_t K, float* y, void* workspace, size_t workspace_bytes, void* stream) {
+  return cbq_gemm_path(a, a_scale, w, M, N, K, y, workspace, workspace_bytes, stream, CBQ_PATH_AUTO);
 }
 
 int cbq_gemm(const uint8_t* a, const float* a_scale, const cbq_weight_t* w, int32_t M, int32_t N,
              int32_t K, float* y, void* stream) {
-  return cbq_gemm_path(a, a_scale, w, M, N, K, y, stream, CBQ_PATH_AUTO);
+  return cbq_gemm_path(a, a_scale, w, M, N, K, y, nullptr, 0, stream, CBQ_PATH_AUTO);
 }
 
 int cbq_grouped_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weight_t* experts,
@@ -262,6 +288,7 @@ int cbq_grouped_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weig
     p.M = M;
     p.N = N;
     p.K = K;
+    p.wait_ns = wait_limit_ns();
     p.E = E;
     p.topk = topk;
     return launch_gemv(p, true, s);
@@ -278,6 +305,7 @@ int cbq_grouped_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weig
   p.M = M;
   p.N = N;
   p.K = K;
+  p.wait_ns = wait_limit_ns();
   p.E = E;
   p.topk = topk;
   return launch_umma(p, true, s);

@@ -35,6 +35,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 
 #include "cbq_device.cuh"
@@ -55,27 +56,36 @@ constexpr int kStages = 4;
 constexpr int kMaxExperts = 4096;
 constexpr int kMaxRouting = 64 * 8;
 
+constexpr long long kDrainLimitNs = 10000000000LL;   // copies always land; 10 s is a backstop
+
 __device__ __forceinline__ void raise(unsigned bits) { atomicOr(&g_status_gemv, bits); }
 
-__device__ __forceinline__ bool status_set() {
-  return *reinterpret_cast<volatile unsigned*>(&g_status_gemv) != 0u;
-}
-
-// Wait for an mbarrier phase, suspended in the barrier between polls.  After
-// ~0.5 ms give up at once if another wait of this kernel already timed out;
-// after kWaitLimitNs raise kErrTimeout and give up.
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+// Wait for an mbarrier phase, suspended in the barrier between polls.  Gives
+// up (returns false) at once when the CTA's abort flag is up, or after
+// `limit_ns`, raising the flag and the library's timeout status.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = global_ns();
   for (;;) {
     if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
-    const long long dt = global_ns() - t0;
-    if (dt > 500000LL) {
-      if (status_set()) return false;
-      if (dt > kWaitLimitNs) {
-        raise(kErrTimeout);
-        return false;
-      }
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      raise(kErrTimeout);
+      return false;
+    }
+  }
+}
+
+// Wait for bulk copies this CTA issued itself, whatever the abort flag says.
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return;
+  const long long t0 = global_ns();
+  while (!mbar_try_wait_suspend(bar, parity, 20000u)) {
+    if (global_ns() - t0 > kDrainLimitNs) {
+      raise(kErrTimeout);
+      return;
     }
   }
 }
@@ -88,7 +98,7 @@ struct SmemLayout {
   template <int TOKC>
   __host__ __device__ static constexpr int bar_off() { return red_off + red_bytes<TOKC>(); }
   template <int TOKC>
-  __host__ __device__ static constexpr int route_off() { return bar_off<TOKC>() + 2 * kStages * 8; }
+  __host__ __device__ static constexpr int route_off() { return bar_off<TOKC>() + 2 * kStages * 8 + 16; }
   // routing area (grouped only): topk copy, token list, used-expert list
   template <int TOKC, bool GROUPED>
   __host__ __device__ static constexpr int total() {
@@ -106,6 +116,8 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
   float* red = reinterpret_cast<float*>(smem + SmemLayout::red_off);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + SmemLayout::bar_off<TOKC>());
   uint64_t* empty_bar = full_bar + kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty_bar + kStages);
+  const long long wait_ns = p.wait_ns;
   uint8_t* route = smem + SmemLayout::route_off<TOKC>();
   int32_t* topk_s = reinterpret_cast<int32_t*>(route);
   int32_t* list_tok = reinterpret_cast<int32_t*>(route + kMaxRouting * 4);  // token | slot<<8
@@ -125,6 +137,7 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kConsumerWarps);
     }
+    *abort_flag = 0;
     fence_barrier_init();
   }
 
@@ -169,8 +182,9 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
   if (warp == kConsumerWarps) {
     if (lane == 0) {
       uint32_t it = 0;
+      bool stop = false;
       const uint64_t pol = l2_evict_first_policy();
-      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
         // the slab's rows inside its 128-row tile; each k-tile piece of the
         // slab is contiguous (rows x 48 B) in the tile-ordered code stream
         const uint8_t* mat = p.codes;
@@ -189,7 +203,16 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
         for (int st = 0; st < nstages_unit; ++st, ++it) {
           const int slot = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          wait_bounded(&empty_bar[slot], ph ^ 1u);
+          if (it >= static_cast<uint32_t>(kStages)) {
+            // the slot's previous stage must be consumed, and its copies
+            // landed (always so after a normal release; checked so that no
+            // give-up elsewhere can re-arm a barrier with copies in flight)
+            if (!wait_bounded(&empty_bar[slot], ph ^ 1u, abort_flag, wait_ns)) {
+              stop = true;
+              break;
+            }
+            wait_drain(&full_bar[slot], ph ^ 1u);
+          }
           const int c0 = st * kConsumerWarps;
           const int nvalid = min(kConsumerWarps, nchunks - c0);
           mbar_arrive_expect_tx(&full_bar[slot], nvalid * piece);
@@ -198,6 +221,10 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
                      tile + static_cast<long long>(c0 + c) * rows_t * 48, piece, &full_bar[slot], pol);
         }
       }
+      // every copy this CTA issued has landed before the thread (and so the
+      // CTA) can end
+      for (uint32_t j = it > static_cast<uint32_t>(kStages) ? it - kStages : 0u; j < it; ++j)
+        wait_drain(&full_bar[j % kStages], (j / kStages) & 1u);
     }
     return;
   }
@@ -289,7 +316,7 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
             av[tc][q] = arow[tc] ? __ldg(reinterpret_cast<const uint2*>(arow[tc] + chunk * 128 + q * 32))
                                  : make_uint2(0, 0);
       }
-      wait_bounded(&full_bar[slot], ph);
+      wait_bounded(&full_bar[slot], ph, abort_flag, wait_ns);
       if (chunk < nchunks) {
         const uint32_t box = smem_u32(stage_buf + slot * kStageBytes + warp * kBoxBytes);
         const uint32_t rowA = box + g * 48, rowB = box + (g + 8) * 48;
@@ -390,8 +417,13 @@ __global__ void unpack_kernel(const uint8_t* __restrict__ codes, const uint8_t* 
 template <int TOKC, bool GROUPED>
 int launch_gemv_t(const GemvParams& p, int units_upper, cudaStream_t stream) {
   const int smem = SmemLayout::total<TOKC, GROUPED>();
-  static int occupancy = 0;  // per template instance, computed once
+  // the shared-memory attribute and the occupancy, once per device and
+  // template instance (the attribute is a per-device setting)
+  static std::atomic<int> occupancy_of[64] = {};
   auto kern = gemv_kernel<TOKC, GROUPED>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CBQ_EDEVICE;
+  int occupancy = occupancy_of[dev].load(std::memory_order_acquire);
   if (occupancy == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return CBQ_ECUDA;
@@ -399,6 +431,7 @@ int launch_gemv_t(const GemvParams& p, int units_upper, cudaStream_t stream) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem) != cudaSuccess)
       return CBQ_ECUDA;
     occupancy = occ > 0 ? occ : 1;
+    occupancy_of[dev].store(occupancy, std::memory_order_release);
   }
   const int grid = std::max(1, std::min(units_upper, device_sm_count() * occupancy));
   kern<<<grid, kThreads, smem, stream>>>(p);

@@ -22,6 +22,7 @@ struct GemvParams {
   const int32_t* topk_idx;    // grouped only: [M][topk]
   int M, N, K;
   int E, topk;                // grouped only
+  long long wait_ns;          // bounded waits give up after this many ns
 };
 
 // Kernel parameters of the tcgen05 kernel (dense and grouped).
@@ -40,25 +41,24 @@ struct UmmaParams {
   int b_bytes;                // shared bytes of the resident activation tile
   int red_bytes;              // shared bytes of the split-K partial tiles (leader CTA)
   int code_stages;            // depth of the code-stage ring (<= kMaxCodeStages)
+  long long wait_ns;          // bounded waits give up after this many ns
 };
 
 // Kernel parameters of the stream-K kernel (dense calls, cbq_sk.cu).
 struct SkParams {
   CUtensorMap a_map;          // activations a[M][K]: box of ntok rows x 128 B, 128-byte swizzle
-                              // (b_layout 0), or the [K/16][M][16] view, box [8][ntok][16] (1)
   const uint8_t* codes;       // code stream (tile order)
   const uint8_t* a;           // [M][K] E4M3
   const float* a_scale;       // [M]
   const uint8_t* scales;      // [N][K/32]
   const uint8_t* codebooks;   // [N][8]
   float* y;                   // [M][N]
-  float* partial;             // scratch: 2 x grid partial tiles of 128 x NTOK fp32
-  unsigned* counters;         // scratch: one arrival counter per 128-row tile, zero between calls
+  float* partial;             // workspace: 2 x grid partial tiles of 128 x NTOK fp32
+  unsigned* counters;         // workspace: one arrival counter per 128-row tile, zero between calls
+  long long wait_ns;          // bounded waits give up after this many ns
   int M, N, K;
   int stages;                 // depth of the code-stage ring
-  int a_slots;                // decoded-unit slots in shared memory
   int b_ktiles;               // k-tiles of resident activations
-  int b_layout;               // 0: 128-byte swizzled rows, 1: core-matrix chunks (no swizzle)
 };
 
 // cuTensorMapEncodeTiled from the driver (nullptr if unavailable).
@@ -69,6 +69,7 @@ EncodeTiledFn encode_tiled_fn();
 
 int device_sm_count();
 void note_launch();
+long long wait_limit_ns();   // current bound of the kernels' mbarrier waits (cbq_set_wait_limit)
 
 int launch_gemv(const GemvParams& p, bool grouped, cudaStream_t stream);
 int launch_unpack(const uint8_t* codes, const uint8_t* scales, const uint8_t* codebooks, int N,
@@ -79,7 +80,8 @@ int launch_umma(const UmmaParams& p, bool grouped, cudaStream_t stream);
 unsigned take_status_umma(cudaStream_t stream);
 
 bool sk_applicable(int M, int N, int K);
-int launch_sk(const SkParams& p, cudaStream_t stream);
+size_t sk_workspace_bytes(int M, int N, int K);   // 0 if the stream-K kernel cannot take the shape
+int launch_sk(const SkParams& p, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 int launch_sk_static(const SkParams& p, cudaStream_t stream);
 unsigned take_status_sk(cudaStream_t stream);
 

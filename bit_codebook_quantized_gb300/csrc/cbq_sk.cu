@@ -1,7 +1,8 @@
 // cbq_sk.cu -- stream-K kernel of the codebook-quantised matmul for dense
 // calls: every SM streams an equal, contiguous share of the packed weights,
-// decodes the 3-bit codes to E4M3 in shared memory and multiplies them with
-// the block-scaled FP8 tensor cores (tcgen05), fp32 accumulators in TMEM.
+// decodes the 3-bit codes to E4M3 straight into tensor memory and multiplies
+// them with the block-scaled FP8 tensor cores (tcgen05), fp32 accumulators in
+// TMEM.
 //
 // "Hibana: Fast Agentic Inference on Unified-Memory Devices", section "Model
 // surgery / Three-bit weights": codes look up an 8-entry FP8 codebook per
@@ -15,38 +16,44 @@
 // their order in the tile-ordered code stream, so CTA b's share
 // [b U / G, (b + 1) U / G) is ONE contiguous byte range of the codes.  A
 // tile whose k-tiles are shared by several CTAs is finished by whichever of
-// them arrives last on the tile's counter: each writes its fp32 partial tile
-// to scratch, the last one sums the parts in part order (deterministic) and
-// writes y.
+// them arrives last on the tile's counter in the caller's workspace: each
+// writes its fp32 partial tile there, the last one sums the parts in part
+// order (deterministic) and writes y.
 //
-// Roles (one CTA per SM, 768 threads; a warp's sub-partition is warp % 4):
-//  * warp 5: 1-D bulk copies of 4 consecutive units (24 KB, one contiguous
+// Roles (one CTA per SM, 24 warps; a warp's sub-partition is warp % 4, and a
+// warp reaches only the TMEM lanes 32 (warp % 4) .. + 31):
+//  * warp 0: 1-D bulk copies of 4 consecutive units (24 KB, one contiguous
 //    piece of the stream) into a ring of shared-memory stages;
-//  * 12 decoder warps, all on sub-partitions 0, 2, 3 (so the MMA issuer on
-//    sub-partition 1 has its issue slots to itself), in 3 groups of 4: group
-//    g decodes the units i = g mod 3, one warp per 32 rows; a thread (one
-//    row) loads its 48 code bytes, releases the stage,
-//    spreads the codes to nibbles and turns them into E4M3 bytes with
-//    byte-permutes through the row's codebook (two registers), and stores
-//    the 128 bytes into the unit's A slot in shared memory (K-major
-//    core-matrix layout, conflict-free 16-byte stores) with the row's 4 E8M0
-//    group scales beside them;
-//  * warp 1 (one lane): per unit one tcgen05.cp of the scales into TMEM and
-//    4 tcgen05.mma kind::mxf8f6f4.block_scale (K = 32) with A and B (the
-//    activations, resident in shared memory for the CTA's k-tiles, landed by
-//    TMA) from shared-memory descriptors; the E8M0 group scale is the MX
-//    block scale of its 32-wide K block;
-//  * warps 16..19: epilogue -- tcgen05.ld the accumulator (two alternate, one
+//  * warps 4..19: 16 decoders in 4 groups; group g decodes position g of
+//    every stage (unit 4 j + g), its warp w takes the 32 rows of lane quadrant
+//    w % 4: a thread (one row = one TMEM lane) loads its 48 code bytes,
+//    spreads the codes to nibbles, turns them into E4M3 bytes with byte
+//    permutes through the row's codebook (two registers), and writes the 128
+//    bytes into one of the group's two A slots in TMEM (32 columns) with the
+//    row's 4 E8M0 group scales as the A scale factors.  Because a group takes
+//    exactly one unit per stage, its stage slot and A slot advance by one per
+//    unit: no division on the decode path;
+//  * warp 1 (one lane): TMEM allocation, the activations by TMA (after the
+//    grid dependency), then per unit 4 tcgen05.mma kind::mxf8f6f4.block_scale
+//    (K = 32) with A from TMEM and B from shared memory; the E8M0 group scale
+//    is exactly the MX block scale of its 32-wide K block;
+//  * warps 20..23: epilogue -- tcgen05.ld the accumulator (two alternate, one
 //    per tile segment), then either y = a_scale * acc or the partial-tile
 //    protocol above.
+//
+// Bounded waits: every mbarrier wait gives up after the call's wait limit and
+// raises the CTA's abort flag; later waits of the CTA then give up at once.
+// Giving up never leaves asynchronous work behind: the producer re-arms a
+// stage only after the copy it held has landed and, before the CTA ends,
+// waits for every copy it issued; the MMA thread waits for all its
+// tensor-core work before TMEM is freed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
-#include <map>
 #include <mutex>
-#include <utility>
 
 #include "cbq_device.cuh"
 #include "cbq_internal.h"
@@ -58,67 +65,64 @@ static __device__ unsigned g_status_sk = 0;
 namespace {
 
 constexpr int kRows = 128;                            // MMA M: weight rows per tile
+constexpr int kUnitBytes = kRows * 48;                // codes of one full unit
 constexpr int kUnitsPerStage = 4;
-constexpr int kStageBytes = kUnitsPerStage * kRows * 48;   // 24 KB
+constexpr int kStageBytes = kUnitsPerStage * kUnitBytes;   // 24 KB
 constexpr int kMaxStages = 8;
-constexpr int kMaxASlots = 8;
-constexpr int kASlotA = kRows * 128;                  // decoded E4M3 A of one unit
-constexpr int kASlotBytes = kASlotA + kRows * 16;     // + one 16-byte scale row per weight row
-constexpr int kTasksPerUnit = 4;                      // 32 rows each
-constexpr int kDecGroups = 3;                         // unit i goes to group i % 3
-static_assert(kDecGroups * kTasksPerUnit == 12, "12 decoder warps");
+constexpr int kGroups = 4;                            // decoder group g <-> stage position g
+static_assert(kGroups == kUnitsPerStage, "one unit per group per stage");
+constexpr int kASlots = 2 * kGroups;                  // group g owns A slots g and g + 4
+constexpr int kProdWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kProdWarp = 5;
-constexpr int kEpiWarp0 = 16;                         // warps 16..19: quadrants 0..3
+constexpr int kDecWarp0 = 4;                          // warps 4..19
+constexpr int kEpiWarp0 = 20;                         // warps 20..23
 constexpr int kNumWarps = 24;
 constexpr int kThreads = kNumWarps * 32;
-constexpr int kTmemCols = 256;
+constexpr int kTmemCols = 512;
+constexpr int kSfbCol = 128;                          // 8 columns of B scale factors (2^0)
+constexpr int kSfaCol = 136;                          // + 4 * A slot (4-column aligned)
+constexpr int kACol = 256;                            // + 32 * A slot
 constexpr int kMaxSmem = 232448;
-constexpr int kMinSmem = 120 * 1024;                  // one CTA per SM
-constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxASlots + 5;
+constexpr int kMinSmem = 120 * 1024;                  // one CTA per SM: it owns all of TMEM
+constexpr int kNumBars = 2 * kMaxStages + 2 * kASlots + 2 + 2 + 2;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
+constexpr long long kDrainLimitNs = 10000000000LL;    // copies and MMAs always finish; 10 s is a backstop
 
-// Decoder index of a warp (0..11), or -1: warps 0..15 off sub-partition 1
-// (sub-partition 1 belongs to the MMA issuer).  Warps 9, 13, 20..23 idle.
-__device__ __forceinline__ int decoder_index(int warp) {
-  if (warp >= 16) return -1;
-  const int q = warp & 3;
-  return q == 1 ? -1 : (warp >> 2) * 3 + (q == 0 ? 0 : q - 1);
-}
-
-// Tensor-memory columns for NTOK token columns: two fp32 accumulators (32-column
-// aligned), 8 columns of B scale factors (2^0), then 4 scale-factor columns per
-// A slot (4-column aligned).
 template <int NTOK>
-struct TmemMap {
-  static constexpr int kAccStride = NTOK < 32 ? 32 : NTOK;
-  static constexpr int kAcc = 0;                              // + kAccStride * buffer
-  static constexpr int kSfb = 2 * kAccStride;
-  static constexpr int kSfa = kSfb + 8;                       // + 4 * slot
-  static_assert(kSfa + 4 * kMaxASlots <= kTmemCols, "TMEM map exceeds the allocation");
+struct AccCols {
+  static constexpr int kStride = NTOK < 32 ? 32 : NTOK;   // accumulator b at column b * kStride
+  static_assert(2 * kStride <= kSfbCol, "accumulators overlap the scale-factor columns");
 };
 
 __device__ __forceinline__ void raise(unsigned bits) { atomicOr(&g_status_sk, bits); }
-__device__ __forceinline__ bool status_set() {
-  return *reinterpret_cast<volatile unsigned*>(&g_status_sk) != 0u;
-}
 
-// Wait for an mbarrier phase, suspended in the barrier rather than spinning
-// (spinning warps would steal issue slots from the warps that work).  After
-// ~0.5 ms give up at once if another wait already timed out; after
-// kWaitLimitNs raise kErrTimeout and give up.
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+// Wait for an mbarrier phase, suspended in the barrier between polls.  Gives
+// up (returns false) at once when the CTA's abort flag is up, or after
+// `limit_ns`, raising the flag and the library's timeout status.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = global_ns();
   for (;;) {
     if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
-    const long long dt = global_ns() - t0;
-    if (dt > 500000LL) {
-      if (status_set()) return false;
-      if (dt > kWaitLimitNs) {
-        raise(kErrTimeout);
-        return false;
-      }
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      raise(kErrTimeout);
+      return false;
+    }
+  }
+}
+
+// Wait for asynchronous work this CTA issued itself (a bulk copy, a TMA load,
+// tensor-core work), whatever the abort flag says: it always completes.
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return;
+  const long long t0 = global_ns();
+  while (!mbar_try_wait_suspend(bar, parity, 20000u)) {
+    if (global_ns() - t0 > kDrainLimitNs) {
+      raise(kErrTimeout);
+      return;
     }
   }
 }
@@ -129,10 +133,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr));
   return v;
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // Unit geometry of an N x K weight in the tile-ordered code stream.  Unit
@@ -160,22 +160,24 @@ struct Geo {
 
 template <int NTOK>
 __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__ SkParams p) {
-  using TM = TmemMap<NTOK>;
+  using AC = AccCols<NTOK>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  const int NS = p.stages, S = p.a_slots;
+  const int NS = p.stages;
   uint8_t* codes_s = smem;
   uint8_t* b_s = smem + NS * kStageBytes;
-  uint8_t* a_s = b_s + p.b_ktiles * NTOK * 128;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(a_s + S * kASlotBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(b_s + p.b_ktiles * NTOK * 128);
   uint64_t* full = bars;
   uint64_t* empty = full + kMaxStages;
   uint64_t* a_full = empty + kMaxStages;
-  uint64_t* a_empty = a_full + kMaxASlots;
-  uint64_t* acc_full = a_empty + kMaxASlots;
+  uint64_t* a_empty = a_full + kASlots;
+  uint64_t* acc_full = a_empty + kASlots;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* b_full = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 1);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* drain = b_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
+  const long long wait_ns = p.wait_ns;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   Geo geo;
@@ -193,10 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kUnitsPerStage * kTasksPerUnit);   // every task of the stage, once
+      mbar_init(&empty[i], 4 * kGroups);              // every decoder warp of a full stage, once
     }
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&a_full[i], kTasksPerUnit);
+    for (int i = 0; i < kASlots; ++i) {
+      mbar_init(&a_full[i], 4);                       // the group's four quadrant warps
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -204,6 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       mbar_init(&acc_empty[i], 4);
     }
     mbar_init(b_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -217,21 +221,34 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     // -------------------------------------------------------- bulk producer --
     if (lane == 0) {
       int ta = t_first, ca = c_first;                 // first unit of stage j
+      int slot = 0;
+      uint32_t ph = 0;
+      int issued = 0;
       const uint64_t pol = l2_evict_first_policy();
       for (int j = 0; j < n_stages; ++j) {
-        const int slot = j % NS;
         const int nu = min(kUnitsPerStage, n_units - j * kUnitsPerStage);
         int tl = ta, cl = ca;
         geo.advance(tl, cl, nu - 1);                   // last unit of the stage
         const long long oa = geo.off(ta, ca);
         const uint32_t bytes = static_cast<uint32_t>(geo.off(tl, cl) + geo.rows(tl) * 48LL - oa);
         geo.advance(ta, ca, kUnitsPerStage);
-        wait_bounded(&empty[slot], ((j / NS) & 1u) ^ 1u);
+        if (j >= NS) {
+          // the slot's previous stage must be decoded, and its copy landed
+          // (always so after a normal release; checked so that no give-up
+          // elsewhere can make a copy re-arm a barrier still in flight)
+          if (!wait_bounded(&empty[slot], ph ^ 1u, abort_flag, wait_ns)) break;
+          wait_drain(&full[slot], ph ^ 1u);
+        }
         mbar_arrive_expect_tx(&full[slot], bytes);
         bulk_g2s(codes_s + slot * kStageBytes, p.codes + oa, bytes, &full[slot], pol);
+        ++issued;
+        if (++slot == NS) {
+          slot = 0;
+          ph ^= 1u;
+        }
       }
-      // every copy has landed before the CTA can leave
-      for (int j = max(0, n_stages - NS); j < n_stages; ++j) wait_bounded(&full[j % NS], (j / NS) & 1u);
+      // every copy this CTA issued has landed before it can leave
+      for (int j = max(0, issued - NS); j < issued; ++j) wait_drain(&full[j % NS], (j / NS) & 1u);
     }
     __syncwarp();
   } else {
@@ -244,15 +261,14 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     tc_fence_after();
     tbase = *tmem_slot;
 
-    const int dec = decoder_index(warp);
     if (warp == kMmaWarp) {
       // --------------------------------------------------------- MMA issuer --
       named_bar_sync(3, 160);                          // B scale factors are in TMEM
       tc_fence_after();
-      if (lane == 0) {
+      if (lane == 0 && n_units > 0) {
         // Resident activations (written by an earlier kernel, so after the
         // grid dependency): k-tile c of this CTA's share lands in slot
-        // (c - c_first) mod KT as ntok rows of 128 bytes in the 128-byte
+        // (c - c_first) mod KT as NTOK rows of 128 bytes in the 128-byte
         // swizzled K-major layout (one TMA box); token rows >= M are outside
         // the tensor and arrive as zeros.
         grid_dependency_wait();
@@ -261,52 +277,35 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         for (int sl = 0; sl < nb; ++sl) {
           int c = c_first + sl;
           if (c >= KT) c -= KT;
-          uint8_t* dst = b_s + sl * NTOK * 128;
-          if (p.b_layout == 0) tma_load_2d(dst, &p.a_map, b_full, c * 128, 0);
-          else tma_load_3d(dst, &p.a_map, b_full, 0, 0, 8 * c);
+          tma_load_2d(b_s + sl * NTOK * 128, &p.a_map, b_full, c * 128, 0);
         }
         // Descriptors advance by adding offsets in their 16-byte address
-        // units (every shared address here is below 256 KB, so the 14-bit
-        // address field never carries): A slot as at as * kASlotBytes, its
-        // K chunk pair j at 2 j * 2048; B slot at bsl * NTOK * 128, its MMA j
-        // at 32 j (swizzled) or 2 j * NTOK * 16 bytes (core matrices).
-        const uint32_t a_base = smem_u32(a_s);
-        const uint64_t ad0 = umma_desc_kmajor(a_base, kRows * 16, 128);
-        const uint64_t sd0 = umma_desc_kmajor(a_base + kASlotA, 128, 128);
-        const uint64_t bd0 = p.b_layout == 0 ? umma_desc_kmajor_sw128(smem_u32(b_s))
-                                             : umma_desc_kmajor(smem_u32(b_s), NTOK * 16, 128);
-        const uint32_t b_step_j = p.b_layout == 0 ? 2u : 2u * NTOK;
+        // units: B slot bsl at bsl * NTOK * 128 bytes, its MMA j at 32 j.
+        const uint64_t bd0 = umma_desc_kmajor_sw128(smem_u32(b_s));
         const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
-        const uint32_t sfa0 = tbase + TM::kSfa, sfb = tbase + TM::kSfb;
-        wait_bounded(b_full, 0);
-        int seg = 0, c = c_first, as = 0, bsl = 0;
-        uint32_t a_phase = 0;
+        const uint32_t a_col = tbase + kACol, sfa_col = tbase + kSfaCol, sfb_col = tbase + kSfbCol;
+        wait_bounded(b_full, 0, abort_flag, wait_ns);
+        tc_fence_after();
+        int seg = 0, c = c_first, bsl = 0;
         for (int i = 0; i < n_units; ++i) {
           const bool seg_first = (i == 0) || (c == 0);
           const int abuf = seg & 1;
           if (seg_first) {
-            wait_bounded(&acc_empty[abuf], ((seg >> 1) & 1u) ^ 1u);
+            wait_bounded(&acc_empty[abuf], ((seg >> 1) & 1u) ^ 1u, abort_flag, wait_ns);
             tc_fence_after();
           }
-          wait_bounded(&a_full[as], a_phase);
+          // unit i: group i % 4, the group's use i / 4 -> A slot and phase
+          const uint32_t use = static_cast<uint32_t>(i) >> 2;
+          const uint32_t as = static_cast<uint32_t>(i & 3) + 4u * (use & 1u);
+          wait_bounded(&a_full[as], (use >> 1) & 1u, abort_flag, wait_ns);
           tc_fence_after();
-          const uint64_t a_off = static_cast<uint64_t>(as * (kASlotBytes >> 4));
-          // the unit's scale rows -> 4 TMEM columns (row r's scale word sits
-          // in every 32-bit word of its 16-byte row, whichever column the MMA
-          // reads for it)
-          tmem_cp_128x128b(sfa0 + 4 * as, sd0 + a_off);
-          const uint64_t adu = ad0 + a_off;
           const uint64_t bdu = bd0 + static_cast<uint64_t>(bsl * NTOK * 8);
-          const uint32_t d_col = tbase + TM::kAcc + abuf * TM::kAccStride;
+          const uint32_t d_col = tbase + abuf * AC::kStride;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            umma_mxf8(d_col, adu + static_cast<uint64_t>(j * 256), bdu + static_cast<uint64_t>(j * b_step_j),
-                      idesc | (uint32_t(j) << 29), sfa0 + 4 * as, sfb, (seg_first && j == 0) ? 0u : 1u);
+            umma_mxf8_ts(d_col, a_col + as * 32 + j * 8, bdu + static_cast<uint64_t>(2 * j),
+                         idesc | (uint32_t(j) << 29), sfa_col + as * 4, sfb_col, (seg_first && j == 0) ? 0u : 1u);
           umma_commit(&a_empty[as]);
-          if (++as == S) {
-            as = 0;
-            a_phase ^= 1u;
-          }
           if (c == KT - 1 || i == n_units - 1) {
             umma_commit(&acc_full[abuf]);
             ++seg;
@@ -314,23 +313,21 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           c = (c + 1 == KT) ? 0 : c + 1;
           bsl = (bsl + 1 == KT) ? 0 : bsl + 1;        // (c - c_first) mod KT
         }
+        // all tensor-core work and the activation loads are done before TMEM
+        // is freed and the CTA ends
+        umma_commit(drain);
+        wait_drain(drain, 0);
+        wait_drain(b_full, 0);
       }
       __syncwarp();
-    } else if (dec >= 0) {
+    } else if (warp >= kDecWarp0 && warp < kEpiWarp0) {
       // ------------------------------------------------------------ decoders --
-      // Decoder d = 4 g + q takes rows 32 q .. 32 q + 31 of the units
-      // i = g, g + 3, ... (group g = i % 3).  A group walks its units in
-      // order and the A-slot count is a multiple of 3, so a slot always goes
-      // back to the same group: the slot's parity wait can never be a phase
-      // (two uses) early.  Row r's 128 bytes go to the A slot as 8 chunks of
-      // 16 (chunk x at x * 2048 + r * 16: core matrices of 8 rows x 16 bytes,
-      // 128 bytes apart along M, 2048 apart along K), its scale word to the
-      // slot's scale row r (4 copies).
+      const int g = (warp - kDecWarp0) >> 2, q = warp & 3;
+      const int r = 32 * q + lane;                      // row inside the tile == TMEM lane
+      const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
       const uint32_t codes_base = smem_u32(codes_s);
-      const uint32_t a_base = smem_u32(a_s);
+      const uint32_t a_lane = tbase + lane_addr + kACol, sf_lane = tbase + lane_addr + kSfaCol + q;
       const int gk = p.K / 32;
-      const int grp = dec / kTasksPerUnit, q = dec % kTasksPerUnit;
-      const int r = 32 * q + lane;                      // row inside the tile
       // scale word and codebook of row r for the unit at (t, c)
       auto load_sc = [&](int t, int c, bool valid, uint32_t& sw, uint2& cb) {
         sw = 0x7F7F7F7Fu;
@@ -341,95 +338,74 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           cb = __ldg(reinterpret_cast<const uint2*>(p.codebooks + static_cast<size_t>(n) * 8));
         }
       };
-      // Stage slot / phase and A slot / phase of the current unit, advanced
-      // incrementally (no division by the runtime ring sizes per unit).
-      int st_j = 0, st_slot = 0, a_slot = 0;
-      uint32_t st_phase = 0, a_phase = 0;
-      auto seek = [&](int i) {                          // i only grows, by 3 at most 1 stage
-        const int j = i / kUnitsPerStage;
-        while (st_j < j) {
-          ++st_j;
-          if (++st_slot == NS) {
-            st_slot = 0;
-            st_phase ^= 1u;
-          }
-        }
-      };
-      auto process = [&](int i, int tu, int cu, uint32_t sw, uint2 cb) {
-        const int k = i % kUnitsPerStage;
-        seek(i);
-        const int slot = st_slot;
-        // every task waits for its stage before releasing it, so an early
-        // release can never count towards an older phase
-        wait_bounded(&full[slot], st_phase);
-        uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, c2 = c0;
-        const int rows_u = geo.rows(tu);
-        if (r < rows_u) {
-          // units before this one in the stage: k of them, min(k, cu) in tile
-          // tu (rows_u rows each; tu may be the ragged last tile) and the
-          // rest in full tiles before it
-          const int kin = min(k, cu);
-          const uint32_t at = codes_base + slot * kStageBytes + (kin * rows_u + (k - kin) * kRows + r) * 48;
+      int t = t_first, c = c_first;
+      geo.advance(t, c, g);                             // unit g: this group's first
+      int slot = 0;                                     // stage j = (i - g) / 4
+      uint32_t ph = 0, use = 0;
+      uint32_t sw;
+      uint2 cb;
+      load_sc(t, c, g < n_units, sw, cb);
+      for (int i = g; i < n_units; i += kGroups) {
+        // next unit of the group: its scale word and codebook in flight now
+        int t2 = t, c2 = c;
+        geo.advance(t2, c2, kGroups);
+        uint32_t sw2;
+        uint2 cb2;
+        load_sc(t2, c2, i + kGroups < n_units, sw2, cb2);
+        wait_bounded(&full[slot], ph, abort_flag, wait_ns);
+        uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, c2v = c0;
+        const int rows_t = geo.rows(t);
+        if (r < rows_t) {
+          // the g units before this one in the stage: min(g, c) of them in
+          // tile t (rows_t rows each; t may be the ragged last tile), the rest
+          // in full tiles before it
+          const int kin = min(g, c);
+          const uint32_t at = codes_base + slot * kStageBytes + (kin * rows_t + (g - kin) * kRows + r) * 48;
           c0 = lds128(at);
           c1 = lds128(at + 16);
-          c2 = lds128(at + 32);
+          c2v = lds128(at + 32);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
         uint32_t v[32];
         decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
         decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
-        decode_group(c1.z, c1.w, c2.x, cb.x, cb.y, v + 16);
-        decode_group(c2.y, c2.z, c2.w, cb.x, cb.y, v + 24);
-        const int as = a_slot;
-        wait_bounded(&a_empty[as], a_phase ^ 1u);
-        const uint32_t slot_addr = a_base + as * kASlotBytes;
-#pragma unroll
-        for (int x = 0; x < 8; ++x)
-          sts128(slot_addr + x * (kRows * 16) + r * 16, v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
-        sts128(slot_addr + kASlotA + r * 16, sw, sw, sw, sw);
-        fence_proxy_async_smem();                       // visible to the tensor core
+        decode_group(c1.z, c1.w, c2v.x, cb.x, cb.y, v + 16);
+        decode_group(c2v.y, c2v.z, c2v.w, cb.x, cb.y, v + 24);
+        const uint32_t as = static_cast<uint32_t>(g) + 4u * (use & 1u);
+        wait_bounded(&a_empty[as], ((use >> 1) & 1u) ^ 1u, abort_flag, wait_ns);
+        tc_fence_after();
+        tmem_st_x32(a_lane + as * 32, v);
+        // A scale of row m is read from TMEM lane m, column (base + m / 32),
+        // byte = the MMA's a_sf_id: quadrant q writes column base + q
+        tmem_st_x1(sf_lane + as * 4, sw);
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[as]);
-        a_slot += kDecGroups;                           // this group's next slot
-        if (a_slot >= S) {
-          a_slot -= S;
-          a_phase ^= 1u;
+        t = t2;
+        c = c2;
+        sw = sw2;
+        cb = cb2;
+        ++use;
+        if (++slot == NS) {
+          slot = 0;
+          ph ^= 1u;
         }
-      };
-      // Two register sets for the scale word and codebook, so the loads for
-      // the group's next unit are in flight during the current one (unrolled
-      // by two: no register copy has to wait for a load).
-      int ta = t_first, ca = c_first;                   // unit i (set A)
-      geo.advance(ta, ca, grp);
-      a_slot = grp;                                     // unit grp's A slot (S is a multiple of 3)
-      uint32_t swA, swB;
-      uint2 cbA, cbB;
-      load_sc(ta, ca, grp < n_units, swA, cbA);
-      for (int i = grp; i < n_units; i += 2 * kDecGroups) {
-        int tb = ta, cbb = ca;                          // unit i + 3 (set B)
-        geo.advance(tb, cbb, kDecGroups);
-        load_sc(tb, cbb, i + kDecGroups < n_units, swB, cbB);
-        process(i, ta, ca, swA, cbA);
-        if (i + kDecGroups >= n_units) break;
-        ta = tb;                                        // unit i + 6 (set A)
-        ca = cbb;
-        geo.advance(ta, ca, kDecGroups);
-        load_sc(ta, ca, i + 2 * kDecGroups < n_units, swA, cbA);
-        process(i + kDecGroups, tb, cbb, swB, cbB);
       }
-    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+    } else if (warp >= kEpiWarp0) {
+      // ------------------------------------------------------------ epilogue --
       const int q = warp & 3;
       const int r = 32 * q + lane;
       const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
       const bool leader = tid == kEpiWarp0 * 32;
       // scale factors of B: 2^0 in every byte of 8 columns, all 128 lanes
       for (int cc = 0; cc < 8; cc += 4)
-        tmem_st_x4(tbase + lane_addr + TM::kSfb + cc, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        tmem_st_x4(tbase + lane_addr + kSfbCol + cc, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       tmem_st_wait();
       tc_fence_before();
       named_bar_sync(3, 160);
-      grid_dependency_wait();                           // y and the scratch may still be in use
+      grid_dependency_wait();                           // y and the workspace may still be in use
       int seg = 0, t = t_first, c = c_first, seg_c = c_first;   // seg_c: k-tile the segment starts at
       for (int i = 0; i < n_units; ++i, geo.advance(t, c, 1)) {
         if (c != KT - 1 && i != n_units - 1) continue;
@@ -437,8 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         const int n = t * kRows + r;
         const bool ok = n < p.N;
         const int abuf = seg & 1;
-        const uint32_t acc_addr = tbase + lane_addr + TM::kAcc + abuf * TM::kAccStride;
-        wait_bounded(&acc_full[abuf], (seg >> 1) & 1u);
+        const uint32_t acc_addr = tbase + lane_addr + abuf * AC::kStride;
+        wait_bounded(&acc_full[abuf], (seg >> 1) & 1u, abort_flag, wait_ns);
         tc_fence_after();
         if (complete) {
 #pragma unroll 1
@@ -454,11 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
             }
           }
         } else {
-          // Partial tile.  Each part's fp32 tile goes to its scratch slot and
-          // bumps the tile's counter; the part that finds every other part
+          // Partial tile.  Each part's fp32 tile goes to its workspace slot
+          // and bumps the tile's counter; the part that finds every other part
           // published sums all parts in part order and writes y.  A CTA's
-          // last segment usually arrives after the other parts (first segments
-          // of later CTAs, finished early), so it first just reads the counter.
+          // last segment usually arrives after the other parts (first
+          // segments of later CTAs, finished early), so it first just reads
+          // the counter.
           const long long tu = static_cast<long long>(t) * KT;
           const long long b_first = geo.owner(tu);
           const int nparts = static_cast<int>(geo.owner(tu + KT - 1) - b_first + 1);
@@ -543,8 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     }
   }
 
-  // ---- teardown: the epilogue waited on the last commit, so every tcgen05
-  // op has completed; the producer saw its last copies land.
+  // ---- teardown: the MMA thread saw all its tensor-core work complete, the
+  // producer saw its last copies land, decoders waited for their TMEM stores.
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -556,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
 int ntok_for(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
 struct Plan {
-  int ntok = 0, grid = 0, stages = 0, a_slots = 0, b_ktiles = 0, smem = 0, tiles = 0;
+  int ntok = 0, grid = 0, stages = 0, b_ktiles = 0, smem = 0, tiles = 0;
 };
 
 bool plan_for(int M, int N, int K, Plan& pl) {
@@ -569,76 +546,37 @@ bool plan_for(int M, int N, int K, Plan& pl) {
   pl.ntok = ntok_for(M);
   pl.b_ktiles = static_cast<int>(std::min<long long>(KT, per));
   const int b_bytes = pl.b_ktiles * pl.ntok * 128;
-  // A slots first (6 or 3: a multiple of the decoder groups), then as many
-  // code stages as fit (3..8)
-  const int room = kMaxSmem - b_bytes - kBarBytes;
-  pl.a_slots = room - 6 * kASlotBytes >= 3 * kStageBytes ? 6 : 3;
-  pl.stages = std::min(kMaxStages, (room - pl.a_slots * kASlotBytes) / kStageBytes);
+  pl.stages = std::min(kMaxStages, (kMaxSmem - b_bytes - kBarBytes) / kStageBytes);
   if (pl.stages < 3) return false;
-  pl.smem = std::max(pl.stages * kStageBytes + b_bytes + pl.a_slots * kASlotBytes + kBarBytes, kMinSmem);
+  pl.smem = std::max(pl.stages * kStageBytes + b_bytes + kBarBytes, kMinSmem);
   pl.grid = static_cast<int>(G);
   pl.tiles = static_cast<int>(tiles);
   return true;
 }
 
-// Per (device, stream) scratch: partial tiles (two slots of 128 x 64 fp32 per
-// CTA) and one arrival counter per tile (all zero between calls).
-struct Scratch {
-  float* partial = nullptr;
-  size_t partial_floats = 0;
-  unsigned* counters = nullptr;
-  size_t n_counters = 0;
-};
-std::mutex g_scratch_mu;
-std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
+// Workspace layout: the tiles' arrival counters (zero between calls), then
+// two partial tiles of 128 x ntok fp32 per CTA, 256-byte aligned.
+size_t counters_bytes(const Plan& pl) { return (static_cast<size_t>(pl.tiles) * 4 + 255) / 256 * 256; }
+size_t workspace_bytes(const Plan& pl) {
+  return counters_bytes(pl) + static_cast<size_t>(2) * pl.grid * kRows * pl.ntok * sizeof(float);
+}
 
-int scratch_for(cudaStream_t s, size_t partial_floats, size_t n_counters, Scratch& out) {
+// cudaFuncSetAttribute once per (device, kernel) and largest size asked.
+template <int NTOK>
+int configure(int smem) {
+  static std::atomic<int> done[64] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return CBQ_ECUDA;
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  Scratch& sc = g_scratch[std::make_pair(dev, s)];
-  if (sc.partial_floats < partial_floats || sc.n_counters < n_counters) {
-    // Growing never frees the old buffers: a kernel in flight, or a graph
-    // captured earlier, may still use them.  cudaMalloc is allowed while the
-    // calling thread captures a graph (relaxed mode); the zeroing of new
-    // counters is ordered on the call's stream.
-    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
-    cudaThreadExchangeStreamCaptureMode(&mode);
-    cudaError_t e = cudaSuccess;
-    if (sc.partial_floats < partial_floats) {
-      const size_t want = std::max(partial_floats, size_t(2) * device_sm_count() * kRows * 64);
-      float* ptr = nullptr;
-      e = cudaMalloc(&ptr, want * sizeof(float));
-      if (e == cudaSuccess) {
-        sc.partial = ptr;
-        sc.partial_floats = want;
-      }
-    }
-    if (e == cudaSuccess && sc.n_counters < n_counters) {
-      const size_t want = std::max<size_t>(n_counters, 1 << 16);
-      unsigned* ptr = nullptr;
-      e = cudaMalloc(&ptr, want * sizeof(unsigned));
-      if (e == cudaSuccess) e = cudaMemsetAsync(ptr, 0, want * sizeof(unsigned), s);
-      if (e == cudaSuccess) {
-        sc.counters = ptr;
-        sc.n_counters = want;
-      }
-    }
-    cudaThreadExchangeStreamCaptureMode(&mode);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return CBQ_ECUDA;
-    }
-  }
-  out = sc;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CBQ_EDEVICE;
+  if (done[dev].load(std::memory_order_acquire) >= smem) return CBQ_OK;
+  if (cudaFuncSetAttribute(sk_kernel<NTOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess)
+    return CBQ_ECUDA;
+  done[dev].store(kMaxSmem, std::memory_order_release);
   return CBQ_OK;
 }
 
 template <int NTOK>
 int launch_t(const SkParams& p, const Plan& pl, cudaStream_t stream) {
-  auto kern = sk_kernel<NTOK>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem) != cudaSuccess)
-    return CBQ_ECUDA;
+  if (const int st = configure<NTOK>(pl.smem); st != CBQ_OK) return st;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.grid);
   cfg.blockDim = dim3(kThreads);
@@ -649,59 +587,33 @@ int launch_t(const SkParams& p, const Plan& pl, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, sk_kernel<NTOK>, p);
   note_launch();
   return e == cudaSuccess ? CBQ_OK : CBQ_ECUDA;
 }
 
 // Activations a[M][K] as a TMA tensor whose box is one k-tile of `ntok`
 // token rows: a 2-D view with a (128 B, ntok) box and the 128-byte swizzle;
-// rows past M read as zeros.  If the driver refuses it, a 3-D view (16 bytes,
-// M rows of stride K, K/16 chunks of stride 16) with a (16, ntok, 8) box that
-// lands in the unswizzled core-matrix layout.
+// rows past M read as zeros.
 int encode_a_map(SkParams& p, int ntok) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return CBQ_ECUDA;
-  void* base = const_cast<uint8_t*>(p.a);
-  {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K)};
-    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(ntok)};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&p.a_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
-      p.b_layout = 0;
-      return CBQ_OK;
-    }
-  }
-  const cuuint64_t dims[3] = {16, static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(p.K / 16)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.K), 16};
-  const cuuint32_t box[3] = {16, static_cast<cuuint32_t>(ntok), 8};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  if (enc(&p.a_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return CBQ_ECUDA;
-  p.b_layout = 1;
-  return CBQ_OK;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K)};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(ntok)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(&p.a_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.a), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? CBQ_OK
+             : CBQ_ECUDA;
 }
-
-}  // namespace
-
-bool sk_applicable(int M, int N, int K) {
-  Plan pl;
-  return plan_for(M, N, K, pl);
-}
-
-namespace {
 
 int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigned* counters, cudaStream_t stream) {
   SkParams p = p_in;
   p.partial = partial;
   p.counters = counters;
   p.stages = pl.stages;
-  p.a_slots = pl.a_slots;
   p.b_ktiles = pl.b_ktiles;
   const int em = encode_a_map(p, pl.ntok);
   if (em != CBQ_OK) return em;
@@ -712,7 +624,7 @@ int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigne
 
 // Static scratch of the allocation-free entry point: partial tiles for up to
 // kStaticCtas CTAs at 64 token columns, and counters for kStaticTiles tiles.
-// Zero at module load; each kernel returns the counters it used to zero.
+// Zero at module load; each call clears the counters it will use.
 constexpr int kStaticCtas = 160;
 constexpr int kStaticTiles = 1 << 16;
 __device__ __align__(256) float g_static_partial[2 * kStaticCtas * kRows * 64];
@@ -720,20 +632,32 @@ __device__ __align__(256) unsigned g_static_counters[kStaticTiles];
 
 }  // namespace
 
-int launch_sk(const SkParams& p_in, cudaStream_t stream) {
+bool sk_applicable(int M, int N, int K) {
+  Plan pl;
+  return plan_for(M, N, K, pl);
+}
+
+size_t sk_workspace_bytes(int M, int N, int K) {
+  Plan pl;
+  return plan_for(M, N, K, pl) ? workspace_bytes(pl) : 0;
+}
+
+int launch_sk(const SkParams& p_in, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   Plan pl;
   if (!plan_for(p_in.M, p_in.N, p_in.K, pl)) return CBQ_EINVAL;
-  Scratch sc;
-  const int st = scratch_for(stream, size_t(2) * pl.grid * kRows * pl.ntok, size_t(pl.tiles), sc);
-  if (st != CBQ_OK) return st;
-  return launch_planned(p_in, pl, sc.partial, sc.counters, stream);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < workspace_bytes(pl))
+    return CBQ_EINVAL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return launch_planned(p_in, pl, reinterpret_cast<float*>(ws + counters_bytes(pl)),
+                        reinterpret_cast<unsigned*>(ws), stream);
 }
 
 int launch_sk_static(const SkParams& p_in, cudaStream_t stream) {
   Plan pl;
   if (!plan_for(p_in.M, p_in.N, p_in.K, pl)) return CBQ_EINVAL;
   if (pl.grid > kStaticCtas || pl.tiles > kStaticTiles) return CBQ_EINVAL;
-  // the static buffers' addresses on the current device
+  // the static buffers' addresses on the current device (looked up on the
+  // first call on each device)
   static std::mutex mu;
   static void* partial_at[64] = {};
   static void* counters_at[64] = {};
@@ -767,12 +691,6 @@ unsigned take_status_sk(cudaStream_t stream) {
     return kErrTimeout;
   cudaMemcpyToSymbolAsync(g_status_sk, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
   cudaStreamSynchronize(stream);
-  if (v != 0) {
-    // a kernel gave up part-way: tile counters may be left non-zero
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    for (auto& kv : g_scratch)
-      if (kv.second.counters) cudaMemset(kv.second.counters, 0, kv.second.n_counters * sizeof(unsigned));
-  }
   return v;
 }
 

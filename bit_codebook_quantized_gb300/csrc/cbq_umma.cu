@@ -83,29 +83,40 @@ constexpr int kMaxRouting = 64 * 8;
 constexpr int kMaxSmem = 232448;
 constexpr int kMinSmem = 120 * 1024;          // > half an SM: one CTA per SM owns all of TMEM
 
+constexpr long long kDrainLimitNs = 10000000000LL;   // copies and MMAs always finish; 10 s is a backstop
+
 __device__ __forceinline__ void raise(unsigned bits) { atomicOr(&g_status_umma, bits); }
-__device__ __forceinline__ bool status_set() {
-  return *reinterpret_cast<volatile unsigned*>(&g_status_umma) != 0u;
-}
 
 // Wait for an mbarrier phase, suspended in the barrier between polls (a
-// polling warp takes issue slots from the warps it waits for).  After ~0.5 ms
-// give up at once if another wait already timed out; after kWaitLimitNs
-// raise kErrTimeout and give up.
+// polling warp takes issue slots from the warps it waits for).  Gives up
+// (returns false) at once when the CTA's abort flag is up, or after
+// `limit_ns`, raising the flag and the library's timeout status.
 template <bool CLUSTER = false>
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             long long limit_ns) {
   if (CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const long long t0 = global_ns();
   for (;;) {
     if (CLUSTER ? mbar_try_wait_cluster_suspend(bar, parity, 20000u) : mbar_try_wait_suspend(bar, parity, 20000u))
       return true;
-    const long long dt = global_ns() - t0;
-    if (dt > 500000LL) {
-      if (status_set()) return false;
-      if (dt > kWaitLimitNs) {
-        raise(kErrTimeout);
-        return false;
-      }
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      raise(kErrTimeout);
+      return false;
+    }
+  }
+}
+
+// Wait for asynchronous work this CTA issued itself (bulk copies, TMA loads,
+// tensor-core work), whatever the abort flag says: it always completes.
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return;
+  const long long t0 = global_ns();
+  while (!mbar_try_wait_suspend(bar, parity, 20000u)) {
+    if (global_ns() - t0 > kDrainLimitNs) {
+      raise(kErrTimeout);
+      return;
     }
   }
 }
@@ -117,10 +128,10 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 }
 
 // mbarriers (codes full/empty, A full/empty, 2 accumulators full/empty,
-// B, split-K full/free), then the TMEM base slot and two ints.
-constexpr int kNumBars = 2 * kMaxCodeStages + 2 * kAStages + 4 + 3;
-constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
-static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area too small");
+// B, split-K full/free, MMA drain), then the TMEM base slot and four ints.
+constexpr int kNumBars = 2 * kMaxCodeStages + 2 * kAStages + 4 + 4;
+constexpr int kBarBytes = (kNumBars * 8 + 24 + 127) / 128 * 128;
+static_assert(kNumBars * 8 + 24 <= kBarBytes, "barrier area too small");
 
 // Shared-memory carve-up (byte offsets), identical on host and device.
 struct Layout {
@@ -153,8 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   uint64_t* b_full = acc_empty + 2;                      // resident activations landed
   uint64_t* red_full = b_full + 1;
   uint64_t* red_free = red_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_free + 1);
+  uint64_t* drain = red_free + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* misc = reinterpret_cast<int*>(tmem_slot + 2);     // [1] experts used (grouped)
+  volatile int* abort_flag = misc + 2;
+  const long long wait_ns = p.wait_ns;
   int32_t* topk_s = reinterpret_cast<int32_t*>(smem + L.route);
   int32_t* slot_of = topk_s + kMaxRouting;               // grouped: y slot of each token for the current expert, or -1
   uint16_t* used_list = reinterpret_cast<uint16_t*>(slot_of + 64 + 4);
@@ -186,6 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     mbar_init(b_full, 1);
     mbar_init(red_full, (cs > 1 ? cs - 1 : 1) * 128);
     mbar_init(red_free, 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -268,20 +284,33 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     // consecutive k-tiles of the tile, contiguous in the code stream.
     if (lane == 0) {
       uint32_t sg = 0;
+      bool stop = false;
       const uint64_t pol = l2_evict_first_policy();
-      for (int ui = 0; ui < n_units; ++ui) {
+      for (int ui = 0; ui < n_units && !stop; ++ui) {
         int rows_t;
         const uint8_t* tile = unit_tile(ui, rows_t);
         for (int st = 0; st < n_stages_u; ++st, ++sg) {
           const int slot = sg % NS;
           const int kb = kt0 + st * kKtPerStage, nk = min(kKtPerStage, kt1 - kb);
           const uint32_t bytes = static_cast<uint32_t>(nk * rows_t * 48);
-          wait_bounded(&codes_empty[slot], ((sg / NS) & 1u) ^ 1u);
+          if (sg >= static_cast<uint32_t>(NS)) {
+            // the slot's previous stage must be released, and its copy
+            // landed (always so after a normal release; checked so that no
+            // give-up elsewhere can re-arm a barrier with a copy in flight)
+            if (!wait_bounded(&codes_empty[slot], ((sg / NS) & 1u) ^ 1u, abort_flag, wait_ns)) {
+              stop = true;
+              break;
+            }
+            wait_drain(&codes_full[slot], ((sg / NS) & 1u) ^ 1u);
+          }
           mbar_arrive_expect_tx(&codes_full[slot], bytes);
           bulk_g2s(codes_s + slot * kCodeStage, tile + static_cast<long long>(kb) * rows_t * 48, bytes,
                    &codes_full[slot], pol);
         }
       }
+      // every copy this CTA issued has landed before it can leave
+      for (uint32_t j = sg > static_cast<uint32_t>(NS) ? sg - NS : 0u; j < sg; ++j)
+        wait_drain(&codes_full[j % NS], (j / NS) & 1u);
     }
     __syncwarp();
     if (cs > 1) cluster_wait();
@@ -323,11 +352,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
         uint32_t nbase[kDecGroups];
 #pragma unroll
         for (int g = 0; g < kDecGroups; ++g) nbase[g] = 0;
-        wait_bounded(b_full, 0);                        // resident activations landed
+        wait_bounded(b_full, 0, abort_flag, wait_ns);   // resident activations landed
         tc_fence_after();
         for (int ui = 0; ui < n_units; ++ui) {
           const int abuf = ui & 1;
-          wait_bounded(&acc_empty[abuf], ((ui >> 1) & 1) ^ 1);
+          wait_bounded(&acc_empty[abuf], ((ui >> 1) & 1) ^ 1, abort_flag, wait_ns);
           tc_fence_after();
           const uint32_t d_col = tbase + abuf * kAccCols;
           for (int i0 = 0; i0 < nk; i0 += kDecGroups) {
@@ -337,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
               if (i < nk) {
                 const uint32_t n = nbase[g] + static_cast<uint32_t>(i0 / kDecGroups);
                 const uint32_t slot = (n & 1u) * kDecGroups + g;
-                wait_bounded(&a_full[slot], (n >> 1) & 1u);
+                wait_bounded(&a_full[slot], (n >> 1) & 1u, abort_flag, wait_ns);
                 tc_fence_after();
                 // B of k-tile i: NTOK swizzled rows of 128 bytes at i * NTOK * 128,
                 // i.e. i * NTOK * 8 in the descriptor's 16-byte address units;
@@ -355,6 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
           for (int g = 0; g < kDecGroups; ++g) nbase[g] += static_cast<uint32_t>((nk + kDecGroups - 1 - g) / kDecGroups);
           umma_commit(&acc_full[abuf]);
         }
+        // all tensor-core work and the activation loads are done before TMEM
+        // is freed and the CTA ends
+        umma_commit(drain);
+        wait_drain(drain, 0);
+        wait_drain(b_full, 0);
       }
       __syncwarp();
     } else if (warp < kEpiWarp0) {
@@ -374,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       auto release_until = [&](int s_end) {
         for (; released < s_end; ++released) {
           const uint32_t sg = sg_unit + released;
-          wait_bounded(&codes_full[sg % NS], (sg / NS) & 1u);
+          wait_bounded(&codes_full[sg % NS], (sg / NS) & 1u, abort_flag, wait_ns);
           __syncwarp();
           if (lane == 0) mbar_arrive(&codes_empty[sg % NS]);
         }
@@ -385,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
         const int s = (kt - kt0) / kKtPerStage, j = (kt - kt0) % kKtPerStage;
         release_until(s);
         const uint32_t sgi = sg_unit + s;
-        wait_bounded(&codes_full[sgi % NS], (sgi / NS) & 1u);
+        wait_bounded(&codes_full[sgi % NS], (sgi / NS) & 1u, abort_flag, wait_ns);
         const uint32_t crow = codes_base + (sgi % NS) * kCodeStage + (j * rows_t + r) * 48;
         const uint4 c0 = lds128(crow), c1 = lds128(crow + 16), c2 = lds128(crow + 32);
         decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
@@ -401,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
       uint32_t uses = 0;
       auto store = [&](uint32_t n, uint32_t sw, const uint32_t (&v)[32]) {
         const int aslot = static_cast<int>(n & 1u) * kDecGroups + dg;
-        wait_bounded(&a_empty[aslot], ((n >> 1) & 1u) ^ 1u);
+        wait_bounded(&a_empty[aslot], ((n >> 1) & 1u) ^ 1u, abort_flag, wait_ns);
         tc_fence_after();
         tmem_st_x32(tbase + lane_addr + kACol + aslot * 32, v);
         // A scale of row m is read from TMEM lane m, column (base + m / 32),
@@ -490,11 +524,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
         const int grow = row0 + r;
         const bool ok = grow < row_end;
         const int abuf = ui & 1;
-        wait_bounded(&acc_full[abuf], (ui >> 1) & 1);
+        wait_bounded(&acc_full[abuf], (ui >> 1) & 1, abort_flag, wait_ns);
         tc_fence_after();
         const bool split = !GROUPED && cs > 1;
-        if (split && rank != 0) wait_bounded<true>(red_free, (ui & 1) ^ 1);
-        if (split && rank == 0) wait_bounded<true>(red_full, ui & 1);
+        if (split && rank != 0) wait_bounded<true>(red_free, (ui & 1) ^ 1, abort_flag, wait_ns);
+        if (split && rank == 0) wait_bounded<true>(red_full, ui & 1, abort_flag, wait_ns);
         // 16 accumulator columns (token rows) at a time: load, reduce, store
 #pragma unroll 1
         for (int c0 = 0; c0 < NTOK; c0 += 16) {

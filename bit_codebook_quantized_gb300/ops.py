@@ -24,8 +24,8 @@ PATH_AUTO, PATH_GEMV, PATH_MMA, PATH_STREAMK = 0, 1, 2, 3
 OK, EINVAL, ECUDA, EDEVICE, ETIMEOUT, EROUTING = 0, -1, -2, -3, -4, -5
 
 # Every symbol include/cbq.h declares.
-EXPORTS = ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path", "cbq_gemm_auto_path",
-           "cbq_gemm_noalloc",
+EXPORTS = ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_ws", "cbq_gemm_workspace_size",
+           "cbq_gemm_path", "cbq_gemm_auto_path", "cbq_gemm_noalloc", "cbq_set_wait_limit",
            "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_launch_count",
            "cbq_status_str", "cbq_draft_length", "cbq_select_budget")
 
@@ -59,8 +59,11 @@ def lib() -> ctypes.CDLL:
         L.cbq_pack.argtypes = [vp, i32, i32, vp, vp, vp]
         L.cbq_unpack.argtypes = [ctypes.POINTER(_Weight), i32, i32, vp, vp]
         L.cbq_gemm.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp]
-        L.cbq_gemm_path.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp, i32]
-        L.cbq_gemm_auto_path.argtypes = [i32, i32, i32]
+        L.cbq_gemm_ws.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp, sz, vp]
+        L.cbq_gemm_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
+        L.cbq_gemm_path.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp, sz, vp, i32]
+        L.cbq_gemm_auto_path.argtypes = [i32, i32, i32, i32]
+        L.cbq_set_wait_limit.argtypes = [ctypes.c_int64]
         L.cbq_gemm_noalloc.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp]
         L.cbq_grouped_gemm.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, vp, i32, i32, i32,
                                        i32, vp, vp]
@@ -74,8 +77,9 @@ def lib() -> ctypes.CDLL:
         dp = ctypes.POINTER(ctypes.c_double)
         L.cbq_draft_length.argtypes = [ctypes.c_double, ctypes.c_double, i32, ctypes.POINTER(i32), dp, dp]
         L.cbq_select_budget.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
-        for name in ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_path", "cbq_gemm_auto_path",
-                     "cbq_gemm_noalloc",
+        for name in ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_ws",
+                     "cbq_gemm_workspace_size", "cbq_gemm_path", "cbq_gemm_auto_path", "cbq_gemm_noalloc",
+                     "cbq_set_wait_limit",
                      "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_draft_length",
                      "cbq_select_budget"):
             getattr(L, name).restype = ctypes.c_int
@@ -83,11 +87,41 @@ def lib() -> ctypes.CDLL:
         return L
 
 
-def auto_path(M: int, N: int, K: int) -> int:
-    """The kernel cbq_gemm picks for an M x N x K call (PATH_GEMV/_MMA/_STREAMK)."""
-    p = lib().cbq_gemm_auto_path(M, N, K)
+def auto_path(M: int, N: int, K: int, with_workspace: bool = True) -> int:
+    """The kernel cbq_gemm_ws picks for an M x N x K call with or without a
+    workspace (PATH_GEMV/_MMA/_STREAMK)."""
+    p = lib().cbq_gemm_auto_path(M, N, K, int(bool(with_workspace)))
     _check(p if p < 0 else OK, "cbq_gemm_auto_path")
     return p
+
+
+def workspace_size(M: int, N: int, K: int) -> int:
+    """Bytes of the workspace cbq_gemm_ws needs for an M x N x K call."""
+    b = ctypes.c_size_t()
+    _check(lib().cbq_gemm_workspace_size(M, N, K, ctypes.byref(b)), "cbq_gemm_workspace_size")
+    return b.value
+
+
+def set_wait_limit(ns: int) -> None:
+    """cbq_set_wait_limit: bound of the kernels' waits (<= 0: the default 2 s)."""
+    _check(lib().cbq_set_wait_limit(int(ns)), "cbq_set_wait_limit")
+
+
+# One zero-filled workspace per (device, stream), allocated by torch (the
+# caller side of the C ABI) on first use and large enough for any call (the
+# library leaves it zero after every call), so that it never has to grow while
+# a CUDA graph is being captured.
+_WS_MIN = 16 << 20
+_workspaces: dict = {}
+
+
+def workspace_for(device: torch.device, stream, need: int) -> torch.Tensor:
+    key = (device.index, stream.cuda_stream)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(max(need, _WS_MIN), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
 
 
 def select_budget(logits: torch.Tensor, k: int, B: int, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
@@ -184,14 +218,23 @@ def unpack(w: PackedWeights, out: torch.Tensor | None = None, stream=None) -> to
 
 
 def gemm(a: torch.Tensor, a_scale: torch.Tensor, w: PackedWeights,
-         out: torch.Tensor | None = None, path: int = PATH_AUTO, stream=None) -> torch.Tensor:
-    """y[M, N] = a_scale * (a[M, K] @ W^T); a is uint8 E4M3 bytes on the GPU."""
+         out: torch.Tensor | None = None, path: int = PATH_AUTO, stream=None,
+         workspace="auto") -> torch.Tensor:
+    """y[M, N] = a_scale * (a[M, K] @ W^T); a is uint8 E4M3 bytes on the GPU.
+
+    workspace: "auto" (a cached zero-filled buffer per device and stream, the
+    cbq_gemm_ws path), None (cbq_gemm: no workspace) or a CUDA uint8 tensor."""
     M = a.shape[0]
     if out is None:
         out = torch.empty((M, w.N), dtype=torch.float32, device=a.device)
-    ws = w.struct()
-    _check(lib().cbq_gemm_path(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(ws), M, w.N, w.K,
-                               out.data_ptr(), _stream(stream), path), "cbq_gemm")
+    st = stream if stream is not None else torch.cuda.current_stream()
+    if isinstance(workspace, str):
+        need = workspace_size(M, w.N, w.K) if M > 0 and w.N > 0 else 0
+        workspace = workspace_for(a.device, st, need) if need > 0 else None
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
+    wt = w.struct()
+    _check(lib().cbq_gemm_path(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(wt), M, w.N, w.K,
+                               out.data_ptr(), ws_ptr, ws_bytes, _stream(st), path), "cbq_gemm")
     return out
 
 

@@ -28,7 +28,10 @@
  *   results agree with an exact evaluation within 1e-3*a_scale*sum|a*w| + 1e-6.
  *
  * Conventions for every entry point:
- *   - the caller owns every buffer; no entry point allocates device memory;
+ *   - the caller owns every buffer; no entry point allocates device memory
+ *     (the fastest dense path takes scratch from a caller-owned workspace,
+ *     see cbq_gemm_ws; cbq_gemm_noalloc uses a fixed static buffer of the
+ *     library instead);
  *   - device pointers must be 16-byte aligned (cudaMalloc gives 256);
  *   - calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
  *     default stream) and never synchronise the host;
@@ -64,10 +67,8 @@ extern "C" {
                                 contiguous share of the weights per SM; needs
                                 ntok(M) * min(K/128, share) * 128 bytes of
                                 activations to fit next to a 3-stage ring
-                                (ntok = 16/32/64), else CBQ_EINVAL.  Uses a
-                                per-(device, stream) scratch buffer allocated
-                                on first use; calls on one stream must not
-                                run concurrently (graph replays included) */
+                                (ntok = 16/32/64), and a caller workspace of
+                                cbq_gemm_workspace_size bytes, else CBQ_EINVAL */
 
 /* One packed matrix in device memory (all three arrays 16-byte aligned). */
 typedef struct cbq_weight {
@@ -111,42 +112,67 @@ int cbq_unpack(const cbq_weight_t *w, int32_t N, int32_t K, float *W_out,
 /* y[M][N] = a_scale * (a[M][K] x W^T): the decode-step / verify-round matmul
  * against packed weights.  a, a_scale, y and w's arrays are DEVICE pointers.
  * 1 <= M <= 64 (M == 0 or N == 0 is a no-op); N >= 0; K % 128 == 0 (K == 0
- * writes y = 0).  Picks the kernel as CBQ_PATH_AUTO says; one launch (plus
- * a scratch allocation and zeroing on the stream's first stream-K call).
- * The result is deterministic: a tile shared by several SMs is summed in a
- * fixed order.  The stream-K kernel is launched as a programmatic dependent
- * of the previous kernel on `stream`: it may start streaming the packed
- * weights before that kernel has finished (a, a_scale and y are touched only
- * after it has), so the weights must not be written by the kernel launched
- * just before it on the same stream (copies and host writes are fine).
+ * writes y = 0).  Picks among the kernels that need no scratch memory
+ * (cbq_gemm_auto_path(M, N, K, 0)); one launch, no allocation.  For the
+ * fastest kernel on most shapes pass a workspace to cbq_gemm_ws.
  * Errors: CBQ_EINVAL, CBQ_EDEVICE, CBQ_ECUDA. */
 int cbq_gemm(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
              int32_t M, int32_t N, int32_t K, float *y, void *stream);
 
-/* The kernel (CBQ_PATH_GEMV / _MMA / _STREAMK) that cbq_gemm picks for an
- * M x N x K call, chosen by measured speed on GB300; CBQ_EINVAL for sizes
- * cbq_gemm rejects.  (If the tile kernel's activations do not fit in shared
- * memory, cbq_gemm then runs the GEMV kernel instead of CBQ_PATH_MMA.)
- * Host only: no device access. */
-int cbq_gemm_auto_path(int32_t M, int32_t N, int32_t K);
+/* Bytes of the workspace cbq_gemm_ws needs for an M x N x K call (0 when
+ * no kernel that uses one takes the shape; cbq_gemm_ws then needs none).
+ * Host only.  Errors: CBQ_EINVAL (NULL `bytes`, sizes cbq_gemm rejects). */
+int cbq_gemm_workspace_size(int32_t M, int32_t N, int32_t K, size_t *bytes);
 
-/* Same as cbq_gemm with an explicit kernel choice (CBQ_PATH_*); used by the
- * tests and the benchmark to exercise each kernel at every M. */
+/* cbq_gemm with a caller-owned DEVICE workspace (256-byte aligned, at least
+ * cbq_gemm_workspace_size bytes; NULL/0 = none, which is cbq_gemm).  With it
+ * the stream-K kernel runs where it fits: every SM streams an equal contiguous
+ * share of the packed weights and a 128-row tile split between SMs is summed
+ * through the workspace, in a fixed order (the result is deterministic).
+ * The workspace must be zero-filled before its first use (cudaMemset); every
+ * call leaves it zero again.  Calls that share one workspace must not run at
+ * the same time (one workspace per stream).  The stream-K kernel is launched
+ * as a programmatic dependent of the previous kernel on `stream`: it may
+ * start streaming the packed weights before that kernel has finished (a,
+ * a_scale, y and the workspace are touched only after it has), so the weights
+ * must not be written by the kernel launched just before it on the same
+ * stream (copies and host writes are fine).
+ * Errors: CBQ_EINVAL (also a workspace that is misaligned or too small for
+ * the kernel chosen), CBQ_EDEVICE, CBQ_ECUDA. */
+int cbq_gemm_ws(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
+                int32_t M, int32_t N, int32_t K, float *y, void *workspace,
+                size_t workspace_bytes, void *stream);
+
+/* The kernel (CBQ_PATH_GEMV / _MMA / _STREAMK) that cbq_gemm_ws picks for an
+ * M x N x K call with (with_workspace != 0) or without a workspace, chosen by
+ * measured speed on GB300; CBQ_EINVAL for sizes cbq_gemm rejects.  (If the
+ * tile kernel's activations do not fit in shared memory, the call then runs
+ * the GEMV kernel instead of CBQ_PATH_MMA.)  Host only: no device access. */
+int cbq_gemm_auto_path(int32_t M, int32_t N, int32_t K, int32_t with_workspace);
+
+/* Same as cbq_gemm_ws with an explicit kernel choice (CBQ_PATH_*); used by
+ * the tests and the benchmark to exercise each kernel at every M.
+ * CBQ_PATH_STREAMK needs the workspace. */
 int cbq_gemm_path(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
-                  int32_t M, int32_t N, int32_t K, float *y, void *stream,
-                  int32_t path);
+                  int32_t M, int32_t N, int32_t K, float *y, void *workspace,
+                  size_t workspace_bytes, void *stream, int32_t path);
 
-/* The stream-K matmul of cbq_gemm (CBQ_PATH_STREAMK) with no allocation at
- * all: its scratch (fp32 partial tiles and per-tile arrival counters) is a
- * fixed static device buffer of the library (10.5 MB of partials for up to
- * 160 SMs at 64 token columns, 65536 tile counters, i.e. N <= 8388608), so
- * the call works where the caller forbids allocations.  The pages have no
- * counterpart: this is a deployment variant of the same kernel.
- * Each call first clears the counters of the tiles it uses (one
- * cudaMemsetAsync on `stream`, no allocation), then launches the kernel.
- * The buffer is shared by every caller on the device: two calls that may run
- * at the same time (different streams, overlapping graph replays) race on it
- * and give wrong results; serialise them.
+/* The stream-K matmul (CBQ_PATH_STREAMK) with no allocation at all and no
+ * workspace argument, for callers that can neither allocate device memory
+ * nor hold a workspace of their own: its scratch (fp32 partial tiles and
+ * per-tile arrival counters) is a fixed static device buffer of the library
+ * (10.5 MB of partials for up to 160 SMs at 64 token columns, 65536 tile
+ * counters, i.e. N <= 8388608), which every GPU that loads the library holds
+ * until the process exits.  The pages have no counterpart: this is a
+ * deployment variant of the same kernel.
+ * The first call on a device looks up the buffer's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Each call first clears the counters of the
+ * tiles it uses (one cudaMemsetAsync on `stream`, no allocation), then
+ * launches the kernel.  The buffer is shared by every call on the device and
+ * keeps the last call's contents: two calls that may run at the same time
+ * (different streams, overlapping graph replays) race on it and give wrong
+ * results; serialise them.
  * Errors: CBQ_EINVAL (bad argument, K == 0, or a problem the stream-K kernel
  * or the static buffer cannot take), CBQ_EDEVICE, CBQ_ECUDA. */
 int cbq_gemm_noalloc(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
@@ -174,6 +200,14 @@ int cbq_grouped_gemm_path(const uint8_t *a, const float *a_scale,
                           const int32_t *topk_idx, int32_t topk, int32_t M,
                           int32_t N, int32_t K, float *y, void *stream,
                           int32_t path);
+
+/* Diagnostic: every kernel launched after this call gives up a bounded wait
+ * (for a copy, a tensor-core result or another role of its block) after `ns`
+ * nanoseconds instead of the default 2 s, returns early and reports
+ * CBQ_ETIMEOUT through cbq_device_status; ns <= 0 restores the default.  A
+ * wait that gives up never leaves the block's own copies or tensor-core work
+ * behind: those are waited for before the block ends. */
+int cbq_set_wait_limit(int64_t ns);
 
 /* Synchronise `stream`, then return and clear the sticky device status of
  * this library on the current device: CBQ_OK, CBQ_ETIMEOUT (a kernel's

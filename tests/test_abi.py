@@ -58,7 +58,12 @@ def test_argument_errors_before_device(L):
     assert L.cbq_gemm(16, 16, p, 1, 8, 96, 16, None) == ops.EINVAL
     assert L.cbq_gemm(16, 16, p, 65, 8, 128, 16, None) == ops.EINVAL
     assert L.cbq_gemm(16, 16, p, -1, 8, 128, 16, None) == ops.EINVAL
-    assert L.cbq_gemm_path(16, 16, p, 1, 8, 128, 16, None, 7) == ops.EINVAL
+    assert L.cbq_gemm_path(16, 16, p, 1, 8, 128, 16, None, 0, None, 7) == ops.EINVAL
+    assert L.cbq_gemm_ws(16, 16, p, 1, 8, 96, 16, None, 0, None) == ops.EINVAL
+    n = ctypes.c_size_t(7)
+    assert L.cbq_gemm_workspace_size(1, 8, 96, ctypes.byref(n)) == ops.EINVAL
+    assert L.cbq_gemm_workspace_size(1, 8, 128, None) == ops.EINVAL
+    assert L.cbq_gemm_workspace_size(0, 8, 128, ctypes.byref(n)) == ops.OK and n.value == 0
     assert L.cbq_grouped_gemm(16, 16, p, 0, 16, 1, 1, 8, 128, 16, None) == ops.EINVAL
     assert L.cbq_grouped_gemm(16, 16, p, 4, 16, 9, 1, 8, 128, 16, None) == ops.EINVAL
     assert L.cbq_grouped_gemm(16, 16, p, 4, 16, 5, 1, 8, 128, 16, None) == ops.EINVAL
@@ -138,18 +143,36 @@ def test_missing_library_fails_loudly():
 
 
 def test_auto_path_choice(L):
-    # host-only decision table of cbq_gemm (no device access)
-    assert L.cbq_gemm_auto_path(1, 12288, 4096) == ops.PATH_GEMV
-    assert L.cbq_gemm_auto_path(8, 12288, 4096) == ops.PATH_GEMV
-    assert L.cbq_gemm_auto_path(1, 151936, 2048) == ops.PATH_MMA
-    assert L.cbq_gemm_auto_path(8, 151936, 2048) == ops.PATH_MMA
-    # the stream-K plan needs no device for these shapes; at M = 64 on the
-    # vocabulary head its resident activations do not fit
-    assert L.cbq_gemm_auto_path(16, 25600, 5120) == ops.PATH_STREAMK
-    assert L.cbq_gemm_auto_path(64, 151936, 2048) == ops.PATH_MMA
-    assert L.cbq_gemm_auto_path(0, 16, 128) == ops.EINVAL
-    assert L.cbq_gemm_auto_path(4, 16, 100) == ops.EINVAL
-    assert L.cbq_gemm_auto_path(65, 16, 128) == ops.EINVAL
+    # host-only decision table (no device access)
+    # without a workspace (cbq_gemm): only the kernels that need no scratch
+    assert L.cbq_gemm_auto_path(1, 12288, 4096, 0) == ops.PATH_GEMV
+    assert L.cbq_gemm_auto_path(8, 12288, 4096, 0) == ops.PATH_GEMV
+    assert L.cbq_gemm_auto_path(1, 151936, 2048, 0) == ops.PATH_MMA
+    assert L.cbq_gemm_auto_path(16, 25600, 5120, 0) == ops.PATH_MMA
+    assert L.cbq_gemm_auto_path(64, 151936, 2048, 0) == ops.PATH_MMA
+    # with one (cbq_gemm_ws): the stream-K kernel wherever its plan fits (the
+    # plan here sees no device, i.e. one CTA holding every k-tile); at M = 64
+    # with K = 25600 its resident activations do not fit
+    for M, N, K in [(1, 12288, 4096), (8, 12288, 4096), (16, 25600, 5120),
+                    (1, 151936, 2048), (64, 151936, 2048)]:
+        assert L.cbq_gemm_auto_path(M, N, K, 1) == ops.PATH_STREAMK, (M, N, K)
+    assert L.cbq_gemm_auto_path(64, 5120, 25600, 1) == ops.PATH_MMA
+    for ws in (0, 1):
+        assert L.cbq_gemm_auto_path(0, 16, 128, ws) == ops.EINVAL
+        assert L.cbq_gemm_auto_path(4, 16, 100, ws) == ops.EINVAL
+        assert L.cbq_gemm_auto_path(65, 16, 128, ws) == ops.EINVAL
+
+
+def test_workspace_size_covers_counters_and_partials(L):
+    # one 4-byte counter per 128-row tile (256-byte aligned), then two partial
+    # tiles of 128 x ntok fp32 per CTA (the plan here sees no device: 1 CTA)
+    n = ctypes.c_size_t()
+    assert L.cbq_gemm_workspace_size(8, 12288, 4096, ctypes.byref(n)) == ops.OK
+    assert n.value == 512 + 2 * 1 * 128 * 16 * 4
+    assert L.cbq_gemm_workspace_size(64, 300, 1024, ctypes.byref(n)) == ops.OK
+    assert n.value == 256 + 2 * 1 * 128 * 64 * 4
+    assert L.cbq_gemm_workspace_size(64, 5120, 25600, ctypes.byref(n)) == ops.OK
+    assert n.value == 0                       # no kernel with a workspace takes it
 
 
 def test_library_pack_matches_the_hand_worked_lloyd_row(golden_dir):

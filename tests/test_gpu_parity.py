@@ -149,36 +149,41 @@ def test_empty_and_zero_k():
     assert ops.device_status() == ops.OK
 
 
-# ---- full workload sizes, sampled rows -------------------------------------------
+# ---- full workload sizes, every element ----------------------------------------
 
 FULL = ["gemv_2048", "decode_4096x12288_m1", "decode_4096x12288_m2", "decode_4096x12288_m4",
         "decode_4096x12288_m8", "verify_up_5120x25600_m16", "verify_down_25600x5120_m16",
         "vocab_head_2048x151936_m1", "vocab_head_2048x151936_m8", "vocab_head_2048x151936_m64"]
 
+_full_cache = {}
 
+
+def full_case(name):
+    """The workload's seeded case and its oracle result (computed once)."""
+    if name not in _full_cache:
+        wl = synth.workloads()[name]
+        c = Case(wl.M, wl.N, wl.K, seed=zlib.crc32(name.encode()) % 1000, a_scale=wl.a_scale,
+                 half_normal=wl.half_normal)
+        _full_cache.clear()                  # keep one workload's arrays at a time
+        _full_cache[name] = (c, c.oracle())
+    return _full_cache[name]
+
+
+@pytest.mark.parametrize("path", [ops.PATH_AUTO, ops.PATH_MMA, ops.PATH_GEMV])
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(name):
-    wl = synth.workloads()[name]
-    c = Case(wl.M, wl.N, wl.K, seed=zlib.crc32(name.encode()) % 1000, a_scale=wl.a_scale,
-             half_normal=wl.half_normal)
-    y = c.run(ops.PATH_AUTO)
-    rows = sample_rows(wl.N, 48, seed=3)
-    yref, b = c.oracle_rows(rows)
-    assert_close(y[:, rows], yref, b, name)
-    assert np.all(np.isfinite(y))
-    assert ops.device_status() == ops.OK
-
-
-@pytest.mark.parametrize("name", ["decode_4096x12288_m8", "verify_down_25600x5120_m16",
-                                  "vocab_head_2048x151936_m64"])
-def test_full_size_sampled_tile_kernel(name):
-    wl = synth.workloads()[name]
-    c = Case(wl.M, wl.N, wl.K, seed=zlib.crc32(name.encode()) % 1000, a_scale=wl.a_scale,
-             half_normal=wl.half_normal)
-    y = c.run(ops.PATH_MMA)
-    rows = sample_rows(wl.N, 48, seed=4)
-    yref, b = c.oracle_rows(rows)
-    assert_close(y[:, rows], yref, b, name)
+def test_full_size_every_element(name, path):
+    """Every output of the workload against the oracle: the automatic choice
+    with a workspace (the stream-K kernel where it fits), the tile kernel,
+    and the GEMV kernel on the workloads it is chosen for without one."""
+    c, (yref, b) = full_case(name)
+    if path == ops.PATH_GEMV and c.M > 8:
+        pytest.skip("the GEMV kernel is chosen only up to 8 token rows")
+    try:
+        y = c.run(path)
+    except ops.CbqError as e:
+        assert path == ops.PATH_MMA and e.status == ops.EINVAL   # activations do not fit
+        return
+    assert_close(y, yref, b, f"{name} path {path}")
     assert ops.device_status() == ops.OK
 
 
@@ -211,19 +216,20 @@ def test_grouped_small(path, E, N, K, M, budget, topk):
     assert ops.device_status() == ops.OK
 
 
+_grouped_full = {}
+
+
 @pytest.mark.parametrize("path", GROUPED_PATHS)
-def test_grouped_full_size_sampled(path):
+def test_grouped_full_size_every_element(path):
     wl = synth.workloads()["moe_verify_e128_2048x1536_m64"]
     E, N, K, M = wl.experts, wl.N, wl.K, wl.M
-    pw, a, s, idx = _grouped_case(E, N, K, M, wl.budget, wl.topk, seed=321)
+    if not _grouped_full:
+        pw, a, s, idx = _grouped_case(E, N, K, M, wl.budget, wl.topk, seed=321)
+        yref, b, reads = oracle.grouped_gemm(a, s, pw.codes, pw.scales, pw.codebooks, E, idx, M, N, K)
+        _grouped_full["case"] = (pw, a, s, idx, yref, b)
+    pw, a, s, idx, yref, b = _grouped_full["case"]
     y = _run_grouped(pw, a, s, idx, E, N, K, path)
-    rows = sample_rows(N, 24, seed=4)
-    for t in range(0, M, 7):
-        for j in range(wl.topk):
-            e = int(idx[t, j])
-            ce, se, be = oracle.expert(pw.codes, pw.scales, pw.codebooks, e, N, K)
-            yr, b = oracle.gemm_rows(a[t:t + 1], s[t:t + 1], ce, se, be, 1, N, K, rows)
-            assert_close(y[t, j, rows][None], yr, b, f"token {t} slot {j}")
+    assert_close(y, yref, b, f"grouped full size path {path}")
     assert ops.device_status() == ops.OK
 
 
