@@ -536,10 +536,16 @@ struct Plan {
   int ntok = 0, grid = 0, stages = 0, b_ktiles = 0, smem = 0, tiles = 0;
 };
 
+// Tile arrival counters live in a fixed area at the start of the workspace,
+// the same for every shape, so that partial tiles a call writes can never
+// land where a later call with more tiles expects a zero counter.
+constexpr int kMaxTiles = 1 << 16;                    // N <= 8388608 rows
+
 bool plan_for(int M, int N, int K, Plan& pl) {
   if (M < 1 || M > 64 || N < 1 || K < 128 || K % 128 != 0) return false;
   const int KT = K / 128;
   const long long tiles = (N + kRows - 1) / kRows;
+  if (tiles > kMaxTiles) return false;
   const long long U = tiles * KT;
   const long long G = std::min<long long>(U, device_sm_count());
   const long long per = (U + G - 1) / G;               // most units of any CTA
@@ -554,11 +560,11 @@ bool plan_for(int M, int N, int K, Plan& pl) {
   return true;
 }
 
-// Workspace layout: the tiles' arrival counters (zero between calls), then
-// two partial tiles of 128 x ntok fp32 per CTA, 256-byte aligned.
-size_t counters_bytes(const Plan& pl) { return (static_cast<size_t>(pl.tiles) * 4 + 255) / 256 * 256; }
+// Workspace layout: kMaxTiles arrival counters (256 KB, zero between calls),
+// then two partial tiles of 128 x ntok fp32 per CTA.
+constexpr size_t kCountersBytes = static_cast<size_t>(kMaxTiles) * 4;
 size_t workspace_bytes(const Plan& pl) {
-  return counters_bytes(pl) + static_cast<size_t>(2) * pl.grid * kRows * pl.ntok * sizeof(float);
+  return kCountersBytes + static_cast<size_t>(2) * pl.grid * kRows * pl.ntok * sizeof(float);
 }
 
 // cudaFuncSetAttribute once per (device, kernel) and largest size asked.
@@ -626,7 +632,7 @@ int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigne
 // kStaticCtas CTAs at 64 token columns, and counters for kStaticTiles tiles.
 // Zero at module load; each call clears the counters it will use.
 constexpr int kStaticCtas = 160;
-constexpr int kStaticTiles = 1 << 16;
+constexpr int kStaticTiles = kMaxTiles;
 __device__ __align__(256) float g_static_partial[2 * kStaticCtas * kRows * 64];
 __device__ __align__(256) unsigned g_static_counters[kStaticTiles];
 
@@ -648,7 +654,7 @@ int launch_sk(const SkParams& p_in, void* workspace, size_t ws_bytes, cudaStream
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < workspace_bytes(pl))
     return CBQ_EINVAL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  return launch_planned(p_in, pl, reinterpret_cast<float*>(ws + counters_bytes(pl)),
+  return launch_planned(p_in, pl, reinterpret_cast<float*>(ws + kCountersBytes),
                         reinterpret_cast<unsigned*>(ws), stream);
 }
 

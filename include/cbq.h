@@ -129,8 +129,10 @@ int cbq_gemm_workspace_size(int32_t M, int32_t N, int32_t K, size_t *bytes);
  * the stream-K kernel runs where it fits: every SM streams an equal contiguous
  * share of the packed weights and a 128-row tile split between SMs is summed
  * through the workspace, in a fixed order (the result is deterministic).
- * The workspace must be zero-filled before its first use (cudaMemset); every
- * call leaves it zero again.  Calls that share one workspace must not run at
+ * The workspace starts with a fixed area of tile counters (the first 256 KB,
+ * the same for every shape); that area must be zero-filled before the
+ * workspace's first use (cudaMemset) and every call leaves it zero again, so
+ * one workspace serves calls of any shape in turn.  Calls that share one workspace must not run at
  * the same time (one workspace per stream).  The stream-K kernel is launched
  * as a programmatic dependent of the previous kernel on `stream`: it may
  * start streaming the packed weights before that kernel has finished (a,
