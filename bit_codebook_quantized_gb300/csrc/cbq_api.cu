@@ -244,6 +244,37 @@ int cbq_gemm_noalloc(const uint8_t* a, const float* a_scale, const cbq_weight_t*
   return launch_sk_static(p, static_cast<cudaStream_t>(stream));
 }
 
+int cbq_gate_up_workspace_size(int32_t M, int32_t F, int32_t K, size_t* bytes) {
+  if (!bytes || M < 1 || M > 64 || F < 1 || K < 128 || K % 128 != 0 || static_cast<int64_t>(F) * 2 > INT32_MAX)
+    return CBQ_EINVAL;
+  *bytes = sk_gate_up_workspace_bytes(M, F, K);
+  return CBQ_OK;
+}
+
+int cbq_gemm_gate_up(const uint8_t* a, const float* a_scale, const cbq_weight_t* w, int32_t M, int32_t F,
+                     int32_t K, uint8_t* h, float* h_scale, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  if (M < 1 || M > 64 || F < 1 || K < 128 || K % 128 != 0 || static_cast<int64_t>(F) * 2 > INT32_MAX)
+    return CBQ_EINVAL;
+  if (!a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(w) || !h || !h_scale ||
+      !aligned(h_scale, 4))
+    return CBQ_EINVAL;
+  int st = current_device_checked(nullptr);
+  if (st != CBQ_OK) return st;
+  SkParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.codes = w->codes;
+  p.a = a;
+  p.a_scale = a_scale;
+  p.scales = w->scales;
+  p.codebooks = w->codebooks;
+  p.M = M;
+  p.N = 2 * F;
+  p.K = K;
+  p.wait_ns = wait_limit_ns();
+  return launch_sk_gate_up(p, workspace, workspace_bytes, h, h_scale, static_cast<cudaStream_t>(stream));
+}
+
 int cbq_gemm_ws(const uint8_t* a, const float* a_scale, const cbq_weight_t* w, int32_t M, int32_t N,
                 int32_t K, float* y, void* workspace, size_t workspace_bytes, void* stream) {
   return cbq_gemm_path(a, a_scale, w, M, N, K, y, workspace, workspace_bytes, stream, CBQ_PATH_AUTO);

@@ -56,7 +56,10 @@ struct SkParams {
   float* partial;             // workspace: 2 x grid partial tiles of 128 x NTOK fp32
   unsigned* counters;         // workspace: one arrival counter per 128-row tile, zero between calls
   long long wait_ns;          // bounded waits give up after this many ns
+  float* h;                   // gate-up only: workspace products h [M][F] fp32
+  unsigned* h_amax;           // gate-up only: workspace running max |h| per token (fp32 bits)
   int M, N, K;
+  int F;                      // gate-up only: features, N / 2
   int stages;                 // depth of the code-stage ring
   int b_ktiles;               // k-tiles of resident activations
 };
@@ -83,6 +86,9 @@ bool sk_applicable(int M, int N, int K);
 size_t sk_workspace_bytes(int M, int N, int K);   // 0 if the stream-K kernel cannot take the shape
 int launch_sk(const SkParams& p, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 int launch_sk_static(const SkParams& p, cudaStream_t stream);
+size_t sk_gate_up_workspace_bytes(int M, int F, int K);   // 0 if the kernel cannot take the shape
+int launch_sk_gate_up(const SkParams& p, void* workspace, size_t workspace_bytes, uint8_t* q, float* q_scale,
+                      cudaStream_t stream);
 unsigned take_status_sk(cudaStream_t stream);
 
 // Host quantiser (cbq_pack.cpp).

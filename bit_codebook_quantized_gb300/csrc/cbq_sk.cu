@@ -41,6 +41,13 @@
 //    per tile segment), then either y = a_scale * acc or the partial-tile
 //    protocol above.
 //
+// Fused gate-up epilogue (GATE_UP): the weight's 128-row tile t holds, for the
+// R/2 features 64 t .., their gate rows followed by their up rows (R = the
+// tile's rows).  The CTA that finishes a tile pairs gate row r with up row
+// r + R/2 through shared memory, writes h = SiLU(a_scale g) * (a_scale u) to
+// the workspace as fp32 and raises the token's running max |h| with an atomic
+// max; gate_up_quant_kernel then turns h into E4M3 with the scale max/448.
+//
 // Bounded waits: every mbarrier wait gives up after the call's wait limit and
 // raises the CTA's abort flag; later waits of the CTA then give up at once.
 // Giving up never leaves asynchronous work behind: the producer re-arms a
@@ -54,6 +61,8 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+
+#include <cuda_fp8.h>
 
 #include "cbq_device.cuh"
 #include "cbq_internal.h"
@@ -85,6 +94,8 @@ constexpr int kACol = 256;                            // + 32 * A slot
 constexpr int kMaxSmem = 232448;
 constexpr int kMinSmem = 120 * 1024;                  // one CTA per SM: it owns all of TMEM
 constexpr int kNumBars = 2 * kMaxStages + 2 * kASlots + 2 + 2 + 2;
+constexpr int kXchgStride = 17;                       // floats per exchanged row (conflict-free)
+constexpr int kXchgBytes = (64 * kXchgStride * 4 + 127) / 128 * 128;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
 constexpr long long kDrainLimitNs = 10000000000LL;    // copies and MMAs always finish; 10 s is a backstop
 
@@ -158,14 +169,15 @@ struct Geo {
   __device__ __forceinline__ long long owner(long long u) const { return ((u + 1) * G + U - 1) / U - 1; }
 };
 
-template <int NTOK>
+template <int NTOK, bool GATE_UP>
 __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__ SkParams p) {
   using AC = AccCols<NTOK>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int NS = p.stages;
   uint8_t* codes_s = smem;
   uint8_t* b_s = smem + NS * kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(b_s + p.b_ktiles * NTOK * 128);
+  float* xchg = reinterpret_cast<float*>(b_s + p.b_ktiles * NTOK * 128);   // GATE_UP: up rows of a tile
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xchg) + (GATE_UP ? kXchgBytes : 0));
   uint64_t* full = bars;
   uint64_t* empty = full + kMaxStages;
   uint64_t* a_full = empty + kMaxStages;
@@ -399,6 +411,44 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       const int r = 32 * q + lane;
       const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
       const bool leader = tid == kEpiWarp0 * 32;
+      // Finished values of one 16-column chunk of tile t (row r, columns
+      // c0..c0+15 = token rows): y = a_scale * v, or the gate-up product.
+      // Every epilogue thread calls it (it may hold named barriers).
+      auto emit = [&](int t, int c0, const float (&v)[16]) {
+        const int n = t * kRows + r;
+        if constexpr (!GATE_UP) {
+          if (n < p.N) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              if (c0 + k < p.M) p.y[static_cast<size_t>(c0 + k) * p.N + n] = v[k] * __ldg(p.a_scale + c0 + k);
+          }
+        } else {
+          const int R = geo.rows(t), half = R >> 1;
+          if (r >= half && r < R) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              xchg[(r - half) * kXchgStride + k] = c0 + k < p.M ? v[k] * __ldg(p.a_scale + c0 + k) : 0.f;
+          }
+          named_bar_sync(2, 128);
+          if (32 * q < half) {                          // warps holding gate rows
+            const int f = 64 * t + r;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              float hv = 0.f;
+              if (r < half && c0 + k < p.M) {
+                const float g = v[k] * __ldg(p.a_scale + c0 + k);
+                hv = g / (1.f + expf(-g)) * xchg[r * kXchgStride + k];
+                p.h[static_cast<size_t>(c0 + k) * p.F + f] = hv;
+              }
+              float mx = fabsf(hv);
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+              if (lane == 0 && c0 + k < p.M) atomicMax(p.h_amax + c0 + k, __float_as_uint(mx));
+            }
+          }
+          named_bar_sync(2, 128);                        // xchg is reused by the next chunk
+        }
+      };
       // scale factors of B: 2^0 in every byte of 8 columns, all 128 lanes
       for (int cc = 0; cc < 8; cc += 4)
         tmem_st_x4(tbase + lane_addr + kSfbCol + cc, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
@@ -410,8 +460,6 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       for (int i = 0; i < n_units; ++i, geo.advance(t, c, 1)) {
         if (c != KT - 1 && i != n_units - 1) continue;
         const bool complete = seg_c == 0 && c == KT - 1;
-        const int n = t * kRows + r;
-        const bool ok = n < p.N;
         const int abuf = seg & 1;
         const uint32_t acc_addr = tbase + lane_addr + abuf * AC::kStride;
         wait_bounded(&acc_full[abuf], (seg >> 1) & 1u, abort_flag, wait_ns);
@@ -422,12 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
             uint32_t tv[16];
             tmem_ld_x16(acc_addr + c0, tv);
             tmem_ld_wait();
-            if (ok) {
+            float v[16];
 #pragma unroll
-              for (int k = 0; k < 16; ++k)
-                if (c0 + k < p.M)
-                  p.y[static_cast<size_t>(c0 + k) * p.N + n] = __uint_as_float(tv[k]) * __ldg(p.a_scale + c0 + k);
-            }
+            for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(tv[k]);
+            emit(t, c0, v);
           }
         } else {
           // Partial tile.  Each part's fp32 tile goes to its workspace slot
@@ -501,11 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
                   acc[4 * k + 3] += f.w;
                 }
               }
-              if (ok) {
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                  if (c0 + k < p.M) p.y[static_cast<size_t>(c0 + k) * p.N + n] = acc[k] * __ldg(p.a_scale + c0 + k);
-              }
+              emit(t, c0, acc);
             }
             if (leader) p.counters[t] = 0u;              // ready for the next call
           }
@@ -532,16 +574,38 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
 
 int ntok_for(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
+// Quantise the gate-up products of one token (one CTA per token): scale
+// s = max|h| / 448 (1 for an all-zero token), q = E4M3(h / s) rounded to
+// nearest even, saturating; then clear the token's running max so the
+// workspace is zero again for the next call.
+__global__ void __launch_bounds__(1024) gate_up_quant_kernel(const float* __restrict__ h, unsigned* amax, int F,
+                                                              uint8_t* __restrict__ q, float* __restrict__ s_out) {
+  grid_dependency_wait();                         // h and the maxima of the matmul kernel
+  const int m = blockIdx.x;
+  const float a = __uint_as_float(*reinterpret_cast<volatile unsigned*>(amax + m));
+  const float s = a > 0.f ? a / 448.f : 1.f;
+  const float* hr = h + static_cast<size_t>(m) * F;
+  uint8_t* qr = q + static_cast<size_t>(m) * F;
+  for (int f = threadIdx.x; f < F; f += blockDim.x)
+    qr[f] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(hr[f] / s, __NV_SATFINITE, __NV_E4M3));
+  if (threadIdx.x == 0) s_out[m] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) amax[m] = 0u;
+}
+
 struct Plan {
   int ntok = 0, grid = 0, stages = 0, b_ktiles = 0, smem = 0, tiles = 0;
 };
 
-// Tile arrival counters live in a fixed area at the start of the workspace,
-// the same for every shape, so that partial tiles a call writes can never
-// land where a later call with more tiles expects a zero counter.
+// Tile arrival counters and the gate-up per-token maxima live in a fixed area
+// at the start of the workspace, the same for every shape, so that partial
+// tiles or products a call writes can never land where a later call with
+// another shape expects zeros.
 constexpr int kMaxTiles = 1 << 16;                    // N <= 8388608 rows
+constexpr size_t kCountersBytes = static_cast<size_t>(kMaxTiles) * 4;
+constexpr size_t kFixedBytes = kCountersBytes + 64 * 4;
 
-bool plan_for(int M, int N, int K, Plan& pl) {
+bool plan_for(int M, int N, int K, bool gate_up, Plan& pl) {
   if (M < 1 || M > 64 || N < 1 || K < 128 || K % 128 != 0) return false;
   const int KT = K / 128;
   const long long tiles = (N + kRows - 1) / kRows;
@@ -551,51 +615,62 @@ bool plan_for(int M, int N, int K, Plan& pl) {
   const long long per = (U + G - 1) / G;               // most units of any CTA
   pl.ntok = ntok_for(M);
   pl.b_ktiles = static_cast<int>(std::min<long long>(KT, per));
-  const int b_bytes = pl.b_ktiles * pl.ntok * 128;
-  pl.stages = std::min(kMaxStages, (kMaxSmem - b_bytes - kBarBytes) / kStageBytes);
+  const int fixed = pl.b_ktiles * pl.ntok * 128 + (gate_up ? kXchgBytes : 0) + kBarBytes;
+  pl.stages = std::min(kMaxStages, (kMaxSmem - fixed) / kStageBytes);
   if (pl.stages < 3) return false;
-  pl.smem = std::max(pl.stages * kStageBytes + b_bytes + kBarBytes, kMinSmem);
+  pl.smem = std::max(pl.stages * kStageBytes + fixed, kMinSmem);
   pl.grid = static_cast<int>(G);
   pl.tiles = static_cast<int>(tiles);
   return true;
 }
 
-// Workspace layout: kMaxTiles arrival counters (256 KB, zero between calls),
-// then two partial tiles of 128 x ntok fp32 per CTA.
-constexpr size_t kCountersBytes = static_cast<size_t>(kMaxTiles) * 4;
-size_t workspace_bytes(const Plan& pl) {
-  return kCountersBytes + static_cast<size_t>(2) * pl.grid * kRows * pl.ntok * sizeof(float);
+// Workspace layout: [tile counters, 256 KB][gate-up maxima, 64 x 4 B]
+// [two partial tiles of 128 x ntok fp32 per CTA][gate-up products, M x F fp32].
+size_t partial_bytes(const Plan& pl) { return static_cast<size_t>(2) * pl.grid * kRows * pl.ntok * sizeof(float); }
+size_t workspace_bytes(const Plan& pl, int M, int F) {
+  return kFixedBytes + partial_bytes(pl) + (F > 0 ? (static_cast<size_t>(M) * F * 4 + 255) / 256 * 256 : 0);
 }
 
-// cudaFuncSetAttribute once per (device, kernel) and largest size asked.
-template <int NTOK>
-int configure(int smem) {
+// cudaFuncSetAttribute once per (device, kernel).
+template <int NTOK, bool GATE_UP>
+int configure() {
   static std::atomic<int> done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CBQ_EDEVICE;
-  if (done[dev].load(std::memory_order_acquire) >= smem) return CBQ_OK;
-  if (cudaFuncSetAttribute(sk_kernel<NTOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess)
+  if (done[dev].load(std::memory_order_acquire)) return CBQ_OK;
+  if (cudaFuncSetAttribute(sk_kernel<NTOK, GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
+      cudaSuccess)
     return CBQ_ECUDA;
-  done[dev].store(kMaxSmem, std::memory_order_release);
+  done[dev].store(1, std::memory_order_release);
   return CBQ_OK;
 }
 
-template <int NTOK>
-int launch_t(const SkParams& p, const Plan& pl, cudaStream_t stream) {
-  if (const int st = configure<NTOK>(pl.smem); st != CBQ_OK) return st;
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel on the stream finishes (it waits on the grid dependency
+// before it touches what that kernel may write).
+template <typename... Args>
+cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, int smem, cudaStream_t stream, Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = pl.smem;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, sk_kernel<NTOK>, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
   note_launch();
-  return e == cudaSuccess ? CBQ_OK : CBQ_ECUDA;
+  return e;
+}
+
+template <int NTOK, bool GATE_UP>
+int launch_t(const SkParams& p, const Plan& pl, cudaStream_t stream) {
+  if (const int st = configure<NTOK, GATE_UP>(); st != CBQ_OK) return st;
+  return launch_pdl(sk_kernel<NTOK, GATE_UP>, dim3(pl.grid), dim3(kThreads), pl.smem, stream, p) == cudaSuccess
+             ? CBQ_OK
+             : CBQ_ECUDA;
 }
 
 // Activations a[M][K] as a TMA tensor whose box is one k-tile of `ntok`
@@ -615,7 +690,8 @@ int encode_a_map(SkParams& p, int ntok) {
              : CBQ_ECUDA;
 }
 
-int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigned* counters, cudaStream_t stream) {
+int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigned* counters, bool gate_up,
+                   cudaStream_t stream) {
   SkParams p = p_in;
   p.partial = partial;
   p.counters = counters;
@@ -623,9 +699,14 @@ int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigne
   p.b_ktiles = pl.b_ktiles;
   const int em = encode_a_map(p, pl.ntok);
   if (em != CBQ_OK) return em;
-  if (pl.ntok == 16) return launch_t<16>(p, pl, stream);
-  if (pl.ntok == 32) return launch_t<32>(p, pl, stream);
-  return launch_t<64>(p, pl, stream);
+  if (gate_up) {
+    if (pl.ntok == 16) return launch_t<16, true>(p, pl, stream);
+    if (pl.ntok == 32) return launch_t<32, true>(p, pl, stream);
+    return launch_t<64, true>(p, pl, stream);
+  }
+  if (pl.ntok == 16) return launch_t<16, false>(p, pl, stream);
+  if (pl.ntok == 32) return launch_t<32, false>(p, pl, stream);
+  return launch_t<64, false>(p, pl, stream);
 }
 
 // Static scratch of the allocation-free entry point: partial tiles for up to
@@ -640,27 +721,54 @@ __device__ __align__(256) unsigned g_static_counters[kStaticTiles];
 
 bool sk_applicable(int M, int N, int K) {
   Plan pl;
-  return plan_for(M, N, K, pl);
+  return plan_for(M, N, K, false, pl);
 }
 
 size_t sk_workspace_bytes(int M, int N, int K) {
   Plan pl;
-  return plan_for(M, N, K, pl) ? workspace_bytes(pl) : 0;
+  return plan_for(M, N, K, false, pl) ? workspace_bytes(pl, M, 0) : 0;
+}
+
+size_t sk_gate_up_workspace_bytes(int M, int F, int K) {
+  Plan pl;
+  return plan_for(M, 2 * F, K, true, pl) ? workspace_bytes(pl, M, F) : 0;
 }
 
 int launch_sk(const SkParams& p_in, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   Plan pl;
-  if (!plan_for(p_in.M, p_in.N, p_in.K, pl)) return CBQ_EINVAL;
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < workspace_bytes(pl))
+  if (!plan_for(p_in.M, p_in.N, p_in.K, false, pl)) return CBQ_EINVAL;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < workspace_bytes(pl, p_in.M, 0))
     return CBQ_EINVAL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  return launch_planned(p_in, pl, reinterpret_cast<float*>(ws + kCountersBytes),
-                        reinterpret_cast<unsigned*>(ws), stream);
+  return launch_planned(p_in, pl, reinterpret_cast<float*>(ws + kFixedBytes), reinterpret_cast<unsigned*>(ws),
+                        false, stream);
+}
+
+int launch_sk_gate_up(const SkParams& p_in, void* workspace, size_t ws_bytes, uint8_t* q, float* q_scale,
+                      cudaStream_t stream) {
+  Plan pl;
+  const int F = p_in.N / 2;
+  if (p_in.N % 2 != 0 || !plan_for(p_in.M, p_in.N, p_in.K, true, pl)) return CBQ_EINVAL;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      ws_bytes < workspace_bytes(pl, p_in.M, F))
+    return CBQ_EINVAL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  SkParams p = p_in;
+  p.F = F;
+  p.h_amax = reinterpret_cast<unsigned*>(ws + kCountersBytes);
+  p.h = reinterpret_cast<float*>(ws + kFixedBytes + partial_bytes(pl));
+  const int st = launch_planned(p, pl, reinterpret_cast<float*>(ws + kFixedBytes), reinterpret_cast<unsigned*>(ws),
+                                true, stream);
+  if (st != CBQ_OK) return st;
+  return launch_pdl(gate_up_quant_kernel, dim3(p.M), dim3(1024), 0, stream, static_cast<const float*>(p.h),
+                    p.h_amax, F, q, q_scale) == cudaSuccess
+             ? CBQ_OK
+             : CBQ_ECUDA;
 }
 
 int launch_sk_static(const SkParams& p_in, cudaStream_t stream) {
   Plan pl;
-  if (!plan_for(p_in.M, p_in.N, p_in.K, pl)) return CBQ_EINVAL;
+  if (!plan_for(p_in.M, p_in.N, p_in.K, false, pl)) return CBQ_EINVAL;
   if (pl.grid > kStaticCtas || pl.tiles > kStaticTiles) return CBQ_EINVAL;
   // the static buffers' addresses on the current device (looked up on the
   // first call on each device)
@@ -688,7 +796,7 @@ int launch_sk_static(const SkParams& p_in, cudaStream_t stream) {
   // the counters of the tiles this call uses start at zero even if an
   // earlier call gave up part-way
   if (cudaMemsetAsync(counters, 0, sizeof(unsigned) * pl.tiles, stream) != cudaSuccess) return CBQ_ECUDA;
-  return launch_planned(p_in, pl, static_cast<float*>(partial), static_cast<unsigned*>(counters), stream);
+  return launch_planned(p_in, pl, static_cast<float*>(partial), static_cast<unsigned*>(counters), false, stream);
 }
 
 unsigned take_status_sk(cudaStream_t stream) {

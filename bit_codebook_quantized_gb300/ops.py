@@ -26,6 +26,7 @@ OK, EINVAL, ECUDA, EDEVICE, ETIMEOUT, EROUTING = 0, -1, -2, -3, -4, -5
 # Every symbol include/cbq.h declares.
 EXPORTS = ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_ws", "cbq_gemm_workspace_size",
            "cbq_gemm_path", "cbq_gemm_auto_path", "cbq_gemm_noalloc", "cbq_set_wait_limit",
+           "cbq_gemm_gate_up", "cbq_gate_up_workspace_size",
            "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_launch_count",
            "cbq_status_str", "cbq_draft_length", "cbq_select_budget")
 
@@ -64,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.cbq_gemm_path.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp, sz, vp, i32]
         L.cbq_gemm_auto_path.argtypes = [i32, i32, i32, i32]
         L.cbq_set_wait_limit.argtypes = [ctypes.c_int64]
+        L.cbq_gemm_gate_up.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp, vp, sz, vp]
+        L.cbq_gate_up_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
         L.cbq_gemm_noalloc.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp]
         L.cbq_grouped_gemm.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, vp, i32, i32, i32,
                                        i32, vp, vp]
@@ -79,7 +82,7 @@ def lib() -> ctypes.CDLL:
         L.cbq_select_budget.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
         for name in ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_ws",
                      "cbq_gemm_workspace_size", "cbq_gemm_path", "cbq_gemm_auto_path", "cbq_gemm_noalloc",
-                     "cbq_set_wait_limit",
+                     "cbq_set_wait_limit", "cbq_gemm_gate_up", "cbq_gate_up_workspace_size",
                      "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_draft_length",
                      "cbq_select_budget"):
             getattr(L, name).restype = ctypes.c_int
@@ -236,6 +239,29 @@ def gemm(a: torch.Tensor, a_scale: torch.Tensor, w: PackedWeights,
     _check(lib().cbq_gemm_path(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(wt), M, w.N, w.K,
                                out.data_ptr(), ws_ptr, ws_bytes, _stream(st), path), "cbq_gemm")
     return out
+
+
+def gate_up(a: torch.Tensor, a_scale: torch.Tensor, w: PackedWeights, out: torch.Tensor | None = None,
+            out_scale: torch.Tensor | None = None, stream=None, workspace="auto"):
+    """cbq_gemm_gate_up: (h uint8 E4M3 [M, F], h_scale fp32 [M]) for the fused
+    gate-up weight w (2F rows in blocks of 64 gate then 64 up rows)."""
+    M, F = a.shape[0], w.N // 2
+    if out is None:
+        out = torch.empty((M, F), dtype=torch.uint8, device=a.device)
+    if out_scale is None:
+        out_scale = torch.empty(M, dtype=torch.float32, device=a.device)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    if isinstance(workspace, str):
+        b = ctypes.c_size_t()
+        _check(lib().cbq_gate_up_workspace_size(M, F, w.K, ctypes.byref(b)), "cbq_gate_up_workspace_size")
+        if b.value == 0:
+            raise CbqError(EINVAL, "cbq_gemm_gate_up: the stream-K kernel cannot take this shape")
+        workspace = workspace_for(a.device, st, b.value)
+    wt = w.struct()
+    _check(lib().cbq_gemm_gate_up(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(wt), M, F, w.K, out.data_ptr(),
+                                  out_scale.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(st)),
+           "cbq_gemm_gate_up")
+    return out, out_scale
 
 
 def gemm_noalloc(a: torch.Tensor, a_scale: torch.Tensor, w: PackedWeights,

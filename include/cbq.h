@@ -145,6 +145,35 @@ int cbq_gemm_ws(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
                 int32_t M, int32_t N, int32_t K, float *y, void *workspace,
                 size_t workspace_bytes, void *stream);
 
+/* Fused gate-up projection of a feed-forward layer, for the verify round
+ * ("Adaptive speculation": the drafted tokens run through the model's FFN):
+ * the packed weight has N = 2F rows in blocks of 64 features -- block b is
+ * rows [128 b, 128 b + 2 R) with R = min(64, F - 64 b): its R gate rows, then
+ * its R up rows -- so a 128-row tile pairs each gate row with its up row.
+ * With g, u the matmul outputs of a feature's gate and up rows (a_scale
+ * applied, fp32 accumulation), the call writes
+ *   h_scale[m] = max_f |SiLU(g[m,f]) * u[m,f]| / 448   (1 if that max is 0),
+ *   h[m][f]    = E4M3(SiLU(g) * u / h_scale[m])  (nearest, ties to even,
+ *                saturating at +-448; SiLU(x) = x / (1 + e^-x)),
+ * the activations and per-token scale the down projection takes.
+ *   a, a_scale, w  as for cbq_gemm (w: 2F rows); 1 <= M <= 64, F >= 1
+ *   h        DEVICE uint8 [M][F] out, E4M3
+ *   h_scale  DEVICE fp32 [M] out
+ *   workspace, workspace_bytes: as for cbq_gemm_ws, at least
+ *            cbq_gate_up_workspace_size bytes (it also holds h in fp32)
+ * Two launches on `stream` (the stream-K matmul with the SiLU-product
+ * epilogue, then the per-token quantisation), each a programmatic dependent
+ * of the kernel before it.
+ * Errors: CBQ_EINVAL (also when the stream-K kernel cannot take the shape:
+ * the size query then gives 0), CBQ_EDEVICE, CBQ_ECUDA. */
+int cbq_gemm_gate_up(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
+                     int32_t M, int32_t F, int32_t K, uint8_t *h, float *h_scale,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of the workspace cbq_gemm_gate_up needs (0 if it cannot take the
+ * shape).  Host only.  Errors: CBQ_EINVAL. */
+int cbq_gate_up_workspace_size(int32_t M, int32_t F, int32_t K, size_t *bytes);
+
 /* The kernel (CBQ_PATH_GEMV / _MMA / _STREAMK) that cbq_gemm_ws picks for an
  * M x N x K call with (with_workspace != 0) or without a workspace, chosen by
  * measured speed on GB300; CBQ_EINVAL for sizes cbq_gemm rejects.  (If the
