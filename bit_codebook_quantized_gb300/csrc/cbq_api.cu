@@ -305,7 +305,8 @@ int cbq_grouped_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weig
   }
   if (!a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(experts))
     return CBQ_EINVAL;
-  if (path == CBQ_PATH_AUTO) path = (M <= 4) ? CBQ_PATH_GEMV : CBQ_PATH_MMA;
+  const bool automatic = path == CBQ_PATH_AUTO;
+  if (automatic) path = (M <= 4) ? CBQ_PATH_GEMV : CBQ_PATH_MMA;
   if (path == CBQ_PATH_GEMV) {
     GemvParams p;
     std::memset(&p, 0, sizeof(p));
@@ -339,7 +340,26 @@ int cbq_grouped_gemm_path(const uint8_t* a, const float* a_scale, const cbq_weig
   p.wait_ns = wait_limit_ns();
   p.E = E;
   p.topk = topk;
-  return launch_umma(p, true, s);
+  const int r = launch_umma(p, true, s);
+  if (r != CBQ_EINVAL || !automatic) return r;
+  // every token's activations do not fit the tile kernel's shared memory
+  // (long K): the GEMV kernel's grouped variant takes any K
+  GemvParams g;
+  std::memset(&g, 0, sizeof(g));
+  g.codes = experts->codes;
+  g.a = a;
+  g.a_scale = a_scale;
+  g.scales = experts->scales;
+  g.codebooks = experts->codebooks;
+  g.y = y;
+  g.topk_idx = topk_idx;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.wait_ns = wait_limit_ns();
+  g.E = E;
+  g.topk = topk;
+  return launch_gemv(g, true, s);
 }
 
 int cbq_grouped_gemm(const uint8_t* a, const float* a_scale, const cbq_weight_t* experts,

@@ -49,6 +49,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <map>
 #include <mutex>
@@ -601,11 +602,21 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   }
 }
 
+// The kernel's attributes (largest dynamic shared memory, non-portable
+// cluster sizes), set once per device and template instance.
 template <int NTOK, bool GROUPED>
 cudaError_t configure(int smem, int cs) {
+  (void)smem;
+  (void)cs;
+  static std::atomic<int> done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
   auto kern = umma_kernel<NTOK, GROUPED>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess && cs > 1) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
   return e;
 }
 

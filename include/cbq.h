@@ -210,12 +210,16 @@ int cbq_gemm_noalloc(const uint8_t *a, const float *a_scale, const cbq_weight_t 
                      int32_t M, int32_t N, int32_t K, float *y, void *stream);
 
 /* Mixture-of-experts verify round ("Adaptive speculation / Expert sharing"):
- * the E experts' packed matrices are stacked (expert e: codes from byte
- * e*3KN/8, scales and codebooks from row e*N), topk_idx is DEVICE int32
+ * the E experts' packed matrices are stacked in ONE cbq_weight_t (expert e:
+ * codes from byte e*3KN/8, scales and codebooks from row e*N) rather than
+ * passed as an array of E separate matrices, so the one kernel launch finds
+ * every expert from a single set of base pointers; topk_idx is DEVICE int32
  * [M][topk] and
  *   y[t][j][:] = a_scale[t] * a[t] x W_{topk_idx[t][j]}^T   (fp32 [M][topk][N]),
  * with no gate weight and no combine.  Only experts that appear in topk_idx
- * are read from memory.  Picks the kernel by M as cbq_gemm does.  The routing is read on the device inside the one
+ * are read from memory.  Picks the kernel by M (GEMV up to 4 token rows, the
+ * tile kernel beyond, the GEMV kernel again where every token's activations
+ * do not fit the tile kernel's shared memory).  The routing is read on the device inside the one
  * kernel launch.  1 <= M <= 64, 1 <= topk <= 8, 1 <= E <= 4096, each row of
  * topk_idx must list distinct experts in [0, E); a violation seen on the
  * device is reported by cbq_device_status as CBQ_EROUTING.

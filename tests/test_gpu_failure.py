@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from bit_codebook_quantized_gb300 import ops
+from bit_codebook_quantized_gb300 import ops, synth
 from tests.gpu_util import Case, assert_close, ensure_built
 
 pytestmark = pytest.mark.gpu
@@ -36,6 +36,47 @@ def test_streamk_gives_up_then_the_next_call_is_exact(M, N, K):
     torch.cuda.synchronize()
     yref, b = c.oracle()
     assert_close(y2.cpu().numpy(), yref, b, "after a give-up")
+    assert ops.device_status() == ops.OK
+
+
+@pytest.mark.parametrize("path", [ops.PATH_GEMV, ops.PATH_MMA])
+def test_gemv_and_tile_kernel_give_up_then_the_next_call_is_exact(path):
+    c = Case(5, 3000, 2048, seed=95 + path)
+    a, s, w = c.device()
+    ops.set_wait_limit(2)
+    try:
+        ops.gemm(a, s, w, path=path)
+        torch.cuda.synchronize()
+    finally:
+        ops.set_wait_limit(0)
+    assert ops.device_status() == ops.ETIMEOUT
+    y = ops.gemm(a, s, w, path=path)
+    torch.cuda.synchronize()
+    yref, b = c.oracle()
+    assert_close(y.cpu().numpy(), yref, b, f"path {path} after a give-up")
+    assert ops.device_status() == ops.OK
+
+
+def test_grouped_gives_up_then_the_next_call_is_exact():
+    E, N, K, M = 12, 200, 512, 16
+    pw = synth.gen_weights(E * N, K, 41)
+    a = synth.gen_activations(M, K, 42)
+    s = synth.gen_a_scale(M, 43, "uniform")
+    idx = synth.gen_moe_routing(M, E, 6, 4, 44)
+    w = ops.PackedWeights.from_host(pw.codes, pw.scales, pw.codebooks, N, K)
+    da, ds, di = torch.from_numpy(a).cuda(), torch.from_numpy(s).cuda(), torch.from_numpy(idx).cuda()
+    ops.set_wait_limit(2)
+    try:
+        ops.grouped_gemm(da, ds, w, E, di, path=ops.PATH_MMA)
+        torch.cuda.synchronize()
+    finally:
+        ops.set_wait_limit(0)
+    assert ops.device_status() == ops.ETIMEOUT
+    y = ops.grouped_gemm(da, ds, w, E, di, path=ops.PATH_MMA)
+    torch.cuda.synchronize()
+    import oracle
+    yref, b, _ = oracle.grouped_gemm(a, s, pw.codes, pw.scales, pw.codebooks, E, idx, M, N, K)
+    assert_close(y.cpu().numpy(), yref, b, "grouped after a give-up")
     assert ops.device_status() == ops.OK
 
 
