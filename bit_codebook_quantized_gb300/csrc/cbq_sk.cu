@@ -80,7 +80,7 @@ constexpr int kStageBytes = kUnitsPerStage * kUnitBytes;   // 24 KB
 constexpr int kMaxStages = 8;
 constexpr int kGroups = 4;                            // decoder group g <-> stage position g
 static_assert(kGroups == kUnitsPerStage, "one unit per group per stage");
-constexpr int kASlots = 2 * kGroups;                  // group g owns A slots g and g + 4
+constexpr int kASlots = kGroups;                      // one A slot per group
 constexpr int kProdWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kDecWarp0 = 4;                          // warps 4..19
@@ -88,21 +88,29 @@ constexpr int kEpiWarp0 = 20;                         // warps 20..23
 constexpr int kNumWarps = 24;
 constexpr int kThreads = kNumWarps * 32;
 constexpr int kTmemCols = 512;
-constexpr int kSfbCol = 128;                          // 8 columns of B scale factors (2^0)
-constexpr int kSfaCol = 136;                          // + 4 * A slot (4-column aligned)
-constexpr int kACol = 256;                            // + 32 * A slot
+constexpr int kACol = 256;                            // + 32 * group
+constexpr int kSfaCol = 384;                          // + 4 * group (4-column aligned)
+constexpr int kSfbCol = 400;                          // 8 columns of B scale factors (2^0)
 constexpr int kMaxSmem = 232448;
 constexpr int kMinSmem = 120 * 1024;                  // one CTA per SM: it owns all of TMEM
-constexpr int kNumBars = 2 * kMaxStages + 2 * kASlots + 2 + 2 + 2;
+// barriers: code stages full/empty, per group A full/empty, per (group,
+// buffer) accumulator full/empty, per group MMA drain, B full
+constexpr int kNumBars = 2 * kMaxStages + 2 * kGroups + 2 * kGroups * 2 + kGroups + 1;
 constexpr int kXchgStride = 17;                       // floats per exchanged row (conflict-free)
 constexpr int kXchgBytes = (64 * kXchgStride * 4 + 127) / 128 * 128;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
 constexpr long long kDrainLimitNs = 10000000000LL;    // copies and MMAs always finish; 10 s is a backstop
 
+// Tensor-memory columns: accumulator (group g, buffer b) at
+// (g * kAccBufs + b) * kStride (two buffers per group up to 32 token columns,
+// one at 64), A slot of group g at kACol + 32 g, its scale factors at
+// kSfaCol + 4 g, B scale factors (2^0) at kSfbCol.
 template <int NTOK>
 struct AccCols {
-  static constexpr int kStride = NTOK < 32 ? 32 : NTOK;   // accumulator b at column b * kStride
-  static_assert(2 * kStride <= kSfbCol, "accumulators overlap the scale-factor columns");
+  static constexpr int kStride = NTOK < 32 ? 32 : NTOK;
+  static constexpr int kBufs = NTOK <= 32 ? 2 : 1;
+  static_assert(kGroups * kBufs * kStride <= kACol, "accumulators overlap the A slots");
+  static __device__ __forceinline__ uint32_t col(int g, int b) { return (g * kBufs + b) * kStride; }
 };
 
 __device__ __forceinline__ void raise(unsigned bits) { atomicOr(&g_status_sk, bits); }
@@ -180,13 +188,13 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xchg) + (GATE_UP ? kXchgBytes : 0));
   uint64_t* full = bars;
   uint64_t* empty = full + kMaxStages;
-  uint64_t* a_full = empty + kMaxStages;
-  uint64_t* a_empty = a_full + kASlots;
-  uint64_t* acc_full = a_empty + kASlots;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* b_full = acc_empty + 2;
-  uint64_t* drain = b_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* a_full = empty + kMaxStages;               // [group]
+  uint64_t* a_empty = a_full + kGroups;                // [group]
+  uint64_t* acc_full = a_empty + kGroups;              // [group][2]
+  uint64_t* acc_empty = acc_full + 2 * kGroups;        // [group][2]
+  uint64_t* drain = acc_empty + 2 * kGroups;           // [group]
+  uint64_t* b_full = drain + kGroups;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
   const long long wait_ns = p.wait_ns;
@@ -209,16 +217,16 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 4 * kGroups);              // every decoder warp of a full stage, once
     }
-    for (int i = 0; i < kASlots; ++i) {
-      mbar_init(&a_full[i], 4);                       // the group's four quadrant warps
-      mbar_init(&a_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+    for (int g = 0; g < kGroups; ++g) {
+      mbar_init(&a_full[g], 4);                       // the group's four quadrant warps
+      mbar_init(&a_empty[g], 1);                      // the group's MMAs read the slot
+      mbar_init(&acc_full[2 * g], 1);
+      mbar_init(&acc_full[2 * g + 1], 1);
+      mbar_init(&acc_empty[2 * g], 4);                // the four epilogue warps
+      mbar_init(&acc_empty[2 * g + 1], 4);
+      mbar_init(&drain[g], 1);
     }
     mbar_init(b_full, 1);
-    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -274,15 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     tbase = *tmem_slot;
 
     if (warp == kMmaWarp) {
-      // --------------------------------------------------------- MMA issuer --
-      named_bar_sync(3, 160);                          // B scale factors are in TMEM
-      tc_fence_after();
+      // ------------------------------------------------- resident activations --
       if (lane == 0 && n_units > 0) {
-        // Resident activations (written by an earlier kernel, so after the
-        // grid dependency): k-tile c of this CTA's share lands in slot
-        // (c - c_first) mod KT as NTOK rows of 128 bytes in the 128-byte
-        // swizzled K-major layout (one TMA box); token rows >= M are outside
-        // the tensor and arrive as zeros.
+        // Written by an earlier kernel, so after the grid dependency: k-tile
+        // c of this CTA's share lands in slot (c - c_first) mod KT as NTOK
+        // rows of 128 bytes in the 128-byte swizzled K-major layout (one TMA
+        // box); token rows >= M are outside the tensor and arrive as zeros.
         grid_dependency_wait();
         const int nb = min(KT, n_units);
         mbar_arrive_expect_tx(b_full, static_cast<uint32_t>(nb * NTOK * 128));
@@ -291,55 +296,36 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           if (c >= KT) c -= KT;
           tma_load_2d(b_s + sl * NTOK * 128, &p.a_map, b_full, c * 128, 0);
         }
-        // Descriptors advance by adding offsets in their 16-byte address
-        // units: B slot bsl at bsl * NTOK * 128 bytes, its MMA j at 32 j.
-        const uint64_t bd0 = umma_desc_kmajor_sw128(smem_u32(b_s));
-        const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
-        const uint32_t a_col = tbase + kACol, sfa_col = tbase + kSfaCol, sfb_col = tbase + kSfbCol;
-        wait_bounded(b_full, 0, abort_flag, wait_ns);
-        tc_fence_after();
-        int seg = 0, c = c_first, bsl = 0;
-        for (int i = 0; i < n_units; ++i) {
-          const bool seg_first = (i == 0) || (c == 0);
-          const int abuf = seg & 1;
-          if (seg_first) {
-            wait_bounded(&acc_empty[abuf], ((seg >> 1) & 1u) ^ 1u, abort_flag, wait_ns);
-            tc_fence_after();
-          }
-          // unit i: group i % 4, the group's use i / 4 -> A slot and phase
-          const uint32_t use = static_cast<uint32_t>(i) >> 2;
-          const uint32_t as = static_cast<uint32_t>(i & 3) + 4u * (use & 1u);
-          wait_bounded(&a_full[as], (use >> 1) & 1u, abort_flag, wait_ns);
-          tc_fence_after();
-          const uint64_t bdu = bd0 + static_cast<uint64_t>(bsl * NTOK * 8);
-          const uint32_t d_col = tbase + abuf * AC::kStride;
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            umma_mxf8_ts(d_col, a_col + as * 32 + j * 8, bdu + static_cast<uint64_t>(2 * j),
-                         idesc | (uint32_t(j) << 29), sfa_col + as * 4, sfb_col, (seg_first && j == 0) ? 0u : 1u);
-          umma_commit(&a_empty[as]);
-          if (c == KT - 1 || i == n_units - 1) {
-            umma_commit(&acc_full[abuf]);
-            ++seg;
-          }
-          c = (c + 1 == KT) ? 0 : c + 1;
-          bsl = (bsl + 1 == KT) ? 0 : bsl + 1;        // (c - c_first) mod KT
-        }
-        // all tensor-core work and the activation loads are done before TMEM
-        // is freed and the CTA ends
-        umma_commit(drain);
-        wait_drain(drain, 0);
-        wait_drain(b_full, 0);
+        wait_drain(b_full, 0);                         // landed before the CTA can end
       }
       __syncwarp();
     } else if (warp >= kDecWarp0 && warp < kEpiWarp0) {
       // ------------------------------------------------------------ decoders --
+      // Group g = (warp - 4) / 4 decodes units g, g + 4, ...; its warp on
+      // sub-partition g (quadrant q == g) also issues the group's MMAs, into
+      // the group's own accumulators, so no single thread issues for all.
       const int g = (warp - kDecWarp0) >> 2, q = warp & 3;
+      const bool issuer = q == g;
       const int r = 32 * q + lane;                      // row inside the tile == TMEM lane
       const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
       const uint32_t codes_base = smem_u32(codes_s);
-      const uint32_t a_lane = tbase + lane_addr + kACol, sf_lane = tbase + lane_addr + kSfaCol + q;
+      const uint32_t a_lane = tbase + lane_addr + kACol + 32 * g;
+      const uint32_t sf_lane = tbase + lane_addr + kSfaCol + 4 * g + q;
       const int gk = p.K / 32;
+      // issuer state: B descriptor, instruction descriptor, the tile of the
+      // group's current segment and the uses of each accumulator buffer
+      const uint64_t bd0 = umma_desc_kmajor_sw128(smem_u32(b_s));
+      const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
+      const uint32_t a_col = tbase + kACol + 32 * g, sfa_col = tbase + kSfaCol + 4 * g,
+                     sfb_col = tbase + kSfbCol;
+      int cur_t = -1;
+      uint32_t buf_par = 0;                             // bit b: parity of the uses of buffer b
+      named_bar_sync(3, 32 * 4 + 32 * 4 * kGroups);     // the epilogue stored the B scale factors
+      tc_fence_after();
+      if (issuer && g < n_units) {
+        wait_bounded(b_full, 0, abort_flag, wait_ns);  // resident activations landed
+        tc_fence_after();
+      }
       // scale word and codebook of row r for the unit at (t, c)
       auto load_sc = [&](int t, int c, bool valid, uint32_t& sw, uint2& cb) {
         sw = 0x7F7F7F7Fu;
@@ -384,17 +370,44 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
         decode_group(c1.z, c1.w, c2v.x, cb.x, cb.y, v + 16);
         decode_group(c2v.y, c2v.z, c2v.w, cb.x, cb.y, v + 24);
-        const uint32_t as = static_cast<uint32_t>(g) + 4u * (use & 1u);
-        wait_bounded(&a_empty[as], ((use >> 1) & 1u) ^ 1u, abort_flag, wait_ns);
+        // the group's A slot: its previous unit's MMAs have read it
+        wait_bounded(&a_empty[g], (use & 1u) ^ 1u, abort_flag, wait_ns);
         tc_fence_after();
-        tmem_st_x32(a_lane + as * 32, v);
+        tmem_st_x32(a_lane, v);
         // A scale of row m is read from TMEM lane m, column (base + m / 32),
         // byte = the MMA's a_sf_id: quadrant q writes column base + q
-        tmem_st_x1(sf_lane + as * 4, sw);
+        tmem_st_x1(sf_lane, sw);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[as]);
+        if (lane == 0) mbar_arrive(&a_full[g]);
+        if (issuer) {
+          if (lane == 0) {
+            wait_bounded(&a_full[g], use & 1u, abort_flag, wait_ns);   // all four quadrants stored
+            tc_fence_after();
+            const bool seg_first = t != cur_t;            // the group's first unit of this tile
+            const int b = AC::kBufs == 2 ? ((t - t_first) & 1) : 0;
+            if (seg_first) {
+              cur_t = t;
+              wait_bounded(&acc_empty[2 * g + b], ((buf_par >> b) & 1u) ^ 1u, abort_flag, wait_ns);
+              tc_fence_after();
+            }
+            int bsl = c - c_first;                        // B slot: (c - c_first) mod KT
+            if (bsl < 0) bsl += KT;
+            const uint64_t bdu = bd0 + static_cast<uint64_t>(bsl * NTOK * 8);
+            const uint32_t d_col = tbase + AC::col(g, b);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              umma_mxf8_ts(d_col, a_col + j * 8, bdu + static_cast<uint64_t>(2 * j), idesc | (uint32_t(j) << 29),
+                           sfa_col, sfb_col, (seg_first && j == 0) ? 0u : 1u);
+            umma_commit(&a_empty[g]);
+            if (t2 != t || i + kGroups >= n_units) {      // the group's last unit of this tile
+              umma_commit(&acc_full[2 * g + b]);
+              buf_par ^= 1u << b;
+            }
+          }
+          __syncwarp();
+        }
         t = t2;
         c = c2;
         sw = sw2;
@@ -404,6 +417,14 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           slot = 0;
           ph ^= 1u;
         }
+      }
+      if (issuer) {
+        // all of the group's tensor-core work is done before TMEM is freed
+        if (lane == 0) {
+          umma_commit(&drain[g]);
+          wait_drain(&drain[g], 0);
+        }
+        __syncwarp();
       }
     } else if (warp >= kEpiWarp0) {
       // ------------------------------------------------------------ epilogue --
@@ -436,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
             for (int k = 0; k < 16; ++k) {
               float hv = 0.f;
               if (r < half && c0 + k < p.M) {
-                const float g = v[k] * __ldg(p.a_scale + c0 + k);
-                hv = g / (1.f + expf(-g)) * xchg[r * kXchgStride + k];
+                const float gv = v[k] * __ldg(p.a_scale + c0 + k);
+                hv = gv / (1.f + expf(-gv)) * xchg[r * kXchgStride + k];
                 p.h[static_cast<size_t>(c0 + k) * p.F + f] = hv;
               }
               float mx = fabsf(hv);
@@ -454,25 +475,47 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         tmem_st_x4(tbase + lane_addr + kSfbCol + cc, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       tmem_st_wait();
       tc_fence_before();
-      named_bar_sync(3, 160);
+      named_bar_sync(3, 32 * 4 + 32 * 4 * kGroups);     // B scale factors are in TMEM (with the decoders)
       grid_dependency_wait();                           // y and the workspace may still be in use
-      int seg = 0, t = t_first, c = c_first, seg_c = c_first;   // seg_c: k-tile the segment starts at
+      uint32_t acc_par = 0;                             // bit 2 g + b: parity of (group, buffer) uses
+      int t = t_first, c = c_first, s0 = 0;             // s0: first unit of the segment
       for (int i = 0; i < n_units; ++i, geo.advance(t, c, 1)) {
         if (c != KT - 1 && i != n_units - 1) continue;
+        const int seg_c = (s0 == 0) ? c_first : 0;
         const bool complete = seg_c == 0 && c == KT - 1;
-        const int abuf = seg & 1;
-        const uint32_t acc_addr = tbase + lane_addr + abuf * AC::kStride;
-        wait_bounded(&acc_full[abuf], (seg >> 1) & 1u, abort_flag, wait_ns);
+        const int span = i - s0;                          // units in the segment - 1
+        const int b = AC::kBufs == 2 ? ((t - t_first) & 1) : 0;
+        // groups with a unit in [s0, i]: all of them if the segment has 4 or more
+        uint32_t part = 0;
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g)
+          if (span >= kGroups - 1 || ((g - s0) & (kGroups - 1)) <= span) part |= 1u << g;
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g)
+          if (part & (1u << g)) {
+            wait_bounded(&acc_full[2 * g + b], (acc_par >> (2 * g + b)) & 1u, abort_flag, wait_ns);
+            acc_par ^= 1u << (2 * g + b);
+          }
         tc_fence_after();
+        // the segment's accumulator, chunk c0: sum of the groups' parts in group order
+        auto load_acc = [&](int c0, float (&v)[16]) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) v[k] = 0.f;
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g)
+            if (part & (1u << g)) {
+              uint32_t tv[16];
+              tmem_ld_x16(tbase + lane_addr + AC::col(g, b) + c0, tv);
+              tmem_ld_wait();
+#pragma unroll
+              for (int k = 0; k < 16; ++k) v[k] += __uint_as_float(tv[k]);
+            }
+        };
         if (complete) {
 #pragma unroll 1
           for (int c0 = 0; c0 < NTOK; c0 += 16) {
-            uint32_t tv[16];
-            tmem_ld_x16(acc_addr + c0, tv);
-            tmem_ld_wait();
             float v[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(tv[k]);
+            load_acc(c0, v);
             emit(t, c0, v);
           }
         } else {
@@ -486,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           const long long b_first = geo.owner(tu);
           const int nparts = static_cast<int>(geo.owner(tu + KT - 1) - b_first + 1);
           const int pme = static_cast<int>(blockIdx.x - b_first);
+          const bool seg_is_first = s0 == 0;
           bool own_published = false, last = false;
           if (i == n_units - 1) {                         // this CTA's last segment
             if (leader) *last_flag = ld_acquire_gpu(p.counters + t) == static_cast<unsigned>(nparts - 1);
@@ -494,17 +538,15 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
             named_bar_sync(2, 128);
           }
           if (!last) {
-            float* part = p.partial + (static_cast<size_t>(2 * blockIdx.x + (seg > 0 ? 1 : 0)) * kRows + r) * NTOK;
+            float* part_dst =
+                p.partial + (static_cast<size_t>(2 * blockIdx.x + (seg_is_first ? 0 : 1)) * kRows + r) * NTOK;
 #pragma unroll 1
             for (int c0 = 0; c0 < NTOK; c0 += 16) {
-              uint32_t tv[16];
-              tmem_ld_x16(acc_addr + c0, tv);
-              tmem_ld_wait();
-              float4* dst = reinterpret_cast<float4*>(part + c0);
+              float v[16];
+              load_acc(c0, v);
+              float4* dst = reinterpret_cast<float4*>(part_dst + c0);
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                dst[k] = make_float4(__uint_as_float(tv[4 * k]), __uint_as_float(tv[4 * k + 1]),
-                                     __uint_as_float(tv[4 * k + 2]), __uint_as_float(tv[4 * k + 3]));
+              for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
             }
             own_published = true;
             __threadfence();
@@ -517,11 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
             __threadfence();
 #pragma unroll 1
             for (int c0 = 0; c0 < NTOK; c0 += 16) {
-              uint32_t tv[16];
-              if (!own_published) {
-                tmem_ld_x16(acc_addr + c0, tv);
-                tmem_ld_wait();
-              }
+              float mine[16];
+              if (!own_published) load_acc(c0, mine);
               float acc[16];
 #pragma unroll
               for (int k = 0; k < 16; ++k) acc[k] = 0.f;
@@ -529,13 +568,13 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
               for (int pi = 0; pi < nparts; ++pi) {
                 if (pi == pme && !own_published) {
 #pragma unroll
-                  for (int k = 0; k < 16; ++k) acc[k] += __uint_as_float(tv[k]);
+                  for (int k = 0; k < 16; ++k) acc[k] += mine[k];
                   continue;
                 }
                 // part 0's CTA reaches this tile as its last segment if its
                 // share started in an earlier tile; every later part as its first
-                const long long b = b_first + pi;
-                const int pslot = 2 * static_cast<int>(b) + ((pi == 0 && geo.first_unit(b) < tu) ? 1 : 0);
+                const long long bb = b_first + pi;
+                const int pslot = 2 * static_cast<int>(bb) + ((pi == 0 && geo.first_unit(bb) < tu) ? 1 : 0);
                 const float4* src =
                     reinterpret_cast<const float4*>(p.partial + (static_cast<size_t>(pslot) * kRows + r) * NTOK + c0);
 #pragma unroll
@@ -555,15 +594,17 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[abuf]);
-        seg_c = c + 1 == KT ? 0 : c + 1;
-        ++seg;
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g)
+          if ((part & (1u << g)) && lane == 0) mbar_arrive(&acc_empty[2 * g + b]);
+        s0 = i + 1;
       }
     }
   }
 
-  // ---- teardown: the MMA thread saw all its tensor-core work complete, the
-  // producer saw its last copies land, decoders waited for their TMEM stores.
+  // ---- teardown: each group's issuer saw its tensor-core work complete, the
+  // producer saw its copies land, the B loads landed, decoders waited for
+  // their TMEM stores and the epilogue for its TMEM loads.
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
