@@ -67,10 +67,12 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
                                              long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = global_ns();
-  // suspend at most 20 us per poll, and never longer than the limit itself
-  const uint32_t hint = limit_ns < 20000 ? static_cast<uint32_t>(limit_ns > 0 ? limit_ns : 1) : 20000u;
+  // suspended polls (20 us hint) for the normal limit; under a limit below
+  // that, plain polls, so that a wait not already satisfied does give up
+  // (a suspended poll may sleep until the phase completes)
+  const bool poll = limit_ns < 20000;
   for (;;) {
-    if (mbar_try_wait_suspend(bar, parity, hint)) return true;
+    if (poll ? mbar_try_wait(bar, parity) : mbar_try_wait_suspend(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
     if (global_ns() - t0 > limit_ns) {
       *abort_flag = 1;
