@@ -65,14 +65,14 @@ __device__ __forceinline__ void raise(unsigned bits) { atomicOr(&g_status_gemv, 
 // `limit_ns`, raising the flag and the library's timeout status.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                              long long limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = global_ns();
   // suspended polls (20 us hint) for the normal limit; under a limit below
-  // that, plain polls, so that a wait not already satisfied does give up
-  // (a suspended poll may sleep until the phase completes)
+  // that, non-blocking tests, so that a wait not already satisfied does give
+  // up (try_wait may block until the phase completes)
   const bool poll = limit_ns < 20000;
   for (;;) {
-    if (poll ? mbar_try_wait(bar, parity) : mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait_suspend(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
     if (global_ns() - t0 > limit_ns) {
       *abort_flag = 1;

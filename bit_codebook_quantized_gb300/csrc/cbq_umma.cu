@@ -95,14 +95,15 @@ __device__ __forceinline__ void raise(unsigned bits) { atomicOr(&g_status_umma, 
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                              long long limit_ns) {
-  if (CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  if (CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
   const long long t0 = global_ns();
   // suspended polls (20 us hint) for the normal limit; under a limit below
-  // that, plain polls, so that a wait not already satisfied does give up
-  // (a suspended poll may sleep until the phase completes)
+  // that, non-blocking tests (cluster-scope waits: plain polls), so that a
+  // wait not already satisfied does give up (try_wait may block until the
+  // phase completes)
   const bool poll = limit_ns < 20000;
   for (;;) {
-    const bool done = poll ? (CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
+    const bool done = poll ? (CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_test_wait(bar, parity))
                            : (CLUSTER ? mbar_try_wait_cluster_suspend(bar, parity, 20000u)
                                       : mbar_try_wait_suspend(bar, parity, 20000u));
     if (done) return true;
