@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       named_bar_sync(3, 32 * 4 + 32 * 4 * kGroups);     // the epilogue stored the B scale factors
       tc_fence_after();
       if (issuer && g < n_units) {
-        wait_bounded(b_full, 0, abort_flag, wait_ns);  // resident activations landed
+        wait_bounded(b_full, 0, abort_flag, wait_ns);  // resident activations landed (whole warp)
         tc_fence_after();
       }
       // scale word and codebook of row r for the unit at (t, c)
@@ -340,20 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           cb = __ldg(reinterpret_cast<const uint2*>(p.codebooks + static_cast<size_t>(n) * 8));
         }
       };
-      int t = t_first, c = c_first;
-      geo.advance(t, c, g);                             // unit g: this group's first
       int slot = 0;                                     // stage j = (i - g) / 4
       uint32_t ph = 0, use = 0;
-      uint32_t sw;
-      uint2 cb;
-      load_sc(t, c, g < n_units, sw, cb);
-      for (int i = g; i < n_units; i += kGroups) {
-        // next unit of the group: its scale word and codebook in flight now
-        int t2 = t, c2 = c;
-        geo.advance(t2, c2, kGroups);
-        uint32_t sw2;
-        uint2 cb2;
-        load_sc(t2, c2, i + kGroups < n_units, sw2, cb2);
+      // One unit of the group: (t, c) its position, (sw, cb) its row's scale
+      // word and codebook, (t2) the tile of the group's next unit.
+      auto process = [&](int i, int t, int c, int t2, uint32_t sw, uint2 cb) {
         wait_bounded(&full[slot], ph, abort_flag, wait_ns);
         uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, c2v = c0;
         const int rows_t = geo.rows(t);
@@ -386,41 +377,59 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[g]);
         if (issuer) {
-          if (lane == 0) {
-            wait_bounded(&a_full[g], use & 1u, abort_flag, wait_ns);   // all four quadrants stored
+          // the whole warp follows (descriptors stay warp-uniform); lane 0
+          // issues, always the same thread, so its commits (the drain below
+          // included) track every MMA of the group
+          wait_bounded(&a_full[g], use & 1u, abort_flag, wait_ns);   // all four quadrants stored
+          tc_fence_after();
+          const bool seg_first = t != cur_t;              // the group's first unit of this tile
+          const int b = AC::kBufs == 2 ? ((t - t_first) & 1) : 0;
+          if (seg_first) {
+            cur_t = t;
+            wait_bounded(&acc_empty[2 * g + b], ((buf_par >> b) & 1u) ^ 1u, abort_flag, wait_ns);
             tc_fence_after();
-            const bool seg_first = t != cur_t;            // the group's first unit of this tile
-            const int b = AC::kBufs == 2 ? ((t - t_first) & 1) : 0;
-            if (seg_first) {
-              cur_t = t;
-              wait_bounded(&acc_empty[2 * g + b], ((buf_par >> b) & 1u) ^ 1u, abort_flag, wait_ns);
-              tc_fence_after();
-            }
-            int bsl = c - c_first;                        // B slot: (c - c_first) mod KT
-            if (bsl < 0) bsl += KT;
-            const uint64_t bdu = bd0 + static_cast<uint64_t>(bsl * NTOK * 8);
-            const uint32_t d_col = tbase + AC::col(g, b);
+          }
+          int bsl = c - c_first;                          // B slot: (c - c_first) mod KT
+          if (bsl < 0) bsl += KT;
+          const uint64_t bdu = bd0 + static_cast<uint64_t>(bsl * NTOK * 8);
+          const uint32_t d_col = tbase + AC::col(g, b);
+          const bool seg_last = t2 != t || i + kGroups >= n_units;   // the group's last unit of this tile
+          if (lane == 0) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               umma_mxf8_ts(d_col, a_col + j * 8, bdu + static_cast<uint64_t>(2 * j), idesc | (uint32_t(j) << 29),
                            sfa_col, sfb_col, (seg_first && j == 0) ? 0u : 1u);
             umma_commit(&a_empty[g]);
-            if (t2 != t || i + kGroups >= n_units) {      // the group's last unit of this tile
-              umma_commit(&acc_full[2 * g + b]);
-              buf_par ^= 1u << b;
-            }
+            if (seg_last) umma_commit(&acc_full[2 * g + b]);
           }
+          if (seg_last) buf_par ^= 1u << b;
           __syncwarp();
         }
-        t = t2;
-        c = c2;
-        sw = sw2;
-        cb = cb2;
         ++use;
         if (++slot == NS) {
           slot = 0;
           ph ^= 1u;
         }
+      };
+      // Two register sets for the scale word and codebook, so the loads for
+      // the group's next unit are in flight during the current one (the loop
+      // is unrolled by two: no register copy waits for a load).
+      int ta = t_first, ca = c_first;                   // unit i (set A)
+      geo.advance(ta, ca, g);
+      uint32_t swA, swB;
+      uint2 cbA, cbB;
+      load_sc(ta, ca, g < n_units, swA, cbA);
+      for (int i = g; i < n_units; i += 2 * kGroups) {
+        int tb = ta, cbb = ca;                          // unit i + 4 (set B)
+        geo.advance(tb, cbb, kGroups);
+        load_sc(tb, cbb, i + kGroups < n_units, swB, cbB);
+        process(i, ta, ca, tb, swA, cbA);
+        if (i + kGroups >= n_units) break;
+        ta = tb;                                        // unit i + 8 (set A)
+        ca = cbb;
+        geo.advance(ta, ca, kGroups);
+        load_sc(ta, ca, i + 2 * kGroups < n_units, swA, cbA);
+        process(i + kGroups, tb, cbb, ta, swB, cbB);
       }
       if (issuer) {
         // all of the group's tensor-core work is done before TMEM is freed
