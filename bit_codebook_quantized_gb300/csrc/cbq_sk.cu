@@ -80,7 +80,7 @@ constexpr int kStageBytes = kUnitsPerStage * kUnitBytes;   // 24 KB
 constexpr int kMaxStages = 8;
 constexpr int kGroups = 4;                            // decoder group g <-> stage position g
 static_assert(kGroups == kUnitsPerStage, "one unit per group per stage");
-constexpr int kASlots = kGroups;                      // one A slot per group
+constexpr int kASlots = 2 * kGroups;                  // at most two A slots per group
 constexpr int kProdWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kDecWarp0 = 4;                          // warps 4..19
@@ -93,24 +93,32 @@ constexpr int kSfaCol = 384;                          // + 4 * group (4-column a
 constexpr int kSfbCol = 400;                          // 8 columns of B scale factors (2^0)
 constexpr int kMaxSmem = 232448;
 constexpr int kMinSmem = 120 * 1024;                  // one CTA per SM: it owns all of TMEM
-// barriers: code stages full/empty, per group A full/empty, per (group,
+// barriers: code stages full/empty, per A slot full/empty, per (group,
 // buffer) accumulator full/empty, per group MMA drain, B full
-constexpr int kNumBars = 2 * kMaxStages + 2 * kGroups + 2 * kGroups * 2 + kGroups + 1;
+constexpr int kNumBars = 2 * kMaxStages + 2 * kASlots + 2 * kGroups * 2 + kGroups + 1;
 constexpr int kXchgStride = 17;                       // floats per exchanged row (conflict-free)
 constexpr int kXchgBytes = (64 * kXchgStride * 4 + 127) / 128 * 128;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
 constexpr long long kDrainLimitNs = 10000000000LL;    // copies and MMAs always finish; 10 s is a backstop
 
-// Tensor-memory columns: accumulator (group g, buffer b) at
-// (g * kAccBufs + b) * kStride (two buffers per group up to 32 token columns,
-// one at 64), A slot of group g at kACol + 32 g, its scale factors at
-// kSfaCol + 4 g, B scale factors (2^0) at kSfbCol.
+// Tensor-memory columns.  Accumulator (group g, buffer b) at
+// (g * kBufs + b) * kStride: two buffers per group up to 32 token columns,
+// one at 64.  A slots of 32 columns from kACol.  With 16 token columns an
+// accumulator region of 32 columns holds 16 unused ones: the scale factors
+// live there (A slot s's at 32 s + 16, B's at 20) and every group gets two A
+// slots (s = g and g + 4, alternately), so it stores its next unit while the
+// tensor core still reads the last; otherwise one A slot per group and the
+// scale factors after the A slots.
 template <int NTOK>
-struct AccCols {
+struct TmemMap {
   static constexpr int kStride = NTOK < 32 ? 32 : NTOK;
   static constexpr int kBufs = NTOK <= 32 ? 2 : 1;
+  static constexpr int kSlots = NTOK == 16 ? 2 : 1;      // A slots per group
   static_assert(kGroups * kBufs * kStride <= kACol, "accumulators overlap the A slots");
-  static __device__ __forceinline__ uint32_t col(int g, int b) { return (g * kBufs + b) * kStride; }
+  static __device__ __forceinline__ uint32_t acc(int g, int b) { return (g * kBufs + b) * kStride; }
+  static __device__ __forceinline__ uint32_t a(int s) { return kACol + 32 * s; }
+  static __device__ __forceinline__ uint32_t sfa(int s) { return kSlots == 2 ? 32 * s + 16 : kSfaCol + 4 * s; }
+  static constexpr int kSfb = kSlots == 2 ? 20 : kSfbCol;
 };
 
 __device__ __forceinline__ void raise(unsigned bits) { atomicOr(&g_status_sk, bits); }
@@ -183,7 +191,7 @@ struct Geo {
 
 template <int NTOK, bool GATE_UP>
 __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__ SkParams p) {
-  using AC = AccCols<NTOK>;
+  using TM = TmemMap<NTOK>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int NS = p.stages;
   uint8_t* codes_s = smem;
@@ -192,9 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xchg) + (GATE_UP ? kXchgBytes : 0));
   uint64_t* full = bars;
   uint64_t* empty = full + kMaxStages;
-  uint64_t* a_full = empty + kMaxStages;               // [group]
-  uint64_t* a_empty = a_full + kGroups;                // [group]
-  uint64_t* acc_full = a_empty + kGroups;              // [group][2]
+  uint64_t* a_full = empty + kMaxStages;               // [A slot]
+  uint64_t* a_empty = a_full + kASlots;                // [A slot]
+  uint64_t* acc_full = a_empty + kASlots;              // [group][2]
   uint64_t* acc_empty = acc_full + 2 * kGroups;        // [group][2]
   uint64_t* drain = acc_empty + 2 * kGroups;           // [group]
   uint64_t* b_full = drain + kGroups;
@@ -221,9 +229,11 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 4 * kGroups);              // every decoder warp of a full stage, once
     }
+    for (int s = 0; s < kASlots; ++s) {
+      mbar_init(&a_full[s], 4);                       // the group's four quadrant warps
+      mbar_init(&a_empty[s], 1);                      // the group's MMAs read the slot
+    }
     for (int g = 0; g < kGroups; ++g) {
-      mbar_init(&a_full[g], 4);                       // the group's four quadrant warps
-      mbar_init(&a_empty[g], 1);                      // the group's MMAs read the slot
       mbar_init(&acc_full[2 * g], 1);
       mbar_init(&acc_full[2 * g + 1], 1);
       mbar_init(&acc_empty[2 * g], 4);                // the four epilogue warps
@@ -313,15 +323,13 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       const int r = 32 * q + lane;                      // row inside the tile == TMEM lane
       const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
       const uint32_t codes_base = smem_u32(codes_s);
-      const uint32_t a_lane = tbase + lane_addr + kACol + 32 * g;
-      const uint32_t sf_lane = tbase + lane_addr + kSfaCol + 4 * g + q;
+      const uint32_t lane_base = tbase + lane_addr;
       const int gk = p.K / 32;
       // issuer state: B descriptor, instruction descriptor, the tile of the
       // group's current segment and the uses of each accumulator buffer
       const uint64_t bd0 = umma_desc_kmajor_sw128(smem_u32(b_s));
       const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
-      const uint32_t a_col = tbase + kACol + 32 * g, sfa_col = tbase + kSfaCol + 4 * g,
-                     sfb_col = tbase + kSfbCol;
+      const uint32_t sfb_col = tbase + TM::kSfb;
       int cur_t = -1;
       uint32_t buf_par = 0;                             // bit b: parity of the uses of buffer b
       named_bar_sync(3, 32 * 4 + 32 * 4 * kGroups);     // the epilogue stored the B scale factors
@@ -365,25 +373,28 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
         decode_group(c1.z, c1.w, c2v.x, cb.x, cb.y, v + 16);
         decode_group(c2v.y, c2v.z, c2v.w, cb.x, cb.y, v + 24);
-        // the group's A slot: its previous unit's MMAs have read it
-        wait_bounded(&a_empty[g], (use & 1u) ^ 1u, abort_flag, wait_ns);
+        // the unit's A slot (the group's uses alternate between its slots):
+        // the MMAs of its previous use have read it
+        const int as = TM::kSlots == 2 ? g + 4 * static_cast<int>(use & 1u) : g;
+        const uint32_t aph = TM::kSlots == 2 ? (use >> 1) & 1u : use & 1u;
+        wait_bounded(&a_empty[as], aph ^ 1u, abort_flag, wait_ns);
         tc_fence_after();
-        tmem_st_x32(a_lane, v);
+        tmem_st_x32(lane_base + TM::a(as), v);
         // A scale of row m is read from TMEM lane m, column (base + m / 32),
         // byte = the MMA's a_sf_id: quadrant q writes column base + q
-        tmem_st_x1(sf_lane, sw);
+        tmem_st_x1(lane_base + TM::sfa(as) + q, sw);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[g]);
+        if (lane == 0) mbar_arrive(&a_full[as]);
         if (issuer) {
           // the whole warp follows (descriptors stay warp-uniform); lane 0
           // issues, always the same thread, so its commits (the drain below
           // included) track every MMA of the group
-          wait_bounded(&a_full[g], use & 1u, abort_flag, wait_ns);   // all four quadrants stored
+          wait_bounded(&a_full[as], aph, abort_flag, wait_ns);       // all four quadrants stored
           tc_fence_after();
           const bool seg_first = t != cur_t;              // the group's first unit of this tile
-          const int b = AC::kBufs == 2 ? ((t - t_first) & 1) : 0;
+          const int b = TM::kBufs == 2 ? ((t - t_first) & 1) : 0;
           if (seg_first) {
             cur_t = t;
             wait_bounded(&acc_empty[2 * g + b], ((buf_par >> b) & 1u) ^ 1u, abort_flag, wait_ns);
@@ -392,14 +403,15 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           int bsl = c - c_first;                          // B slot: (c - c_first) mod KT
           if (bsl < 0) bsl += KT;
           const uint64_t bdu = bd0 + static_cast<uint64_t>(bsl * NTOK * 8);
-          const uint32_t d_col = tbase + AC::col(g, b);
+          const uint32_t d_col = tbase + TM::acc(g, b);
+          const uint32_t a_col = tbase + TM::a(as), sfa_col = tbase + TM::sfa(as);
           const bool seg_last = t2 != t || i + kGroups >= n_units;   // the group's last unit of this tile
           if (lane == 0) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               umma_mxf8_ts(d_col, a_col + j * 8, bdu + static_cast<uint64_t>(2 * j), idesc | (uint32_t(j) << 29),
                            sfa_col, sfb_col, (seg_first && j == 0) ? 0u : 1u);
-            umma_commit(&a_empty[g]);
+            umma_commit(&a_empty[as]);
             if (seg_last) umma_commit(&acc_full[2 * g + b]);
           }
           if (seg_last) buf_par ^= 1u << b;
@@ -485,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       };
       // scale factors of B: 2^0 in every byte of 8 columns, all 128 lanes
       for (int cc = 0; cc < 8; cc += 4)
-        tmem_st_x4(tbase + lane_addr + kSfbCol + cc, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        tmem_st_x4(tbase + lane_addr + TM::kSfb + cc, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       tmem_st_wait();
       tc_fence_before();
       named_bar_sync(3, 32 * 4 + 32 * 4 * kGroups);     // B scale factors are in TMEM (with the decoders)
@@ -497,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         const int seg_c = (s0 == 0) ? c_first : 0;
         const bool complete = seg_c == 0 && c == KT - 1;
         const int span = i - s0;                          // units in the segment - 1
-        const int b = AC::kBufs == 2 ? ((t - t_first) & 1) : 0;
+        const int b = TM::kBufs == 2 ? ((t - t_first) & 1) : 0;
         // groups with a unit in [s0, i]: all of them if the segment has 4 or more
         uint32_t part = 0;
 #pragma unroll
@@ -518,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           for (int g = 0; g < kGroups; ++g)
             if (part & (1u << g)) {
               uint32_t tv[16];
-              tmem_ld_x16(tbase + lane_addr + AC::col(g, b) + c0, tv);
+              tmem_ld_x16(tbase + lane_addr + TM::acc(g, b) + c0, tv);
               tmem_ld_wait();
 #pragma unroll
               for (int k = 0; k < 16; ++k) v[k] += __uint_as_float(tv[k]);
