@@ -20,26 +20,31 @@
 // writes its fp32 partial tile there, the last one sums the parts in part
 // order (deterministic) and writes y.
 //
-// Roles (one CTA per SM, 24 warps; a warp's sub-partition is warp % 4, and a
-// warp reaches only the TMEM lanes 32 (warp % 4) .. + 31):
+// Roles (one CTA per SM, 24 warps; a warp's sub-partition is warp % 4).
+// The tensor core's throughput drops by half when the sub-partition of the
+// thread that issues its MMAs also runs decode arithmetic (measured: 48 ->
+// ~100 cycles per K = 32 MMA), so decoding and issuing live on different
+// sub-partitions and the decoded weights go through shared memory:
 //  * warp 0: 1-D bulk copies of 4 consecutive units (24 KB, one contiguous
 //    piece of the stream) into a ring of shared-memory stages;
-//  * warps 4..19: 16 decoders in 4 groups; group g decodes position g of
-//    every stage (unit 4 j + g), its warp w takes the 32 rows of lane quadrant
-//    w % 4: a thread (one row = one TMEM lane) loads its 48 code bytes,
-//    spreads the codes to nibbles, turns them into E4M3 bytes with byte
-//    permutes through the row's codebook (two registers), and writes the 128
-//    bytes into one of the group's two A slots in TMEM (32 columns) with the
-//    row's 4 E8M0 group scales as the A scale factors.  Because a group takes
-//    exactly one unit per stage, its stage slot and A slot advance by one per
-//    unit: no division on the decode path;
-//  * warp 1 (one lane): TMEM allocation, the activations by TMA (after the
-//    grid dependency), then per unit 4 tcgen05.mma kind::mxf8f6f4.block_scale
-//    (K = 32) with A from TMEM and B from shared memory; the E8M0 group scale
-//    is exactly the MX block scale of its 32-wide K block;
-//  * warps 20..23: epilogue -- tcgen05.ld the accumulator (two alternate, one
-//    per tile segment), then either y = a_scale * acc or the partial-tile
-//    protocol above.
+//  * 12 decoder warps, all on sub-partitions 0, 2 and 3, in 3 groups of 4
+//    (each group with warps on all three); group g decodes the units
+//    i = g mod 3, its warp d takes rows 32 d .. 32 d + 31 of a unit: a thread
+//    (one row) loads its 48 code bytes, spreads the codes to nibbles, turns
+//    them into E4M3 bytes with byte permutes through the row's codebook (two
+//    registers) and stores the 128 bytes into one of the group's A slots in
+//    shared memory (K-major core matrices, conflict-free 16-byte stores) with
+//    its 4 E8M0 group scales beside them;
+//  * warps 5, 9, 13 on sub-partition 1, one per group: the group's MMAs --
+//    per unit one tcgen05.cp of the scale rows into TMEM and 4 tcgen05.mma
+//    kind::mxf8f6f4.block_scale (K = 32) with A and B (the activations,
+//    resident for the CTA's k-tiles) from shared memory, into the group's own
+//    accumulator; the E8M0 group scale is exactly the MX block scale of its
+//    32-wide K block;
+//  * warp 1: TMEM allocation and the activations by TMA;
+//  * warps 20..23: epilogue -- tcgen05.ld the groups' accumulators (two per
+//    group alternate between tile segments) and sum them in group order, then
+//    either y = a_scale * acc or the partial-tile protocol above.
 //
 // Fused gate-up epilogue (GATE_UP): the weight's 128-row tile t holds, for the
 // R/2 features 64 t .., their gate rows followed by their up rows (R = the
@@ -78,19 +83,19 @@ constexpr int kUnitBytes = kRows * 48;                // codes of one full unit
 constexpr int kUnitsPerStage = 4;
 constexpr int kStageBytes = kUnitsPerStage * kUnitBytes;   // 24 KB
 constexpr int kMaxStages = 8;
-constexpr int kGroups = 4;                            // decoder group g <-> stage position g
-static_assert(kGroups == kUnitsPerStage, "one unit per group per stage");
-constexpr int kASlots = 2 * kGroups;                  // at most two A slots per group
+constexpr int kGroups = 3;                            // decoder groups: unit i -> group i % 3
+constexpr int kMaxSlotsPerGroup = 2;
+constexpr int kASlots = kGroups * kMaxSlotsPerGroup;
+constexpr int kASlotA = kRows * 128;                  // decoded E4M3 A of one unit
+constexpr int kASlotBytes = kASlotA + kRows * 16;     // + one 16-byte scale row per weight row
 constexpr int kProdWarp = 0;
-constexpr int kMmaWarp = 1;
-constexpr int kDecWarp0 = 4;                          // warps 4..19
-constexpr int kEpiWarp0 = 20;                         // warps 20..23
+constexpr int kAllocWarp = 1;                         // TMEM allocation, activations by TMA
+constexpr int kEpiWarp0 = 20;                         // warps 20..23: quadrants 0..3
 constexpr int kNumWarps = 24;
 constexpr int kThreads = kNumWarps * 32;
 constexpr int kTmemCols = 512;
-constexpr int kACol = 256;                            // + 32 * group
-constexpr int kSfaCol = 384;                          // + 4 * group (4-column aligned)
-constexpr int kSfbCol = 400;                          // 8 columns of B scale factors (2^0)
+constexpr int kSfaCol = 448;                          // + 4 * A slot (4-column aligned)
+constexpr int kSfbCol = 480;                          // 8 columns of B scale factors (2^0)
 constexpr int kMaxSmem = 232448;
 constexpr int kMinSmem = 120 * 1024;                  // one CTA per SM: it owns all of TMEM
 // barriers: code stages full/empty, per A slot full/empty, per (group,
@@ -101,24 +106,31 @@ constexpr int kXchgBytes = (64 * kXchgStride * 4 + 127) / 128 * 128;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
 constexpr long long kDrainLimitNs = 10000000000LL;    // copies and MMAs always finish; 10 s is a backstop
 
-// Tensor-memory columns.  Accumulator (group g, buffer b) at
-// (g * kBufs + b) * kStride: two buffers per group up to 32 token columns,
-// one at 64.  A slots of 32 columns from kACol.  With 16 token columns an
-// accumulator region of 32 columns holds 16 unused ones: the scale factors
-// live there (A slot s's at 32 s + 16, B's at 20) and every group gets two A
-// slots (s = g and g + 4, alternately), so it stores its next unit while the
-// tensor core still reads the last; otherwise one A slot per group and the
-// scale factors after the A slots.
+// Decoder warp d (0..11) of group d / 4, rows 32 (d % 4) ..: warps on
+// sub-partitions 0, 2 and 3 only, each group spread over all three.
+__device__ __forceinline__ int decoder_warp(int d) {
+  constexpr int kMap[12] = {4, 2, 3, 8, 6, 7, 12, 10, 11, 16, 14, 15};
+  return kMap[d];
+}
+// Decoder index of a warp, or -1.
+__device__ __forceinline__ int decoder_of(int warp) {
+  switch (warp) {
+    case 4: return 0;  case 2: return 1;  case 3: return 2;  case 8: return 3;
+    case 6: return 4;  case 7: return 5;  case 12: return 6; case 10: return 7;
+    case 11: return 8; case 16: return 9; case 14: return 10; case 15: return 11;
+    default: return -1;
+  }
+}
+// The MMA warp of group g: sub-partition 1.
+__host__ __device__ constexpr int issuer_warp(int g) { return 5 + 4 * g; }
+
+// Tensor-memory columns: accumulator (group g, buffer b) at (2 g + b) * kStride,
+// A slot s's scale factors at kSfaCol + 4 s, B's at kSfbCol.
 template <int NTOK>
 struct TmemMap {
   static constexpr int kStride = NTOK < 32 ? 32 : NTOK;
-  static constexpr int kBufs = NTOK <= 32 ? 2 : 1;
-  static constexpr int kSlots = NTOK == 16 ? 2 : 1;      // A slots per group
-  static_assert(kGroups * kBufs * kStride <= kACol, "accumulators overlap the A slots");
-  static __device__ __forceinline__ uint32_t acc(int g, int b) { return (g * kBufs + b) * kStride; }
-  static __device__ __forceinline__ uint32_t a(int s) { return kACol + 32 * s; }
-  static __device__ __forceinline__ uint32_t sfa(int s) { return kSlots == 2 ? 32 * s + 16 : kSfaCol + 4 * s; }
-  static constexpr int kSfb = kSlots == 2 ? 20 : kSfbCol;
+  static_assert(2 * kGroups * kStride <= kSfaCol, "accumulators overlap the scale factors");
+  static __device__ __forceinline__ uint32_t acc(int g, int b) { return (2 * g + b) * kStride; }
 };
 
 __device__ __forceinline__ void raise(unsigned bits) { atomicOr(&g_status_sk, bits); }
@@ -158,6 +170,10 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -193,10 +209,11 @@ template <int NTOK, bool GATE_UP>
 __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__ SkParams p) {
   using TM = TmemMap<NTOK>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  const int NS = p.stages;
+  const int NS = p.stages, SPG = p.slots_pg;           // code stages, A slots per group
   uint8_t* codes_s = smem;
   uint8_t* b_s = smem + NS * kStageBytes;
-  float* xchg = reinterpret_cast<float*>(b_s + p.b_ktiles * NTOK * 128);   // GATE_UP: up rows of a tile
+  uint8_t* a_s = b_s + p.b_ktiles * NTOK * 128;        // A slot s at s * kASlotBytes (1 KB multiples)
+  float* xchg = reinterpret_cast<float*>(a_s + kGroups * SPG * kASlotBytes);   // GATE_UP: up rows
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xchg) + (GATE_UP ? kXchgBytes : 0));
   uint64_t* full = bars;
   uint64_t* empty = full + kMaxStages;
@@ -227,11 +244,11 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 4 * kGroups);              // every decoder warp of a full stage, once
+      mbar_init(&empty[i], 4 * kUnitsPerStage);       // four row blocks of each unit of a full stage
     }
-    for (int s = 0; s < kASlots; ++s) {
-      mbar_init(&a_full[s], 4);                       // the group's four quadrant warps
-      mbar_init(&a_empty[s], 1);                      // the group's MMAs read the slot
+    for (int sl = 0; sl < kASlots; ++sl) {
+      mbar_init(&a_full[sl], 4);                      // the group's four decoder warps
+      mbar_init(&a_empty[sl], 1);                     // the group's MMAs read the slot
     }
     for (int g = 0; g < kGroups; ++g) {
       mbar_init(&acc_full[2 * g], 1);
@@ -251,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   grid_launch_dependents();
 
   uint32_t tbase = 0;
+  const int dec = decoder_of(warp);
   if (warp == kProdWarp) {
     // -------------------------------------------------------- bulk producer --
     if (lane == 0) {
@@ -286,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     }
     __syncwarp();
   } else {
-    if (warp == kMmaWarp) {
+    if (warp == kAllocWarp) {
       tmem_alloc(tmem_slot, kTmemCols);
       tmem_relinquish();
     }
@@ -295,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     tc_fence_after();
     tbase = *tmem_slot;
 
-    if (warp == kMmaWarp) {
+    if (warp == kAllocWarp) {
       // ------------------------------------------------- resident activations --
       if (lane == 0 && n_units > 0) {
         // Written by an earlier kernel, so after the grid dependency: k-tile
@@ -313,31 +331,85 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         wait_drain(b_full, 0);                         // landed before the CTA can end
       }
       __syncwarp();
-    } else if (warp >= kDecWarp0 && warp < kEpiWarp0) {
-      // ------------------------------------------------------------ decoders --
-      // Group g = (warp - 4) / 4 decodes units g, g + 4, ...; its warp on
-      // sub-partition g (quadrant q == g) also issues the group's MMAs, into
-      // the group's own accumulators, so no single thread issues for all.
-      const int g = (warp - kDecWarp0) >> 2, q = warp & 3;
-      const bool issuer = q == g;
-      const int r = 32 * q + lane;                      // row inside the tile == TMEM lane
-      const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-      const uint32_t codes_base = smem_u32(codes_s);
-      const uint32_t lane_base = tbase + lane_addr;
-      const int gk = p.K / 32;
-      // issuer state: B descriptor, instruction descriptor, the tile of the
-      // group's current segment and the uses of each accumulator buffer
-      const uint64_t bd0 = umma_desc_kmajor_sw128(smem_u32(b_s));
-      const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
-      const uint32_t sfb_col = tbase + TM::kSfb;
-      int cur_t = -1;
-      uint32_t buf_par = 0;                             // bit b: parity of the uses of buffer b
-      named_bar_sync(3, 32 * 4 + 32 * 4 * kGroups);     // the epilogue stored the B scale factors
+    } else if (warp == issuer_warp(0) || warp == issuer_warp(1) || warp == issuer_warp(2)) {
+      // ----------------------------------------------------------- MMA warps --
+      // Group g's units g, g + 3, ... in order: per unit the scale rows to
+      // TMEM (tcgen05.cp) and 4 MMAs from the group's A slot, into the
+      // group's accumulator for the unit's tile.  The whole warp follows the
+      // loop (its values stay warp-uniform); lane 0 issues, always the same
+      // thread, so its commits track all of the group's tensor-core work.
+      const int g = (warp - issuer_warp(0)) >> 2;
+      named_bar_sync(3, 32 * 4 + 32 * kGroups);        // the epilogue stored the B scale factors
       tc_fence_after();
-      if (issuer && g < n_units) {
-        wait_bounded(b_full, 0, abort_flag, wait_ns);  // resident activations landed (whole warp)
+      if (g < n_units) {
+        wait_bounded(b_full, 0, abort_flag, wait_ns);  // resident activations landed
         tc_fence_after();
       }
+      const uint64_t bd0 = umma_desc_kmajor_sw128(smem_u32(b_s));
+      const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
+      const uint32_t sfb_col = tbase + kSfbCol;
+      int t = t_first, c = c_first;
+      geo.advance(t, c, g);
+      int cur_t = -1;
+      uint32_t buf_par = 0;                            // bit b: parity of the uses of buffer b
+      uint32_t use = 0;
+      for (int i = g; i < n_units; i += kGroups, ++use) {
+        int t2 = t, c2 = c;
+        geo.advance(t2, c2, kGroups);
+        const int as = g * SPG + (SPG == 2 ? static_cast<int>(use & 1u) : 0);
+        const uint32_t aph = SPG == 2 ? (use >> 1) & 1u : use & 1u;
+        wait_bounded(&a_full[as], aph, abort_flag, wait_ns);    // the group's four warps stored
+        tc_fence_after();
+        const bool seg_first = t != cur_t;              // the group's first unit of this tile
+        const int b = (t - t_first) & 1;
+        if (seg_first) {
+          cur_t = t;
+          wait_bounded(&acc_empty[2 * g + b], ((buf_par >> b) & 1u) ^ 1u, abort_flag, wait_ns);
+          tc_fence_after();
+        }
+        int bsl = c - c_first;                          // B slot: (c - c_first) mod KT
+        if (bsl < 0) bsl += KT;
+        const uint32_t a_addr = smem_u32(a_s) + as * kASlotBytes;
+        const uint64_t ad = umma_desc_kmajor(a_addr, kRows * 16, 128);
+        const uint64_t sd = umma_desc_kmajor(a_addr + kASlotA, 128, 128);
+        const uint64_t bdu = bd0 + static_cast<uint64_t>(bsl * NTOK * 8);
+        const uint32_t d_col = tbase + TM::acc(g, b), sfa_col = tbase + kSfaCol + 4 * as;
+        const bool seg_last = t2 != t || i + kGroups >= n_units;   // the group's last unit of this tile
+        if (lane == 0) {
+          // the unit's scale rows -> 4 TMEM columns (row r's scale word sits
+          // in every 32-bit word of its 16-byte row, whichever column the MMA
+          // reads for it); in order with this thread's MMAs
+          tmem_cp_128x128b(sfa_col, sd);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            umma_mxf8(d_col, ad + static_cast<uint64_t>(j * 256), bdu + static_cast<uint64_t>(2 * j),
+                      idesc | (uint32_t(j) << 29), sfa_col, sfb_col, (seg_first && j == 0) ? 0u : 1u);
+          umma_commit(&a_empty[as]);
+          if (seg_last) umma_commit(&acc_full[2 * g + b]);
+        }
+        if (seg_last) buf_par ^= 1u << b;
+        __syncwarp();
+        t = t2;
+        c = c2;
+      }
+      // all of the group's tensor-core work is done before TMEM is freed
+      if (lane == 0) {
+        umma_commit(&drain[g]);
+        wait_drain(&drain[g], 0);
+      }
+      __syncwarp();
+    } else if (dec >= 0) {
+      // ------------------------------------------------------------ decoders --
+      // Decoder d = 4 g + rq: group g's units g, g + 3, ..., rows
+      // r = 32 rq + lane of each.  A unit's 128 decoded bytes of row r go to
+      // the group's A slot as 8 chunks of 16 (chunk x at x * 2048 + r * 16:
+      // core matrices of 8 rows x 16 bytes, 128 bytes apart along M, 2048
+      // apart along K), its scale word to the slot's scale row r (4 copies).
+      const int g = dec >> 2, rq = dec & 3;
+      const int r = 32 * rq + lane;                     // row inside the tile
+      const uint32_t codes_base = smem_u32(codes_s);
+      const uint32_t a_base = smem_u32(a_s);
+      const int gk = p.K / 32;
       // scale word and codebook of row r for the unit at (t, c)
       auto load_sc = [&](int t, int c, bool valid, uint32_t& sw, uint2& cb) {
         sw = 0x7F7F7F7Fu;
@@ -348,20 +420,19 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           cb = __ldg(reinterpret_cast<const uint2*>(p.codebooks + static_cast<size_t>(n) * 8));
         }
       };
-      int slot = 0;                                     // stage j = (i - g) / 4
+      // stage of unit i: i / 4, position i % 4; advanced by 3 units per step
+      int slot = 0, pos = g;
       uint32_t ph = 0, use = 0;
-      // One unit of the group: (t, c) its position, (sw, cb) its row's scale
-      // word and codebook, (t2) the tile of the group's next unit.
-      auto process = [&](int i, int t, int c, int t2, uint32_t sw, uint2 cb) {
+      auto process = [&](int t, int c, uint32_t sw, uint2 cb) {
         wait_bounded(&full[slot], ph, abort_flag, wait_ns);
         uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, c2v = c0;
         const int rows_t = geo.rows(t);
         if (r < rows_t) {
-          // the g units before this one in the stage: min(g, c) of them in
+          // the pos units before this one in the stage: min(pos, c) of them in
           // tile t (rows_t rows each; t may be the ragged last tile), the rest
           // in full tiles before it
-          const int kin = min(g, c);
-          const uint32_t at = codes_base + slot * kStageBytes + (kin * rows_t + (g - kin) * kRows + r) * 48;
+          const int kin = min(pos, c);
+          const uint32_t at = codes_base + slot * kStageBytes + (kin * rows_t + (pos - kin) * kRows + r) * 48;
           c0 = lds128(at);
           c1 = lds128(at + 16);
           c2v = lds128(at + 32);
@@ -373,54 +444,25 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
         decode_group(c1.z, c1.w, c2v.x, cb.x, cb.y, v + 16);
         decode_group(c2v.y, c2v.z, c2v.w, cb.x, cb.y, v + 24);
-        // the unit's A slot (the group's uses alternate between its slots):
-        // the MMAs of its previous use have read it
-        const int as = TM::kSlots == 2 ? g + 4 * static_cast<int>(use & 1u) : g;
-        const uint32_t aph = TM::kSlots == 2 ? (use >> 1) & 1u : use & 1u;
+        const int as = g * SPG + (SPG == 2 ? static_cast<int>(use & 1u) : 0);
+        const uint32_t aph = SPG == 2 ? (use >> 1) & 1u : use & 1u;
         wait_bounded(&a_empty[as], aph ^ 1u, abort_flag, wait_ns);
-        tc_fence_after();
-        tmem_st_x32(lane_base + TM::a(as), v);
-        // A scale of row m is read from TMEM lane m, column (base + m / 32),
-        // byte = the MMA's a_sf_id: quadrant q writes column base + q
-        tmem_st_x1(lane_base + TM::sfa(as) + q, sw);
-        tmem_st_wait();
-        tc_fence_before();
+        const uint32_t slot_addr = a_base + as * kASlotBytes;
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+          sts128(slot_addr + x * (kRows * 16) + r * 16, v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+        sts128(slot_addr + kASlotA + r * 16, sw, sw, sw, sw);
+        fence_proxy_async_smem();                       // visible to the tensor core
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[as]);
-        if (issuer) {
-          // the whole warp follows (descriptors stay warp-uniform); lane 0
-          // issues, always the same thread, so its commits (the drain below
-          // included) track every MMA of the group
-          wait_bounded(&a_full[as], aph, abort_flag, wait_ns);       // all four quadrants stored
-          tc_fence_after();
-          const bool seg_first = t != cur_t;              // the group's first unit of this tile
-          const int b = TM::kBufs == 2 ? ((t - t_first) & 1) : 0;
-          if (seg_first) {
-            cur_t = t;
-            wait_bounded(&acc_empty[2 * g + b], ((buf_par >> b) & 1u) ^ 1u, abort_flag, wait_ns);
-            tc_fence_after();
-          }
-          int bsl = c - c_first;                          // B slot: (c - c_first) mod KT
-          if (bsl < 0) bsl += KT;
-          const uint64_t bdu = bd0 + static_cast<uint64_t>(bsl * NTOK * 8);
-          const uint32_t d_col = tbase + TM::acc(g, b);
-          const uint32_t a_col = tbase + TM::a(as), sfa_col = tbase + TM::sfa(as);
-          const bool seg_last = t2 != t || i + kGroups >= n_units;   // the group's last unit of this tile
-          if (lane == 0) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              umma_mxf8_ts(d_col, a_col + j * 8, bdu + static_cast<uint64_t>(2 * j), idesc | (uint32_t(j) << 29),
-                           sfa_col, sfb_col, (seg_first && j == 0) ? 0u : 1u);
-            umma_commit(&a_empty[as]);
-            if (seg_last) umma_commit(&acc_full[2 * g + b]);
-          }
-          if (seg_last) buf_par ^= 1u << b;
-          __syncwarp();
-        }
         ++use;
-        if (++slot == NS) {
-          slot = 0;
-          ph ^= 1u;
+        pos += kGroups;                                 // next unit of the group: 3 further
+        if (pos >= kUnitsPerStage) {
+          pos -= kUnitsPerStage;
+          if (++slot == NS) {
+            slot = 0;
+            ph ^= 1u;
+          }
         }
       };
       // Two register sets for the scale word and codebook, so the loads for
@@ -432,24 +474,16 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       uint2 cbA, cbB;
       load_sc(ta, ca, g < n_units, swA, cbA);
       for (int i = g; i < n_units; i += 2 * kGroups) {
-        int tb = ta, cbb = ca;                          // unit i + 4 (set B)
+        int tb = ta, cbb = ca;                          // unit i + 3 (set B)
         geo.advance(tb, cbb, kGroups);
         load_sc(tb, cbb, i + kGroups < n_units, swB, cbB);
-        process(i, ta, ca, tb, swA, cbA);
+        process(ta, ca, swA, cbA);
         if (i + kGroups >= n_units) break;
-        ta = tb;                                        // unit i + 8 (set A)
+        ta = tb;                                        // unit i + 6 (set A)
         ca = cbb;
         geo.advance(ta, ca, kGroups);
         load_sc(ta, ca, i + 2 * kGroups < n_units, swA, cbA);
-        process(i + kGroups, tb, cbb, ta, swB, cbB);
-      }
-      if (issuer) {
-        // all of the group's tensor-core work is done before TMEM is freed
-        if (lane == 0) {
-          umma_commit(&drain[g]);
-          wait_drain(&drain[g], 0);
-        }
-        __syncwarp();
+        process(tb, cbb, swB, cbB);
       }
     } else if (warp >= kEpiWarp0) {
       // ------------------------------------------------------------ epilogue --
@@ -497,10 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       };
       // scale factors of B: 2^0 in every byte of 8 columns, all 128 lanes
       for (int cc = 0; cc < 8; cc += 4)
-        tmem_st_x4(tbase + lane_addr + TM::kSfb + cc, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        tmem_st_x4(tbase + lane_addr + kSfbCol + cc, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       tmem_st_wait();
       tc_fence_before();
-      named_bar_sync(3, 32 * 4 + 32 * 4 * kGroups);     // B scale factors are in TMEM (with the decoders)
+      named_bar_sync(3, 32 * 4 + 32 * kGroups);        // B scale factors are in TMEM (with the MMA warps)
       grid_dependency_wait();                           // y and the workspace may still be in use
       uint32_t acc_par = 0;                             // bit 2 g + b: parity of (group, buffer) uses
       int t = t_first, c = c_first, s0 = 0;             // s0: first unit of the segment
@@ -509,12 +543,13 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         const int seg_c = (s0 == 0) ? c_first : 0;
         const bool complete = seg_c == 0 && c == KT - 1;
         const int span = i - s0;                          // units in the segment - 1
-        const int b = TM::kBufs == 2 ? ((t - t_first) & 1) : 0;
-        // groups with a unit in [s0, i]: all of them if the segment has 4 or more
+        const int b = (t - t_first) & 1;
+        // groups with a unit in [s0, i] (unit u belongs to group u % 3): all
+        // of them if the segment has 3 or more
         uint32_t part = 0;
 #pragma unroll
         for (int g = 0; g < kGroups; ++g)
-          if (span >= kGroups - 1 || ((g - s0) & (kGroups - 1)) <= span) part |= 1u << g;
+          if (span >= kGroups - 1 || (g - s0 % kGroups + kGroups) % kGroups <= span) part |= 1u << g;
 #pragma unroll
         for (int g = 0; g < kGroups; ++g)
           if (part & (1u << g)) {
@@ -627,12 +662,12 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     }
   }
 
-  // ---- teardown: each group's issuer saw its tensor-core work complete, the
-  // producer saw its copies land, the B loads landed, decoders waited for
-  // their TMEM stores and the epilogue for its TMEM loads.
+  // ---- teardown: each group's MMA warp saw its tensor-core work complete,
+  // the producer saw its copies land, the B loads landed, the epilogue
+  // waited for its TMEM loads.
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kAllocWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
@@ -660,7 +695,7 @@ __global__ void __launch_bounds__(1024) gate_up_quant_kernel(const float* __rest
 }
 
 struct Plan {
-  int ntok = 0, grid = 0, stages = 0, b_ktiles = 0, smem = 0, tiles = 0;
+  int ntok = 0, grid = 0, stages = 0, b_ktiles = 0, slots_pg = 0, smem = 0, tiles = 0;
 };
 
 // Tile arrival counters and the gate-up per-token maxima live in a fixed area
@@ -682,9 +717,15 @@ bool plan_for(int M, int N, int K, bool gate_up, Plan& pl) {
   pl.ntok = ntok_for(M);
   pl.b_ktiles = static_cast<int>(std::min<long long>(KT, per));
   const int fixed = pl.b_ktiles * pl.ntok * 128 + (gate_up ? kXchgBytes : 0) + kBarBytes;
-  pl.stages = std::min(kMaxStages, (kMaxSmem - fixed) / kStageBytes);
-  if (pl.stages < 3) return false;
-  pl.smem = std::max(pl.stages * kStageBytes + fixed, kMinSmem);
+  // two A slots per group if 3 or more code stages still fit, else one
+  pl.slots_pg = 2;
+  pl.stages = std::min(kMaxStages, (kMaxSmem - fixed - kGroups * 2 * kASlotBytes) / kStageBytes);
+  if (pl.stages < 3) {
+    pl.slots_pg = 1;
+    pl.stages = std::min(kMaxStages, (kMaxSmem - fixed - kGroups * kASlotBytes) / kStageBytes);
+  }
+  if (pl.stages < 2) return false;
+  pl.smem = std::max(pl.stages * kStageBytes + kGroups * pl.slots_pg * kASlotBytes + fixed, kMinSmem);
   pl.grid = static_cast<int>(G);
   pl.tiles = static_cast<int>(tiles);
   return true;
@@ -763,6 +804,7 @@ int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigne
   p.counters = counters;
   p.stages = pl.stages;
   p.b_ktiles = pl.b_ktiles;
+  p.slots_pg = pl.slots_pg;
   const int em = encode_a_map(p, pl.ntok);
   if (em != CBQ_OK) return em;
   if (gate_up) {
