@@ -197,6 +197,17 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
+// Add with release and acquire semantics at GPU scope: the caller's earlier
+// writes -- and, after a CTA barrier, those of the threads that took part in
+// it -- are visible to whoever acquires the new value; writes released by
+// the earlier adders are visible to the caller (and, after a barrier, to the
+// CTA).  Returns the old value.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Programmatic dependent launch: wait until the grids this one depends on
 // have completed and their writes are visible / let dependent grids start.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -550,6 +550,22 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
 #pragma unroll
         for (int g = 0; g < kGroups; ++g)
           if (span >= kGroups - 1 || (g - s0 % kGroups + kGroups) % kGroups <= span) part |= 1u << g;
+        // A partial tile's parts: CTAs b_first .. b_first + nparts - 1, this
+        // one part pme.  This CTA's last segment usually arrives after the
+        // other parts (first segments of later CTAs, finished early): it reads
+        // the tile's counter before its own accumulators are ready, so that
+        // round trip overlaps the last MMAs.
+        const long long tu = static_cast<long long>(t) * KT;
+        const long long b_first = geo.owner(tu);
+        const int nparts = complete ? 1 : static_cast<int>(geo.owner(tu + KT - 1) - b_first + 1);
+        const int pme = static_cast<int>(blockIdx.x - b_first);
+        bool last = false;
+        if (!complete && i == n_units - 1) {
+          if (leader) *last_flag = ld_acquire_gpu(p.counters + t) == static_cast<unsigned>(nparts - 1);
+          named_bar_sync(2, 128);
+          last = *last_flag;
+          named_bar_sync(2, 128);
+        }
 #pragma unroll
         for (int g = 0; g < kGroups; ++g)
           if (part & (1u << g)) {
@@ -581,22 +597,12 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         } else {
           // Partial tile.  Each part's fp32 tile goes to its workspace slot
           // and bumps the tile's counter; the part that finds every other part
-          // published sums all parts in part order and writes y.  A CTA's
-          // last segment usually arrives after the other parts (first
-          // segments of later CTAs, finished early), so it first just reads
-          // the counter.
-          const long long tu = static_cast<long long>(t) * KT;
-          const long long b_first = geo.owner(tu);
-          const int nparts = static_cast<int>(geo.owner(tu + KT - 1) - b_first + 1);
-          const int pme = static_cast<int>(blockIdx.x - b_first);
+          // published (by the read above, or by the value its own add
+          // returns) sums all parts in part order and writes y.  One thread
+          // releases the block's stores after a barrier, and acquires the
+          // others' before one.
           const bool seg_is_first = s0 == 0;
-          bool own_published = false, last = false;
-          if (i == n_units - 1) {                         // this CTA's last segment
-            if (leader) *last_flag = ld_acquire_gpu(p.counters + t) == static_cast<unsigned>(nparts - 1);
-            named_bar_sync(2, 128);
-            last = *last_flag;
-            named_bar_sync(2, 128);
-          }
+          bool own_published = false;
           if (!last) {
             float* part_dst =
                 p.partial + (static_cast<size_t>(2 * blockIdx.x + (seg_is_first ? 0 : 1)) * kRows + r) * NTOK;
@@ -609,14 +615,20 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
               for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
             }
             own_published = true;
-            __threadfence();
-            named_bar_sync(2, 128);
-            if (leader) *last_flag = atomicAdd(p.counters + t, 1u) == static_cast<unsigned>(nparts - 1);
+            named_bar_sync(2, 128);                      // every thread's stores precede the release
+            if (leader) *last_flag = atom_add_acq_rel_gpu(p.counters + t, 1u) == static_cast<unsigned>(nparts - 1);
             named_bar_sync(2, 128);
             last = *last_flag;
           }
           if (last) {
-            __threadfence();
+            // part pi's workspace slot: part 0's CTA reaches this tile as its
+            // last segment if its share started in an earlier tile, every
+            // later part as its first
+            auto part_src = [&](int pi, int c0) {
+              const long long bb = b_first + pi;
+              const int pslot = 2 * static_cast<int>(bb) + ((pi == 0 && geo.first_unit(bb) < tu) ? 1 : 0);
+              return reinterpret_cast<const float4*>(p.partial + (static_cast<size_t>(pslot) * kRows + r) * NTOK + c0);
+            };
 #pragma unroll 1
             for (int c0 = 0; c0 < NTOK; c0 += 16) {
               float mine[16];
@@ -624,26 +636,52 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
               float acc[16];
 #pragma unroll
               for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+              // two parts' loads in flight at a time, summed in part order
 #pragma unroll 1
-              for (int pi = 0; pi < nparts; ++pi) {
-                if (pi == pme && !own_published) {
+              for (int pi = 0; pi < nparts; pi += 2) {
+                const bool ld0 = pi != pme || own_published;
+                const bool has1 = pi + 1 < nparts;
+                const bool ld1 = has1 && (pi + 1 != pme || own_published);
+                float4 f0[4], f1[4];
+                if (ld0) {
+                  const float4* src = part_src(pi, c0);
 #pragma unroll
-                  for (int k = 0; k < 16; ++k) acc[k] += mine[k];
-                  continue;
+                  for (int k = 0; k < 4; ++k) f0[k] = __ldcg(src + k);
                 }
-                // part 0's CTA reaches this tile as its last segment if its
-                // share started in an earlier tile; every later part as its first
-                const long long bb = b_first + pi;
-                const int pslot = 2 * static_cast<int>(bb) + ((pi == 0 && geo.first_unit(bb) < tu) ? 1 : 0);
-                const float4* src =
-                    reinterpret_cast<const float4*>(p.partial + (static_cast<size_t>(pslot) * kRows + r) * NTOK + c0);
+                if (ld1) {
+                  const float4* src = part_src(pi + 1, c0);
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) f1[k] = __ldcg(src + k);
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                  const float4 f = __ldcg(src + k);
-                  acc[4 * k] += f.x;
-                  acc[4 * k + 1] += f.y;
-                  acc[4 * k + 2] += f.z;
-                  acc[4 * k + 3] += f.w;
+                  if (ld0) {
+                    acc[4 * k] += f0[k].x;
+                    acc[4 * k + 1] += f0[k].y;
+                    acc[4 * k + 2] += f0[k].z;
+                    acc[4 * k + 3] += f0[k].w;
+                  } else {
+                    acc[4 * k] += mine[4 * k];
+                    acc[4 * k + 1] += mine[4 * k + 1];
+                    acc[4 * k + 2] += mine[4 * k + 2];
+                    acc[4 * k + 3] += mine[4 * k + 3];
+                  }
+                }
+                if (has1) {
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    if (ld1) {
+                      acc[4 * k] += f1[k].x;
+                      acc[4 * k + 1] += f1[k].y;
+                      acc[4 * k + 2] += f1[k].z;
+                      acc[4 * k + 3] += f1[k].w;
+                    } else {
+                      acc[4 * k] += mine[4 * k];
+                      acc[4 * k + 1] += mine[4 * k + 1];
+                      acc[4 * k + 2] += mine[4 * k + 2];
+                      acc[4 * k + 3] += mine[4 * k + 3];
+                    }
+                  }
                 }
               }
               emit(t, c0, acc);
