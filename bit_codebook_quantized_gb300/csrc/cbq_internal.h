@@ -62,7 +62,6 @@ struct SkParams {
   int F;                      // gate-up only: features, N / 2
   int stages;                 // depth of the code-stage ring
   int b_ktiles;               // k-tiles of resident activations
-  int slots_pg;               // decoded-unit slots in shared memory per decoder group (1 or 2)
 };
 
 // cuTensorMapEncodeTiled from the driver (nullptr if unavailable).

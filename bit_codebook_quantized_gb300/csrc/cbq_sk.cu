@@ -20,31 +20,29 @@
 // writes its fp32 partial tile there, the last one sums the parts in part
 // order (deterministic) and writes y.
 //
-// Roles (one CTA per SM, 24 warps; a warp's sub-partition is warp % 4).
-// The tensor core's throughput drops by half when the sub-partition of the
-// thread that issues its MMAs also runs decode arithmetic (measured: 48 ->
-// ~100 cycles per K = 32 MMA), so decoding and issuing live on different
-// sub-partitions and the decoded weights go through shared memory:
+// Roles (one CTA per SM, 20 warps; a warp's sub-partition is warp % 4, and
+// a warp reaches only TMEM lane quarter warp % 4):
 //  * warp 0: 1-D bulk copies of 4 consecutive units (24 KB, one contiguous
 //    piece of the stream) into a ring of shared-memory stages;
-//  * 12 decoder warps, all on sub-partitions 0, 2 and 3, in 3 groups of 4
-//    (each group with warps on all three); group g decodes the units
-//    i = g mod 3, its warp d takes rows 32 d .. 32 d + 31 of a unit: a thread
-//    (one row) loads its 48 code bytes, spreads the codes to nibbles, turns
-//    them into E4M3 bytes with byte permutes through the row's codebook (two
-//    registers) and stores the 128 bytes into one of the group's A slots in
-//    shared memory (K-major core matrices, conflict-free 16-byte stores) with
-//    its 4 E8M0 group scales beside them;
-//  * warps 5, 9, 13 on sub-partition 1, one per group: the group's MMAs --
-//    per unit one tcgen05.cp of the scale rows into TMEM and 4 tcgen05.mma
-//    kind::mxf8f6f4.block_scale (K = 32) with A and B (the activations,
-//    resident for the CTA's k-tiles) from shared memory, into the group's own
-//    accumulator; the E8M0 group scale is exactly the MX block scale of its
-//    32-wide K block;
-//  * warp 1: TMEM allocation and the activations by TMA;
-//  * warps 20..23: epilogue -- tcgen05.ld the groups' accumulators (two per
-//    group alternate between tile segments) and sum them in group order, then
-//    either y = a_scale * acc or the partial-tile protocol above.
+//  * warps 4..15: decoders in 3 groups of 4, warp 4 + 4 g + q decoding rows
+//    32 q .. 32 q + 31 of group g's units (i = g mod 3): a thread (one row)
+//    loads its 48 code bytes, spreads the codes to nibbles, turns them into
+//    E4M3 bytes with byte permutes through the row's codebook (two
+//    registers) and stores the 128 bytes straight into one of the group's A
+//    slots in TMEM (tcgen05.st, 32 columns of its lane), its 4 E8M0 group
+//    scales into the slot's scale-factor columns;
+//  * warps 1..3, one per group: the group's MMAs -- per unit 4 tcgen05.mma
+//    kind::mxf8f6f4.block_scale (K = 32) with A and its scale factors from
+//    TMEM and B (the activations, resident for the CTA's k-tiles) from
+//    shared memory, into the group's own accumulator; the E8M0 group scale is
+//    exactly the MX block scale of its 32-wide K block.  A thread issues MMAs
+//    at about half the tensor core's rate when its sub-partition also runs
+//    decode arithmetic (measured: 48 -> ~100 cycles per K = 32 MMA), so the
+//    three groups issue side by side;
+//  * warps 16..19: epilogue -- the leader loads the activations by TMA once
+//    the grid dependency resolves; tcgen05.ld the groups' accumulators (two
+//    per group alternate between tile segments) and sum them in group order,
+//    then either y = a_scale * acc or the partial-tile protocol above.
 //
 // Fused gate-up epilogue (GATE_UP): the weight's 128-row tile t holds, for the
 // R/2 features 64 t .., their gate rows followed by their up rows (R = the
@@ -57,7 +55,7 @@
 // raises the CTA's abort flag; later waits of the CTA then give up at once.
 // Giving up never leaves asynchronous work behind: the producer re-arms a
 // stage only after the copy it held has landed and, before the CTA ends,
-// waits for every copy it issued; the MMA thread waits for all its
+// waits for every copy it issued; each MMA thread waits for all its
 // tensor-core work before TMEM is freed.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -84,52 +82,39 @@ constexpr int kUnitsPerStage = 4;
 constexpr int kStageBytes = kUnitsPerStage * kUnitBytes;   // 24 KB
 constexpr int kMaxStages = 8;
 constexpr int kGroups = 3;                            // decoder groups: unit i -> group i % 3
-constexpr int kMaxSlotsPerGroup = 2;
-constexpr int kASlots = kGroups * kMaxSlotsPerGroup;
-constexpr int kASlotA = kRows * 128;                  // decoded E4M3 A of one unit
-constexpr int kASlotBytes = kASlotA + kRows * 16;     // + one 16-byte scale row per weight row
-constexpr int kProdWarp = 0;
-constexpr int kAllocWarp = 1;                         // TMEM allocation, activations by TMA
-constexpr int kEpiWarp0 = 20;                         // warps 20..23: quadrants 0..3
-constexpr int kNumWarps = 24;
+constexpr int kMaxSlots = 2;                          // decoded units in TMEM per group (at most)
+constexpr int kProdWarp = 0;                          // code stream
+constexpr int kAllocWarp = 1;                         // TMEM allocation (also group 0's MMA warp)
+constexpr int kMmaWarp0 = 1;                          // warps 1..3: group g's MMAs
+constexpr int kDecWarp0 = 4;                          // warps 4..15: group (w - 4) / 4, quarter w % 4
+constexpr int kEpiWarp0 = 16;                         // warps 16..19: quarter w % 4 (warp 16 also loads B)
+constexpr int kNumWarps = 20;
 constexpr int kThreads = kNumWarps * 32;
 constexpr int kTmemCols = 512;
-constexpr int kSfaCol = 448;                          // + 4 * A slot (4-column aligned)
-constexpr int kSfbCol = 480;                          // 8 columns of B scale factors (2^0)
+constexpr int kSfbCol = 504;                          // 8 columns of B scale factors (2^0)
+static_assert(kDecWarp0 % 4 == 0 && kEpiWarp0 % 4 == 0, "a warp's TMEM lane quarter is warp % 4");
 constexpr int kMaxSmem = 232448;
 constexpr int kMinSmem = 120 * 1024;                  // one CTA per SM: it owns all of TMEM
-// barriers: code stages full/empty, per A slot full/empty, per (group,
-// buffer) accumulator full/empty, per group MMA drain, B full
-constexpr int kNumBars = 2 * kMaxStages + 2 * kASlots + 2 * kGroups * 2 + kGroups + 1;
+// barriers: code stages full/empty, A slots full/empty, per (group, buffer)
+// accumulator full/empty, per group MMA drain, B full
+constexpr int kNumBars = 2 * kMaxStages + 2 * kGroups * kMaxSlots + 2 * kGroups * 2 + kGroups + 1;
 constexpr int kXchgStride = 17;                       // floats per exchanged row (conflict-free)
 constexpr int kXchgBytes = (64 * kXchgStride * 4 + 127) / 128 * 128;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
 constexpr long long kDrainLimitNs = 10000000000LL;    // copies and MMAs always finish; 10 s is a backstop
 
-// Decoder warp d (0..11) of group d / 4, rows 32 (d % 4) ..: warps on
-// sub-partitions 0, 2 and 3 only, each group spread over all three.
-__device__ __forceinline__ int decoder_warp(int d) {
-  constexpr int kMap[12] = {4, 2, 3, 8, 6, 7, 12, 10, 11, 16, 14, 15};
-  return kMap[d];
-}
-// Decoder index of a warp, or -1.
-__device__ __forceinline__ int decoder_of(int warp) {
-  switch (warp) {
-    case 4: return 0;  case 2: return 1;  case 3: return 2;  case 8: return 3;
-    case 6: return 4;  case 7: return 5;  case 12: return 6; case 10: return 7;
-    case 11: return 8; case 16: return 9; case 14: return 10; case 15: return 11;
-    default: return -1;
-  }
-}
-// The MMA warp of group g: sub-partition 1.
-__host__ __device__ constexpr int issuer_warp(int g) { return 5 + 4 * g; }
-
-// Tensor-memory columns: accumulator (group g, buffer b) at (2 g + b) * kStride,
-// A slot s's scale factors at kSfaCol + 4 s, B's at kSfbCol.
+// Tensor-memory columns: accumulator (group g, buffer b) at (2 g + b) *
+// kStride (two per group alternate between tile segments), then the groups'
+// A slots (kSlots each, 32 columns: 128 E4M3 bytes of a row per lane), then
+// each slot's 4 scale-factor columns, B's scale factors at kSfbCol.
 template <int NTOK>
 struct TmemMap {
   static constexpr int kStride = NTOK < 32 ? 32 : NTOK;
-  static_assert(2 * kGroups * kStride <= kSfaCol, "accumulators overlap the scale factors");
+  static constexpr int kSlots = NTOK > 32 ? 1 : 2;
+  static constexpr int kACol = 2 * kGroups * kStride;
+  static constexpr int kSfaCol = kACol + 32 * kGroups * kSlots;
+  static_assert(kSlots <= kMaxSlots, "A slots");
+  static_assert(kSfaCol + 4 * kGroups * kSlots <= kSfbCol, "A scale factors overlap B's");
   static __device__ __forceinline__ uint32_t acc(int g, int b) { return (2 * g + b) * kStride; }
 };
 
@@ -170,10 +155,6 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -209,17 +190,16 @@ template <int NTOK, bool GATE_UP>
 __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__ SkParams p) {
   using TM = TmemMap<NTOK>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  const int NS = p.stages, SPG = p.slots_pg;           // code stages, A slots per group
+  const int NS = p.stages;                             // code stages
   uint8_t* codes_s = smem;
   uint8_t* b_s = smem + NS * kStageBytes;
-  uint8_t* a_s = b_s + p.b_ktiles * NTOK * 128;        // A slot s at s * kASlotBytes (1 KB multiples)
-  float* xchg = reinterpret_cast<float*>(a_s + kGroups * SPG * kASlotBytes);   // GATE_UP: up rows
+  float* xchg = reinterpret_cast<float*>(b_s + p.b_ktiles * NTOK * 128);   // GATE_UP: up rows
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xchg) + (GATE_UP ? kXchgBytes : 0));
   uint64_t* full = bars;
   uint64_t* empty = full + kMaxStages;
-  uint64_t* a_full = empty + kMaxStages;               // [A slot]
-  uint64_t* a_empty = a_full + kASlots;                // [A slot]
-  uint64_t* acc_full = a_empty + kASlots;              // [group][2]
+  uint64_t* a_full = empty + kMaxStages;               // [group][slot]
+  uint64_t* a_empty = a_full + kGroups * kMaxSlots;    // [group][slot]
+  uint64_t* acc_full = a_empty + kGroups * kMaxSlots;  // [group][2]
   uint64_t* acc_empty = acc_full + 2 * kGroups;        // [group][2]
   uint64_t* drain = acc_empty + 2 * kGroups;           // [group]
   uint64_t* b_full = drain + kGroups;
@@ -246,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 4 * kUnitsPerStage);       // four row blocks of each unit of a full stage
     }
-    for (int sl = 0; sl < kASlots; ++sl) {
+    for (int sl = 0; sl < kGroups * kMaxSlots; ++sl) {
       mbar_init(&a_full[sl], 4);                      // the group's four decoder warps
       mbar_init(&a_empty[sl], 1);                     // the group's MMAs read the slot
     }
@@ -268,7 +248,6 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   grid_launch_dependents();
 
   uint32_t tbase = 0;
-  const int dec = decoder_of(warp);
   if (warp == kProdWarp) {
     // -------------------------------------------------------- bulk producer --
     if (lane == 0) {
@@ -312,34 +291,21 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     named_bar_sync(1, kThreads - 32);                  // everyone but the producer
     tc_fence_after();
     tbase = *tmem_slot;
+    constexpr int S = TM::kSlots;
 
-    if (warp == kAllocWarp) {
-      // ------------------------------------------------- resident activations --
-      if (lane == 0 && n_units > 0) {
-        // Written by an earlier kernel, so after the grid dependency: k-tile
-        // c of this CTA's share lands in slot (c - c_first) mod KT as NTOK
-        // rows of 128 bytes in the 128-byte swizzled K-major layout (one TMA
-        // box); token rows >= M are outside the tensor and arrive as zeros.
-        grid_dependency_wait();
-        const int nb = min(KT, n_units);
-        mbar_arrive_expect_tx(b_full, static_cast<uint32_t>(nb * NTOK * 128));
-        for (int sl = 0; sl < nb; ++sl) {
-          int c = c_first + sl;
-          if (c >= KT) c -= KT;
-          tma_load_2d(b_s + sl * NTOK * 128, &p.a_map, b_full, c * 128, 0);
-        }
-        wait_drain(b_full, 0);                         // landed before the CTA can end
-      }
-      __syncwarp();
-    } else if (warp == issuer_warp(0) || warp == issuer_warp(1) || warp == issuer_warp(2)) {
+    if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kGroups) {
       // ----------------------------------------------------------- MMA warps --
-      // Group g's units g, g + 3, ... in order: per unit the scale rows to
-      // TMEM (tcgen05.cp) and 4 MMAs from the group's A slot, into the
-      // group's accumulator for the unit's tile.  The whole warp follows the
-      // loop (its values stay warp-uniform); lane 0 issues, always the same
-      // thread, so its commits track all of the group's tensor-core work.
-      const int g = (warp - issuer_warp(0)) >> 2;
-      named_bar_sync(3, 32 * 4 + 32 * kGroups);        // the epilogue stored the B scale factors
+      // Group g's units g, g + 3, ... in order: 4 MMAs (K = 32 each) with A and
+      // its scale factors from the unit's TMEM slot and B from shared memory,
+      // into the group's accumulator for the unit's tile segment.  One warp
+      // per group, each on its own sub-partition: an MMA thread whose
+      // sub-partition also runs decode arithmetic issues at about half the
+      // tensor core's rate, so three issue side by side.  The whole warp
+      // follows the loop (its values stay warp-uniform); lane 0 issues,
+      // always the same thread, so its commits track all of the group's
+      // tensor-core work.
+      const int g = warp - kMmaWarp0;
+      named_bar_sync(3, 32 * kGroups + 32 * 4);        // the epilogue stored the B scale factors
       tc_fence_after();
       if (g < n_units) {
         wait_bounded(b_full, 0, abort_flag, wait_ns);  // resident activations landed
@@ -350,15 +316,17 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       const uint32_t sfb_col = tbase + kSfbCol;
       int t = t_first, c = c_first;
       geo.advance(t, c, g);
+      int bsl = c - c_first;                           // B slot: (c - c_first) mod KT
+      if (bsl < 0) bsl += KT;
       int cur_t = -1;
       uint32_t buf_par = 0;                            // bit b: parity of the uses of buffer b
-      uint32_t use = 0;
-      for (int i = g; i < n_units; i += kGroups, ++use) {
+      int su = 0;                                      // slot of the group's use: use % S
+      uint32_t aph = 0;                                // its phase: (use / S) & 1
+      for (int i = g; i < n_units; i += kGroups) {
         int t2 = t, c2 = c;
         geo.advance(t2, c2, kGroups);
-        const int as = g * SPG + (SPG == 2 ? static_cast<int>(use & 1u) : 0);
-        const uint32_t aph = SPG == 2 ? (use >> 1) & 1u : use & 1u;
-        wait_bounded(&a_full[as], aph, abort_flag, wait_ns);    // the group's four warps stored
+        const int as = g * S + su;
+        wait_bounded(&a_full[as], aph, abort_flag, wait_ns);    // the group's four warps stored it
         tc_fence_after();
         const bool seg_first = t != cur_t;              // the group's first unit of this tile
         const int b = (t - t_first) & 1;
@@ -367,23 +335,15 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           wait_bounded(&acc_empty[2 * g + b], ((buf_par >> b) & 1u) ^ 1u, abort_flag, wait_ns);
           tc_fence_after();
         }
-        int bsl = c - c_first;                          // B slot: (c - c_first) mod KT
-        if (bsl < 0) bsl += KT;
-        const uint32_t a_addr = smem_u32(a_s) + as * kASlotBytes;
-        const uint64_t ad = umma_desc_kmajor(a_addr, kRows * 16, 128);
-        const uint64_t sd = umma_desc_kmajor(a_addr + kASlotA, 128, 128);
-        const uint64_t bdu = bd0 + static_cast<uint64_t>(bsl * NTOK * 8);
-        const uint32_t d_col = tbase + TM::acc(g, b), sfa_col = tbase + kSfaCol + 4 * as;
         const bool seg_last = t2 != t || i + kGroups >= n_units;   // the group's last unit of this tile
         if (lane == 0) {
-          // the unit's scale rows -> 4 TMEM columns (row r's scale word sits
-          // in every 32-bit word of its 16-byte row, whichever column the MMA
-          // reads for it); in order with this thread's MMAs
-          tmem_cp_128x128b(sfa_col, sd);
+          const uint32_t a_col = tbase + TM::kACol + 32 * as, sfa_col = tbase + TM::kSfaCol + 4 * as;
+          const uint64_t bdu = bd0 + static_cast<uint64_t>(bsl * NTOK * 8);
+          const uint32_t d_col = tbase + TM::acc(g, b);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            umma_mxf8(d_col, ad + static_cast<uint64_t>(j * 256), bdu + static_cast<uint64_t>(2 * j),
-                      idesc | (uint32_t(j) << 29), sfa_col, sfb_col, (seg_first && j == 0) ? 0u : 1u);
+            umma_mxf8_ts(d_col, a_col + 8 * j, bdu + static_cast<uint64_t>(2 * j), idesc | (uint32_t(j) << 29),
+                         sfa_col, sfb_col, (seg_first && j == 0) ? 0u : 1u);
           umma_commit(&a_empty[as]);
           if (seg_last) umma_commit(&acc_full[2 * g + b]);
         }
@@ -391,6 +351,12 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         __syncwarp();
         t = t2;
         c = c2;
+        bsl += kGroups;
+        if (bsl >= KT) bsl -= KT;
+        if (++su == S) {
+          su = 0;
+          aph ^= 1u;
+        }
       }
       // all of the group's tensor-core work is done before TMEM is freed
       if (lane == 0) {
@@ -398,17 +364,16 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         wait_drain(&drain[g], 0);
       }
       __syncwarp();
-    } else if (dec >= 0) {
+    } else if (warp >= kDecWarp0 && warp < kEpiWarp0) {
       // ------------------------------------------------------------ decoders --
-      // Decoder d = 4 g + rq: group g's units g, g + 3, ..., rows
-      // r = 32 rq + lane of each.  A unit's 128 decoded bytes of row r go to
-      // the group's A slot as 8 chunks of 16 (chunk x at x * 2048 + r * 16:
-      // core matrices of 8 rows x 16 bytes, 128 bytes apart along M, 2048
-      // apart along K), its scale word to the slot's scale row r (4 copies).
-      const int g = dec >> 2, rq = dec & 3;
-      const int r = 32 * rq + lane;                     // row inside the tile
+      // Warp 4 + 4 g + q: group g's units g, g + 3, ..., rows r = 32 q + lane
+      // of each -- the warp's own TMEM lane quarter.  A unit's 128 decoded
+      // bytes of row r go to 32 columns of one of the group's A slots, its
+      // scale word to the slot's 4 scale-factor columns.
+      const int g = (warp - kDecWarp0) >> 2, q = warp & 3;
+      const int r = 32 * q + lane;                      // row inside the tile
+      const uint32_t lane_base = tbase + (static_cast<uint32_t>(32 * q) << 16);
       const uint32_t codes_base = smem_u32(codes_s);
-      const uint32_t a_base = smem_u32(a_s);
       const int gk = p.K / 32;
       // scale word and codebook of row r for the unit at (t, c)
       auto load_sc = [&](int t, int c, bool valid, uint32_t& sw, uint2& cb) {
@@ -422,7 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       };
       // stage of unit i: i / 4, position i % 4; advanced by 3 units per step
       int slot = 0, pos = g;
-      uint32_t ph = 0, use = 0;
+      uint32_t ph = 0;
+      int su = 0;                                       // the group's A slot: use % S
+      uint32_t aph = 0;                                 // its phase: (use / S) & 1
       auto process = [&](int t, int c, uint32_t sw, uint2 cb) {
         wait_bounded(&full[slot], ph, abort_flag, wait_ns);
         uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, c2v = c0;
@@ -444,18 +411,21 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
         decode_group(c1.z, c1.w, c2v.x, cb.x, cb.y, v + 16);
         decode_group(c2v.y, c2v.z, c2v.w, cb.x, cb.y, v + 24);
-        const int as = g * SPG + (SPG == 2 ? static_cast<int>(use & 1u) : 0);
-        const uint32_t aph = SPG == 2 ? (use >> 1) & 1u : use & 1u;
-        wait_bounded(&a_empty[as], aph ^ 1u, abort_flag, wait_ns);
-        const uint32_t slot_addr = a_base + as * kASlotBytes;
-#pragma unroll
-        for (int x = 0; x < 8; ++x)
-          sts128(slot_addr + x * (kRows * 16) + r * 16, v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
-        sts128(slot_addr + kASlotA + r * 16, sw, sw, sw, sw);
-        fence_proxy_async_smem();                       // visible to the tensor core
+        const int as = g * S + su;
+        wait_bounded(&a_empty[as], aph ^ 1u, abort_flag, wait_ns);   // the MMAs of its last use are done
+        tc_fence_after();
+        tmem_st_x32(lane_base + TM::kACol + 32 * as, v);
+        // row r's scale word in all 4 columns: the MMA finds it whichever
+        // column of the 4 it reads for the row
+        tmem_st_x4(lane_base + TM::kSfaCol + 4 * as, sw, sw, sw, sw);
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[as]);
-        ++use;
+        if (++su == S) {
+          su = 0;
+          aph ^= 1u;
+        }
         pos += kGroups;                                 // next unit of the group: 3 further
         if (pos >= kUnitsPerStage) {
           pos -= kUnitsPerStage;
@@ -535,7 +505,20 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       tmem_st_wait();
       tc_fence_before();
       named_bar_sync(3, 32 * 4 + 32 * kGroups);        // B scale factors are in TMEM (with the MMA warps)
-      grid_dependency_wait();                           // y and the workspace may still be in use
+      grid_dependency_wait();                           // y, the workspace and the activations may still be in use
+      if (leader && n_units > 0) {
+        // Resident activations, written by an earlier kernel: k-tile c of this
+        // CTA's share lands in slot (c - c_first) mod KT as NTOK rows of 128
+        // bytes in the 128-byte swizzled K-major layout (one TMA box); token
+        // rows >= M are outside the tensor and arrive as zeros.
+        const int nb = min(KT, n_units);
+        mbar_arrive_expect_tx(b_full, static_cast<uint32_t>(nb * NTOK * 128));
+        for (int sl = 0; sl < nb; ++sl) {
+          int cc = c_first + sl;
+          if (cc >= KT) cc -= KT;
+          tma_load_2d(b_s + sl * NTOK * 128, &p.a_map, b_full, cc * 128, 0);
+        }
+      }
       uint32_t acc_par = 0;                             // bit 2 g + b: parity of (group, buffer) uses
       int t = t_first, c = c_first, s0 = 0;             // s0: first unit of the segment
       for (int i = 0; i < n_units; ++i, geo.advance(t, c, 1)) {
@@ -697,6 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           if ((part & (1u << g)) && lane == 0) mbar_arrive(&acc_empty[2 * g + b]);
         s0 = i + 1;
       }
+      if (leader && n_units > 0) wait_drain(b_full, 0);   // the activations landed before the CTA can end
     }
   }
 
@@ -733,7 +717,7 @@ __global__ void __launch_bounds__(1024) gate_up_quant_kernel(const float* __rest
 }
 
 struct Plan {
-  int ntok = 0, grid = 0, stages = 0, b_ktiles = 0, slots_pg = 0, smem = 0, tiles = 0;
+  int ntok = 0, grid = 0, stages = 0, b_ktiles = 0, smem = 0, tiles = 0;
 };
 
 // Tile arrival counters and the gate-up per-token maxima live in a fixed area
@@ -755,15 +739,9 @@ bool plan_for(int M, int N, int K, bool gate_up, Plan& pl) {
   pl.ntok = ntok_for(M);
   pl.b_ktiles = static_cast<int>(std::min<long long>(KT, per));
   const int fixed = pl.b_ktiles * pl.ntok * 128 + (gate_up ? kXchgBytes : 0) + kBarBytes;
-  // two A slots per group if 3 or more code stages still fit, else one
-  pl.slots_pg = 2;
-  pl.stages = std::min(kMaxStages, (kMaxSmem - fixed - kGroups * 2 * kASlotBytes) / kStageBytes);
-  if (pl.stages < 3) {
-    pl.slots_pg = 1;
-    pl.stages = std::min(kMaxStages, (kMaxSmem - fixed - kGroups * kASlotBytes) / kStageBytes);
-  }
+  pl.stages = std::min(kMaxStages, (kMaxSmem - fixed) / kStageBytes);
   if (pl.stages < 2) return false;
-  pl.smem = std::max(pl.stages * kStageBytes + kGroups * pl.slots_pg * kASlotBytes + fixed, kMinSmem);
+  pl.smem = std::max(pl.stages * kStageBytes + fixed, kMinSmem);
   pl.grid = static_cast<int>(G);
   pl.tiles = static_cast<int>(tiles);
   return true;
@@ -842,7 +820,6 @@ int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigne
   p.counters = counters;
   p.stages = pl.stages;
   p.b_ktiles = pl.b_ktiles;
-  p.slots_pg = pl.slots_pg;
   const int em = encode_a_map(p, pl.ntok);
   if (em != CBQ_OK) return em;
   if (gate_up) {

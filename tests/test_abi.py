@@ -152,12 +152,10 @@ def test_auto_path_choice(L):
     assert L.cbq_gemm_auto_path(64, 151936, 2048, 0) == ops.PATH_MMA
     # with one (cbq_gemm_ws): the stream-K kernel wherever its plan fits (the
     # plan here sees no device, i.e. one CTA holding every k-tile); at M = 64
-    # (64 token columns) the resident activations of K = 2048 or 25600 leave
-    # too little shared memory for the code ring and the decoded-A slots
+    # with K = 25600 its resident activations do not fit
     for M, N, K in [(1, 12288, 4096), (8, 12288, 4096), (16, 25600, 5120),
-                    (1, 151936, 2048), (64, 300, 1024)]:
+                    (1, 151936, 2048), (64, 151936, 2048), (64, 300, 1024)]:
         assert L.cbq_gemm_auto_path(M, N, K, 1) == ops.PATH_STREAMK, (M, N, K)
-    assert L.cbq_gemm_auto_path(64, 151936, 2048, 1) == ops.PATH_MMA
     assert L.cbq_gemm_auto_path(64, 5120, 25600, 1) == ops.PATH_MMA
     for ws in (0, 1):
         assert L.cbq_gemm_auto_path(0, 16, 128, ws) == ops.EINVAL
