@@ -390,6 +390,20 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       uint32_t ph = 0;
       int su = 0;                                       // the group's A slot: use % S
       uint32_t aph = 0;                                 // its phase: (use / S) & 1
+      // With two slots per group a unit's TMEM stores complete while the warp
+      // decodes its next unit; then the unit goes to the MMA warp (pend_as:
+      // its slot, -1 if none).  With one slot the next store waits for the
+      // MMAs of this unit, so it goes at once.
+      int pend_as = -1;
+      auto publish = [&]() {
+        if (pend_as >= 0) {
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[pend_as]);
+          pend_as = -1;
+        }
+      };
       auto process = [&](int t, int c, uint32_t sw, uint2 cb) {
         wait_bounded(&full[slot], ph, abort_flag, wait_ns);
         uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, c2v = c0;
@@ -411,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
         decode_group(c1.z, c1.w, c2v.x, cb.x, cb.y, v + 16);
         decode_group(c2v.y, c2v.z, c2v.w, cb.x, cb.y, v + 24);
+        publish();                                      // the previous unit
         const int as = g * S + su;
         wait_bounded(&a_empty[as], aph ^ 1u, abort_flag, wait_ns);   // the MMAs of its last use are done
         tc_fence_after();
@@ -418,10 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         // row r's scale word in all 4 columns: the MMA finds it whichever
         // column of the 4 it reads for the row
         tmem_st_x4(lane_base + TM::kSfaCol + 4 * as, sw, sw, sw, sw);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[as]);
+        pend_as = as;
+        if (S == 1) publish();
         if (++su == S) {
           su = 0;
           aph ^= 1u;
@@ -455,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         load_sc(ta, ca, i + 2 * kGroups < n_units, swA, cbA);
         process(tb, cbb, swB, cbB);
       }
+      publish();                                        // the group's last unit
     } else if (warp >= kEpiWarp0) {
       // ------------------------------------------------------------ epilogue --
       const int q = warp & 3;
