@@ -504,6 +504,62 @@ def run_per_config(dev, stream, peak, calls=250):
                        "weight_copies": R})
         del g, copies, w0, y
         torch.cuda.empty_cache()
+    points += run_gate_up_points(dev, stream, peak, calls, l2)
+    return points
+
+
+# the fused gate-up step on the two gate+up shapes of the specification:
+# (name, M, F, K); the packed weight holds N = 2F rows
+GATE_UP_POINTS = [("gate_up_4096x6144_m1", 1, 6144, 4096), ("gate_up_4096x6144_m8", 8, 6144, 4096),
+                  ("gate_up_5120x12800_m16", 16, 12800, 5120)]
+
+
+def run_gate_up_points(dev, stream, peak, calls, l2):
+    """cbq_gemm_gate_up timed like the other points: the matmul against the
+    2F-row gate+up weight, SiLU(gate) * up, and the per-token E4M3
+    quantisation of the products.  Algorithmic bytes: the packed weight, the
+    activations and their scales in, the E4M3 products and their per-token
+    scales out."""
+    points = []
+    for name, M, F, K in GATE_UP_POINTS:
+        N = 2 * F
+        pw = synth.gen_weights(N, K, seed=1)
+        w0 = ops.PackedWeights.from_host(pw.codes, pw.scales, pw.codebooks, N, K, device=dev)
+        R = int(min(512, max(2, -(-4 * l2 // w0.nbytes))))
+        copies = [w0] + [ops.PackedWeights(w0.codes.clone(), w0.scales.clone(), w0.codebooks.clone(), N, K)
+                         for _ in range(R - 1)]
+        a = torch.from_numpy(synth.gen_activations(M, K, seed=2)).to(dev)
+        s = torch.from_numpy(synth.gen_a_scale(M, seed=3, mode="uniform")).to(dev)
+        q = torch.empty((M, F), dtype=torch.uint8, device=dev)
+        qs = torch.empty((M,), dtype=torch.float32, device=dev)
+        run = lambda w: ops.gate_up(a, s, w, out=q, out_scale=qs, stream=stream)  # noqa: E731
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                run(copies[i % R])
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(calls):
+                run(copies[i % R])
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(PC_REPS + 1)]
+        with torch.cuda.stream(stream):
+            g.replay()
+            ev[0].record(stream)
+            for r in range(PC_REPS):
+                g.replay()
+                ev[r + 1].record(stream)
+        stream.synchronize()
+        if ops.device_status(stream) != ops.OK:
+            raise RuntimeError(f"device status not ok after {name}")
+        us = ev[0].elapsed_time(ev[-1]) * 1e3 / (PC_REPS * calls)
+        wb = weight_bytes(N, K)
+        alg = wb + M * K + 4 * M + M * F + 4 * M
+        points.append({"workload": name, "M": M, "F": F, "N": N, "K": K,
+                       "kernel": "sk_kernel (gate-up epilogue) + gate_up_quant_kernel", "us": round(us, 3),
+                       "weight_GBps": round(wb / us / 1e3, 1), "roofline_frac": round(alg / us / 1e3 / peak, 4),
+                       "tokens_per_s": round(M / us * 1e6, 1), "weight_copies": R})
+        del g, copies, w0
+        torch.cuda.empty_cache()
     return points
 
 

@@ -118,13 +118,17 @@ int cbq_unpack(const cbq_weight_t* w, int32_t N, int32_t K, float* W_out, void* 
 int cbq_gemm_auto_path(int32_t M, int32_t N, int32_t K, int32_t with_workspace) {
   if (M < 1 || M > 64 || N < 1 || K < 128 || K % 128 != 0) return CBQ_EINVAL;
   // Measured on GB300 (CUDA graphs of back-to-back calls, weights beyond L2).
-  // With a workspace the stream-K kernel (equal contiguous weight share per
-  // SM) takes every shape it fits.  Without one: up to 8 token rows the GEMV
+  // Up to 8 token rows the GEMV kernel has the least fixed cost per call and
+  // wins up to ~32 M weights (2048 x 2048: 3.9 us against 8.9 us for the
+  // stream-K kernel; the two meet near 2^25 weights).  Otherwise, with a
+  // workspace, the stream-K kernel (equal contiguous weight share per SM)
+  // takes every shape it fits.  Without one: up to 8 token rows the GEMV
   // kernel on matrices up to ~64 M weights and the tile kernel beyond; from 9
   // rows the tile kernel.  The tile kernel needs its activations resident;
   // where they do not fit, the GEMV kernel runs (see cbq_gemm_path).
-  if (with_workspace && sk_applicable(M, N, K)) return CBQ_PATH_STREAMK;
   const long long weights = static_cast<long long>(N) * K;
+  if (M <= 8 && weights <= (1LL << 25)) return CBQ_PATH_GEMV;
+  if (with_workspace && sk_applicable(M, N, K)) return CBQ_PATH_STREAMK;
   if (M <= 8) return weights <= (1LL << 26) ? CBQ_PATH_GEMV : CBQ_PATH_MMA;
   return CBQ_PATH_MMA;
 }

@@ -157,6 +157,11 @@ def test_auto_path_choice(L):
                     (1, 151936, 2048), (64, 151936, 2048), (64, 300, 1024)]:
         assert L.cbq_gemm_auto_path(M, N, K, 1) == ops.PATH_STREAMK, (M, N, K)
     assert L.cbq_gemm_auto_path(64, 5120, 25600, 1) == ops.PATH_MMA
+    # small matrices at up to 8 rows: the GEMV kernel either way
+    for ws in (0, 1):
+        assert L.cbq_gemm_auto_path(1, 2048, 2048, ws) == ops.PATH_GEMV
+        assert L.cbq_gemm_auto_path(8, 4096, 8192, ws) == ops.PATH_GEMV
+    assert L.cbq_gemm_auto_path(16, 2048, 2048, 1) == ops.PATH_STREAMK
     for ws in (0, 1):
         assert L.cbq_gemm_auto_path(0, 16, 128, ws) == ops.EINVAL
         assert L.cbq_gemm_auto_path(4, 16, 100, ws) == ops.EINVAL
