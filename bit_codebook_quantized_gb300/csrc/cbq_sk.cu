@@ -748,7 +748,12 @@ bool plan_for(int M, int N, int K, bool gate_up, Plan& pl) {
   const long long tiles = (N + kRows - 1) / kRows;
   if (tiles > kMaxTiles) return false;
   const long long U = tiles * KT;
-  const long long G = std::min<long long>(U, device_sm_count());
+  // Stream-K shares (an equal number of units per CTA, tiles split between
+  // CTAs) -- except where the tiles alone fill most of the GPU: then one
+  // whole tile per CTA, which needs no partial-tile fix-up (decode 4096 x
+  // 12288: 96 tiles on 152 SMs, 11.4-11.8 us against 12.1-12.3 us per call).
+  const long long sms = device_sm_count();
+  const long long G = (tiles <= sms && 5 * tiles >= 3 * sms) ? tiles : std::min<long long>(U, sms);
   const long long per = (U + G - 1) / G;               // most units of any CTA
   pl.ntok = ntok_for(M);
   pl.b_ktiles = static_cast<int>(std::min<long long>(KT, per));
