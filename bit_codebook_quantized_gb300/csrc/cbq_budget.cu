@@ -19,18 +19,23 @@
 // (-0 and +0 equal) and puts NaN below every other value, so the kernel is
 // total: any input gives k valid, distinct expert ids per token.
 //
-// One CTA of 32 warps.  A (key, id) pair is one 64-bit word, key in the high
+// A (key, id) pair is one 64-bit word, key in the high
 // half and (2^32 - 1 - id) in the low half, so "ranks before" is plain
-// unsigned ">".  Steps 1 and 4: one warp per token; every lane keeps the
-// best 8 words of its experts (a branch-free insertion chain, taken only when
-// a word beats the lane's 8th), then k rounds of a warp-wide maximum merge the
-// 32 lists.  Step 2: shared-memory atomic adds of (k - r) into the high half
-// of each expert's word.  Step 3: one bitonic sort of those words.
+// unsigned ">".  Three kernels, each launched to overlap the previous one's
+// tail (programmatic dependent launch): step 1 with one warp per token over
+// ceil(T / 8) CTAs, steps 2-3 in one CTA of 32 warps, step 4 with one warp
+// per token again.  Steps 1 and 4: one warp per
+// token; every lane keeps the best 8 words of its experts (a branch-free
+// insertion chain, taken only when a word beats the lane's 8th; 8 loads in
+// flight per lane), then k rounds of a warp-wide maximum merge the 32 lists.
+// Step 2: shared-memory atomic adds of (k - r) into the high half of each
+// expert's word.  Step 3: one bitonic sort of those words.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "cbq_budget.h"
+#include "cbq_device.cuh"
 #include "cbq_internal.h"
 
 namespace cbq {
@@ -39,6 +44,7 @@ namespace {
 constexpr int kBudgetWarps = 32;
 constexpr int kBudgetThreads = kBudgetWarps * 32;
 constexpr int kListLen = kMaxBudgetK;                  // per-lane candidate list
+constexpr int kLoadBatch = 8;                         // loads in flight per lane and batch
 
 // Order-preserving key of a logit: larger logit -> larger key; -0 == +0;
 // NaN -> 0, below every other value (no other float maps to 0).
@@ -75,17 +81,29 @@ __device__ __forceinline__ void insert(uint64_t (&list)[kListLen], uint64_t w) {
 
 // The token's top-k among `count` experts (expert of candidate j: ids ? ids[j]
 // : j), merged over the warp; calls emit(r, e) on lane 0 for rank r = 0..k-1.
+// `row` is in shared or global memory.
 template <typename Emit>
-__device__ __forceinline__ void token_topk(const float* __restrict__ row, const int16_t* ids, int count, int k,
-                                           Emit emit) {
+__device__ __forceinline__ void token_topk(const float* row, const int16_t* ids, int count, int k, Emit emit) {
   const int lane = threadIdx.x & 31;
   uint64_t list[kListLen];
 #pragma unroll
   for (int i = 0; i < kListLen; ++i) list[i] = 0;     // below every real word
-  for (int j = lane; j < count; j += 32) {
-    const int e = ids ? ids[j] : j;
-    const uint64_t w = rank_word(logit_key(__ldg(row + e)), e);
-    if (w > list[kListLen - 1]) insert(list, w);
+  for (int j0 = lane; j0 < count; j0 += 32 * kLoadBatch) {
+    int ee[kLoadBatch];
+    float v[kLoadBatch];
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      const int j = j0 + 32 * u;
+      ee[u] = j < count ? (ids ? ids[j] : j) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) v[u] = ee[u] >= 0 ? row[ee[u]] : 0.f;
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u)
+      if (ee[u] >= 0) {
+        const uint64_t w = rank_word(logit_key(v[u]), ee[u]);
+        if (w > list[kListLen - 1]) insert(list, w);
+      }
   }
   for (int r = 0; r < k; ++r) {
     const uint64_t m = warp_max_u64(list[0]);
@@ -98,25 +116,42 @@ __device__ __forceinline__ void token_topk(const float* __restrict__ row, const 
   }
 }
 
-__global__ void __launch_bounds__(kBudgetThreads) budget_kernel(const float* __restrict__ logits, int T, int E,
-                                                                 int k, int B, int32_t* __restrict__ budget_out,
-                                                                 int32_t* __restrict__ topk_out) {
+constexpr int kOwnWarps = 8;                          // tokens per CTA of the first kernel
+
+// Steps 1 (first kernel, one warp per token over ceil(T / 8) CTAs): every
+// token's own top-k, written to topk_out, which holds it until the second
+// kernel has read it.
+__global__ void __launch_bounds__(kOwnWarps * 32) budget_own_kernel(const float* __restrict__ logits, int T, int E,
+                                                                     int k, int32_t* __restrict__ topk_out) {
+  grid_launch_dependents();                                 // the second kernel may start its prologue
+  grid_dependency_wait();                                   // the logits of an earlier kernel
+  const int t = blockIdx.x * kOwnWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  token_topk(logits + static_cast<size_t>(t) * E, nullptr, E, k,
+             [&](int r, int e) { topk_out[static_cast<size_t>(t) * k + r] = e; });
+}
+
+// Steps 2-3 (second kernel, one CTA of 32 warps): scores from all the own
+// top-k lists, the budget by one bitonic sort, written in ascending order.
+__global__ void __launch_bounds__(kBudgetThreads) budget_sort_kernel(int T, int E, int k, int B,
+                                                                      const int32_t* __restrict__ own,
+                                                                      int32_t* __restrict__ budget_out) {
   __shared__ unsigned long long words[kMaxBudgetExperts];   // (score, id) of every expert
   __shared__ uint8_t in_budget[kMaxBudgetExperts];
-  __shared__ int16_t blist[kMaxBudgetExperts];              // budget ids, ascending
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  grid_launch_dependents();
   int P = 32;                                               // sort width: power of two >= E
   while (P < E) P <<= 1;
   for (int e = tid; e < P; e += kBudgetThreads) {
     words[e] = e < E ? rank_word(0u, e) : 0ull;             // padding sorts last
     in_budget[e] = 0;
   }
+  grid_dependency_wait();                                   // the own top-k lists
   __syncthreads();
-  // 1, 2: own top-k of every token; score (k - r) into the expert's high half
-  for (int t = warp; t < T; t += kBudgetWarps)
-    token_topk(logits + static_cast<size_t>(t) * E, nullptr, E, k, [&](int r, int e) {
-      atomicAdd(&words[e], static_cast<unsigned long long>(k - r) << 32);
-    });
+  // 2: score (k - r) into the high half of the word of each token's rank-r expert
+  const int tk = T * k;
+  for (int i = tid; i < tk; i += kBudgetThreads)
+    atomicAdd(&words[own[i]], static_cast<unsigned long long>(k - i % k) << 32);
   __syncthreads();
   // 3: bitonic sort, descending: words[0..B) are the budget
   for (int size = 2; size <= P; size <<= 1) {
@@ -136,35 +171,67 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_kernel(const float* __r
   }
   for (int j = tid; j < B; j += kBudgetThreads) in_budget[word_id(words[j])] = 1;
   __syncthreads();
-  // the budget in ascending expert order
-  if (warp == 0) {
+  if (warp == 0) {                                          // ascending expert order
     int base = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
       const bool f = e < E && in_budget[e];
       const unsigned m = __ballot_sync(0xffffffffu, f);
-      if (f) {
-        const int at = base + __popc(m & ((1u << lane) - 1u));
-        budget_out[at] = e;
-        blist[at] = static_cast<int16_t>(e);
-      }
+      if (f) budget_out[base + __popc(m & ((1u << lane) - 1u))] = e;
       base += __popc(m);
     }
   }
+}
+
+// Step 4 (third kernel, one warp per token over ceil(T / 8) CTAs): the
+// token's top-k among the budget experts (their logits only), over its own
+// list (read by the second kernel, which has finished).
+__global__ void __launch_bounds__(kOwnWarps * 32) budget_pick_kernel(const float* __restrict__ logits, int T, int E,
+                                                                      int k, int B,
+                                                                      const int32_t* __restrict__ budget,
+                                                                      int32_t* __restrict__ topk_out) {
+  __shared__ int16_t blist[kMaxBudgetExperts];
+  grid_dependency_wait();                                   // the budget
+  for (int j = threadIdx.x; j < B; j += kOwnWarps * 32) blist[j] = static_cast<int16_t>(budget[j]);
   __syncthreads();
-  // 4: every token's top-k inside the budget
-  for (int t = warp; t < T; t += kBudgetWarps)
-    token_topk(logits + static_cast<size_t>(t) * E, blist, B, k,
-               [&](int r, int e) { topk_out[static_cast<size_t>(t) * k + r] = e; });
+  const int t = blockIdx.x * kOwnWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  token_topk(logits + static_cast<size_t>(t) * E, blist, B, k,
+             [&](int r, int e) { topk_out[static_cast<size_t>(t) * k + r] = e; });
 }
 
 }  // namespace
 
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous one runs and waits for it with griddepcontrol.wait.
+template <typename... Args>
+cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  note_launch();
+  return e;
+}
+
 int launch_budget(const float* logits, int T, int E, int k, int B, int32_t* budget, int32_t* topk,
                   cudaStream_t stream) {
-  budget_kernel<<<1, kBudgetThreads, 0, stream>>>(logits, T, E, k, B, budget, topk);
-  note_launch();
-  return cudaGetLastError() == cudaSuccess ? CBQ_OK : CBQ_ECUDA;
+  const dim3 tok_grid((T + kOwnWarps - 1) / kOwnWarps), tok_block(kOwnWarps * 32);
+  // topk_idx holds every token's own top-k until the sort kernel has read it
+  if (launch_pdl(budget_own_kernel, tok_grid, tok_block, stream, logits, T, E, k, topk) != cudaSuccess ||
+      launch_pdl(budget_sort_kernel, dim3(1), dim3(kBudgetThreads), stream, T, E, k, B,
+                 static_cast<const int32_t*>(topk), budget) != cudaSuccess ||
+      launch_pdl(budget_pick_kernel, tok_grid, tok_block, stream, logits, T, E, k, B,
+                 static_cast<const int32_t*>(budget), topk) != cudaSuccess)
+    return CBQ_ECUDA;
+  return CBQ_OK;
 }
 
 }  // namespace cbq
