@@ -62,6 +62,8 @@ struct SkParams {
   int F;                      // gate-up only: features, N / 2
   int stages;                 // depth of the code-stage ring
   int b_ktiles;               // k-tiles of resident activations
+  const int32_t* topk_idx;    // grouped only: [M][topk] expert ids; codes/scales/codebooks stack E experts
+  int E, topk;                // grouped only
 };
 
 // cuTensorMapEncodeTiled from the driver (nullptr if unavailable).
@@ -89,6 +91,8 @@ int launch_sk_static(const SkParams& p, cudaStream_t stream);
 size_t sk_gate_up_workspace_bytes(int M, int F, int K);   // 0 if the kernel cannot take the shape
 int launch_sk_gate_up(const SkParams& p, void* workspace, size_t workspace_bytes, uint8_t* q, float* q_scale,
                       cudaStream_t stream);
+size_t sk_grouped_workspace_bytes(int E, int topk, int M, int N, int K);   // 0 if the kernel cannot take it
+int launch_sk_grouped(const SkParams& p, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 unsigned take_status_sk(cudaStream_t stream);
 
 // Host quantiser (cbq_pack.cpp).

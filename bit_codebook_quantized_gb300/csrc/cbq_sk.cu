@@ -164,15 +164,49 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 }
 
 // Unit geometry of an N x K weight in the tile-ordered code stream.  Unit
-// u = t * KT + c is k-tile c of 128-row tile t; positions inside the loops
-// advance incrementally (no division per unit).
-struct Geo {
+// u = T * KT + c is k-tile c of tile T; positions inside the loops advance
+// incrementally (no division per unit).  Grouped calls number the tiles of
+// the experts the routing uses one after the other (T = i * tiles + t: tile
+// t of the i-th used expert, used[i]); a dense call is one expert.
+//
+// Division by the tile count is by multiplication (Granlund and Montgomery,
+// "Division by invariant integers using multiplication", 1994): with
+// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1, n / d equals
+// (mulhi(n, m) + n) >> l for every n < 2^31.
+struct FastDiv {
+  uint32_t d, m, l;
+  __device__ __forceinline__ void init(uint32_t dd) {
+    d = dd;
+    l = 0;
+    while ((1ull << l) < dd) ++l;
+    m = static_cast<uint32_t>(((1ull << 32) * ((1ull << l) - dd)) / dd + 1);
+  }
+  __device__ __forceinline__ int div(int n) const {
+    return static_cast<int>((__umulhi(static_cast<uint32_t>(n), m) + static_cast<uint32_t>(n)) >> l);
+  }
+};
+
+template <bool GROUPED>
+struct GeoT {
   int N, K, KT;                       // KT = k-tiles per row
+  int tiles;                          // 128-row tiles per expert
   long long U, G;                     // units, CTAs
-  __device__ __forceinline__ int rows(int t) const { return min(kRows, N - kRows * t); }
-  // byte offset of unit (t, c): tile t at 48 K t, k-tile block c at c * rows * 48
-  __device__ __forceinline__ long long off(int t, int c) const {
-    return 48LL * K * t + static_cast<long long>(c) * rows(t) * 48;
+  const uint16_t* used;               // grouped: the used experts, ascending
+  long long eb;                       // grouped: code bytes per expert, 3 K N / 8
+  FastDiv by_tiles;                   // grouped: division by tiles
+  __device__ __forceinline__ int local_tile(int T) const { return GROUPED ? T - by_tiles.div(T) * tiles : T; }
+  __device__ __forceinline__ int expert(int T) const { return GROUPED ? used[by_tiles.div(T)] : 0; }
+  __device__ __forceinline__ int rows(int T) const { return min(kRows, N - kRows * local_tile(T)); }
+  // weight row (of the stacked experts) of row r of tile T
+  __device__ __forceinline__ long long row_of(int T, int r) const {
+    return GROUPED ? static_cast<long long>(expert(T)) * N + kRows * local_tile(T) + r
+                   : static_cast<long long>(kRows) * T + r;
+  }
+  // byte offset of unit (T, c) in the code stream: the expert's codes, tile
+  // t at 48 K t, k-tile block c at c * rows * 48
+  __device__ __forceinline__ long long off(int T, int c) const {
+    const long long base = GROUPED ? expert(T) * eb : 0;
+    return base + 48LL * K * local_tile(T) + static_cast<long long>(c) * rows(T) * 48;
   }
   __device__ __forceinline__ void advance(int& t, int& c, int n) const {
     c += n;
@@ -186,8 +220,14 @@ struct Geo {
   __device__ __forceinline__ long long owner(long long u) const { return ((u + 1) * G + U - 1) / U - 1; }
 };
 
-template <int NTOK, bool GATE_UP>
+// Routing of a grouped call in shared memory: used-expert bit mask, the used
+// experts (ascending), a copy of topk_idx, their count.
+constexpr int kMaxRouted = 512;                       // M x topk <= 64 x 8
+constexpr int kRouteBytes = 128 * 4 + kMaxRouted * 2 + kMaxRouted * 4 + 128;
+
+template <int NTOK, bool GATE_UP, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__ SkParams p) {
+  static_assert(!(GATE_UP && GROUPED), "one epilogue");
   using TM = TmemMap<NTOK>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int NS = p.stages;                             // code stages
@@ -206,20 +246,13 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
+  uint8_t* route_s = reinterpret_cast<uint8_t*>(bars) + kBarBytes;   // GROUPED: routing
+  uint32_t* umask = reinterpret_cast<uint32_t*>(route_s);
+  uint16_t* used_s = reinterpret_cast<uint16_t*>(umask + 128);
+  int32_t* topk_s = reinterpret_cast<int32_t*>(used_s + kMaxRouted);
+  volatile int* n_used_s = reinterpret_cast<volatile int*>(topk_s + kMaxRouted);
   const long long wait_ns = p.wait_ns;
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  Geo geo;
-  geo.N = p.N;
-  geo.K = p.K;
-  geo.KT = p.K / 128;
-  geo.U = static_cast<long long>((p.N + kRows - 1) / kRows) * geo.KT;
-  geo.G = gridDim.x;
-  const int KT = geo.KT;
-  const long long u0 = geo.first_unit(blockIdx.x), u1 = geo.first_unit(blockIdx.x + 1LL);
-  const int n_units = static_cast<int>(u1 - u0);
-  const int n_stages = (n_units + kUnitsPerStage - 1) / kUnitsPerStage;
-  const int t_first = static_cast<int>(u0 / KT), c_first = static_cast<int>(u0 % KT);
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -242,6 +275,67 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     fence_barrier_init();
   }
   __syncthreads();
+
+  // ---- grouped: the experts the routing uses (every CTA reads the routing)
+  int n_used = 1;
+  if constexpr (GROUPED) {
+    const int nw = (p.E + 31) >> 5, nr = p.M * p.topk;
+    for (int w = tid; w < nw; w += kThreads) umask[w] = 0;
+    grid_dependency_wait();                            // the routing, written by an earlier kernel
+    __syncthreads();
+    for (int i = tid; i < nr; i += kThreads) {
+      const int e = p.topk_idx[i];
+      topk_s[i] = e;
+      if (e >= 0 && e < p.E) atomicOr(&umask[e >> 5], 1u << (e & 31));
+      else raise(kErrRouting);                         // its outputs are not written
+    }
+    __syncthreads();
+    for (int i = tid; i < nr; i += kThreads) {         // each token lists distinct experts
+      const int row0 = (i / p.topk) * p.topk;
+      for (int j = row0; j < i; ++j)
+        if (topk_s[j] == topk_s[i]) raise(kErrRouting);
+    }
+    if (warp == 0) {                                   // ascending list of the set bits
+      int base = 0;
+      for (int w0 = 0; w0 < nw; w0 += 32) {
+        const int w = w0 + lane;
+        const uint32_t bits = w < nw ? umask[w] : 0u;
+        const int cnt = __popc(bits);
+        int incl = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        int at = base + incl - cnt;
+        for (uint32_t b = bits; b; b &= b - 1) used_s[at++] = static_cast<uint16_t>(32 * w + __ffs(b) - 1);
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) *n_used_s = base;
+    }
+    __syncthreads();
+    n_used = *n_used_s;
+  }
+
+  GeoT<GROUPED> geo;
+  geo.N = p.N;
+  geo.K = p.K;
+  geo.KT = p.K / 128;
+  geo.tiles = (p.N + kRows - 1) / kRows;
+  geo.by_tiles.init(static_cast<uint32_t>(geo.tiles));
+  geo.U = static_cast<long long>(n_used) * geo.tiles * geo.KT;
+  // shares over at most U CTAs, so that every sharing CTA has a unit (a
+  // grouped call is planned for the most experts its routing can name; with
+  // fewer, the CTAs from G on have no share)
+  geo.G = geo.U < static_cast<long long>(gridDim.x) ? (geo.U > 0 ? geo.U : 1) : static_cast<long long>(gridDim.x);
+  geo.used = used_s;
+  geo.eb = 3LL * p.K * p.N / 8;
+  const int KT = geo.KT;
+  const long long b0 = blockIdx.x, b1 = blockIdx.x + 1LL;
+  const long long u0 = geo.first_unit(b0 < geo.G ? b0 : geo.G), u1 = geo.first_unit(b1 < geo.G ? b1 : geo.G);
+  const int n_units = static_cast<int>(u1 - u0);
+  const int n_stages = (n_units + kUnitsPerStage - 1) / kUnitsPerStage;
+  const int t_first = static_cast<int>(u0 / KT), c_first = static_cast<int>(u0 % KT);
   // The next kernel on the stream may start its prologue (and, if it is this
   // one, its weight stream) as soon as SMs free up; whatever this grid reads
   // from or writes for earlier kernels waits on grid_dependency_wait below.
@@ -258,10 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       const uint64_t pol = l2_evict_first_policy();
       for (int j = 0; j < n_stages; ++j) {
         const int nu = min(kUnitsPerStage, n_units - j * kUnitsPerStage);
-        int tl = ta, cl = ca;
-        geo.advance(tl, cl, nu - 1);                   // last unit of the stage
-        const long long oa = geo.off(ta, ca);
-        const uint32_t bytes = static_cast<uint32_t>(geo.off(tl, cl) + geo.rows(tl) * 48LL - oa);
+        const int ts = ta, cs = ca;                     // first unit of the stage
         geo.advance(ta, ca, kUnitsPerStage);
         if (j >= NS) {
           // the slot's previous stage must be decoded, and its copy landed
@@ -270,8 +361,38 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           if (!wait_bounded(&empty[slot], ph ^ 1u, abort_flag, wait_ns)) break;
           wait_drain(&full[slot], ph ^ 1u);
         }
-        mbar_arrive_expect_tx(&full[slot], bytes);
-        bulk_g2s(codes_s + slot * kStageBytes, p.codes + oa, bytes, &full[slot], pol);
+        if constexpr (!GROUPED) {
+          // one contiguous piece of the stream
+          int tl = ts, cl = cs;
+          geo.advance(tl, cl, nu - 1);                 // last unit of the stage
+          const long long oa = geo.off(ts, cs);
+          const uint32_t bytes = static_cast<uint32_t>(geo.off(tl, cl) + geo.rows(tl) * 48LL - oa);
+          mbar_arrive_expect_tx(&full[slot], bytes);
+          bulk_g2s(codes_s + slot * kStageBytes, p.codes + oa, bytes, &full[slot], pol);
+        } else {
+          // the stage's units in runs of one expert each (each run contiguous
+          // in the stacked codes), back to back in the stage
+          uint32_t total = 0;
+          {
+            int tr = ts, cr = cs;
+            for (int k = 0; k < nu; ++k, geo.advance(tr, cr, 1)) total += geo.rows(tr) * 48;
+          }
+          mbar_arrive_expect_tx(&full[slot], total);
+          int tr = ts, cr = cs, left = nu;
+          uint32_t dst = 0;
+          while (left > 0) {
+            const int run_e = geo.by_tiles.div(tr);
+            const long long src = geo.off(tr, cr);
+            uint32_t run = 0;
+            while (left > 0 && geo.by_tiles.div(tr) == run_e) {
+              run += geo.rows(tr) * 48;
+              geo.advance(tr, cr, 1);
+              --left;
+            }
+            bulk_g2s(codes_s + slot * kStageBytes + dst, p.codes + src, run, &full[slot], pol);
+            dst += run;
+          }
+        }
         ++issued;
         if (++slot == NS) {
           slot = 0;
@@ -379,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       auto load_sc = [&](int t, int c, bool valid, uint32_t& sw, uint2& cb) {
         sw = 0x7F7F7F7Fu;
         cb = make_uint2(0, 0);
-        const int n = t * kRows + r;
-        if (valid && n < p.N) {
+        if (valid && geo.local_tile(t) * kRows + r < p.N) {
+          const long long n = geo.row_of(t, r);          // row of the (stacked) weight
           sw = __ldg(reinterpret_cast<const uint32_t*>(p.scales + static_cast<size_t>(n) * gk + 4 * c));
           cb = __ldg(reinterpret_cast<const uint2*>(p.codebooks + static_cast<size_t>(n) * 8));
         }
@@ -409,11 +530,28 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, c2v = c0;
         const int rows_t = geo.rows(t);
         if (r < rows_t) {
-          // the pos units before this one in the stage: min(pos, c) of them in
-          // tile t (rows_t rows each; t may be the ragged last tile), the rest
-          // in full tiles before it
-          const int kin = min(pos, c);
-          const uint32_t at = codes_base + slot * kStageBytes + (kin * rows_t + (pos - kin) * kRows + r) * 48;
+          // rows of the pos units before this one in the stage: min(pos, c)
+          // of them in tile t (rows_t rows each; t may be the ragged last
+          // tile), the rest in full tiles before it -- or, grouped, in the
+          // last tile of the previous expert, which may be ragged too
+          int before;
+          if constexpr (!GROUPED) {
+            const int kin = min(pos, c);
+            before = kin * rows_t + (pos - kin) * kRows;
+          } else {
+            before = 0;
+            int tp = t, cp = c;
+            for (int k = 0; k < pos; ++k) {
+              if (cp == 0) {
+                cp = KT - 1;
+                --tp;
+              } else {
+                --cp;
+              }
+              before += geo.rows(tp);
+            }
+          }
+          const uint32_t at = codes_base + slot * kStageBytes + (before + r) * 48;
           c0 = lds128(at);
           c1 = lds128(at + 16);
           c2v = lds128(at + 32);
@@ -479,8 +617,26 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       // c0..c0+15 = token rows): y = a_scale * v, or the gate-up product.
       // Every epilogue thread calls it (it may hold named barriers).
       auto emit = [&](int t, int c0, const float (&v)[16]) {
-        const int n = t * kRows + r;
-        if constexpr (!GATE_UP) {
+        if constexpr (GROUPED) {
+          // y[m][j][n] for every slot j where token m chose this tile's expert:
+          // lane k works out token c0 + k's slots, every lane learns them
+          const int e = geo.expert(t);
+          const int nl = geo.local_tile(t) * kRows + r;
+          uint32_t mask = 0;
+          if (lane < 16 && c0 + lane < p.M)
+            for (int j = 0; j < p.topk; ++j)
+              if (topk_s[(c0 + lane) * p.topk + j] == e) mask |= 1u << j;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            uint32_t mk = __shfl_sync(0xffffffffu, mask, k);
+            if (nl < p.N && mk) {
+              const float yv = v[k] * __ldg(p.a_scale + c0 + k);
+              for (; mk; mk &= mk - 1)
+                p.y[(static_cast<size_t>(c0 + k) * p.topk + (__ffs(mk) - 1)) * p.N + nl] = yv;
+            }
+          }
+        } else if constexpr (!GATE_UP) {
+          const int n = t * kRows + r;
           if (n < p.N) {
 #pragma unroll
             for (int k = 0; k < 16; ++k)
@@ -742,22 +898,30 @@ constexpr int kMaxTiles = 1 << 16;                    // N <= 8388608 rows
 constexpr size_t kCountersBytes = static_cast<size_t>(kMaxTiles) * 4;
 constexpr size_t kFixedBytes = kCountersBytes + 64 * 4;
 
-bool plan_for(int M, int N, int K, bool gate_up, Plan& pl) {
+enum Mode { kDense, kGateUp, kGrouped };
+
+// Grouped calls: E experts stacked, each N x K; at most min(E, M topk) of
+// them are used (the kernel finds which), and the plan is made for that many.
+bool plan_for(int M, int N, int K, Mode mode, Plan& pl, int E = 1, int topk = 1) {
   if (M < 1 || M > 64 || N < 1 || K < 128 || K % 128 != 0) return false;
+  if (mode == kGrouped && (E < 1 || E > 4096 || topk < 1 || topk > 8 || M * topk > kMaxRouted)) return false;
   const int KT = K / 128;
-  const long long tiles = (N + kRows - 1) / kRows;
+  const long long experts = mode == kGrouped ? std::min<long long>(E, static_cast<long long>(M) * topk) : 1;
+  const long long tiles = experts * ((N + kRows - 1) / kRows);
   if (tiles > kMaxTiles) return false;
   const long long U = tiles * KT;
   // Stream-K shares (an equal number of units per CTA, tiles split between
   // CTAs) -- except where the tiles alone fill most of the GPU: then one
   // whole tile per CTA, which needs no partial-tile fix-up (decode 4096 x
   // 12288: 96 tiles on 152 SMs, 11.4-11.8 us against 12.1-12.3 us per call).
+  // A grouped call's unit count is known on the device only: shares.
   const long long sms = device_sm_count();
-  const long long G = (tiles <= sms && 5 * tiles >= 3 * sms) ? tiles : std::min<long long>(U, sms);
+  const long long G = (mode != kGrouped && tiles <= sms && 5 * tiles >= 3 * sms) ? tiles : std::min<long long>(U, sms);
   const long long per = (U + G - 1) / G;               // most units of any CTA
   pl.ntok = ntok_for(M);
   pl.b_ktiles = static_cast<int>(std::min<long long>(KT, per));
-  const int fixed = pl.b_ktiles * pl.ntok * 128 + (gate_up ? kXchgBytes : 0) + kBarBytes;
+  const int fixed = pl.b_ktiles * pl.ntok * 128 + (mode == kGateUp ? kXchgBytes : 0) + kBarBytes +
+                    (mode == kGrouped ? kRouteBytes : 0);
   pl.stages = std::min(kMaxStages, (kMaxSmem - fixed) / kStageBytes);
   if (pl.stages < 2) return false;
   pl.smem = std::max(pl.stages * kStageBytes + fixed, kMinSmem);
@@ -774,13 +938,14 @@ size_t workspace_bytes(const Plan& pl, int M, int F) {
 }
 
 // cudaFuncSetAttribute once per (device, kernel).
-template <int NTOK, bool GATE_UP>
+template <int NTOK, bool GATE_UP, bool GROUPED>
 int configure() {
   static std::atomic<int> done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CBQ_EDEVICE;
   if (done[dev].load(std::memory_order_acquire)) return CBQ_OK;
-  if (cudaFuncSetAttribute(sk_kernel<NTOK, GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
+  if (cudaFuncSetAttribute(sk_kernel<NTOK, GATE_UP, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxSmem) !=
       cudaSuccess)
     return CBQ_ECUDA;
   done[dev].store(1, std::memory_order_release);
@@ -807,10 +972,11 @@ cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, int smem, c
   return e;
 }
 
-template <int NTOK, bool GATE_UP>
+template <int NTOK, bool GATE_UP, bool GROUPED>
 int launch_t(const SkParams& p, const Plan& pl, cudaStream_t stream) {
-  if (const int st = configure<NTOK, GATE_UP>(); st != CBQ_OK) return st;
-  return launch_pdl(sk_kernel<NTOK, GATE_UP>, dim3(pl.grid), dim3(kThreads), pl.smem, stream, p) == cudaSuccess
+  if (const int st = configure<NTOK, GATE_UP, GROUPED>(); st != CBQ_OK) return st;
+  return launch_pdl(sk_kernel<NTOK, GATE_UP, GROUPED>, dim3(pl.grid), dim3(kThreads), pl.smem, stream, p) ==
+                 cudaSuccess
              ? CBQ_OK
              : CBQ_ECUDA;
 }
@@ -832,7 +998,7 @@ int encode_a_map(SkParams& p, int ntok) {
              : CBQ_ECUDA;
 }
 
-int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigned* counters, bool gate_up,
+int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigned* counters, Mode mode,
                    cudaStream_t stream) {
   SkParams p = p_in;
   p.partial = partial;
@@ -841,14 +1007,19 @@ int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigne
   p.b_ktiles = pl.b_ktiles;
   const int em = encode_a_map(p, pl.ntok);
   if (em != CBQ_OK) return em;
-  if (gate_up) {
-    if (pl.ntok == 16) return launch_t<16, true>(p, pl, stream);
-    if (pl.ntok == 32) return launch_t<32, true>(p, pl, stream);
-    return launch_t<64, true>(p, pl, stream);
+  if (mode == kGateUp) {
+    if (pl.ntok == 16) return launch_t<16, true, false>(p, pl, stream);
+    if (pl.ntok == 32) return launch_t<32, true, false>(p, pl, stream);
+    return launch_t<64, true, false>(p, pl, stream);
   }
-  if (pl.ntok == 16) return launch_t<16, false>(p, pl, stream);
-  if (pl.ntok == 32) return launch_t<32, false>(p, pl, stream);
-  return launch_t<64, false>(p, pl, stream);
+  if (mode == kGrouped) {
+    if (pl.ntok == 16) return launch_t<16, false, true>(p, pl, stream);
+    if (pl.ntok == 32) return launch_t<32, false, true>(p, pl, stream);
+    return launch_t<64, false, true>(p, pl, stream);
+  }
+  if (pl.ntok == 16) return launch_t<16, false, false>(p, pl, stream);
+  if (pl.ntok == 32) return launch_t<32, false, false>(p, pl, stream);
+  return launch_t<64, false, false>(p, pl, stream);
 }
 
 // Static scratch of the allocation-free entry point: partial tiles for up to
@@ -863,34 +1034,49 @@ __device__ __align__(256) unsigned g_static_counters[kStaticTiles];
 
 bool sk_applicable(int M, int N, int K) {
   Plan pl;
-  return plan_for(M, N, K, false, pl);
+  return plan_for(M, N, K, kDense, pl);
 }
 
 size_t sk_workspace_bytes(int M, int N, int K) {
   Plan pl;
-  return plan_for(M, N, K, false, pl) ? workspace_bytes(pl, M, 0) : 0;
+  return plan_for(M, N, K, kDense, pl) ? workspace_bytes(pl, M, 0) : 0;
 }
 
 size_t sk_gate_up_workspace_bytes(int M, int F, int K) {
   Plan pl;
-  return plan_for(M, 2 * F, K, true, pl) ? workspace_bytes(pl, M, F) : 0;
+  return plan_for(M, 2 * F, K, kGateUp, pl) ? workspace_bytes(pl, M, F) : 0;
 }
 
 int launch_sk(const SkParams& p_in, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   Plan pl;
-  if (!plan_for(p_in.M, p_in.N, p_in.K, false, pl)) return CBQ_EINVAL;
+  if (!plan_for(p_in.M, p_in.N, p_in.K, kDense, pl)) return CBQ_EINVAL;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < workspace_bytes(pl, p_in.M, 0))
     return CBQ_EINVAL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   return launch_planned(p_in, pl, reinterpret_cast<float*>(ws + kFixedBytes), reinterpret_cast<unsigned*>(ws),
-                        false, stream);
+                        kDense, stream);
+}
+
+size_t sk_grouped_workspace_bytes(int E, int topk, int M, int N, int K) {
+  Plan pl;
+  return plan_for(M, N, K, kGrouped, pl, E, topk) ? workspace_bytes(pl, M, 0) : 0;
+}
+
+int launch_sk_grouped(const SkParams& p_in, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  Plan pl;
+  if (!plan_for(p_in.M, p_in.N, p_in.K, kGrouped, pl, p_in.E, p_in.topk)) return CBQ_EINVAL;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < workspace_bytes(pl, p_in.M, 0))
+    return CBQ_EINVAL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return launch_planned(p_in, pl, reinterpret_cast<float*>(ws + kFixedBytes), reinterpret_cast<unsigned*>(ws),
+                        kGrouped, stream);
 }
 
 int launch_sk_gate_up(const SkParams& p_in, void* workspace, size_t ws_bytes, uint8_t* q, float* q_scale,
                       cudaStream_t stream) {
   Plan pl;
   const int F = p_in.N / 2;
-  if (p_in.N % 2 != 0 || !plan_for(p_in.M, p_in.N, p_in.K, true, pl)) return CBQ_EINVAL;
+  if (p_in.N % 2 != 0 || !plan_for(p_in.M, p_in.N, p_in.K, kGateUp, pl)) return CBQ_EINVAL;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       ws_bytes < workspace_bytes(pl, p_in.M, F))
     return CBQ_EINVAL;
@@ -900,7 +1086,7 @@ int launch_sk_gate_up(const SkParams& p_in, void* workspace, size_t ws_bytes, ui
   p.h_amax = reinterpret_cast<unsigned*>(ws + kCountersBytes);
   p.h = reinterpret_cast<float*>(ws + kFixedBytes + partial_bytes(pl));
   const int st = launch_planned(p, pl, reinterpret_cast<float*>(ws + kFixedBytes), reinterpret_cast<unsigned*>(ws),
-                                true, stream);
+                                kGateUp, stream);
   if (st != CBQ_OK) return st;
   return launch_pdl(gate_up_quant_kernel, dim3(p.M), dim3(1024), 0, stream, static_cast<const float*>(p.h),
                     p.h_amax, F, q, q_scale) == cudaSuccess
@@ -910,7 +1096,7 @@ int launch_sk_gate_up(const SkParams& p_in, void* workspace, size_t ws_bytes, ui
 
 int launch_sk_static(const SkParams& p_in, cudaStream_t stream) {
   Plan pl;
-  if (!plan_for(p_in.M, p_in.N, p_in.K, false, pl)) return CBQ_EINVAL;
+  if (!plan_for(p_in.M, p_in.N, p_in.K, kDense, pl)) return CBQ_EINVAL;
   if (pl.grid > kStaticCtas || pl.tiles > kStaticTiles) return CBQ_EINVAL;
   // the static buffers' addresses on the current device (looked up on the
   // first call on each device)
@@ -938,7 +1124,7 @@ int launch_sk_static(const SkParams& p_in, cudaStream_t stream) {
   // the counters of the tiles this call uses start at zero even if an
   // earlier call gave up part-way
   if (cudaMemsetAsync(counters, 0, sizeof(unsigned) * pl.tiles, stream) != cudaSuccess) return CBQ_ECUDA;
-  return launch_planned(p_in, pl, static_cast<float*>(partial), static_cast<unsigned*>(counters), false, stream);
+  return launch_planned(p_in, pl, static_cast<float*>(partial), static_cast<unsigned*>(counters), kDense, stream);
 }
 
 unsigned take_status_sk(cudaStream_t stream) {

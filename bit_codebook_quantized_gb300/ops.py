@@ -27,8 +27,8 @@ OK, EINVAL, ECUDA, EDEVICE, ETIMEOUT, EROUTING = 0, -1, -2, -3, -4, -5
 EXPORTS = ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_ws", "cbq_gemm_workspace_size",
            "cbq_gemm_path", "cbq_gemm_auto_path", "cbq_gemm_noalloc", "cbq_set_wait_limit",
            "cbq_gemm_gate_up", "cbq_gate_up_workspace_size",
-           "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_launch_count",
-           "cbq_status_str", "cbq_draft_length", "cbq_select_budget")
+           "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_grouped_gemm_ws", "cbq_grouped_workspace_size",
+           "cbq_device_status", "cbq_launch_count", "cbq_status_str", "cbq_draft_length", "cbq_select_budget")
 
 
 class CbqError(RuntimeError):
@@ -72,6 +72,9 @@ def lib() -> ctypes.CDLL:
                                        i32, vp, vp]
         L.cbq_grouped_gemm_path.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, vp, i32, i32,
                                             i32, i32, vp, vp, i32]
+        L.cbq_grouped_gemm_ws.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, vp, i32, i32, i32, i32, vp, vp,
+                                          sz, vp, i32]
+        L.cbq_grouped_workspace_size.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
         L.cbq_device_status.argtypes = [vp]
         L.cbq_launch_count.argtypes = []
         L.cbq_launch_count.restype = ctypes.c_uint64
@@ -83,8 +86,8 @@ def lib() -> ctypes.CDLL:
         for name in ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_ws",
                      "cbq_gemm_workspace_size", "cbq_gemm_path", "cbq_gemm_auto_path", "cbq_gemm_noalloc",
                      "cbq_set_wait_limit", "cbq_gemm_gate_up", "cbq_gate_up_workspace_size",
-                     "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_device_status", "cbq_draft_length",
-                     "cbq_select_budget"):
+                     "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_grouped_gemm_ws",
+                     "cbq_grouped_workspace_size", "cbq_device_status", "cbq_draft_length", "cbq_select_budget"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
         return L
@@ -274,17 +277,31 @@ def gemm_noalloc(a: torch.Tensor, a_scale: torch.Tensor, w: PackedWeights,
     return out
 
 
+def grouped_workspace_size(E: int, topk: int, M: int, N: int, K: int) -> int:
+    """Bytes of workspace a grouped stream-K call needs (0: it cannot take the shape)."""
+    b = ctypes.c_size_t()
+    _check(lib().cbq_grouped_workspace_size(E, topk, M, N, K, ctypes.byref(b)), "cbq_grouped_workspace_size")
+    return b.value
+
+
 def grouped_gemm(a: torch.Tensor, a_scale: torch.Tensor, experts: PackedWeights, E: int,
                  topk_idx: torch.Tensor, out: torch.Tensor | None = None,
-                 path: int = PATH_AUTO, stream=None) -> torch.Tensor:
-    """y[M, topk, N] for stacked experts (experts.N = rows per expert)."""
+                 path: int = PATH_AUTO, stream=None, workspace="auto") -> torch.Tensor:
+    """y[M, topk, N] for stacked experts (experts.N = rows per expert).
+    workspace: "auto" (a cached one per device and stream, for the paths
+    that use it), None (no workspace: cbq_grouped_gemm_path) or a device
+    tensor."""
     M, topk = topk_idx.shape
     if out is None:
         out = torch.empty((M, topk, experts.N), dtype=torch.float32, device=a.device)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    if isinstance(workspace, str):
+        need = grouped_workspace_size(E, topk, M, experts.N, experts.K) if path == PATH_STREAMK else 0
+        workspace = workspace_for(a.device, st, need) if need > 0 else None
     ws = experts.struct()
-    _check(lib().cbq_grouped_gemm_path(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(ws), E,
-                                       topk_idx.data_ptr(), topk, M, experts.N, experts.K,
-                                       out.data_ptr(), _stream(stream), path),
+    wp, wb = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
+    _check(lib().cbq_grouped_gemm_ws(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(ws), E, topk_idx.data_ptr(),
+                                     topk, M, experts.N, experts.K, out.data_ptr(), wp, wb, _stream(st), path),
            "cbq_grouped_gemm")
     return out
 

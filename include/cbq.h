@@ -57,18 +57,20 @@ extern "C" {
 #define CBQ_EROUTING (-5)    /* grouped call: an expert id outside [0,E) or a
                                 token listing one expert twice was seen */
 
-/* Which kernel cbq_gemm_path / cbq_grouped_gemm_path runs. */
+/* Which kernel cbq_gemm_path / cbq_grouped_gemm_ws runs. */
 #define CBQ_PATH_AUTO 0      /* dense: see cbq_gemm_auto_path; grouped:
                                 M <= 4 GEMV, else the tile kernel */
 #define CBQ_PATH_GEMV 1      /* register-decode + warp MMA kernel, any M <= 64 */
 #define CBQ_PATH_MMA 2       /* tcgen05 block-scaled FP8 tile kernel (K split
                                 over a cluster), any M <= 64 */
-#define CBQ_PATH_STREAMK 3   /* dense only: tcgen05 kernel with an equal
-                                contiguous share of the weights per SM; needs
-                                ntok(M) * min(K/128, share) * 128 bytes of
-                                activations to fit next to a 3-stage ring
-                                (ntok = 16/32/64), and a caller workspace of
-                                cbq_gemm_workspace_size bytes, else CBQ_EINVAL */
+#define CBQ_PATH_STREAMK 3   /* tcgen05 kernel with an equal contiguous share
+                                of the weights per SM; needs ntok(M) *
+                                min(K/128, share) * 128 bytes of activations
+                                to fit next to a 2-stage ring (ntok =
+                                16/32/64), and a caller workspace of
+                                cbq_gemm_workspace_size (dense) or
+                                cbq_grouped_workspace_size (grouped) bytes,
+                                else CBQ_EINVAL */
 
 /* One packed matrix in device memory (all three arrays 16-byte aligned). */
 typedef struct cbq_weight {
@@ -229,12 +231,36 @@ int cbq_grouped_gemm(const uint8_t *a, const float *a_scale,
                      const int32_t *topk_idx, int32_t topk, int32_t M,
                      int32_t N, int32_t K, float *y, void *stream);
 
-/* Same as cbq_grouped_gemm with an explicit kernel choice (CBQ_PATH_*). */
+/* Same as cbq_grouped_gemm with an explicit kernel choice (CBQ_PATH_GEMV or
+ * CBQ_PATH_MMA; CBQ_PATH_STREAMK needs a workspace: cbq_grouped_gemm_ws). */
 int cbq_grouped_gemm_path(const uint8_t *a, const float *a_scale,
                           const cbq_weight_t *experts, int32_t E,
                           const int32_t *topk_idx, int32_t topk, int32_t M,
                           int32_t N, int32_t K, float *y, void *stream,
                           int32_t path);
+
+/* Workspace of a grouped stream-K call: bytes for (E, topk, M, N, K), 0 if
+ * the stream-K kernel cannot take the shape.  Arguments as in
+ * cbq_grouped_gemm.  Errors: CBQ_EINVAL. */
+int cbq_grouped_workspace_size(int32_t E, int32_t topk, int32_t M, int32_t N,
+                               int32_t K, size_t *bytes);
+
+/* cbq_grouped_gemm with a caller-owned DEVICE workspace (the same layout and
+ * rules as cbq_gemm_ws's: 256-byte aligned, at least
+ * cbq_grouped_workspace_size bytes, its first 256 KB zero-filled once before
+ * first use, one call at a time) and a kernel choice.  CBQ_PATH_STREAMK runs
+ * the stream-K kernel (CBQ_PATH_AUTO picks as cbq_grouped_gemm does):
+ * every SM takes an equal contiguous share of the (used expert, tile,
+ * k-tile) units of the experts the routing names -- each used expert
+ * multiplied by all M token rows, only the routed (token, slot) outputs
+ * written.  workspace may be NULL for the other paths.  No allocation.
+ * Errors: CBQ_EINVAL, CBQ_EDEVICE, CBQ_ECUDA; routing errors as in
+ * cbq_grouped_gemm (reported by cbq_device_status). */
+int cbq_grouped_gemm_ws(const uint8_t *a, const float *a_scale,
+                        const cbq_weight_t *experts, int32_t E,
+                        const int32_t *topk_idx, int32_t topk, int32_t M,
+                        int32_t N, int32_t K, float *y, void *workspace,
+                        size_t workspace_bytes, void *stream, int32_t path);
 
 /* Diagnostic: every kernel launched after this call gives up a bounded wait
  * (for a copy, a tensor-core result or another role of its block) after `ns`

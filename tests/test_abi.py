@@ -67,6 +67,14 @@ def test_argument_errors_before_device(L):
     assert L.cbq_grouped_gemm(16, 16, p, 0, 16, 1, 1, 8, 128, 16, None) == ops.EINVAL
     assert L.cbq_grouped_gemm(16, 16, p, 4, 16, 9, 1, 8, 128, 16, None) == ops.EINVAL
     assert L.cbq_grouped_gemm(16, 16, p, 4, 16, 5, 1, 8, 128, 16, None) == ops.EINVAL
+    # grouped stream-K needs a workspace; workspace sizes of valid shapes only
+    assert L.cbq_grouped_gemm_path(16, 16, p, 4, 16, 2, 1, 8, 128, 16, None, ops.PATH_STREAMK) == ops.EINVAL
+    assert L.cbq_grouped_gemm_ws(16, 16, p, 4, 16, 2, 1, 8, 128, 16, None, 0, None, 4) == ops.EINVAL
+    assert L.cbq_grouped_gemm_ws(16, 16, p, 4, 16, 9, 1, 8, 128, 16, None, 0, None, 0) == ops.EINVAL
+    assert L.cbq_grouped_workspace_size(4, 2, 1, 8, 96, ctypes.byref(n)) == ops.EINVAL
+    assert L.cbq_grouped_workspace_size(0, 1, 1, 8, 128, ctypes.byref(n)) == ops.EINVAL
+    assert L.cbq_grouped_workspace_size(4, 2, 1, 8, 128, None) == ops.EINVAL
+    assert L.cbq_grouped_workspace_size(4, 2, 0, 8, 128, ctypes.byref(n)) == ops.OK and n.value == 0
     assert L.cbq_unpack(p, 8, 100, 16, None) == ops.EINVAL
     # expert budget: k in [1, B], B <= E <= 4096, T >= 1, outputs present and aligned
     assert L.cbq_select_budget(16, 4, 12, 0, 4, 16, 16, None) == ops.EINVAL
@@ -183,6 +191,10 @@ def test_workspace_size_covers_counters_and_partials(L):
     assert n.value == fixed + 2 * 1 * 128 * 16 * 4 + 8 * 6144 * 4
     assert L.cbq_gemm_workspace_size(64, 5120, 25600, ctypes.byref(n)) == ops.OK
     assert n.value == 0                       # no kernel with a workspace takes it
+    # grouped: the same layout, planned for min(E, M topk) used experts
+    assert L.cbq_grouped_workspace_size(128, 8, 64, 1536, 2048, ctypes.byref(n)) == ops.OK
+    assert n.value == fixed + 2 * 1 * 128 * 64 * 4
+    assert L.cbq_grouped_workspace_size(5000, 8, 64, 1536, 2048, ctypes.byref(n)) == ops.EINVAL
 
 
 def test_library_pack_matches_the_hand_worked_lloyd_row(golden_dir):

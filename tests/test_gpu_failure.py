@@ -57,7 +57,8 @@ def test_gemv_and_tile_kernel_give_up_then_the_next_call_is_exact(path):
     assert ops.device_status() == ops.OK
 
 
-def test_grouped_gives_up_then_the_next_call_is_exact():
+@pytest.mark.parametrize("path", [ops.PATH_MMA, ops.PATH_STREAMK])
+def test_grouped_gives_up_then_the_next_call_is_exact(path):
     E, N, K, M = 12, 200, 512, 16
     pw = synth.gen_weights(E * N, K, 41)
     a = synth.gen_activations(M, K, 42)
@@ -67,12 +68,12 @@ def test_grouped_gives_up_then_the_next_call_is_exact():
     da, ds, di = torch.from_numpy(a).cuda(), torch.from_numpy(s).cuda(), torch.from_numpy(idx).cuda()
     ops.set_wait_limit(2)
     try:
-        ops.grouped_gemm(da, ds, w, E, di, path=ops.PATH_MMA)
+        ops.grouped_gemm(da, ds, w, E, di, path=path)
         torch.cuda.synchronize()
     finally:
         ops.set_wait_limit(0)
     assert ops.device_status() == ops.ETIMEOUT
-    y = ops.grouped_gemm(da, ds, w, E, di, path=ops.PATH_MMA)
+    y = ops.grouped_gemm(da, ds, w, E, di, path=path)
     torch.cuda.synchronize()
     import oracle
     yref, b, _ = oracle.grouped_gemm(a, s, pw.codes, pw.scales, pw.codebooks, E, idx, M, N, K)

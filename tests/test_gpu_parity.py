@@ -14,7 +14,7 @@ from tests.gpu_util import Case, assert_close, ensure_built, sample_rows
 pytestmark = pytest.mark.gpu
 
 PATHS = [ops.PATH_GEMV, ops.PATH_MMA, ops.PATH_STREAMK]
-GROUPED_PATHS = [ops.PATH_GEMV, ops.PATH_MMA]
+GROUPED_PATHS = [ops.PATH_GEMV, ops.PATH_MMA, ops.PATH_STREAMK]
 
 
 @pytest.fixture(scope="module", autouse=True)
