@@ -329,6 +329,9 @@ def run_ours(args):
             "algorithmic_bytes_per_launch": int(dom_bytes), "peak_source": peak_src,
             "share_of_step": round(sum(per_m_us[M] for M in fam[dom]) / sum(per_m_us.values()), 3)}
 
+    # ---- the floor of one launch that only reads the same bytes ----------------
+    floor = run_read_floor(stream, copies, peak, calls=min(250, max(20, args.steps)))
+
     # ---- every workload of the specification, >= 200 graphed calls each ------
     per_config = None
     if args.per_config_calls > 0:
@@ -360,7 +363,7 @@ def run_ours(args):
                              f"({ROTATE * weight_bytes() / 1e6:.0f} MB) vs 129 MB L2",
                        "timing": f"per-M CUDA graphs of {S} calls, {reps} rounds; {kernel_timing}",
                        "parallelism": f"replicas x{ws}"},
-            "roofline": roof, "per_call": per_call,
+            "roofline": roof, "per_call": per_call, "read_floor": floor,
             "e2e": e2e, "cpu_baseline": cpu, "per_config": per_config,
             "gpu_launches": int(launches_per_step * args.steps),
             "clocks": clk.summary(),
@@ -563,6 +566,39 @@ def run_gate_up_points(dev, stream, peak, calls, l2):
     return points
 
 
+def run_read_floor(stream, copies, peak, calls=250):
+    """Where one launch's floor is on this workload: a read-only reduction
+    (torch.sum of the codes read as float32, one library launch per call) over the
+    code bytes of one call, on the same rotating copies and timed the same way
+    as the calls (a CUDA graph of back-to-back launches, CUDA events around
+    PC_REPS replays).  Its bytes / time is what a single launch that streams
+    these bytes and does nothing else reaches."""
+    views = [w.codes.view(torch.float32) for w in copies]
+    out = torch.empty((), dtype=torch.float32, device=views[0].device)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            torch.sum(views[i % len(views)], dim=0, out=out)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(calls):
+            torch.sum(views[i % len(views)], dim=0, out=out)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(PC_REPS + 1)]
+    with torch.cuda.stream(stream):
+        g.replay()
+        ev[0].record(stream)
+        for r in range(PC_REPS):
+            g.replay()
+            ev[r + 1].record(stream)
+    stream.synchronize()
+    us = ev[0].elapsed_time(ev[-1]) * 1e3 / (PC_REPS * calls)
+    nbytes = views[0].numel() * 4
+    return {"op": "torch.sum of one call's code bytes read as float32 (read-only, one launch per call)",
+            "bytes": nbytes, "us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
+            "frac": round(nbytes / us / 1e3 / peak, 4), "calls": calls,
+            "copies": len(copies)}
+
+
 def run_e2e_eager(dev, stream, copies, steps):
     """The e2e step without CUDA graphs: every step copies the inputs from
     pinned host memory, calls cbq_gemm for M = 1, 2, 4, 8 from the host (one
@@ -720,7 +756,7 @@ def main(argv=None):
                     help="--impl reference: CPU seconds the whole run should take")
     ap.add_argument("--single", default=None,
                     help="run --calls calls of one workload (see synth.workloads()) and exit")
-    ap.add_argument("--path", type=int, default=0, help="kernel for --single: 0 auto, 1 gemv, 2 mma")
+    ap.add_argument("--path", type=int, default=0, help="kernel for --single: 0 auto, 1 gemv, 2 mma, 3 stream-K")
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--per-config-calls", type=int, default=250,
                     help="graphed calls per point of the all-workload leg (0 disables)")
