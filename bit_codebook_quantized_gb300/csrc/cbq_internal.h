@@ -58,6 +58,10 @@ struct SkParams {
   long long wait_ns;          // bounded waits give up after this many ns
   float* h;                   // gate-up only: workspace products h [M][F] fp32
   unsigned* h_amax;           // gate-up only: workspace running max |h| per token (fp32 bits)
+  unsigned* h_done;           // gate-up only: workspace count of CTAs whose products are written
+  uint8_t* q;                 // gate-up only: E4M3 products [M][F] out
+  float* q_scale;             // gate-up only: per-token scales [M] out
+  int fuse_quant;             // gate-up only: the last CTA quantises (else a second kernel does)
   int M, N, K;
   int F;                      // gate-up only: features, N / 2
   int stages;                 // depth of the code-stage ring

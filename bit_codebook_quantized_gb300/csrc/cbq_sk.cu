@@ -49,7 +49,11 @@
 // tile's rows).  The CTA that finishes a tile pairs gate row r with up row
 // r + R/2 through shared memory, writes h = SiLU(a_scale g) * (a_scale u) to
 // the workspace as fp32 and raises the token's running max |h| with an atomic
-// max; gate_up_quant_kernel then turns h into E4M3 with the scale max/448.
+// max.  Up to kFusedQuant products, the CTA that finishes last (a
+// release-acquire count of finished CTAs in the workspace) then turns every
+// product into E4M3 with its token's scale max/448, with all its threads, and
+// returns the maxima and the count to zero; beyond that (one SM would read
+// too many products) gate_up_quant_kernel does it, one CTA per token.
 //
 // Bounded waits: every mbarrier wait gives up after the call's wait limit and
 // raises the CTA's abort flag; later waits of the CTA then give up at once.
@@ -851,6 +855,13 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         s0 = i + 1;
       }
       if (leader && n_units > 0) wait_drain(b_full, 0);   // the activations landed before the CTA can end
+      if constexpr (GATE_UP) {
+        // every product and maximum of this CTA is written: one release-
+        // acquire add after a barrier counts the CTA; the last one learns
+        // that all CTAs' are visible
+        named_bar_sync(2, 128);
+        if (leader) *last_flag = p.fuse_quant && atom_add_acq_rel_gpu(p.h_done, 1u) == gridDim.x - 1u;
+      }
     }
   }
 
@@ -859,6 +870,53 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   // waited for its TMEM loads.
   tc_fence_before();
   __syncthreads();
+  if constexpr (GATE_UP) {
+    if (*last_flag) {
+      // The last CTA: per token the scale s = max|h| / 448 (1 for an
+      // all-zero token), then every product h / s to E4M3 (nearest even,
+      // saturating), all threads over each token's row; then the maxima and
+      // the count go back to zero for the next call.
+      float* s_tok = xchg;                           // [M] scales
+      if (tid < p.M) {
+        const float a = __uint_as_float(__ldcg(p.h_amax + tid));
+        const float sc = a > 0.f ? a / 448.f : 1.f;
+        s_tok[tid] = sc;
+        p.q_scale[tid] = sc;
+      }
+      __syncthreads();
+      // the M x F products as one flat array (rows are contiguous in h and
+      // q): four float4 loads in flight per thread, token of element i = i / F
+      FastDiv by_f;
+      by_f.init(static_cast<uint32_t>(p.F));
+      const int total = p.M * p.F, n4 = total >> 2;
+      const float4* h4 = reinterpret_cast<const float4*>(p.h);
+      for (int i0 = tid; i0 < n4; i0 += 4 * kThreads) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (i0 + u * kThreads < n4) v[u] = __ldcg(h4 + i0 + u * kThreads);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = i0 + u * kThreads;
+          if (j < n4) {
+            const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int i = 4 * j + c;
+              p.q[i] = static_cast<uint8_t>(
+                  __nv_cvt_float_to_fp8(e[c] / s_tok[by_f.div(i)], __NV_SATFINITE, __NV_E4M3));
+            }
+          }
+        }
+      }
+      for (int i = 4 * n4 + tid; i < total; i += kThreads)   // the last total % 4 products
+        p.q[i] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(__ldcg(p.h + i) / s_tok[by_f.div(i)], __NV_SATFINITE,
+                                                             __NV_E4M3));
+      __syncthreads();
+      if (tid < p.M) p.h_amax[tid] = 0u;
+      if (tid == 0) *p.h_done = 0u;
+    }
+  }
   if (warp == kAllocWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
@@ -886,6 +944,9 @@ __global__ void __launch_bounds__(1024) gate_up_quant_kernel(const float* __rest
   if (threadIdx.x == 0) amax[m] = 0u;
 }
 
+// Products up to which the last CTA of the matmul quantises them itself.
+constexpr int kFusedQuant = 1 << 13;
+
 struct Plan {
   int ntok = 0, grid = 0, stages = 0, b_ktiles = 0, smem = 0, tiles = 0;
 };
@@ -896,7 +957,7 @@ struct Plan {
 // another shape expects zeros.
 constexpr int kMaxTiles = 1 << 16;                    // N <= 8388608 rows
 constexpr size_t kCountersBytes = static_cast<size_t>(kMaxTiles) * 4;
-constexpr size_t kFixedBytes = kCountersBytes + 64 * 4;
+constexpr size_t kFixedBytes = kCountersBytes + 512;  // + gate-up maxima [64], finished-CTA count
 
 enum Mode { kDense, kGateUp, kGrouped };
 
@@ -1084,10 +1145,14 @@ int launch_sk_gate_up(const SkParams& p_in, void* workspace, size_t ws_bytes, ui
   SkParams p = p_in;
   p.F = F;
   p.h_amax = reinterpret_cast<unsigned*>(ws + kCountersBytes);
+  p.h_done = reinterpret_cast<unsigned*>(ws + kCountersBytes + 256);
   p.h = reinterpret_cast<float*>(ws + kFixedBytes + partial_bytes(pl));
+  p.q = q;
+  p.q_scale = q_scale;
+  p.fuse_quant = static_cast<long long>(p.M) * F <= kFusedQuant ? 1 : 0;
   const int st = launch_planned(p, pl, reinterpret_cast<float*>(ws + kFixedBytes), reinterpret_cast<unsigned*>(ws),
                                 kGateUp, stream);
-  if (st != CBQ_OK) return st;
+  if (st != CBQ_OK || p.fuse_quant) return st;
   return launch_pdl(gate_up_quant_kernel, dim3(p.M), dim3(1024), 0, stream, static_cast<const float*>(p.h),
                     p.h_amax, F, q, q_scale) == cudaSuccess
              ? CBQ_OK

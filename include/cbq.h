@@ -131,8 +131,9 @@ int cbq_gemm_workspace_size(int32_t M, int32_t N, int32_t K, size_t *bytes);
  * the stream-K kernel runs where it fits: every SM streams an equal contiguous
  * share of the packed weights and a 128-row tile split between SMs is summed
  * through the workspace, in a fixed order (the result is deterministic).
- * The workspace starts with a fixed area of tile counters (the first 256 KB,
- * the same for every shape); that area must be zero-filled before the
+ * The workspace starts with a fixed area (the first 262 656 bytes = 256.5 KB,
+ * the same for every shape: tile counters, and the gate-up step's per-token
+ * maxima and finished-CTA count); that area must be zero-filled before the
  * workspace's first use (cudaMemset) and every call leaves it zero again, so
  * one workspace serves calls of any shape in turn.  Calls that share one workspace must not run at
  * the same time (one workspace per stream).  The stream-K kernel is launched
@@ -163,9 +164,10 @@ int cbq_gemm_ws(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
  *   h_scale  DEVICE fp32 [M] out
  *   workspace, workspace_bytes: as for cbq_gemm_ws, at least
  *            cbq_gate_up_workspace_size bytes (it also holds h in fp32)
- * Two launches on `stream` (the stream-K matmul with the SiLU-product
- * epilogue, then the per-token quantisation), each a programmatic dependent
- * of the kernel before it.
+ * One launch on `stream` up to M * F = 8192 products (the stream-K matmul
+ * with the SiLU-product epilogue; the CTA that finishes last quantises every
+ * product), else two (a per-token quantisation kernel follows); each a
+ * programmatic dependent of the kernel before it.
  * Errors: CBQ_EINVAL (also when the stream-K kernel cannot take the shape:
  * the size query then gives 0), CBQ_EDEVICE, CBQ_ECUDA. */
 int cbq_gemm_gate_up(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
@@ -247,7 +249,7 @@ int cbq_grouped_workspace_size(int32_t E, int32_t topk, int32_t M, int32_t N,
 
 /* cbq_grouped_gemm with a caller-owned DEVICE workspace (the same layout and
  * rules as cbq_gemm_ws's: 256-byte aligned, at least
- * cbq_grouped_workspace_size bytes, its first 256 KB zero-filled once before
+ * cbq_grouped_workspace_size bytes, its first 256.5 KB zero-filled once before
  * first use, one call at a time) and a kernel choice.  CBQ_PATH_STREAMK runs
  * the stream-K kernel (CBQ_PATH_AUTO picks as cbq_grouped_gemm does):
  * every SM takes an equal contiguous share of the (used expert, tile,

@@ -177,11 +177,11 @@ def test_auto_path_choice(L):
 
 
 def test_workspace_size_covers_counters_and_partials(L):
-    # a fixed area of 65536 4-byte tile counters and 64 4-byte token maxima
-    # (the same for every shape), then two partial tiles of 128 x ntok fp32 per
-    # CTA (the plan here sees no device: 1 CTA); the gate-up call adds M x F
-    # fp32 products
-    fixed = 65536 * 4 + 64 * 4
+    # a fixed area of 65536 4-byte tile counters, 64 4-byte token maxima and a
+    # finished-CTA count (512 bytes after the counters; the same for every
+    # shape), then two partial tiles of 128 x ntok fp32 per CTA (the plan here
+    # sees no device: 1 CTA); the gate-up call adds M x F fp32 products
+    fixed = 65536 * 4 + 512
     n = ctypes.c_size_t()
     assert L.cbq_gemm_workspace_size(8, 12288, 4096, ctypes.byref(n)) == ops.OK
     assert n.value == fixed + 2 * 1 * 128 * 16 * 4
