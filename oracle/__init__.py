@@ -85,6 +85,14 @@ def configure(lib):
         lib.orc_grouped_gemm.restype = None
         lib.orc_pack.argtypes = [f32p, i64, i64, u8p, u8p, u8p]
         lib.orc_pack.restype = None
+        lib.orc_group_offset2.argtypes = [i64, i64, i64, i64]
+        lib.orc_group_offset2.restype = i64
+        lib.orc_code2.argtypes = [u8p, i64, i64, i64, i64]
+        lib.orc_code2.restype = ctypes.c_int
+        lib.orc_gemm2.argtypes = [u8p, f32p, u8p, u8p, u8p, i64, i64, i64, f32p, f64p]
+        lib.orc_gemm2.restype = None
+        lib.orc_rescore8.argtypes = [u8p, f32p, u8p, f32p, i64, i64, i64, i32p, i64, f32p, f64p]
+        lib.orc_rescore8.restype = None
         lib.orc_num_threads.argtypes = []
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_set_num_threads.argtypes = [ctypes.c_int]

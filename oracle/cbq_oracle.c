@@ -248,6 +248,112 @@ void orc_grouped_gemm(const uint8_t *a, const float *a_scale,
     free(touched);
 }
 
+/* ---- two-bit draft head ------------------------------------------------- */
+/*
+ * "Hibana: Fast Agentic Inference on Unified-Memory Devices", section "Model
+ * surgery / Two-bit draft head": the drafter's vocabulary head is stored in
+ * 2 bits, scores every token, keeps a shortlist of 16 and rescores the
+ * shortlist with the FP8 head.  The pages fix neither the 2-bit format nor
+ * the FP8 head's; the readings taken here mirror the 3-bit format:
+ *   codes2     : one group (n, g = k/32) is 8 bytes, read as a 64-bit
+ *                little-endian number with code j = k%32 at bits 2j..2j+1;
+ *                groups in 128-row tiles as for 3 bits, with 32 bytes per row
+ *                and k-tile (8 per group): tile t starts at byte 128t * K/4,
+ *                k-tile c of a tile with R rows at c*R*32, row n%128 at
+ *                (n%128)*W (W = 8 x the k-tile's groups), group g%4 at (g%4)*8.
+ *                Total KN/4 bytes.
+ *   scales2    : uint8 [N][K/32], E8M0 (2^(s-127)).
+ *   codebooks2 : uint8 [N][4], E4M3.
+ *   2 + 8/32 = 2.25 bits per weight.
+ *   head8      : the FP8 head, uint8 E4M3 [N][K] row-major, with one fp32
+ *                scale per row: w8[n,k] = E4M3(head8[n,k]) * row_scale[n].
+ */
+int64_t orc_group_offset2(int64_t N, int64_t K, int64_t n, int64_t g)
+{
+    int64_t t = n / 128;
+    int64_t R = (N - 128 * t < 128) ? N - 128 * t : 128;
+    int64_t tile_base = 128 * t * (K / 4);
+    int64_t c = g / 4;
+    int64_t G = K / 32;
+    int64_t W = (G - 4 * c < 4) ? 8 * (G - 4 * c) : 32;
+    return tile_base + c * R * 32 + (n % 128) * W + (g % 4) * 8;
+}
+
+/* Code of weight (n, k): bits 2j, 2j+1 of the 64-bit little-endian group. */
+int orc_code2(const uint8_t *codes, int64_t N, int64_t K, int64_t n, int64_t k)
+{
+    int64_t base = orc_group_offset2(N, K, n, k / 32);
+    int j = (int)(k % 32);
+    int code = 0;
+    for (int i = 0; i < 2; i++) {
+        int pos = 2 * j + i;
+        int bit = (codes[base + pos / 8] >> (pos % 8)) & 1;
+        code |= bit << i;
+    }
+    return code;
+}
+
+/* Dequantised weight of the 2-bit head, exact. */
+double orc_weight2(const uint8_t *codes, const uint8_t *scales,
+                   const uint8_t *codebooks, int64_t N, int64_t K, int64_t n, int64_t k)
+{
+    int c = orc_code2(codes, N, K, n, k);
+    return orc_e4m3_value(codebooks[n * 4 + c]) *
+           orc_e8m0_value(scales[n * (K / 32) + k / 32]);
+}
+
+/* Scores of the 2-bit head: s[m,n] = a_scale[m] * sum_k a[m,k] w2[n,k]
+ * (sum in k order in double, one rounding to fp32), and the bound base
+ * |a_scale| * sum |a w2|, as orc_gemm. */
+void orc_gemm2(const uint8_t *a, const float *a_scale,
+               const uint8_t *codes, const uint8_t *scales,
+               const uint8_t *codebooks, int64_t M, int64_t N, int64_t K,
+               float *y, double *bound)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; n++) {
+        for (int64_t m = 0; m < M; m++) {
+            double acc = 0.0, accabs = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                double p = orc_e4m3_value(a[m * K + k]) *
+                           orc_weight2(codes, scales, codebooks, N, K, n, k);
+                acc += p;
+                accabs += fabs(p);
+            }
+            y[m * N + n] = (float)((double)a_scale[m] * acc);
+            if (bound)
+                bound[m * N + n] = fabs((double)a_scale[m]) * accabs;
+        }
+    }
+}
+
+/* FP8 rescoring of chosen rows: for token m and its rows rows[m][i]
+ * (i < R), logit = a_scale[m] * row_scale[n] * sum_k a[m,k] E4M3(head8[n,k])
+ * (sum in k order in double, then the two scales, one rounding to fp32), and
+ * the bound base |a_scale * row_scale| * sum |a w8|. */
+void orc_rescore8(const uint8_t *a, const float *a_scale, const uint8_t *head8,
+                  const float *row_scale, int64_t M, int64_t N, int64_t K,
+                  const int32_t *rows, int64_t R, float *logits, double *bound)
+{
+    for (int64_t m = 0; m < M; m++) {
+        for (int64_t i = 0; i < R; i++) {
+            int64_t n = rows[m * R + i];
+            double acc = 0.0, accabs = 0.0;
+            if (n >= 0 && n < N) {
+                for (int64_t k = 0; k < K; k++) {
+                    double p = orc_e4m3_value(a[m * K + k]) * orc_e4m3_value(head8[n * K + k]);
+                    acc += p;
+                    accabs += fabs(p);
+                }
+            }
+            double sc = (double)a_scale[m] * (double)((n >= 0 && n < N) ? row_scale[n] : 0.0f);
+            logits[m * R + i] = (float)(sc * acc);
+            if (bound)
+                bound[m * R + i] = fabs(sc) * accabs;
+        }
+    }
+}
+
 /* ---- pack (quantiser) -------------------------------------------------- */
 /*
  * The pages state only that each 32-weight group is mapped onto an 8-entry
