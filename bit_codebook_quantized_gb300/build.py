@@ -16,7 +16,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcbq.so")
 ROOT = os.path.dirname(PKG)
 
-SOURCES = ["cbq_api.cu", "cbq_sk.cu", "cbq_gemv.cu", "cbq_umma.cu", "cbq_budget.cu", "cbq_pack.cpp", "cbq_draft.cpp"]
+SOURCES = ["cbq_api.cu", "cbq_sk.cu", "cbq_gemv.cu", "cbq_umma.cu", "cbq_budget.cu", "cbq_head.cu", "cbq_pack.cpp",
+           "cbq_draft.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-ffp-contract=off", "-Xcompiler", "-Wall",

@@ -409,6 +409,85 @@ int cbq_grouped_gemm(const uint8_t* a, const float* a_scale, const cbq_weight_t*
                                CBQ_PATH_AUTO);
 }
 
+// ---- two-bit draft head ---------------------------------------------------
+
+int cbq_head2_sizes(int32_t N, int32_t K, size_t* codes_bytes, size_t* scales_bytes, size_t* codebook_bytes) {
+  if (N < 0 || K < 0 || K % 128 != 0 || !codes_bytes || !scales_bytes || !codebook_bytes) return CBQ_EINVAL;
+  *codes_bytes = static_cast<size_t>(K) * N / 4;
+  *scales_bytes = static_cast<size_t>(K) * N / 32;
+  *codebook_bytes = static_cast<size_t>(4) * N;
+  return CBQ_OK;
+}
+
+int cbq_gemm2_ws(const uint8_t* a, const float* a_scale, const cbq_weight_t* head2, int32_t M, int32_t N, int32_t K,
+                 float* y, void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 0 || M > 64 || N < 0 || K < 0 || K % 128 != 0) return CBQ_EINVAL;
+  if (M == 0 || N == 0) return CBQ_OK;
+  if (!y || !aligned(y, 4)) return CBQ_EINVAL;
+  int st = current_device_checked(nullptr);
+  if (st != CBQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0)
+    return cudaMemsetAsync(y, 0, sizeof(float) * size_t(M) * size_t(N), s) == cudaSuccess ? CBQ_OK : CBQ_ECUDA;
+  if (!a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(head2) || !sk_applicable(M, N, K))
+    return CBQ_EINVAL;
+  SkParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.codes = head2->codes;
+  p.a = a;
+  p.a_scale = a_scale;
+  p.scales = head2->scales;
+  p.codebooks = head2->codebooks;
+  p.y = y;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.wait_ns = wait_limit_ns();
+  return launch_sk(p, workspace, workspace_bytes, s, 2);
+}
+
+namespace {
+// Draft-head workspace: [the stream-K workspace][scores M x N fp32]
+// [chunk candidates M x chunks x 16 x 8 bytes], each part 256-byte aligned.
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+size_t head_parts(int M, int N, int K, size_t* sk, size_t* scores) {
+  *sk = round256(sk_workspace_bytes(M, N, K));
+  *scores = round256(static_cast<size_t>(M) * N * sizeof(float));
+  int chunk = 0;
+  const int nchunks = head_chunking(N, &chunk);
+  return *sk == 0 ? 0 : *sk + *scores + round256(static_cast<size_t>(M) * nchunks * kHeadShortlist * 8);
+}
+}  // namespace
+
+int cbq_draft_head_workspace_size(int32_t M, int32_t N, int32_t K, size_t* bytes) {
+  if (!bytes || M < 1 || M > 64 || N < kHeadShortlist || K < 128 || K % 128 != 0) return CBQ_EINVAL;
+  size_t sk = 0, sc = 0;
+  *bytes = head_parts(M, N, K, &sk, &sc);
+  return CBQ_OK;
+}
+
+int cbq_draft_head(const uint8_t* a, const float* a_scale, const cbq_weight_t* head2, const uint8_t* head8,
+                   const float* row_scale, int32_t M, int32_t N, int32_t K, int32_t* shortlist, float* logits,
+                   int32_t* pick, void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 1 || M > 64 || N < kHeadShortlist || K < 128 || K % 128 != 0) return CBQ_EINVAL;
+  if (!a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(head2) || !head8 ||
+      !aligned(head8, 16) || !row_scale || !aligned(row_scale, 4) || !shortlist || !aligned(shortlist, 4) ||
+      !logits || !aligned(logits, 4) || !pick || !aligned(pick, 4) || !workspace || !aligned(workspace, 256))
+    return CBQ_EINVAL;
+  size_t sk = 0, sc = 0;
+  const size_t need = head_parts(M, N, K, &sk, &sc);
+  if (need == 0 || workspace_bytes < need) return CBQ_EINVAL;
+  int st = current_device_checked(nullptr);
+  if (st != CBQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* scores = reinterpret_cast<float*>(ws + sk);
+  st = cbq_gemm2_ws(a, a_scale, head2, M, N, K, scores, ws, sk, stream);
+  if (st != CBQ_OK) return st;
+  return launch_head_select(scores, M, N, K, a, a_scale, head8, row_scale, reinterpret_cast<uint64_t*>(ws + sk + sc),
+                            shortlist, logits, pick, s);
+}
+
 int cbq_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return CBQ_ECUDA;

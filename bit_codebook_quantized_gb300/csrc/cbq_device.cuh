@@ -67,6 +67,36 @@ __device__ __forceinline__ void decode_group(uint32_t w0, uint32_t w1, uint32_t 
   v[7] = lookup4(cb_lo, cb_hi, s3 >> 16);
 }
 
+// Two-bit codes (the draft head's format: code j of a 32-weight group at bits
+// 2j..2j+1 of its 64-bit little-endian group).  Spread the 8 codes in bits
+// 0..15 of f (bits 16..31 ignored) so that code j lands in nibble j (bits
+// 4j, 4j+1; bits 4j+2, 4j+3 clear): three steps that each move the upper
+// half of every field up by half the field's width, with a mask and a
+// multiply-add (no two moved pieces overlap, so the adds carry nothing).
+__device__ __forceinline__ uint32_t spread_codes2x8(uint32_t f) {
+  uint32_t h = f & 0x0000FFFFu;
+  h += (h & 0x0000FF00u) * 255u;                  // codes 4-7 up by 8 bits
+  h += (h & 0x00F000F0u) * 15u;                   // codes 2, 3 and 6, 7 up by 4
+  h += (h & 0x0C0C0C0Cu) * 3u;                    // odd codes up by 2
+  return h;
+}
+
+// Decode one two-bit group (two 32-bit words, 32 codes) into 32 E4M3 bytes
+// through the row's 4-entry codebook (one register): v[0..7] = the bytes of
+// codes 0..31, four per column.
+__device__ __forceinline__ void decode_group2(uint32_t w0, uint32_t w1, uint32_t cb, uint32_t* v) {
+  const uint32_t s0 = spread_codes2x8(w0), s1 = spread_codes2x8(w0 >> 16);
+  const uint32_t s2 = spread_codes2x8(w1), s3 = spread_codes2x8(w1 >> 16);
+  v[0] = __byte_perm(cb, cb, s0);
+  v[1] = __byte_perm(cb, cb, s0 >> 16);
+  v[2] = __byte_perm(cb, cb, s1);
+  v[3] = __byte_perm(cb, cb, s1 >> 16);
+  v[4] = __byte_perm(cb, cb, s2);
+  v[5] = __byte_perm(cb, cb, s2 >> 16);
+  v[6] = __byte_perm(cb, cb, s3);
+  v[7] = __byte_perm(cb, cb, s3 >> 16);
+}
+
 // E8M0 byte -> fp32 2^(s-127) (s = 0 gives the subnormal 2^-127).
 __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
   return s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);

@@ -90,7 +90,9 @@ unsigned take_status_umma(cudaStream_t stream);
 
 bool sk_applicable(int M, int N, int K);
 size_t sk_workspace_bytes(int M, int N, int K);   // 0 if the stream-K kernel cannot take the shape
-int launch_sk(const SkParams& p, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+// bits: 3 (the 3.25-bit weights) or 2 (the two-bit draft head: 4-entry
+// codebooks [N][4], 8 code bytes per group)
+int launch_sk(const SkParams& p, void* workspace, size_t workspace_bytes, cudaStream_t stream, int bits = 3);
 int launch_sk_static(const SkParams& p, cudaStream_t stream);
 size_t sk_gate_up_workspace_bytes(int M, int F, int K);   // 0 if the kernel cannot take the shape
 int launch_sk_gate_up(const SkParams& p, void* workspace, size_t workspace_bytes, uint8_t* q, float* q_scale,
@@ -98,6 +100,16 @@ int launch_sk_gate_up(const SkParams& p, void* workspace, size_t workspace_bytes
 size_t sk_grouped_workspace_bytes(int E, int topk, int M, int N, int K);   // 0 if the kernel cannot take it
 int launch_sk_grouped(const SkParams& p, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 unsigned take_status_sk(cudaStream_t stream);
+
+// Two-bit draft head (cbq_head.cu): the 16-row shortlist of every token from
+// its 2-bit scores [M][N], the FP8 rescoring and the pick.  cand: scratch of
+// M x (row chunks) x 16 words.
+constexpr int kHeadShortlist = 16;
+constexpr int kHeadMaxChunks = 64;
+int head_chunking(int N, int* chunk);   // number of row chunks; *chunk rows each
+int launch_head_select(const float* scores, int M, int N, int K, const uint8_t* a, const float* a_scale,
+                       const uint8_t* head8, const float* row_scale, uint64_t* cand, int32_t* rows, float* logits,
+                       int32_t* pick, cudaStream_t stream);
 
 // Host quantiser (cbq_pack.cpp).
 int pack_host(const float* W, int N, int K, uint8_t* codes, uint8_t* scales,

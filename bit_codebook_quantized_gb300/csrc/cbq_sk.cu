@@ -190,8 +190,9 @@ struct FastDiv {
   }
 };
 
-template <bool GROUPED>
+template <bool GROUPED, int BITS>
 struct GeoT {
+  static constexpr int RB = BITS * 16;                // code bytes of one row of a unit (128 codes)
   int N, K, KT;                       // KT = k-tiles per row
   int tiles;                          // 128-row tiles per expert
   long long U, G;                     // units, CTAs
@@ -210,7 +211,7 @@ struct GeoT {
   // t at 48 K t, k-tile block c at c * rows * 48
   __device__ __forceinline__ long long off(int T, int c) const {
     const long long base = GROUPED ? expert(T) * eb : 0;
-    return base + 48LL * K * local_tile(T) + static_cast<long long>(c) * rows(T) * 48;
+    return base + static_cast<long long>(RB) * K * local_tile(T) + static_cast<long long>(c) * rows(T) * RB;
   }
   __device__ __forceinline__ void advance(int& t, int& c, int n) const {
     c += n;
@@ -229,9 +230,11 @@ struct GeoT {
 constexpr int kMaxRouted = 512;                       // M x topk <= 64 x 8
 constexpr int kRouteBytes = 128 * 4 + kMaxRouted * 2 + kMaxRouted * 4 + 128;
 
-template <int NTOK, bool GATE_UP, bool GROUPED>
+template <int NTOK, bool GATE_UP, bool GROUPED, int BITS>
 __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__ SkParams p) {
   static_assert(!(GATE_UP && GROUPED), "one epilogue");
+  static_assert(BITS == 3 || (BITS == 2 && !GATE_UP && !GROUPED), "two-bit codes: dense calls only");
+  constexpr int RB = BITS * 16;                         // code bytes of one row of a unit
   using TM = TmemMap<NTOK>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int NS = p.stages;                             // code stages
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     n_used = *n_used_s;
   }
 
-  GeoT<GROUPED> geo;
+  GeoT<GROUPED, BITS> geo;
   geo.N = p.N;
   geo.K = p.K;
   geo.KT = p.K / 128;
@@ -333,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   // fewer, the CTAs from G on have no share)
   geo.G = geo.U < static_cast<long long>(gridDim.x) ? (geo.U > 0 ? geo.U : 1) : static_cast<long long>(gridDim.x);
   geo.used = used_s;
-  geo.eb = 3LL * p.K * p.N / 8;
+  geo.eb = static_cast<long long>(BITS) * p.K * p.N / 8;
   const int KT = geo.KT;
   const long long b0 = blockIdx.x, b1 = blockIdx.x + 1LL;
   const long long u0 = geo.first_unit(b0 < geo.G ? b0 : geo.G), u1 = geo.first_unit(b1 < geo.G ? b1 : geo.G);
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           int tl = ts, cl = cs;
           geo.advance(tl, cl, nu - 1);                 // last unit of the stage
           const long long oa = geo.off(ts, cs);
-          const uint32_t bytes = static_cast<uint32_t>(geo.off(tl, cl) + geo.rows(tl) * 48LL - oa);
+          const uint32_t bytes = static_cast<uint32_t>(geo.off(tl, cl) + geo.rows(tl) * static_cast<long long>(RB) - oa);
           mbar_arrive_expect_tx(&full[slot], bytes);
           bulk_g2s(codes_s + slot * kStageBytes, p.codes + oa, bytes, &full[slot], pol);
         } else {
@@ -379,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           uint32_t total = 0;
           {
             int tr = ts, cr = cs;
-            for (int k = 0; k < nu; ++k, geo.advance(tr, cr, 1)) total += geo.rows(tr) * 48;
+            for (int k = 0; k < nu; ++k, geo.advance(tr, cr, 1)) total += geo.rows(tr) * RB;
           }
           mbar_arrive_expect_tx(&full[slot], total);
           int tr = ts, cr = cs, left = nu;
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
             const long long src = geo.off(tr, cr);
             uint32_t run = 0;
             while (left > 0 && geo.by_tiles.div(tr) == run_e) {
-              run += geo.rows(tr) * 48;
+              run += geo.rows(tr) * RB;
               geo.advance(tr, cr, 1);
               --left;
             }
@@ -507,7 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         if (valid && geo.local_tile(t) * kRows + r < p.N) {
           const long long n = geo.row_of(t, r);          // row of the (stacked) weight
           sw = __ldg(reinterpret_cast<const uint32_t*>(p.scales + static_cast<size_t>(n) * gk + 4 * c));
-          cb = __ldg(reinterpret_cast<const uint2*>(p.codebooks + static_cast<size_t>(n) * 8));
+          if constexpr (BITS == 3)
+            cb = __ldg(reinterpret_cast<const uint2*>(p.codebooks + static_cast<size_t>(n) * 8));
+          else
+            cb.x = __ldg(reinterpret_cast<const uint32_t*>(p.codebooks + static_cast<size_t>(n) * 4));
         }
       };
       // stage of unit i: i / 4, position i % 4; advanced by 3 units per step
@@ -555,18 +561,25 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
               before += geo.rows(tp);
             }
           }
-          const uint32_t at = codes_base + slot * kStageBytes + (before + r) * 48;
+          const uint32_t at = codes_base + slot * kStageBytes + (before + r) * RB;
           c0 = lds128(at);
           c1 = lds128(at + 16);
-          c2v = lds128(at + 32);
+          if constexpr (BITS == 3) c2v = lds128(at + 32);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
         uint32_t v[32];
-        decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
-        decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
-        decode_group(c1.z, c1.w, c2v.x, cb.x, cb.y, v + 16);
-        decode_group(c2v.y, c2v.z, c2v.w, cb.x, cb.y, v + 24);
+        if constexpr (BITS == 3) {
+          decode_group(c0.x, c0.y, c0.z, cb.x, cb.y, v);
+          decode_group(c0.w, c1.x, c1.y, cb.x, cb.y, v + 8);
+          decode_group(c1.z, c1.w, c2v.x, cb.x, cb.y, v + 16);
+          decode_group(c2v.y, c2v.z, c2v.w, cb.x, cb.y, v + 24);
+        } else {                                        // 8 bytes per group, 4-entry codebook in cb.x
+          decode_group2(c0.x, c0.y, cb.x, v);
+          decode_group2(c0.z, c0.w, cb.x, v + 8);
+          decode_group2(c1.x, c1.y, cb.x, v + 16);
+          decode_group2(c1.z, c1.w, cb.x, v + 24);
+        }
         publish();                                      // the previous unit
         const int as = g * S + su;
         wait_bounded(&a_empty[as], aph ^ 1u, abort_flag, wait_ns);   // the MMAs of its last use are done
@@ -999,13 +1012,13 @@ size_t workspace_bytes(const Plan& pl, int M, int F) {
 }
 
 // cudaFuncSetAttribute once per (device, kernel).
-template <int NTOK, bool GATE_UP, bool GROUPED>
+template <int NTOK, bool GATE_UP, bool GROUPED, int BITS>
 int configure() {
   static std::atomic<int> done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CBQ_EDEVICE;
   if (done[dev].load(std::memory_order_acquire)) return CBQ_OK;
-  if (cudaFuncSetAttribute(sk_kernel<NTOK, GATE_UP, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(sk_kernel<NTOK, GATE_UP, GROUPED, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kMaxSmem) !=
       cudaSuccess)
     return CBQ_ECUDA;
@@ -1033,10 +1046,10 @@ cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, int smem, c
   return e;
 }
 
-template <int NTOK, bool GATE_UP, bool GROUPED>
+template <int NTOK, bool GATE_UP, bool GROUPED, int BITS = 3>
 int launch_t(const SkParams& p, const Plan& pl, cudaStream_t stream) {
-  if (const int st = configure<NTOK, GATE_UP, GROUPED>(); st != CBQ_OK) return st;
-  return launch_pdl(sk_kernel<NTOK, GATE_UP, GROUPED>, dim3(pl.grid), dim3(kThreads), pl.smem, stream, p) ==
+  if (const int st = configure<NTOK, GATE_UP, GROUPED, BITS>(); st != CBQ_OK) return st;
+  return launch_pdl(sk_kernel<NTOK, GATE_UP, GROUPED, BITS>, dim3(pl.grid), dim3(kThreads), pl.smem, stream, p) ==
                  cudaSuccess
              ? CBQ_OK
              : CBQ_ECUDA;
@@ -1060,7 +1073,7 @@ int encode_a_map(SkParams& p, int ntok) {
 }
 
 int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigned* counters, Mode mode,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, int bits = 3) {
   SkParams p = p_in;
   p.partial = partial;
   p.counters = counters;
@@ -1077,6 +1090,11 @@ int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigne
     if (pl.ntok == 16) return launch_t<16, false, true>(p, pl, stream);
     if (pl.ntok == 32) return launch_t<32, false, true>(p, pl, stream);
     return launch_t<64, false, true>(p, pl, stream);
+  }
+  if (bits == 2) {
+    if (pl.ntok == 16) return launch_t<16, false, false, 2>(p, pl, stream);
+    if (pl.ntok == 32) return launch_t<32, false, false, 2>(p, pl, stream);
+    return launch_t<64, false, false, 2>(p, pl, stream);
   }
   if (pl.ntok == 16) return launch_t<16, false, false>(p, pl, stream);
   if (pl.ntok == 32) return launch_t<32, false, false>(p, pl, stream);
@@ -1108,14 +1126,14 @@ size_t sk_gate_up_workspace_bytes(int M, int F, int K) {
   return plan_for(M, 2 * F, K, kGateUp, pl) ? workspace_bytes(pl, M, F) : 0;
 }
 
-int launch_sk(const SkParams& p_in, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+int launch_sk(const SkParams& p_in, void* workspace, size_t ws_bytes, cudaStream_t stream, int bits) {
   Plan pl;
   if (!plan_for(p_in.M, p_in.N, p_in.K, kDense, pl)) return CBQ_EINVAL;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < workspace_bytes(pl, p_in.M, 0))
     return CBQ_EINVAL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   return launch_planned(p_in, pl, reinterpret_cast<float*>(ws + kFixedBytes), reinterpret_cast<unsigned*>(ws),
-                        kDense, stream);
+                        kDense, stream, bits);
 }
 
 size_t sk_grouped_workspace_bytes(int E, int topk, int M, int N, int K) {

@@ -28,7 +28,8 @@ EXPORTS = ("cbq_packed_sizes", "cbq_pack", "cbq_unpack", "cbq_gemm", "cbq_gemm_w
            "cbq_gemm_path", "cbq_gemm_auto_path", "cbq_gemm_noalloc", "cbq_set_wait_limit",
            "cbq_gemm_gate_up", "cbq_gate_up_workspace_size",
            "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_grouped_gemm_ws", "cbq_grouped_workspace_size",
-           "cbq_device_status", "cbq_launch_count", "cbq_status_str", "cbq_draft_length", "cbq_select_budget")
+           "cbq_device_status", "cbq_launch_count", "cbq_status_str", "cbq_draft_length", "cbq_select_budget",
+           "cbq_head2_sizes", "cbq_gemm2_ws", "cbq_draft_head_workspace_size", "cbq_draft_head")
 
 
 class CbqError(RuntimeError):
@@ -75,6 +76,10 @@ def lib() -> ctypes.CDLL:
         L.cbq_grouped_gemm_ws.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, vp, i32, i32, i32, i32, vp, vp,
                                           sz, vp, i32]
         L.cbq_grouped_workspace_size.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
+        L.cbq_head2_sizes.argtypes = [i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz), ctypes.POINTER(sz)]
+        L.cbq_gemm2_ws.argtypes = [vp, vp, ctypes.POINTER(_Weight), i32, i32, i32, vp, vp, sz, vp]
+        L.cbq_draft_head_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
+        L.cbq_draft_head.argtypes = [vp, vp, ctypes.POINTER(_Weight), vp, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp]
         L.cbq_device_status.argtypes = [vp]
         L.cbq_launch_count.argtypes = []
         L.cbq_launch_count.restype = ctypes.c_uint64
@@ -87,7 +92,8 @@ def lib() -> ctypes.CDLL:
                      "cbq_gemm_workspace_size", "cbq_gemm_path", "cbq_gemm_auto_path", "cbq_gemm_noalloc",
                      "cbq_set_wait_limit", "cbq_gemm_gate_up", "cbq_gate_up_workspace_size",
                      "cbq_grouped_gemm", "cbq_grouped_gemm_path", "cbq_grouped_gemm_ws",
-                     "cbq_grouped_workspace_size", "cbq_device_status", "cbq_draft_length", "cbq_select_budget"):
+                     "cbq_grouped_workspace_size", "cbq_device_status", "cbq_draft_length", "cbq_select_budget",
+                     "cbq_head2_sizes", "cbq_gemm2_ws", "cbq_draft_head_workspace_size", "cbq_draft_head"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
         return L
@@ -304,6 +310,46 @@ def grouped_gemm(a: torch.Tensor, a_scale: torch.Tensor, experts: PackedWeights,
                                      topk, M, experts.N, experts.K, out.data_ptr(), wp, wb, _stream(st), path),
            "cbq_grouped_gemm")
     return out
+
+
+def gemm2(a: torch.Tensor, a_scale: torch.Tensor, head2: PackedWeights, out: torch.Tensor | None = None,
+          stream=None, workspace="auto") -> torch.Tensor:
+    """cbq_gemm2_ws: the two-bit head's scores [M, N] (head2: codes KN/4 bytes,
+    scales [N][K/32], codebooks [N][4])."""
+    M = a.shape[0]
+    if out is None:
+        out = torch.empty((M, head2.N), dtype=torch.float32, device=a.device)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    if isinstance(workspace, str):
+        need = workspace_size(M, head2.N, head2.K) if M > 0 and head2.N > 0 else 0
+        workspace = workspace_for(a.device, st, need) if need > 0 else None
+    wp, wb = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
+    wt = head2.struct()
+    _check(lib().cbq_gemm2_ws(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(wt), M, head2.N, head2.K,
+                              out.data_ptr(), wp, wb, _stream(st)), "cbq_gemm2_ws")
+    return out
+
+
+def draft_head(a: torch.Tensor, a_scale: torch.Tensor, head2: PackedWeights, head8: torch.Tensor,
+               row_scale: torch.Tensor, stream=None, workspace="auto"):
+    """cbq_draft_head: (shortlist int32 [M, 16], FP8 logits fp32 [M, 16],
+    pick int32 [M]) of the two-bit draft head and the FP8 head."""
+    M, N, K = a.shape[0], head2.N, head2.K
+    rows = torch.empty((M, 16), dtype=torch.int32, device=a.device)
+    logits = torch.empty((M, 16), dtype=torch.float32, device=a.device)
+    pick = torch.empty(M, dtype=torch.int32, device=a.device)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    if isinstance(workspace, str):
+        b = ctypes.c_size_t()
+        _check(lib().cbq_draft_head_workspace_size(M, N, K, ctypes.byref(b)), "cbq_draft_head_workspace_size")
+        if b.value == 0:
+            raise CbqError(EINVAL, "cbq_draft_head: the stream-K kernel cannot take this shape")
+        workspace = workspace_for(a.device, st, b.value)
+    wt = head2.struct()
+    _check(lib().cbq_draft_head(a.data_ptr(), a_scale.data_ptr(), ctypes.byref(wt), head8.data_ptr(),
+                                row_scale.data_ptr(), M, N, K, rows.data_ptr(), logits.data_ptr(), pick.data_ptr(),
+                                workspace.data_ptr(), workspace.numel(), _stream(st)), "cbq_draft_head")
+    return rows, logits, pick
 
 
 def device_status(stream=None) -> int:

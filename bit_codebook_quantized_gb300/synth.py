@@ -74,6 +74,27 @@ def gen_weights(N: int, K: int, seed: int, scale_lo: int = 120, scale_hi: int = 
     return PackedWeights(codes, scales, np.ascontiguousarray(cbs), N, K)
 
 
+def gen_head2(N: int, K: int, seed: int, scale_lo: int = 120, scale_hi: int = 127) -> PackedWeights:
+    """A two-bit draft head: uniform 2-bit codes (random bytes: every 2-bit
+    field uniform over 0..3), uniform scale bytes in [scale_lo, scale_hi] and
+    one sorted 4-entry N(0,1) codebook per row, rounded to E4M3."""
+    assert K % 32 == 0
+    rng = rng_for(seed)
+    codes = rng.integers(0, 256, size=(N, K // 32 * 8), dtype=np.uint8)
+    scales = rng.integers(scale_lo, scale_hi + 1, size=(N, K // 32), dtype=np.uint8)
+    cbs = to_e4m3_bytes(np.sort(rng.standard_normal((N, 4)), axis=1)).reshape(N, 4)
+    return PackedWeights(codes, scales, np.ascontiguousarray(cbs), N, K)
+
+
+def gen_head8(N: int, K: int, seed: int) -> tuple[np.ndarray, np.ndarray]:
+    """An FP8 head: (E4M3 bytes [N, K] of N(0,1) draws, fp32 per-row scales
+    uniform in [0.01, 0.05])."""
+    rng = rng_for(seed)
+    w = to_e4m3_bytes(rng.standard_normal((N, K))).reshape(N, K)
+    rs = rng.uniform(0.01, 0.05, size=N).astype(np.float32)
+    return np.ascontiguousarray(w), rs
+
+
 def gen_activations(M: int, K: int, seed: int, half_normal: bool = False) -> np.ndarray:
     rng = rng_for(seed)
     x = rng.standard_normal((M, K))
@@ -147,3 +168,10 @@ def workloads() -> dict[str, Workload]:
         w[f"vocab_head_2048x151936_m{m}"] = Workload(f"vocab_head_2048x151936_m{m}", m, 151936,
                                                      2048)
     return w
+
+
+def draft_head_workloads() -> dict[str, Workload]:
+    """The two-bit draft head on the vocabulary-head shape (the drafter
+    proposes one token per step; M = 8 covers a batch of requests)."""
+    return {f"draft_head_2048x151936_m{m}": Workload(f"draft_head_2048x151936_m{m}", m, 151936, 2048)
+            for m in (1, 8)}

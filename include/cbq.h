@@ -264,6 +264,58 @@ int cbq_grouped_gemm_ws(const uint8_t *a, const float *a_scale,
                         int32_t N, int32_t K, float *y, void *workspace,
                         size_t workspace_bytes, void *stream, int32_t path);
 
+/* ---- Two-bit draft head ("Hibana: Fast Agentic Inference on Unified-Memory
+ * Devices", section "Model surgery / Two-bit draft head"): the drafter's
+ * vocabulary head scores every token from a 2-bit copy of its weights, keeps
+ * a shortlist of 16 and rescores only those with the FP8 head.
+ *
+ * The 2-bit head (this library's reading; the pages fix no format): per row
+ * a 4-entry E4M3 codebook, 2-bit codes (code j of a 32-weight group at bits
+ * 2j..2j+1 of its 64-bit little-endian group), one E8M0 scale per group;
+ * groups in the same tile order as the 3-bit codes with 32 bytes per row and
+ * 128-wide k-tile (8 bytes per group): 2 + 8/32 = 2.25 bits per weight.  A
+ * cbq_weight_t describes it: codes KN/4 bytes, scales [N][K/32],
+ * codebooks [N][4].  The FP8 head: head8 DEVICE uint8 E4M3 [N][K] row-major
+ * (16-byte aligned) with row_scale DEVICE fp32 [N]. */
+
+/* Byte sizes of a 2-bit head's codes, scales and codebooks.  Host only.
+ * Errors: CBQ_EINVAL (K not a multiple of 128, NULL outputs). */
+int cbq_head2_sizes(int32_t N, int32_t K, size_t *codes_bytes,
+                    size_t *scales_bytes, size_t *codebook_bytes);
+
+/* 2-bit scores s[m][n] = a_scale[m] * sum_k a[m,k] w2[n,k] (fp32 out,
+ * DEVICE [M][N]) on the stream-K kernel; the workspace is as for
+ * cbq_gemm_ws, at least cbq_gemm_workspace_size(M, N, K) bytes (required).
+ * Errors: CBQ_EINVAL (also when the stream-K kernel cannot take the shape),
+ * CBQ_EDEVICE, CBQ_ECUDA. */
+int cbq_gemm2_ws(const uint8_t *a, const float *a_scale, const cbq_weight_t *head2,
+                 int32_t M, int32_t N, int32_t K, float *y, void *workspace,
+                 size_t workspace_bytes, void *stream);
+
+/* Workspace of cbq_draft_head (0: the shape cannot be taken).  1 <= M <= 64,
+ * N >= 16, K a positive multiple of 128.  Host only.  Errors: CBQ_EINVAL. */
+int cbq_draft_head_workspace_size(int32_t M, int32_t N, int32_t K, size_t *bytes);
+
+/* The draft head's step for M token rows a (E4M3 [M][K], a_scale fp32 [M]):
+ *   shortlist DEVICE int32 [M][16]: the 16 rows with the highest 2-bit
+ *             scores, descending, equal scores -> lower row first;
+ *   logits    DEVICE fp32 [M][16]: their FP8 logits
+ *             a_scale[m] * row_scale[n] * sum_k a[m,k] E4M3(head8[n,k]);
+ *   pick      DEVICE int32 [M]: the shortlisted row with the highest logit,
+ *             equal logits -> the earlier one in the shortlist.
+ * The workspace (DEVICE, 256-byte aligned, at least
+ * cbq_draft_head_workspace_size bytes; its first 256.5 KB zero-filled once
+ * before first use and left zero by every call; one call at a time) holds
+ * the stream-K scratch, the scores and the shortlist candidates.  Three
+ * launches on `stream` (2-bit scores, per-chunk candidates, shortlist +
+ * rescoring + pick), each a programmatic dependent of the one before.
+ * Errors: CBQ_EINVAL, CBQ_EDEVICE, CBQ_ECUDA. */
+int cbq_draft_head(const uint8_t *a, const float *a_scale, const cbq_weight_t *head2,
+                   const uint8_t *head8, const float *row_scale, int32_t M,
+                   int32_t N, int32_t K, int32_t *shortlist, float *logits,
+                   int32_t *pick, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
 /* Diagnostic: every kernel launched after this call gives up a bounded wait
  * (for a copy, a tensor-core result or another role of its block) after `ns`
  * nanoseconds instead of the default 2 s, returns early and reports

@@ -24,7 +24,7 @@ def L():
 def _declared():
     text = open(os.path.join(ROOT, "include", "cbq.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(cbq_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(cbq_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(L):
