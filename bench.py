@@ -508,6 +508,57 @@ def run_per_config(dev, stream, peak, calls=250):
         del g, copies, w0, y
         torch.cuda.empty_cache()
     points += run_gate_up_points(dev, stream, peak, calls, l2)
+    points += run_draft_head_points(dev, stream, peak, calls, l2)
+    return points
+
+
+def run_draft_head_points(dev, stream, peak, calls, l2):
+    """cbq_draft_head on the vocabulary-head shape, timed like the other
+    points (the 2-bit head rotated over copies >= 4x L2; one FP8 head, of
+    which a call reads 16 rows per token).  Algorithmic bytes: the 2-bit head
+    (KN/4 + KN/32 + 4N), the FP8 rows and row scales read, the activations
+    and their scales, the shortlist, logits and picks written."""
+    points = []
+    for name, wl in synth.draft_head_workloads().items():
+        M, N, K = wl.M, wl.N, wl.K
+        h2 = synth.gen_head2(N, K, seed=1)
+        w0 = ops.PackedWeights.from_host(h2.codes, h2.scales, h2.codebooks, N, K, device=dev)
+        R = int(min(512, max(2, -(-4 * l2 // w0.nbytes))))
+        copies = [w0] + [ops.PackedWeights(w0.codes.clone(), w0.scales.clone(), w0.codebooks.clone(), N, K)
+                         for _ in range(R - 1)]
+        h8, rs = synth.gen_head8(N, K, seed=2)
+        h8, rs = torch.from_numpy(h8).to(dev), torch.from_numpy(rs).to(dev)
+        a = torch.from_numpy(synth.gen_activations(M, K, seed=3)).to(dev)
+        s = torch.from_numpy(synth.gen_a_scale(M, seed=4, mode="uniform")).to(dev)
+        run = lambda w: ops.draft_head(a, s, w, h8, rs, stream=stream)  # noqa: E731
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                run(copies[i % R])
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(calls):
+                run(copies[i % R])
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(PC_REPS + 1)]
+        with torch.cuda.stream(stream):
+            g.replay()
+            ev[0].record(stream)
+            for r in range(PC_REPS):
+                g.replay()
+                ev[r + 1].record(stream)
+        stream.synchronize()
+        if ops.device_status(stream) != ops.OK:
+            raise RuntimeError(f"device status not ok after {name}")
+        us = ev[0].elapsed_time(ev[-1]) * 1e3 / (PC_REPS * calls)
+        wb = K * N // 4 + K * N // 32 + 4 * N
+        alg = wb + M * 16 * (K + 4) + M * K + 4 * M + M * 16 * 8 + 4 * M
+        points.append({"workload": name, "M": M, "N": N, "K": K,
+                       "kernel": "sk_kernel (2-bit) + head_topk_chunk_kernel + head_select_kernel",
+                       "us": round(us, 3), "weight_GBps": round(wb / us / 1e3, 1),
+                       "roofline_frac": round(alg / us / 1e3 / peak, 4),
+                       "tokens_per_s": round(M / us * 1e6, 1), "weight_copies": R})
+        del g, copies, w0, h8
+        torch.cuda.empty_cache()
     return points
 
 
@@ -567,22 +618,23 @@ def run_gate_up_points(dev, stream, peak, calls, l2):
 
 
 def run_read_floor(stream, copies, peak, calls=250):
-    """Where one launch's floor is on this workload: a read-only reduction
-    (torch.sum of the codes read as float32, one library launch per call) over the
-    code bytes of one call, on the same rotating copies and timed the same way
-    as the calls (a CUDA graph of back-to-back launches, CUDA events around
-    PC_REPS replays).  Its bytes / time is what a single launch that streams
-    these bytes and does nothing else reaches."""
-    views = [w.codes.view(torch.float32) for w in copies]
-    out = torch.empty((), dtype=torch.float32, device=views[0].device)
+    """Where one launch's floor is on this workload: a device-to-device copy
+    (Tensor.copy_, one library launch per call) of the code bytes of one call,
+    from the same rotating copies, timed the same way as the calls (a CUDA
+    graph of back-to-back launches, CUDA events around PC_REPS replays).  It
+    moves twice the code bytes (read + write), as the measured copy peak does;
+    `read_us` is the time a launch that only reads the call's code bytes
+    would take at the copy's rate (half the copy's time)."""
+    src = [w.codes for w in copies]
+    dst = torch.empty_like(src[0])
     with torch.cuda.stream(stream):
         for i in range(3):
-            torch.sum(views[i % len(views)], dim=0, out=out)
+            dst.copy_(src[i % len(src)])
     stream.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for i in range(calls):
-            torch.sum(views[i % len(views)], dim=0, out=out)
+            dst.copy_(src[i % len(src)])
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(PC_REPS + 1)]
     with torch.cuda.stream(stream):
         g.replay()
@@ -592,10 +644,11 @@ def run_read_floor(stream, copies, peak, calls=250):
             ev[r + 1].record(stream)
     stream.synchronize()
     us = ev[0].elapsed_time(ev[-1]) * 1e3 / (PC_REPS * calls)
-    nbytes = views[0].numel() * 4
-    return {"op": "torch.sum of one call's code bytes read as float32 (read-only, one launch per call)",
-            "bytes": nbytes, "us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
-            "frac": round(nbytes / us / 1e3 / peak, 4), "calls": calls,
+    nbytes = src[0].numel()
+    moved = 2 * nbytes
+    return {"op": "Tensor.copy_ of one call's code bytes, device to device (one launch per call)",
+            "bytes": nbytes, "bytes_moved": moved, "us": round(us, 3), "read_us": round(us / 2, 3),
+            "GBps": round(moved / us / 1e3, 1), "frac": round(moved / us / 1e3 / peak, 4), "calls": calls,
             "copies": len(copies)}
 
 

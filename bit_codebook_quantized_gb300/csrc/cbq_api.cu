@@ -453,14 +453,14 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 size_t head_parts(int M, int N, int K, size_t* sk, size_t* scores) {
   *sk = round256(sk_workspace_bytes(M, N, K));
   *scores = round256(static_cast<size_t>(M) * N * sizeof(float));
-  int chunk = 0;
-  const int nchunks = head_chunking(N, &chunk);
+  const int nchunks = head_chunks(N);
   return *sk == 0 ? 0 : *sk + *scores + round256(static_cast<size_t>(M) * nchunks * kHeadShortlist * 8);
 }
 }  // namespace
 
 int cbq_draft_head_workspace_size(int32_t M, int32_t N, int32_t K, size_t* bytes) {
-  if (!bytes || M < 1 || M > 64 || N < kHeadShortlist || K < 128 || K % 128 != 0) return CBQ_EINVAL;
+  if (!bytes || M < 1 || M > 64 || N < kHeadShortlist || N > kHeadMaxRows || K < 128 || K % 128 != 0)
+    return CBQ_EINVAL;
   size_t sk = 0, sc = 0;
   *bytes = head_parts(M, N, K, &sk, &sc);
   return CBQ_OK;
@@ -469,7 +469,7 @@ int cbq_draft_head_workspace_size(int32_t M, int32_t N, int32_t K, size_t* bytes
 int cbq_draft_head(const uint8_t* a, const float* a_scale, const cbq_weight_t* head2, const uint8_t* head8,
                    const float* row_scale, int32_t M, int32_t N, int32_t K, int32_t* shortlist, float* logits,
                    int32_t* pick, void* workspace, size_t workspace_bytes, void* stream) {
-  if (M < 1 || M > 64 || N < kHeadShortlist || K < 128 || K % 128 != 0) return CBQ_EINVAL;
+  if (M < 1 || M > 64 || N < kHeadShortlist || N > kHeadMaxRows || K < 128 || K % 128 != 0) return CBQ_EINVAL;
   if (!a || !aligned(a, 16) || !a_scale || !aligned(a_scale, 4) || !weight_ok(head2) || !head8 ||
       !aligned(head8, 16) || !row_scale || !aligned(row_scale, 4) || !shortlist || !aligned(shortlist, 4) ||
       !logits || !aligned(logits, 4) || !pick || !aligned(pick, 4) || !workspace || !aligned(workspace, 256))

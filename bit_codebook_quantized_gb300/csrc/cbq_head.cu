@@ -5,17 +5,26 @@
 // token from a 2-bit copy of its weights (the stream-K kernel with 2-bit
 // codes writes the scores), keeps the 16 best and rescores only those with
 // the FP8 head.  Here:
-//  * head_topk_chunk_kernel: grid (row chunks, tokens); the 16 best (score,
-//    row) pairs of each chunk -- per lane a sorted list of 16, merged over the
-//    warp by 16 rounds of a warp-wide maximum, then over the CTA's warps;
-//  * head_select_kernel: one CTA per token; the 16 best of all chunks' lists
-//    (the shortlist: descending score, equal scores -> lower row), then each
-//    shortlisted row's FP8 logit a_scale * row_scale * sum_k a w8 (products
-//    exact in fp32, sums in fp32), and the pick: the highest logit, equal
-//    logits -> the earlier row of the shortlist.
+//  * head_topk_chunk_kernel: grid (1024-row chunks, tokens), 256 threads, four
+//    rows a thread; the 16 best (score, row) pairs of each chunk.  A
+//    threshold T that at least 16 of the chunk's pairs reach: every warp sorts
+//    its 32 lane maxima (bitonic network over shuffles), its 16th is reached by
+//    16 pairs, and T is the largest of the warps' 16ths.  The pairs >= T (at
+//    most 8 x 16 lanes x 4) go to shared memory and each finds its place among
+//    them by counting the larger ones; places 0..15 are the chunk's list.
+//  * head_select_kernel: one CTA of 16 warps per token.  The 16th largest of
+//    the chunks' first entries is reached by 16 chunks' lists, so only those
+//    chunks' entries at or above it (at most 16 x 16) can be in the
+//    shortlist; they are ranked by counting as above (the shortlist:
+//    descending score, equal scores -> lower row).  Warp i then the FP8 logit
+//    of shortlisted row i, a_scale * row_scale * sum_k a w8 (products exact in
+//    fp32, sums in fp32; all of a lane's loads in flight at once), and the
+//    pick: the highest logit, equal logits -> the earlier row of the
+//    shortlist.
 // A (score, row) pair is one 64-bit word: an order-preserving key of the fp32
 // score (-0 equals +0, NaN below every number) in the high half and
-// 2^32 - 1 - row in the low half, so "ranks before" is unsigned ">".
+// 2^32 - 1 - row in the low half, so "ranks before" is unsigned ">", no two
+// rows' words are equal and no word is 0 (0 marks an empty list entry).
 #include <cuda_runtime.h>
 
 #include <cuda_fp8.h>
@@ -30,7 +39,9 @@ namespace {
 
 constexpr int kList = kHeadShortlist;                  // 16
 constexpr int kChunkWarps = 8;
-constexpr int kSelectWarps = 4;
+constexpr int kPerThread = kHeadChunkRows / (kChunkWarps * 32);   // 4
+constexpr int kSelectWarps = kList;                    // one warp per shortlisted row
+constexpr int kSelectCand = kList * kList;             // entries of the 16 leading chunks
 
 __device__ __forceinline__ uint32_t score_key(float v) {
   if (v != v) return 0u;
@@ -43,107 +54,151 @@ __device__ __forceinline__ uint64_t pair_word(float v, int row) {
 }
 __device__ __forceinline__ int word_row(uint64_t w) { return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(w)); }
 
-__device__ __forceinline__ uint64_t warp_max64(uint64_t v) {
+// The warp's 32 words sorted descending over the lanes (lane 0 the largest):
+// a bitonic network, one compare-exchange with lane ^ j per step.
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const uint64_t o = __shfl_xor_sync(0xffffffffu, v, off);
-    v = o > v ? o : v;
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
+      const bool take_max = ((lane & j) == 0) == ((lane & k) == 0);
+      v = take_max == (o > v) ? o : v;
+    }
   }
   return v;
 }
 
-// Insert w into a descending list (called when it beats the last entry).
-__device__ __forceinline__ void insert16(uint64_t (&list)[kList], uint64_t w) {
-#pragma unroll
-  for (int i = 0; i < kList; ++i) {
-    const uint64_t hi = list[i] > w ? list[i] : w;
-    w = list[i] > w ? w : list[i];
-    list[i] = hi;
-  }
+// Append w to list[] (shared memory, count *n) for every lane whose flag is
+// set: one atomic per warp.
+__device__ __forceinline__ void warp_append(bool flag, uint64_t w, uint64_t* list, unsigned* n) {
+  const unsigned ballot = __ballot_sync(0xffffffffu, flag);
+  if (ballot == 0u) return;
+  const int lane = threadIdx.x & 31;
+  unsigned base = 0;
+  if (lane == 0) base = atomicAdd(n, static_cast<unsigned>(__popc(ballot)));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  if (flag) list[base + __popc(ballot & ((1u << lane) - 1u))] = w;
 }
 
-// The warp's 16 best words from every lane's descending list; lane 0 gets
-// them in order in out[0..15] (shared memory).
-__device__ __forceinline__ void warp_merge16(uint64_t (&list)[kList], uint64_t* out) {
-  const int lane = threadIdx.x & 31;
-  for (int r = 0; r < kList; ++r) {
-    const uint64_t m = warp_max64(list[0]);
-    if (list[0] == m && m != 0ull) {                   // the one lane that held it pops it
+// How many of list[0..n) are larger than w (eight loads in flight).
+__device__ __forceinline__ unsigned count_larger(const uint64_t* list, unsigned n, uint64_t w) {
+  unsigned c = 0;
+  for (unsigned j0 = 0; j0 < n; j0 += 8) {
+    uint64_t x[8];
 #pragma unroll
-      for (int i = 0; i + 1 < kList; ++i) list[i] = list[i + 1];
-      list[kList - 1] = 0ull;
-    }
-    if (lane == 0) out[r] = m;
+    for (unsigned u = 0; u < 8; ++u) x[u] = list[min(j0 + u, n - 1u)];
+#pragma unroll
+    for (unsigned u = 0; u < 8; ++u) c += (j0 + u < n && x[u] > w) ? 1u : 0u;
+  }
+  return c;
+}
+
+// Each of the n distinct words of list[] finds its place among them by
+// counting the larger ones; the words of places 0..15 go to out[place].
+__device__ __forceinline__ void rank_places(const uint64_t* list, unsigned n, uint64_t* out, int nthreads) {
+  for (unsigned i = threadIdx.x; i < n; i += nthreads) {
+    const uint64_t w = list[i];
+    const unsigned place = count_larger(list, n, w);
+    if (place < static_cast<unsigned>(kList)) out[place] = w;
   }
 }
 
 __global__ void __launch_bounds__(kChunkWarps * 32) head_topk_chunk_kernel(const float* __restrict__ scores, int N,
-                                                                           int chunk, uint64_t* __restrict__ cand) {
-  __shared__ uint64_t warp_best[kChunkWarps][kList];
-  __shared__ uint64_t best[kList];
+                                                                           uint64_t* __restrict__ cand) {
+  __shared__ uint64_t pool[kChunkWarps * 16 * kPerThread];
+  __shared__ uint64_t warp_t[kChunkWarps];
+  __shared__ unsigned npool;
   grid_dependency_wait();                              // the scores of the matmul kernel
-  const int m = blockIdx.y, nchunks = gridDim.x;
-  const int lo = blockIdx.x * chunk, hi = min(N, lo + chunk);
+  const int m = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lo = blockIdx.x * kHeadChunkRows;
   const float* s = scores + static_cast<size_t>(m) * N;
-  uint64_t list[kList];
+  if (threadIdx.x == 0) npool = 0;
+  uint64_t w[kPerThread], mx = 0ull;
 #pragma unroll
-  for (int i = 0; i < kList; ++i) list[i] = 0ull;      // below every real word
-  for (int n = lo + threadIdx.x; n < hi; n += kChunkWarps * 32) {
-    const uint64_t w = pair_word(__ldg(s + n), n);
-    if (w > list[kList - 1]) insert16(list, w);
+  for (int j = 0; j < kPerThread; ++j) {
+    const int n = lo + threadIdx.x + j * kChunkWarps * 32;
+    w[j] = n < N ? pair_word(__ldg(s + n), n) : 0ull;   // 0: no row
+    mx = w[j] > mx ? w[j] : mx;
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  warp_merge16(list, warp_best[warp]);
+  // 16 lanes of this warp hold a word >= its 16th largest lane maximum
+  const uint64_t t = __shfl_sync(0xffffffffu, warp_sort_desc(mx), kList - 1);
+  if (lane == 0) warp_t[warp] = t;
   __syncthreads();
-  if (warp == 0) {
-    // the CTA's 16 best of the warps' 8 x 16 words
-    uint64_t l2[kList];
+  uint64_t T = warp_t[0];
 #pragma unroll
-    for (int i = 0; i < kList; ++i) l2[i] = 0ull;
-    for (int i = lane; i < kChunkWarps * kList; i += 32) {
-      const uint64_t w = warp_best[i / kList][i % kList];
-      if (w > l2[kList - 1]) insert16(l2, w);
-    }
-    uint64_t* dst = cand + (static_cast<size_t>(m) * nchunks + blockIdx.x) * kList;
-    warp_merge16(l2, best);
-    __syncwarp();
-    if (lane < kList) dst[lane] = best[lane];
-  }
+  for (int i = 1; i < kChunkWarps; ++i) T = warp_t[i] > T ? warp_t[i] : T;
+  // at least 16 words reach T; the words >= T come from at most 16 lanes a
+  // warp (T = 0 only when no warp has 16 lanes with a row)
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) warp_append(w[j] != 0ull && w[j] >= T, w[j], pool, &npool);
+  __syncthreads();
+  const unsigned n = npool;
+  uint64_t* dst = cand + (static_cast<size_t>(m) * gridDim.x + blockIdx.x) * kList;
+  rank_places(pool, n, dst, kChunkWarps * 32);
+  if (threadIdx.x < kList && threadIdx.x >= n) dst[threadIdx.x] = 0ull;   // fewer than 16 rows
 }
 
 __global__ void __launch_bounds__(kSelectWarps * 32) head_select_kernel(
     const uint64_t* __restrict__ cand, int nchunks, const uint8_t* __restrict__ a, const float* __restrict__ a_scale,
     const uint8_t* __restrict__ head8, const float* __restrict__ row_scale, int N, int K,
     int32_t* __restrict__ rows_out, float* __restrict__ logits_out, int32_t* __restrict__ pick_out) {
+  __shared__ uint64_t lead[kHeadMaxChunks];
+  __shared__ uint64_t pool[kSelectCand];
   __shared__ uint64_t best[kList];
   __shared__ float logit_s[kList];
+  __shared__ int lead_chunk[kList];
+  __shared__ uint64_t T_s;
+  __shared__ unsigned npool;
   grid_dependency_wait();                              // the chunks' lists
   const int m = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == 0) {
-    uint64_t list[kList];
-#pragma unroll
-    for (int i = 0; i < kList; ++i) list[i] = 0ull;
-    const uint64_t* c = cand + static_cast<size_t>(m) * nchunks * kList;
-    for (int i = lane; i < nchunks * kList; i += 32) {
-      const uint64_t w = c[i];
-      if (w > list[kList - 1]) insert16(list, w);
-    }
-    warp_merge16(list, best);
-    __syncwarp();
-    if (lane < kList) rows_out[static_cast<size_t>(m) * kList + lane] = word_row(best[lane]);
+  const uint64_t* c = cand + static_cast<size_t>(m) * nchunks * kList;
+  if (threadIdx.x == 0) {
+    npool = 0;
+    T_s = 0ull;                                        // fewer than 16 chunks: every entry
+  }
+  for (int i = threadIdx.x; i < nchunks; i += kSelectWarps * 32) lead[i] = c[static_cast<size_t>(i) * kList];
+  __syncthreads();
+  // the chunks in order of their first entries (distinct: no chunk is empty);
+  // the 16 leading ones hold every entry that reaches the 16th first entry T
+  for (int i = threadIdx.x; i < nchunks; i += kSelectWarps * 32) {
+    const unsigned place = count_larger(lead, static_cast<unsigned>(nchunks), lead[i]);
+    if (place < static_cast<unsigned>(kList)) lead_chunk[place] = i;
+    if (place == kList - 1) T_s = lead[i];
   }
   __syncthreads();
-  // FP8 rescoring: warp w takes shortlisted rows w, w + 4, ...; a lane takes
-  // 16 consecutive k per step
+  const uint64_t T = T_s;
+  const int nlead = nchunks < kList ? nchunks : kList;
+  {
+    const int i = threadIdx.x;                         // entry i % 16 of leading chunk i / 16
+    const uint64_t w = i < nlead * kList ? c[static_cast<size_t>(lead_chunk[i / kList]) * kList + i % kList] : 0ull;
+    warp_append(w != 0ull && w >= T, w, pool, &npool);
+  }
+  __syncthreads();
+  rank_places(pool, npool, best, kSelectWarps * 32);
+  __syncthreads();
+  if (threadIdx.x < kList) rows_out[static_cast<size_t>(m) * kList + threadIdx.x] = word_row(best[threadIdx.x]);
+  // FP8 rescoring: warp i takes shortlisted row i; a lane takes 16
+  // consecutive k per step, four steps' loads in flight together
   const uint8_t* am = a + static_cast<size_t>(m) * K;
-  for (int i = warp; i < kList; i += kSelectWarps) {
-    const int n = word_row(best[i]);
-    const uint8_t* wn = head8 + static_cast<size_t>(n) * K;
-    float acc = 0.f;
-    for (int k = 16 * lane; k < K; k += 16 * 32) {
-      const uint4 av = __ldg(reinterpret_cast<const uint4*>(am + k));
-      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wn + k));
-      const uint32_t aw[4] = {av.x, av.y, av.z, av.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+  const int n = word_row(best[warp]);
+  const uint8_t* wn = head8 + static_cast<size_t>(n) * K;
+  float acc = 0.f;
+  for (int k0 = 16 * lane; k0 < K; k0 += 4 * 16 * 32) {
+    uint4 av[4], wv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = k0 + u * 16 * 32;
+      if (k < K) {
+        av[u] = __ldg(reinterpret_cast<const uint4*>(am + k));
+        wv[u] = __ldg(reinterpret_cast<const uint4*>(wn + k));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (k0 + u * 16 * 32 >= K) continue;
+      const uint32_t aw[4] = {av[u].x, av[u].y, av[u].z, av[u].w}, ww[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
 #pragma unroll
@@ -156,13 +211,13 @@ __global__ void __launch_bounds__(kSelectWarps * 32) head_select_kernel(
         }
       }
     }
+  }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-      const float lg = acc * (__ldg(a_scale + m) * __ldg(row_scale + n));
-      logit_s[i] = lg;
-      logits_out[static_cast<size_t>(m) * kList + i] = lg;
-    }
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    const float lg = acc * (__ldg(a_scale + m) * __ldg(row_scale + n));
+    logit_s[warp] = lg;
+    logits_out[static_cast<size_t>(m) * kList + warp] = lg;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -193,20 +248,14 @@ cudaError_t launch_pdl_head(void (*kern)(Args...), dim3 grid, dim3 block, cudaSt
 
 }  // namespace
 
-int head_chunking(int N, int* chunk) {
-  // at most kHeadMaxChunks chunks of at least 4096 rows
-  int c = 4096;
-  while ((N + c - 1) / c > kHeadMaxChunks) c *= 2;
-  *chunk = c;
-  return (N + c - 1) / c;
-}
+int head_chunks(int N) { return (N + kHeadChunkRows - 1) / kHeadChunkRows; }
 
 int launch_head_select(const float* scores, int M, int N, int K, const uint8_t* a, const float* a_scale,
                        const uint8_t* head8, const float* row_scale, uint64_t* cand, int32_t* rows, float* logits,
                        int32_t* pick, cudaStream_t stream) {
-  int chunk = 0;
-  const int nchunks = head_chunking(N, &chunk);
-  if (launch_pdl_head(head_topk_chunk_kernel, dim3(nchunks, M), dim3(kChunkWarps * 32), stream, scores, N, chunk,
+  const int nchunks = head_chunks(N);
+  if (nchunks > kHeadMaxChunks) return CBQ_EINVAL;
+  if (launch_pdl_head(head_topk_chunk_kernel, dim3(nchunks, M), dim3(kChunkWarps * 32), stream, scores, N,
                       cand) != cudaSuccess ||
       launch_pdl_head(head_select_kernel, dim3(M), dim3(kSelectWarps * 32), stream,
                       static_cast<const uint64_t*>(cand), nchunks, a, a_scale, head8, row_scale, N, K, rows, logits,

@@ -105,8 +105,10 @@ unsigned take_status_sk(cudaStream_t stream);
 // its 2-bit scores [M][N], the FP8 rescoring and the pick.  cand: scratch of
 // M x (row chunks) x 16 words.
 constexpr int kHeadShortlist = 16;
-constexpr int kHeadMaxChunks = 64;
-int head_chunking(int N, int* chunk);   // number of row chunks; *chunk rows each
+constexpr int kHeadChunkRows = 1024;
+constexpr int kHeadMaxChunks = 256;
+constexpr int kHeadMaxRows = kHeadChunkRows * kHeadMaxChunks;   // 262144 vocabulary rows
+int head_chunks(int N);                 // number of 1024-row chunks
 int launch_head_select(const float* scores, int M, int N, int K, const uint8_t* a, const float* a_scale,
                        const uint8_t* head8, const float* row_scale, uint64_t* cand, int32_t* rows, float* logits,
                        int32_t* pick, cudaStream_t stream);

@@ -479,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         __syncwarp();
         t = t2;
         c = c2;
-        bsl += kGroups;
-        if (bsl >= KT) bsl -= KT;
+        bsl += kGroups;                                  // (bsl + 3) mod KT; KT may be 1 or 2
+        while (bsl >= KT) bsl -= KT;
         if (++su == S) {
           su = 0;
           aph ^= 1u;

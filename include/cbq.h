@@ -293,7 +293,8 @@ int cbq_gemm2_ws(const uint8_t *a, const float *a_scale, const cbq_weight_t *hea
                  size_t workspace_bytes, void *stream);
 
 /* Workspace of cbq_draft_head (0: the shape cannot be taken).  1 <= M <= 64,
- * N >= 16, K a positive multiple of 128.  Host only.  Errors: CBQ_EINVAL. */
+ * 16 <= N <= 262144 (at most 256 chunks of 1024 vocabulary rows), K a
+ * positive multiple of 128.  Host only.  Errors: CBQ_EINVAL. */
 int cbq_draft_head_workspace_size(int32_t M, int32_t N, int32_t K, size_t *bytes);
 
 /* The draft head's step for M token rows a (E4M3 [M][K], a_scale fp32 [M]):
@@ -307,8 +308,9 @@ int cbq_draft_head_workspace_size(int32_t M, int32_t N, int32_t K, size_t *bytes
  * cbq_draft_head_workspace_size bytes; its first 256.5 KB zero-filled once
  * before first use and left zero by every call; one call at a time) holds
  * the stream-K scratch, the scores and the shortlist candidates.  Three
- * launches on `stream` (2-bit scores, per-chunk candidates, shortlist +
- * rescoring + pick), each a programmatic dependent of the one before.
+ * launches on `stream` (2-bit scores, the 16 best of every 1024-row chunk,
+ * shortlist + rescoring + pick), each a programmatic dependent of the one
+ * before.  Shapes as for cbq_draft_head_workspace_size.
  * Errors: CBQ_EINVAL, CBQ_EDEVICE, CBQ_ECUDA. */
 int cbq_draft_head(const uint8_t *a, const float *a_scale, const cbq_weight_t *head2,
                    const uint8_t *head8, const float *row_scale, int32_t M,

@@ -58,7 +58,9 @@ def _check_head(M, N, K, seed, zero_codebooks=False):
     return rows
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 200, 640), (3, 130, 256), (16, 1000, 384), (64, 300, 1024), (8, 16, 128)])
+@pytest.mark.parametrize("M,N,K", [(1, 200, 640), (3, 130, 256), (16, 1000, 384), (64, 300, 1024), (8, 16, 128),
+                                   (2, 1024, 128), (2, 1030, 256), (1, 16 * 1024 + 7, 128), (4, 40000, 256),
+                                   (2, 100000, 256), (1, 150000, 128)])
 def test_draft_head_small(M, N, K):
     _check_head(M, N, K, seed=M + N + K)
 
@@ -82,6 +84,8 @@ def test_draft_head_rejects_bad_arguments():
     assert L.cbq_draft_head_workspace_size(1, 15, 128, ctypes.byref(n)) == ops.EINVAL     # N < 16
     assert L.cbq_draft_head_workspace_size(1, 64, 96, ctypes.byref(n)) == ops.EINVAL      # K % 128
     assert L.cbq_draft_head_workspace_size(65, 64, 128, ctypes.byref(n)) == ops.EINVAL    # M > 64
+    assert L.cbq_draft_head_workspace_size(1, 262145, 128, ctypes.byref(n)) == ops.EINVAL  # N > 256 chunks
+    assert L.cbq_draft_head_workspace_size(1, 262144, 128, ctypes.byref(n)) == ops.OK
     h2, h8, rs, a, s = _case(1, 64, 128, 1)
     w, dh8, drs, da, ds = _device(h2, h8, rs, a, s)
     out = torch.empty(64, 16, dtype=torch.int32, device="cuda")

@@ -108,6 +108,16 @@ def test_streamk_many_parts_deterministic():
     assert ops.device_status() == ops.OK
 
 
+@pytest.mark.parametrize("M,N,K", [(3, 150000, 128), (2, 150000, 256), (5, 40000, 256)])
+def test_streamk_fewer_k_tiles_than_mma_groups(M, N, K):
+    # one or two k-tiles per row and up to 15 units per CTA: each of the three
+    # MMA groups steps through the resident activation slots modulo K / 128
+    c = Case(M, N, K, seed=N + K + M)
+    yref, b = c.oracle()
+    assert_close(c.run(ops.PATH_STREAMK), yref, b, f"M {M} N {N} K {K}")
+    assert ops.device_status() == ops.OK
+
+
 def test_streamk_shape_sequence_on_one_stream():
     # tile counters are back to zero after every call, whatever the shape; a
     # call with many tiles (129, and 96 at the decode shape) after calls that
