@@ -6,21 +6,22 @@
 // codes writes the scores), keeps the 16 best and rescores only those with
 // the FP8 head.  Here:
 //  * head_topk_chunk_kernel: grid (1024-row chunks, tokens), 256 threads, four
-//    rows a thread; the 16 best (score, row) pairs of each chunk.  A
-//    threshold T that at least 16 of the chunk's pairs reach: every warp sorts
-//    its 32 lane maxima (bitonic network over shuffles), its 16th is reached by
-//    16 pairs, and T is the largest of the warps' 16ths.  The pairs >= T (at
-//    most 8 x 16 lanes x 4) go to shared memory and each finds its place among
-//    them by counting the larger ones; places 0..15 are the chunk's list.
-//  * head_select_kernel: one CTA of 16 warps per token.  The 16th largest of
-//    the chunks' first entries is reached by 16 chunks' lists, so only those
-//    chunks' entries at or above it (at most 16 x 16) can be in the
-//    shortlist; they are ranked by counting as above (the shortlist:
-//    descending score, equal scores -> lower row).  Warp i then the FP8 logit
-//    of shortlisted row i, a_scale * row_scale * sum_k a w8 (products exact in
-//    fp32, sums in fp32; all of a lane's loads in flight at once), and the
-//    pick: the highest logit, equal logits -> the earlier row of the
-//    shortlist.
+//    rows a thread; the 16 best (score, row) pairs of each chunk.  Every warp
+//    sorts its 32 lane maxima (a bitonic network over shuffles); a tree of
+//    bitonic merges of the warps' 16 largest gives the 16 largest lane maxima
+//    of the chunk, and the 16th, T, is reached by exactly the 16 lanes that
+//    hold them.  Their pairs >= T (at most 64) go to shared memory and each
+//    finds its place among them by counting the larger ones; places 0..15
+//    are the chunk's list.
+//  * head_select_kernel: one CTA of 16 warps per token.  The same sort and
+//    merge tree over the chunks' first entries gives the 16 leading chunks
+//    and T, their 16th first entry; only their entries >= T (at most 16 x 16)
+//    can be in the shortlist, and they are ranked by counting as above (the
+//    shortlist: descending score, equal scores -> lower row).  Warp i then the
+//    FP8 logit of shortlisted row i, a_scale * row_scale * sum_k a w8
+//    (products exact in fp32, sums in fp32; all of a lane's loads in flight
+//    at once), and the pick: the highest logit, equal logits -> the earlier
+//    row of the shortlist.
 // A (score, row) pair is one 64-bit word: an order-preserving key of the fp32
 // score (-0 equals +0, NaN below every number) in the high half and
 // 2^32 - 1 - row in the low half, so "ranks before" is unsigned ">", no two
@@ -42,6 +43,7 @@ constexpr int kChunkWarps = 8;
 constexpr int kPerThread = kHeadChunkRows / (kChunkWarps * 32);   // 4
 constexpr int kSelectWarps = kList;                    // one warp per shortlisted row
 constexpr int kSelectCand = kList * kList;             // entries of the 16 leading chunks
+constexpr int kChunkCand = kList * kPerThread;         // words of the 16 leading lanes
 
 __device__ __forceinline__ uint32_t score_key(float v) {
   if (v != v) return 0u;
@@ -68,6 +70,35 @@ __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
     }
   }
   return v;
+}
+
+// Lanes 0..15 hold one descending list, lanes 16..31 another in ascending
+// order (a bitonic sequence); afterwards the 32 words are descending.
+__device__ __forceinline__ uint64_t warp_merge_desc(uint64_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
+    v = ((lane & j) == 0) == (o > v) ? o : v;
+  }
+  return v;
+}
+
+// lists[16 i .. 16 i + 15], i < nl (a power of two, nl <= 2 x warps): nl
+// descending lists in shared memory.  Afterwards lists[0..15] holds the 16
+// largest words of all, descending: a tree of pairwise bitonic merges, warp w
+// merging lists 2 s w and 2 s w + s at step s.  Every thread of the block
+// calls it.
+__device__ __forceinline__ void merge_tree16(uint64_t* lists, int nl) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int st = 1; st < nl; st <<= 1) {
+    const int a = 2 * st * warp, b = a + st;
+    uint64_t v = 0ull;
+    if (b < nl) v = warp_merge_desc(lane < kList ? lists[a * kList + lane] : lists[b * kList + 31 - lane]);
+    __syncthreads();
+    if (b < nl && lane < kList) lists[a * kList + lane] = v;
+    __syncthreads();
+  }
 }
 
 // Append w to list[] (shared memory, count *n) for every lane whose flag is
@@ -107,14 +138,14 @@ __device__ __forceinline__ void rank_places(const uint64_t* list, unsigned n, ui
 
 __global__ void __launch_bounds__(kChunkWarps * 32) head_topk_chunk_kernel(const float* __restrict__ scores, int N,
                                                                            uint64_t* __restrict__ cand) {
-  __shared__ uint64_t pool[kChunkWarps * 16 * kPerThread];
-  __shared__ uint64_t warp_t[kChunkWarps];
+  __shared__ uint64_t tops[kChunkWarps * kList];
+  __shared__ uint64_t pool[kChunkCand];
   __shared__ unsigned npool;
+  grid_launch_dependents();                            // the select kernel may start (it waits for this grid)
   grid_dependency_wait();                              // the scores of the matmul kernel
   const int m = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int lo = blockIdx.x * kHeadChunkRows;
   const float* s = scores + static_cast<size_t>(m) * N;
-  if (threadIdx.x == 0) npool = 0;
   uint64_t w[kPerThread], mx = 0ull;
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) {
@@ -122,15 +153,14 @@ __global__ void __launch_bounds__(kChunkWarps * 32) head_topk_chunk_kernel(const
     w[j] = n < N ? pair_word(__ldg(s + n), n) : 0ull;   // 0: no row
     mx = w[j] > mx ? w[j] : mx;
   }
-  // 16 lanes of this warp hold a word >= its 16th largest lane maximum
-  const uint64_t t = __shfl_sync(0xffffffffu, warp_sort_desc(mx), kList - 1);
-  if (lane == 0) warp_t[warp] = t;
+  const uint64_t srt = warp_sort_desc(mx);
+  if (lane < kList) tops[warp * kList + lane] = srt;
+  if (threadIdx.x == 0) npool = 0;
   __syncthreads();
-  uint64_t T = warp_t[0];
-#pragma unroll
-  for (int i = 1; i < kChunkWarps; ++i) T = warp_t[i] > T ? warp_t[i] : T;
-  // at least 16 words reach T; the words >= T come from at most 16 lanes a
-  // warp (T = 0 only when no warp has 16 lanes with a row)
+  merge_tree16(tops, kChunkWarps);                     // the chunk's 16 largest lane maxima
+  // T is reached by the 16 lanes whose maxima are tops[0..15] (T = 0: fewer
+  // than 16 lanes hold a row, and those hold every word)
+  const uint64_t T = tops[kList - 1];
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) warp_append(w[j] != 0ull && w[j] >= T, w[j], pool, &npool);
   __syncthreads();
@@ -144,35 +174,33 @@ __global__ void __launch_bounds__(kSelectWarps * 32) head_select_kernel(
     const uint64_t* __restrict__ cand, int nchunks, const uint8_t* __restrict__ a, const float* __restrict__ a_scale,
     const uint8_t* __restrict__ head8, const float* __restrict__ row_scale, int N, int K,
     int32_t* __restrict__ rows_out, float* __restrict__ logits_out, int32_t* __restrict__ pick_out) {
-  __shared__ uint64_t lead[kHeadMaxChunks];
+  __shared__ uint64_t tops[kSelectWarps * kList];
   __shared__ uint64_t pool[kSelectCand];
   __shared__ uint64_t best[kList];
   __shared__ float logit_s[kList];
-  __shared__ int lead_chunk[kList];
-  __shared__ uint64_t T_s;
   __shared__ unsigned npool;
+  // the next kernel may start: it waits for this grid before it writes
+  // anything this one reads (the next matmul's scores and workspace)
+  grid_launch_dependents();
   grid_dependency_wait();                              // the chunks' lists
   const int m = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t* c = cand + static_cast<size_t>(m) * nchunks * kList;
-  if (threadIdx.x == 0) {
-    npool = 0;
-    T_s = 0ull;                                        // fewer than 16 chunks: every entry
-  }
-  for (int i = threadIdx.x; i < nchunks; i += kSelectWarps * 32) lead[i] = c[static_cast<size_t>(i) * kList];
-  __syncthreads();
-  // the chunks in order of their first entries (distinct: no chunk is empty);
-  // the 16 leading ones hold every entry that reaches the 16th first entry T
-  for (int i = threadIdx.x; i < nchunks; i += kSelectWarps * 32) {
-    const unsigned place = count_larger(lead, static_cast<unsigned>(nchunks), lead[i]);
-    if (place < static_cast<unsigned>(kList)) lead_chunk[place] = i;
-    if (place == kList - 1) T_s = lead[i];
-  }
-  __syncthreads();
-  const uint64_t T = T_s;
-  const int nlead = nchunks < kList ? nchunks : kList;
   {
-    const int i = threadIdx.x;                         // entry i % 16 of leading chunk i / 16
-    const uint64_t w = i < nlead * kList ? c[static_cast<size_t>(lead_chunk[i / kList]) * kList + i % kList] : 0ull;
+    // thread i: the first entry of chunk i (nchunks <= 256 < threads)
+    const int i = threadIdx.x;
+    const uint64_t srt = warp_sort_desc(i < nchunks ? c[static_cast<size_t>(i) * kList] : 0ull);
+    if (lane < kList) tops[warp * kList + lane] = srt;
+  }
+  if (threadIdx.x == 0) npool = 0;
+  __syncthreads();
+  merge_tree16(tops, kSelectWarps);                    // the 16 largest first entries (distinct)
+  // every entry >= T lies in one of the leading chunks; fewer than 16 chunks:
+  // T = 0, every entry
+  const uint64_t T = nchunks >= kList ? tops[kList - 1] : 0ull;
+  {
+    const int q = threadIdx.x / kList, e = threadIdx.x % kList;   // entry e of leading chunk q
+    const uint64_t lead = q < kList ? tops[q] : 0ull;
+    const uint64_t w = lead != 0ull ? c[static_cast<size_t>(word_row(lead) / kHeadChunkRows) * kList + e] : 0ull;
     warp_append(w != 0ull && w >= T, w, pool, &npool);
   }
   __syncthreads();
