@@ -99,9 +99,12 @@ constexpr int kSfbCol = 504;                          // 8 columns of B scale fa
 static_assert(kDecWarp0 % 4 == 0 && kEpiWarp0 % 4 == 0, "a warp's TMEM lane quarter is warp % 4");
 constexpr int kMaxSmem = 232448;
 constexpr int kMinSmem = 120 * 1024;                  // one CTA per SM: it owns all of TMEM
+// k-tiles of resident activations, each with its own barrier (a CTA's share
+// of at most this many k-tiles of one row, or all K / 128 of them)
+constexpr int kMaxBSlots = 128;
 // barriers: code stages full/empty, A slots full/empty, per (group, buffer)
-// accumulator full/empty, per group MMA drain, B full
-constexpr int kNumBars = 2 * kMaxStages + 2 * kGroups * kMaxSlots + 2 * kGroups * 2 + kGroups + 1;
+// accumulator full/empty, per group MMA drain, per B slot full
+constexpr int kNumBars = 2 * kMaxStages + 2 * kGroups * kMaxSlots + 2 * kGroups * 2 + kGroups + kMaxBSlots;
 constexpr int kXchgStride = 17;                       // floats per exchanged row (conflict-free)
 constexpr int kXchgBytes = (64 * kXchgStride * 4 + 127) / 128 * 128;
 constexpr int kBarBytes = (kNumBars * 8 + 16 + 127) / 128 * 128;
@@ -195,7 +198,8 @@ struct GeoT {
   static constexpr int RB = BITS * 16;                // code bytes of one row of a unit (128 codes)
   int N, K, KT;                       // KT = k-tiles per row
   int tiles;                          // 128-row tiles per expert
-  long long U, G;                     // units, CTAs
+  long long U, G;                     // units (< 2^31), CTAs
+  uint32_t uq, ur;                    // U = uq G + ur
   const uint16_t* used;               // grouped: the used experts, ascending
   long long eb;                       // grouped: code bytes per expert, 3 K N / 8
   FastDiv by_tiles;                   // grouped: division by tiles
@@ -220,7 +224,11 @@ struct GeoT {
       ++t;
     }
   }
-  __device__ __forceinline__ long long first_unit(long long b) const { return b * U / G; }
+  // floor(b U / G) = b uq + floor(b ur / G), in 32-bit arithmetic (b ur < G^2)
+  __device__ __forceinline__ long long first_unit(long long b) const {
+    const uint32_t b32 = static_cast<uint32_t>(b);
+    return static_cast<long long>(b32 * uq + (b32 * ur) / static_cast<uint32_t>(G));
+  }
   // the CTA whose share holds unit u
   __device__ __forceinline__ long long owner(long long u) const { return ((u + 1) * G + U - 1) / U - 1; }
 };
@@ -249,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   uint64_t* acc_full = a_empty + kGroups * kMaxSlots;  // [group][2]
   uint64_t* acc_empty = acc_full + 2 * kGroups;        // [group][2]
   uint64_t* drain = acc_empty + 2 * kGroups;           // [group]
-  uint64_t* b_full = drain + kGroups;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 1);
+  uint64_t* b_full = drain + kGroups;                  // [B slot]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + kMaxBSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
   uint8_t* route_s = reinterpret_cast<uint8_t*>(bars) + kBarBytes;   // GROUPED: routing
@@ -261,24 +269,27 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   const long long wait_ns = p.wait_ns;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  if (tid == 0) {
-    for (int i = 0; i < NS; ++i) {
+  if (warp == 0) {                                     // barriers initialised by the lanes side by side
+    for (int i = lane; i < NS; i += 32) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 4 * kUnitsPerStage);       // four row blocks of each unit of a full stage
     }
-    for (int sl = 0; sl < kGroups * kMaxSlots; ++sl) {
+    for (int sl = lane; sl < kGroups * kMaxSlots; sl += 32) {
       mbar_init(&a_full[sl], 4);                      // the group's four decoder warps
       mbar_init(&a_empty[sl], 1);                     // the group's MMAs read the slot
     }
-    for (int g = 0; g < kGroups; ++g) {
+    if (lane < kGroups) {
+      const int g = lane;
       mbar_init(&acc_full[2 * g], 1);
       mbar_init(&acc_full[2 * g + 1], 1);
       mbar_init(&acc_empty[2 * g], 4);                // the four epilogue warps
       mbar_init(&acc_empty[2 * g + 1], 4);
       mbar_init(&drain[g], 1);
     }
-    mbar_init(b_full, 1);
-    *abort_flag = 0;
+    if (lane == 0) *abort_flag = 0;
+    fence_barrier_init();
+  } else if (warp == 1) {                              // the B slots' barriers, one per lane
+    for (int sl = lane; sl < p.b_ktiles; sl += 32) mbar_init(&b_full[sl], 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -329,12 +340,14 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   geo.K = p.K;
   geo.KT = p.K / 128;
   geo.tiles = (p.N + kRows - 1) / kRows;
-  geo.by_tiles.init(static_cast<uint32_t>(geo.tiles));
+  if constexpr (GROUPED) geo.by_tiles.init(static_cast<uint32_t>(geo.tiles));
   geo.U = static_cast<long long>(n_used) * geo.tiles * geo.KT;
   // shares over at most U CTAs, so that every sharing CTA has a unit (a
   // grouped call is planned for the most experts its routing can name; with
   // fewer, the CTAs from G on have no share)
   geo.G = geo.U < static_cast<long long>(gridDim.x) ? (geo.U > 0 ? geo.U : 1) : static_cast<long long>(gridDim.x);
+  geo.uq = static_cast<uint32_t>(geo.U) / static_cast<uint32_t>(geo.G);
+  geo.ur = static_cast<uint32_t>(geo.U) - geo.uq * static_cast<uint32_t>(geo.G);
   geo.used = used_s;
   geo.eb = static_cast<long long>(BITS) * p.K * p.N / 8;
   const int KT = geo.KT;
@@ -342,7 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   const long long u0 = geo.first_unit(b0 < geo.G ? b0 : geo.G), u1 = geo.first_unit(b1 < geo.G ? b1 : geo.G);
   const int n_units = static_cast<int>(u1 - u0);
   const int n_stages = (n_units + kUnitsPerStage - 1) / kUnitsPerStage;
-  const int t_first = static_cast<int>(u0 / KT), c_first = static_cast<int>(u0 % KT);
+  const int t_first = static_cast<int>(static_cast<uint32_t>(u0) / static_cast<uint32_t>(KT));
+  const int c_first = static_cast<int>(u0) - t_first * KT;
   // The next kernel on the stream may start its prologue (and, if it is this
   // one, its weight stream) as soon as SMs free up; whatever this grid reads
   // from or writes for earlier kernels waits on grid_dependency_wait below.
@@ -435,10 +449,6 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       const int g = warp - kMmaWarp0;
       named_bar_sync(3, 32 * kGroups + 32 * 4);        // the epilogue stored the B scale factors
       tc_fence_after();
-      if (g < n_units) {
-        wait_bounded(b_full, 0, abort_flag, wait_ns);  // resident activations landed
-        tc_fence_after();
-      }
       const uint64_t bd0 = umma_desc_kmajor_sw128(smem_u32(b_s));
       const uint32_t idesc = umma_idesc_mxf8(NTOK, 0, 0);
       const uint32_t sfb_col = tbase + kSfbCol;
@@ -454,6 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         int t2 = t, c2 = c;
         geo.advance(t2, c2, kGroups);
         const int as = g * S + su;
+        // this k-tile's activations landed (from unit 3 KT on, the group
+        // waited for this slot at unit i - 3 KT)
+        if (i < 3 * KT) wait_bounded(&b_full[bsl], 0, abort_flag, wait_ns);
         wait_bounded(&a_full[as], aph, abort_flag, wait_ns);    // the group's four warps stored it
         tc_fence_after();
         const bool seg_first = t != cur_t;              // the group's first unit of this tile
@@ -693,17 +706,19 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       tc_fence_before();
       named_bar_sync(3, 32 * 4 + 32 * kGroups);        // B scale factors are in TMEM (with the MMA warps)
       grid_dependency_wait();                           // y, the workspace and the activations may still be in use
-      if (leader && n_units > 0) {
+      if (warp == kEpiWarp0 && n_units > 0) {
         // Resident activations, written by an earlier kernel: k-tile c of this
         // CTA's share lands in slot (c - c_first) mod KT as NTOK rows of 128
-        // bytes in the 128-byte swizzled K-major layout (one TMA box); token
-        // rows >= M are outside the tensor and arrive as zeros.
+        // bytes in the 128-byte swizzled K-major layout (one TMA box, one
+        // barrier per slot, the warp's lanes issuing slots 0, 1, ... in the
+        // order the MMAs take them); token rows >= M are outside the tensor
+        // and arrive as zeros.
         const int nb = min(KT, n_units);
-        mbar_arrive_expect_tx(b_full, static_cast<uint32_t>(nb * NTOK * 128));
-        for (int sl = 0; sl < nb; ++sl) {
+        for (int sl = lane; sl < nb; sl += 32) {
           int cc = c_first + sl;
           if (cc >= KT) cc -= KT;
-          tma_load_2d(b_s + sl * NTOK * 128, &p.a_map, b_full, cc * 128, 0);
+          mbar_arrive_expect_tx(&b_full[sl], static_cast<uint32_t>(NTOK * 128));
+          tma_load_2d(b_s + sl * NTOK * 128, &p.a_map, &b_full[sl], cc * 128, 0);
         }
       }
       uint32_t acc_par = 0;                             // bit 2 g + b: parity of (group, buffer) uses
@@ -867,7 +882,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           if ((part & (1u << g)) && lane == 0) mbar_arrive(&acc_empty[2 * g + b]);
         s0 = i + 1;
       }
-      if (leader && n_units > 0) wait_drain(b_full, 0);   // the activations landed before the CTA can end
+      if (warp == kEpiWarp0)                             // the activations landed before the CTA can end
+        for (int sl = lane; sl < min(KT, n_units); sl += 32) wait_drain(&b_full[sl], 0);
       if constexpr (GATE_UP) {
         // every product and maximum of this CTA is written: one release-
         // acquire add after a barrier counts the CTA; the last one learns
@@ -984,6 +1000,7 @@ bool plan_for(int M, int N, int K, Mode mode, Plan& pl, int E = 1, int topk = 1)
   const long long tiles = experts * ((N + kRows - 1) / kRows);
   if (tiles > kMaxTiles) return false;
   const long long U = tiles * KT;
+  if (U >= (1LL << 31)) return false;                 // unit numbers are 32-bit on the device
   // Stream-K shares (an equal number of units per CTA, tiles split between
   // CTAs) -- except where the tiles alone fill most of the GPU: then one
   // whole tile per CTA, which needs no partial-tile fix-up (decode 4096 x
@@ -994,6 +1011,7 @@ bool plan_for(int M, int N, int K, Mode mode, Plan& pl, int E = 1, int topk = 1)
   const long long per = (U + G - 1) / G;               // most units of any CTA
   pl.ntok = ntok_for(M);
   pl.b_ktiles = static_cast<int>(std::min<long long>(KT, per));
+  if (pl.b_ktiles > kMaxBSlots) return false;
   const int fixed = pl.b_ktiles * pl.ntok * 128 + (mode == kGateUp ? kXchgBytes : 0) + kBarBytes +
                     (mode == kGrouped ? kRouteBytes : 0);
   pl.stages = std::min(kMaxStages, (kMaxSmem - fixed) / kStageBytes);

@@ -192,24 +192,24 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   const int gk = p.K / 32;                                // scale bytes per row
   const int n_stages_u = (kt1 - kt0 + kKtPerStage - 1) / kKtPerStage;   // code stages per unit
 
-  if (tid == 0) {
-    for (int i = 0; i < NS; ++i) {
+  if (warp == 0) {                                        // barriers initialised by the lanes side by side
+    for (int i = lane; i < NS; i += 32) {
       mbar_init(&codes_full[i], 1);
       mbar_init(&codes_empty[i], kDecWarps);            // every decoder warp, once per stage
     }
-    for (int i = 0; i < kAStages; ++i) {
+    for (int i = lane; i < kAStages; i += 32) {
       mbar_init(&a_full[i], 4);
       mbar_init(&a_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+    if (lane < 2) {
+      mbar_init(&acc_full[lane], 1);
+      mbar_init(&acc_empty[lane], 4);
     }
-    mbar_init(b_full, 1);
-    mbar_init(red_full, (cs > 1 ? cs - 1 : 1) * 128);
-    mbar_init(red_free, 128);
-    mbar_init(drain, 1);
-    *abort_flag = 0;
+    if (lane == 2) mbar_init(b_full, 1);
+    if (lane == 3) mbar_init(red_full, (cs > 1 ? cs - 1 : 1) * 128);
+    if (lane == 4) mbar_init(red_free, 128);
+    if (lane == 5) mbar_init(drain, 1);
+    if (lane == 0) *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
