@@ -269,6 +269,51 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   const long long wait_ns = p.wait_ns;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  // The CTA's share of the units.  A dense call knows it before anything
+  // else, so the producer issues its first copy while the block sets up; a
+  // grouped call knows it after the routing scan.
+  GeoT<GROUPED, BITS> geo;
+  struct Share {
+    long long u0;
+    int n_units, n_stages, t_first, c_first;
+  };
+  auto make_share = [&](int n_used_) {
+    geo.N = p.N;
+    geo.K = p.K;
+    geo.KT = p.K / 128;
+    geo.tiles = (p.N + kRows - 1) / kRows;
+    if constexpr (GROUPED) geo.by_tiles.init(static_cast<uint32_t>(geo.tiles));
+    geo.U = static_cast<long long>(n_used_) * geo.tiles * geo.KT;
+    // shares over at most U CTAs, so that every sharing CTA has a unit (a
+    // grouped call is planned for the most experts its routing can name;
+    // with fewer, the CTAs from G on have no share)
+    geo.G = geo.U < static_cast<long long>(gridDim.x) ? (geo.U > 0 ? geo.U : 1) : static_cast<long long>(gridDim.x);
+    geo.uq = static_cast<uint32_t>(geo.U) / static_cast<uint32_t>(geo.G);
+    geo.ur = static_cast<uint32_t>(geo.U) - geo.uq * static_cast<uint32_t>(geo.G);
+    geo.used = used_s;
+    geo.eb = static_cast<long long>(BITS) * p.K * p.N / 8;
+    const long long b0 = blockIdx.x, b1 = blockIdx.x + 1LL;
+    Share r;
+    r.u0 = geo.first_unit(b0 < geo.G ? b0 : geo.G);
+    r.n_units = static_cast<int>(geo.first_unit(b1 < geo.G ? b1 : geo.G) - r.u0);
+    r.n_stages = (r.n_units + kUnitsPerStage - 1) / kUnitsPerStage;
+    r.t_first = static_cast<int>(static_cast<uint32_t>(r.u0) / static_cast<uint32_t>(geo.KT));
+    r.c_first = static_cast<int>(r.u0) - r.t_first * geo.KT;
+    return r;
+  };
+  Share sh{0, 0, 0, 0, 0};
+  if constexpr (!GROUPED) sh = make_share(1);
+  // Dense: stage j's copy, one contiguous piece of the stream (units from
+  // (ts, cs) on, nu of them) into code slot `slot`.
+  auto issue_dense_stage = [&](int ts, int cs, int nu, int slot, uint64_t pol) {
+    int tl = ts, cl = cs;
+    geo.advance(tl, cl, nu - 1);                       // last unit of the stage
+    const long long oa = geo.off(ts, cs);
+    const uint32_t bytes = static_cast<uint32_t>(geo.off(tl, cl) + geo.rows(tl) * static_cast<long long>(RB) - oa);
+    mbar_arrive_expect_tx(&full[slot], bytes);
+    bulk_g2s(codes_s + slot * kStageBytes, p.codes + oa, bytes, &full[slot], pol);
+  };
+
   if (warp == 0) {                                     // barriers initialised by the lanes side by side
     for (int i = lane; i < NS; i += 32) {
       mbar_init(&full[i], 1);
@@ -288,6 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     }
     if (lane == 0) *abort_flag = 0;
     fence_barrier_init();
+    if constexpr (!GROUPED) {
+      // this lane initialised full[0]: stage 0's copy goes out now
+      if (lane == 0 && sh.n_stages > 0)
+        issue_dense_stage(sh.t_first, sh.c_first, min(kUnitsPerStage, sh.n_units), 0, l2_evict_first_policy());
+    }
   } else if (warp == 1) {                              // the B slots' barriers, one per lane
     for (int sl = lane; sl < p.b_ktiles; sl += 32) mbar_init(&b_full[sl], 1);
     fence_barrier_init();
@@ -335,28 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     n_used = *n_used_s;
   }
 
-  GeoT<GROUPED, BITS> geo;
-  geo.N = p.N;
-  geo.K = p.K;
-  geo.KT = p.K / 128;
-  geo.tiles = (p.N + kRows - 1) / kRows;
-  if constexpr (GROUPED) geo.by_tiles.init(static_cast<uint32_t>(geo.tiles));
-  geo.U = static_cast<long long>(n_used) * geo.tiles * geo.KT;
-  // shares over at most U CTAs, so that every sharing CTA has a unit (a
-  // grouped call is planned for the most experts its routing can name; with
-  // fewer, the CTAs from G on have no share)
-  geo.G = geo.U < static_cast<long long>(gridDim.x) ? (geo.U > 0 ? geo.U : 1) : static_cast<long long>(gridDim.x);
-  geo.uq = static_cast<uint32_t>(geo.U) / static_cast<uint32_t>(geo.G);
-  geo.ur = static_cast<uint32_t>(geo.U) - geo.uq * static_cast<uint32_t>(geo.G);
-  geo.used = used_s;
-  geo.eb = static_cast<long long>(BITS) * p.K * p.N / 8;
+  if constexpr (GROUPED) sh = make_share(n_used);
   const int KT = geo.KT;
-  const long long b0 = blockIdx.x, b1 = blockIdx.x + 1LL;
-  const long long u0 = geo.first_unit(b0 < geo.G ? b0 : geo.G), u1 = geo.first_unit(b1 < geo.G ? b1 : geo.G);
-  const int n_units = static_cast<int>(u1 - u0);
-  const int n_stages = (n_units + kUnitsPerStage - 1) / kUnitsPerStage;
-  const int t_first = static_cast<int>(static_cast<uint32_t>(u0) / static_cast<uint32_t>(KT));
-  const int c_first = static_cast<int>(u0) - t_first * KT;
+  const int n_units = sh.n_units, n_stages = sh.n_stages, t_first = sh.t_first, c_first = sh.c_first;
   // The next kernel on the stream may start its prologue (and, if it is this
   // one, its weight stream) as soon as SMs free up; whatever this grid reads
   // from or writes for earlier kernels waits on grid_dependency_wait below.
@@ -371,7 +402,16 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       uint32_t ph = 0;
       int issued = 0;
       const uint64_t pol = l2_evict_first_policy();
-      for (int j = 0; j < n_stages; ++j) {
+      int j0 = 0;
+      if constexpr (!GROUPED) {
+        if (n_stages > 0) {                            // stage 0 went out during setup
+          geo.advance(ta, ca, kUnitsPerStage);
+          slot = 1;                                    // NS >= 2
+          issued = 1;
+          j0 = 1;
+        }
+      }
+      for (int j = j0; j < n_stages; ++j) {
         const int nu = min(kUnitsPerStage, n_units - j * kUnitsPerStage);
         const int ts = ta, cs = ca;                     // first unit of the stage
         geo.advance(ta, ca, kUnitsPerStage);
@@ -383,13 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           wait_drain(&full[slot], ph ^ 1u);
         }
         if constexpr (!GROUPED) {
-          // one contiguous piece of the stream
-          int tl = ts, cl = cs;
-          geo.advance(tl, cl, nu - 1);                 // last unit of the stage
-          const long long oa = geo.off(ts, cs);
-          const uint32_t bytes = static_cast<uint32_t>(geo.off(tl, cl) + geo.rows(tl) * static_cast<long long>(RB) - oa);
-          mbar_arrive_expect_tx(&full[slot], bytes);
-          bulk_g2s(codes_s + slot * kStageBytes, p.codes + oa, bytes, &full[slot], pol);
+          issue_dense_stage(ts, cs, nu, slot, pol);
         } else {
           // the stage's units in runs of one expert each (each run contiguous
           // in the stacked codes), back to back in the stage
@@ -415,6 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           }
         }
         ++issued;
+        // stage 0 lands before the later stages' copies compete with it
+        if (j == 1) wait_bounded(&full[0], 0, abort_flag, wait_ns);
         if (++slot == NS) {
           slot = 0;
           ph ^= 1u;
