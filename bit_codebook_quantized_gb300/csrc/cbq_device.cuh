@@ -48,6 +48,15 @@ __device__ __forceinline__ uint32_t lookup4(uint32_t cb_lo, uint32_t cb_hi, uint
   return __byte_perm(cb_lo, cb_hi, sel);
 }
 
+// x >> 16 as the high word of x * 2^16: a multiply-high runs on the
+// integer multiply-add pipe, which the decode leaves mostly idle, instead of
+// the shift/logic pipe that its masks and byte permutes keep busy.
+__device__ __forceinline__ uint32_t upper_half(uint32_t x) {
+  uint32_t r;
+  asm("mul.hi.u32 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(0x10000u));
+  return r;
+}
+
 // Decode one group (three 32-bit words) of a row into 32 E4M3 bytes
 // (8 TMEM columns):
 // v[0..7] = E4M3 bytes of codes 0..31, four per column.
@@ -58,13 +67,13 @@ __device__ __forceinline__ void decode_group(uint32_t w0, uint32_t w1, uint32_t 
   const uint32_t s2 = spread_codes8(__funnelshift_r(w1, w2, 16));
   const uint32_t s3 = spread_codes8(w2 >> 8);
   v[0] = lookup4(cb_lo, cb_hi, s0);
-  v[1] = lookup4(cb_lo, cb_hi, s0 >> 16);
+  v[1] = lookup4(cb_lo, cb_hi, upper_half(s0));
   v[2] = lookup4(cb_lo, cb_hi, s1);
-  v[3] = lookup4(cb_lo, cb_hi, s1 >> 16);
+  v[3] = lookup4(cb_lo, cb_hi, upper_half(s1));
   v[4] = lookup4(cb_lo, cb_hi, s2);
-  v[5] = lookup4(cb_lo, cb_hi, s2 >> 16);
+  v[5] = lookup4(cb_lo, cb_hi, upper_half(s2));
   v[6] = lookup4(cb_lo, cb_hi, s3);
-  v[7] = lookup4(cb_lo, cb_hi, s3 >> 16);
+  v[7] = lookup4(cb_lo, cb_hi, upper_half(s3));
 }
 
 // Two-bit codes (the draft head's format: code j of a 32-weight group at bits
@@ -88,13 +97,13 @@ __device__ __forceinline__ void decode_group2(uint32_t w0, uint32_t w1, uint32_t
   const uint32_t s0 = spread_codes2x8(w0), s1 = spread_codes2x8(w0 >> 16);
   const uint32_t s2 = spread_codes2x8(w1), s3 = spread_codes2x8(w1 >> 16);
   v[0] = __byte_perm(cb, cb, s0);
-  v[1] = __byte_perm(cb, cb, s0 >> 16);
+  v[1] = __byte_perm(cb, cb, upper_half(s0));
   v[2] = __byte_perm(cb, cb, s1);
-  v[3] = __byte_perm(cb, cb, s1 >> 16);
+  v[3] = __byte_perm(cb, cb, upper_half(s1));
   v[4] = __byte_perm(cb, cb, s2);
-  v[5] = __byte_perm(cb, cb, s2 >> 16);
+  v[5] = __byte_perm(cb, cb, upper_half(s2));
   v[6] = __byte_perm(cb, cb, s3);
-  v[7] = __byte_perm(cb, cb, s3 >> 16);
+  v[7] = __byte_perm(cb, cb, upper_half(s3));
 }
 
 // E8M0 byte -> fp32 2^(s-127) (s = 0 gives the subnormal 2^-127).

@@ -330,9 +330,9 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
           uint32_t fB = __funnelshift_r(lds32(rowB + 12 * q + lo_off), lds32(rowB + 12 * q + hi_off), sh);
           uint32_t selA = spread_codes8(fA), selB = spread_codes8(fB);
           uint32_t a0 = lookup4(cbA.x, cbA.y, selA);
-          uint32_t a2 = lookup4(cbA.x, cbA.y, selA >> 16);
+          uint32_t a2 = lookup4(cbA.x, cbA.y, upper_half(selA));
           uint32_t a1 = lookup4(cbB.x, cbB.y, selB);
-          uint32_t a3 = lookup4(cbB.x, cbB.y, selB >> 16);
+          uint32_t a3 = lookup4(cbB.x, cbB.y, upper_half(selB));
           const float fsA = e8m0_word_byte_to_f32(sA, q);
           const float fsB = e8m0_word_byte_to_f32(sB, q);
 #pragma unroll
@@ -403,7 +403,7 @@ __global__ void unpack_kernel(const uint8_t* __restrict__ codes, const uint8_t* 
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const uint32_t sel = spread_codes8(group_field(w0, w1, w2, q));
-      const uint32_t b_lo = lookup4(cb.x, cb.y, sel), b_hi = lookup4(cb.x, cb.y, sel >> 16);
+      const uint32_t b_lo = lookup4(cb.x, cb.y, sel), b_hi = lookup4(cb.x, cb.y, upper_half(sel));
       float v[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
