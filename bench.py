@@ -773,8 +773,25 @@ def run_single(args):
     profiler captures (cold cache per profiler pass)."""
     from bit_codebook_quantized_gb300 import build as _b
     _b.build()
-    wl = synth.workloads()[args.single]
     dev = torch.device("cuda", 0)
+    if args.single in synth.draft_head_workloads():
+        # the draft head: 2-bit scores, shortlist, FP8 rescoring and pick
+        wl = synth.draft_head_workloads()[args.single]
+        h2 = synth.gen_head2(wl.N, wl.K, seed=1)
+        h8, rs = synth.gen_head8(wl.N, wl.K, seed=2)
+        w = ops.PackedWeights.from_host(h2.codes, h2.scales, h2.codebooks, wl.N, wl.K, device=dev)
+        h8, rs = torch.from_numpy(h8).to(dev), torch.from_numpy(rs).to(dev)
+        a = torch.from_numpy(synth.gen_activations(wl.M, wl.K, seed=3)).to(dev)
+        s = torch.from_numpy(synth.gen_a_scale(wl.M, seed=4, mode="uniform")).to(dev)
+        for _ in range(args.calls):
+            ops.draft_head(a, s, w, h8, rs)
+        torch.cuda.synchronize()
+        st = ops.device_status()
+        print(json.dumps({"single": args.single, "calls": args.calls, "status": st}))
+        if st != ops.OK:
+            sys.exit(1)
+        return
+    wl = synth.workloads()[args.single]
     if wl.experts:
         pw = synth.gen_weights(wl.experts * wl.N, wl.K, seed=1)
         idx = torch.from_numpy(synth.gen_moe_routing(wl.M, wl.experts, wl.budget, wl.topk, seed=4)).to(dev)
@@ -808,7 +825,8 @@ def main(argv=None):
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="--impl reference: CPU seconds the whole run should take")
     ap.add_argument("--single", default=None,
-                    help="run --calls calls of one workload (see synth.workloads()) and exit")
+                    help="run --calls calls of one workload (see synth.workloads() and "
+                         "synth.draft_head_workloads()) and exit")
     ap.add_argument("--path", type=int, default=0, help="kernel for --single: 0 auto, 1 gemv, 2 mma, 3 stream-K")
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--per-config-calls", type=int, default=250,
