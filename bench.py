@@ -509,6 +509,42 @@ def run_per_config(dev, stream, peak, calls=250):
         torch.cuda.empty_cache()
     points += run_gate_up_points(dev, stream, peak, calls, l2)
     points += run_draft_head_points(dev, stream, peak, calls, l2)
+    points += run_budget_points(dev, stream, calls)
+    return points
+
+
+def run_budget_points(dev, stream, calls):
+    """cbq_select_budget (the verify round's shared expert budget and each
+    token's top-k inside it) on seeded N(0,1) router logits, timed like the
+    other points.  Its input is a few KB to 1 MB of logits, so the time is
+    latency, not bandwidth: no roofline fraction."""
+    points = []
+    for name, (T, E, k, B) in synth.budget_workloads().items():
+        logits = torch.from_numpy(synth.gen_router_logits(T, E, seed=5)).to(dev)
+        run = lambda: ops.select_budget(logits, k, B, stream=stream)  # noqa: E731
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                run()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(calls):
+                run()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(PC_REPS + 1)]
+        with torch.cuda.stream(stream):
+            g.replay()
+            ev[0].record(stream)
+            for r in range(PC_REPS):
+                g.replay()
+                ev[r + 1].record(stream)
+        stream.synchronize()
+        if ops.device_status(stream) != ops.OK:
+            raise RuntimeError(f"device status not ok after {name}")
+        us = ev[0].elapsed_time(ev[-1]) * 1e3 / (PC_REPS * calls)
+        points.append({"workload": name, "T": T, "E": E, "k": k, "B": B,
+                       "kernel": "budget_own_kernel + budget_sort_kernel + budget_pick_kernel",
+                       "us": round(us, 3), "roofline_frac": None})
+        del g
     return points
 
 
@@ -774,6 +810,18 @@ def run_single(args):
     from bit_codebook_quantized_gb300 import build as _b
     _b.build()
     dev = torch.device("cuda", 0)
+    if args.single in synth.budget_workloads():
+        # the verify round's expert budget on seeded router logits
+        T, E, k, B = synth.budget_workloads()[args.single]
+        logits = torch.from_numpy(synth.gen_router_logits(T, E, seed=5)).to(dev)
+        for _ in range(args.calls):
+            ops.select_budget(logits, k, B)
+        torch.cuda.synchronize()
+        st = ops.device_status()
+        print(json.dumps({"single": args.single, "calls": args.calls, "status": st}))
+        if st != ops.OK:
+            sys.exit(1)
+        return
     if args.single in synth.draft_head_workloads():
         # the draft head: 2-bit scores, shortlist, FP8 rescoring and pick
         wl = synth.draft_head_workloads()[args.single]
@@ -825,8 +873,8 @@ def main(argv=None):
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="--impl reference: CPU seconds the whole run should take")
     ap.add_argument("--single", default=None,
-                    help="run --calls calls of one workload (see synth.workloads() and "
-                         "synth.draft_head_workloads()) and exit")
+                    help="run --calls calls of one workload (see synth.workloads(), "
+                         "synth.draft_head_workloads() and synth.budget_workloads()) and exit")
     ap.add_argument("--path", type=int, default=0, help="kernel for --single: 0 auto, 1 gemv, 2 mma, 3 stream-K")
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--per-config-calls", type=int, default=250,

@@ -29,7 +29,10 @@
 // insertion chain, taken only when a word beats the lane's 8th; 8 loads in
 // flight per lane), then k rounds of a warp-wide maximum merge the 32 lists.
 // Step 2: shared-memory atomic adds of (k - r) into the high half of each
-// expert's word.  Step 3: one bitonic sort of those words.
+// expert's word.  Step 3: up to 256 experts, each expert's place among those
+// words (all distinct) by counting the larger ones (E^2/32 broadcast loads);
+// beyond, one bitonic sort of the words (fewer steps than that); places
+// 0..B-1 are the budget.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -131,8 +134,24 @@ __global__ void __launch_bounds__(kOwnWarps * 32) budget_own_kernel(const float*
              [&](int r, int e) { topk_out[static_cast<size_t>(t) * k + r] = e; });
 }
 
+// How many of words[0..n) are larger than w (eight loads in flight).
+__device__ __forceinline__ unsigned count_larger(const unsigned long long* words, unsigned n, unsigned long long w) {
+  unsigned c = 0;
+  for (unsigned j0 = 0; j0 < n; j0 += 8) {
+    unsigned long long x[8];
+#pragma unroll
+    for (unsigned u = 0; u < 8; ++u) x[u] = words[min(j0 + u, n - 1u)];
+#pragma unroll
+    for (unsigned u = 0; u < 8; ++u) c += (j0 + u < n && x[u] > w) ? 1u : 0u;
+  }
+  return c;
+}
+
+constexpr int kCountMaxExperts = 256;                 // place by counting up to here, else sort
+
 // Steps 2-3 (second kernel, one CTA of 32 warps): scores from all the own
-// top-k lists, the budget by one bitonic sort, written in ascending order.
+// top-k lists, then the B best words (the words are distinct: the id is in
+// the low half), written in ascending expert order.
 __global__ void __launch_bounds__(kBudgetThreads) budget_sort_kernel(int T, int E, int k, int B,
                                                                       const int32_t* __restrict__ own,
                                                                       int32_t* __restrict__ budget_out) {
@@ -153,23 +172,29 @@ __global__ void __launch_bounds__(kBudgetThreads) budget_sort_kernel(int T, int 
   for (int i = tid; i < tk; i += kBudgetThreads)
     atomicAdd(&words[own[i]], static_cast<unsigned long long>(k - i % k) << 32);
   __syncthreads();
-  // 3: bitonic sort, descending: words[0..B) are the budget
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < P / 2; i += kBudgetThreads) {
-        const int lo = 2 * i - (i & (stride - 1));          // first of the pair
-        const int hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const unsigned long long a = words[lo], b = words[hi];
-        if ((a < b) == desc) {
-          words[lo] = b;
-          words[hi] = a;
+  if (E <= kCountMaxExperts) {
+    // 3: the B experts whose words no more than B - 1 others beat
+    for (int e = tid; e < E; e += kBudgetThreads)
+      in_budget[e] = count_larger(words, static_cast<unsigned>(E), words[e]) < static_cast<unsigned>(B) ? 1 : 0;
+  } else {
+    // 3: bitonic sort, descending: words[0..B) are the budget
+    for (int size = 2; size <= P; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < P / 2; i += kBudgetThreads) {
+          const int lo = 2 * i - (i & (stride - 1));        // first of the pair
+          const int hi = lo + stride;
+          const bool desc = (lo & size) == 0;
+          const unsigned long long a = words[lo], b = words[hi];
+          if ((a < b) == desc) {
+            words[lo] = b;
+            words[hi] = a;
+          }
         }
+        __syncthreads();
       }
-      __syncthreads();
     }
+    for (int j = tid; j < B; j += kBudgetThreads) in_budget[word_id(words[j])] = 1;
   }
-  for (int j = tid; j < B; j += kBudgetThreads) in_budget[word_id(words[j])] = 1;
   __syncthreads();
   if (warp == 0) {                                          // ascending expert order
     int base = 0;
@@ -224,7 +249,7 @@ cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, cudaStream_
 int launch_budget(const float* logits, int T, int E, int k, int B, int32_t* budget, int32_t* topk,
                   cudaStream_t stream) {
   const dim3 tok_grid((T + kOwnWarps - 1) / kOwnWarps), tok_block(kOwnWarps * 32);
-  // topk_idx holds every token's own top-k until the sort kernel has read it
+  // topk_idx holds every token's own top-k until the second kernel has read it
   if (launch_pdl(budget_own_kernel, tok_grid, tok_block, stream, logits, T, E, k, topk) != cudaSuccess ||
       launch_pdl(budget_sort_kernel, dim3(1), dim3(kBudgetThreads), stream, T, E, k, B,
                  static_cast<const int32_t*>(topk), budget) != cudaSuccess ||

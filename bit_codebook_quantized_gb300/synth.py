@@ -111,6 +111,18 @@ def gen_a_scale(M: int, seed: int, mode: str = "one") -> np.ndarray:
     raise ValueError(mode)
 
 
+def gen_router_logits(T: int, E: int, seed: int) -> np.ndarray:
+    """Router logits of a verify round: fp32 N(0,1) draws [T, E]."""
+    return rng_for(seed).standard_normal((T, E)).astype(np.float32)
+
+
+def budget_workloads() -> dict[str, tuple[int, int, int, int]]:
+    """(tokens T, experts E, per-token top-k, budget B) of a verify round's
+    expert budget: the MoE round of the grouped workload (64 tokens, 128
+    experts, top-8 inside 24) and a wide router (4096 experts, budget 64)."""
+    return {"budget_t64_e128": (64, 128, 8, 24), "budget_t64_e4096": (64, 4096, 8, 64)}
+
+
 def gen_moe_routing(M: int, E: int, budget: int, topk: int, seed: int) -> np.ndarray:
     """Per-round shared expert budget: `budget` distinct experts drawn
     uniformly; every token takes the top-`topk` of its N(0,1) router logits

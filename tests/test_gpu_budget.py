@@ -28,7 +28,7 @@ def _logits(T, E, seed, ties):
 
 
 @pytest.mark.parametrize("T,E,k,B", [(1, 12, 2, 4), (6, 12, 2, 4), (64, 128, 8, 24), (64, 4096, 8, 64),
-                                     (33, 100, 3, 3), (5, 17, 1, 17), (70, 257, 8, 31)])
+                                     (33, 100, 3, 3), (5, 17, 1, 17), (70, 257, 8, 31), (16, 256, 4, 40)])
 @pytest.mark.parametrize("ties", [False, True])
 def test_budget_matches_the_oracle(T, E, k, B, ties):
     logits = _logits(T, E, T * 1000 + E + k + B, ties)
