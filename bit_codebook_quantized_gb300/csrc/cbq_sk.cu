@@ -53,7 +53,9 @@
 // release-acquire count of finished CTAs in the workspace) then turns every
 // product into E4M3 with its token's scale max/448, with all its threads, and
 // returns the maxima and the count to zero; beyond that (one SM would read
-// too many products) gate_up_quant_kernel does it, one CTA per token.
+// too many products) the last CTA writes the scales and returns the maxima
+// and the count to zero, and gate_up_quant_kernel quantises the products in
+// chunks of 2048 (a CTA per chunk and token).
 //
 // Bounded waits: every mbarrier wait gives up after the call's wait limit and
 // raises the CTA's abort flag; later waits of the CTA then give up at once.
@@ -718,19 +720,35 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
           named_bar_sync(2, 128);
           if (32 * q < half) {                          // warps holding gate rows
             const int f = 64 * t + r;
+            float hv[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-              float hv = 0.f;
+              hv[k] = 0.f;
               if (r < half && c0 + k < p.M) {
                 const float gv = v[k] * __ldg(p.a_scale + c0 + k);
-                hv = gv / (1.f + expf(-gv)) * xchg[r * kXchgStride + k];
-                p.h[static_cast<size_t>(c0 + k) * p.F + f] = hv;
+                hv[k] = gv / (1.f + expf(-gv)) * xchg[r * kXchgStride + k];
+                p.h[static_cast<size_t>(c0 + k) * p.F + f] = hv[k];
               }
-              float mx = fabsf(hv);
-#pragma unroll
-              for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-              if (lane == 0 && c0 + k < p.M) atomicMax(p.h_amax + c0 + k, __float_as_uint(mx));
+              hv[k] = fabsf(hv[k]);
             }
+            // per token the warp's max|h| by a transposing butterfly (16
+            // shuffles for the 16 tokens): at each step a lane keeps half of
+            // its tokens and takes the partner's values of them; lane l ends
+            // with token 8 b4 + 4 b3 + 2 b2 + b1 (b: the bits of l)
+#pragma unroll
+            for (int st = 0; st < 4; ++st) {
+              const int mask = 16 >> st, hn = 8 >> st;
+              const bool hi = (lane & mask) != 0;
+#pragma unroll
+              for (int i = 0; i < hn; ++i) {
+                const float keep = hi ? hv[hn + i] : hv[i];
+                const float send = hi ? hv[i] : hv[hn + i];
+                hv[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, mask));
+              }
+            }
+            hv[0] = fmaxf(hv[0], __shfl_xor_sync(0xffffffffu, hv[0], 1));
+            const int tk = 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
+            if ((lane & 1) == 0 && c0 + tk < p.M) atomicMax(p.h_amax + c0 + tk, __float_as_uint(hv[0]));
           }
           named_bar_sync(2, 128);                        // xchg is reused by the next chunk
         }
@@ -925,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         // acquire add after a barrier counts the CTA; the last one learns
         // that all CTAs' are visible
         named_bar_sync(2, 128);
-        if (leader) *last_flag = p.fuse_quant && atom_add_acq_rel_gpu(p.h_done, 1u) == gridDim.x - 1u;
+        if (leader) *last_flag = atom_add_acq_rel_gpu(p.h_done, 1u) == gridDim.x - 1u;
       }
     }
   }
@@ -938,8 +956,9 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
   if constexpr (GATE_UP) {
     if (*last_flag) {
       // The last CTA: per token the scale s = max|h| / 448 (1 for an
-      // all-zero token), then every product h / s to E4M3 (nearest even,
-      // saturating), all threads over each token's row; then the maxima and
+      // all-zero token); with few products, every product h / s to E4M3
+      // (nearest even, saturating), all threads over each token's row (else
+      // gate_up_quant_kernel does that from the scales); then the maxima and
       // the count go back to zero for the next call.
       float* s_tok = xchg;                           // [M] scales
       if (tid < p.M) {
@@ -949,6 +968,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
         p.q_scale[tid] = sc;
       }
       __syncthreads();
+      if (p.fuse_quant) {
       // the M x F products as one flat array (rows are contiguous in h and
       // q): four float4 loads in flight per thread, token of element i = i / F
       FastDiv by_f;
@@ -977,6 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
       for (int i = 4 * n4 + tid; i < total; i += kThreads)   // the last total % 4 products
         p.q[i] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(__ldcg(p.h + i) / s_tok[by_f.div(i)], __NV_SATFINITE,
                                                              __NV_E4M3));
+      }
       __syncthreads();
       if (tid < p.M) p.h_amax[tid] = 0u;
       if (tid == 0) *p.h_done = 0u;
@@ -990,23 +1011,35 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
 
 int ntok_for(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
-// Quantise the gate-up products of one token (one CTA per token): scale
-// s = max|h| / 448 (1 for an all-zero token), q = E4M3(h / s) rounded to
-// nearest even, saturating; then clear the token's running max so the
-// workspace is zero again for the next call.
-__global__ void __launch_bounds__(1024) gate_up_quant_kernel(const float* __restrict__ h, unsigned* amax, int F,
-                                                              uint8_t* __restrict__ q, float* __restrict__ s_out) {
-  grid_dependency_wait();                         // h and the maxima of the matmul kernel
-  const int m = blockIdx.x;
-  const float a = __uint_as_float(*reinterpret_cast<volatile unsigned*>(amax + m));
-  const float s = a > 0.f ? a / 448.f : 1.f;
+constexpr int kQuantThreads = 256;
+constexpr int kQuantChunk = 8 * kQuantThreads;        // products of one CTA: eight a thread
+
+// The products of one token in chunks of 2048, eight consecutive products a
+// thread: h / s to E4M3 (nearest even, saturating) with the token's scale s,
+// which the matmul's last CTA wrote.
+__global__ void __launch_bounds__(kQuantThreads) gate_up_quant_kernel(const float* __restrict__ h,
+                                                                      const float* __restrict__ scale, int F,
+                                                                      uint8_t* __restrict__ q) {
+  grid_dependency_wait();                         // h and the scales of the matmul kernel
+  const int m = blockIdx.y;
+  const float s = scale[m];
   const float* hr = h + static_cast<size_t>(m) * F;
   uint8_t* qr = q + static_cast<size_t>(m) * F;
-  for (int f = threadIdx.x; f < F; f += blockDim.x)
-    qr[f] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(hr[f] / s, __NV_SATFINITE, __NV_E4M3));
-  if (threadIdx.x == 0) s_out[m] = s;
-  __syncthreads();
-  if (threadIdx.x == 0) amax[m] = 0u;
+  const int f0 = blockIdx.x * kQuantChunk + 8 * threadIdx.x;
+  const bool vec = (F & 7) == 0 && (reinterpret_cast<uintptr_t>(q) & 7) == 0;   // 32-byte rows of h, 8 of q
+  if (vec && f0 + 8 <= F) {
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(hr + f0));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(hr + f0 + 4));
+    const float e[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i >> 2] |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(e[i] / s, __NV_SATFINITE, __NV_E4M3)) << (8 * (i & 3));
+    *reinterpret_cast<uint2*>(qr + f0) = make_uint2(w[0], w[1]);
+  } else {
+    for (int f = f0; f < min(F, f0 + 8); ++f)
+      qr[f] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(__ldcg(hr + f) / s, __NV_SATFINITE, __NV_E4M3));
+  }
 }
 
 // Products up to which the last CTA of the matmul quantises them itself.
@@ -1225,8 +1258,8 @@ int launch_sk_gate_up(const SkParams& p_in, void* workspace, size_t ws_bytes, ui
   const int st = launch_planned(p, pl, reinterpret_cast<float*>(ws + kFixedBytes), reinterpret_cast<unsigned*>(ws),
                                 kGateUp, stream);
   if (st != CBQ_OK || p.fuse_quant) return st;
-  return launch_pdl(gate_up_quant_kernel, dim3(p.M), dim3(1024), 0, stream, static_cast<const float*>(p.h),
-                    p.h_amax, F, q, q_scale) == cudaSuccess
+  return launch_pdl(gate_up_quant_kernel, dim3((F + kQuantChunk - 1) / kQuantChunk, p.M), dim3(kQuantThreads), 0,
+                    stream, static_cast<const float*>(p.h), static_cast<const float*>(q_scale), F, q) == cudaSuccess
              ? CBQ_OK
              : CBQ_ECUDA;
 }

@@ -166,8 +166,9 @@ int cbq_gemm_ws(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
  *            cbq_gate_up_workspace_size bytes (it also holds h in fp32)
  * One launch on `stream` up to M * F = 8192 products (the stream-K matmul
  * with the SiLU-product epilogue; the CTA that finishes last quantises every
- * product), else two (a per-token quantisation kernel follows); each a
- * programmatic dependent of the kernel before it.
+ * product), else two (the matmul's last CTA writes the per-token scales,
+ * and a quantisation kernel over chunks of 2048 products per token follows);
+ * each a programmatic dependent of the kernel before it.
  * Errors: CBQ_EINVAL (also when the stream-K kernel cannot take the shape:
  * the size query then gives 0), CBQ_EDEVICE, CBQ_ECUDA. */
 int cbq_gemm_gate_up(const uint8_t *a, const float *a_scale, const cbq_weight_t *w,
