@@ -87,6 +87,27 @@ def test_gate_up_full_size(name, M):
     assert ops.device_status() == ops.OK
 
 
+@pytest.mark.parametrize("M,F,K", [(3, 100, 640), (16, 1100, 384)])
+def test_gate_up_gives_up_then_the_next_call_is_exact(M, F, K):
+    # quantised by the matmul's last CTA (M F <= 8192) and by the separate
+    # kernel (M F > 8192): after a forced give-up every CTA still counts
+    # itself, so the per-token maxima and the count of finished CTAs are back
+    # to zero and the next call on the same workspace is exact
+    c = Case(M, 2 * F, K, seed=800 + M + F)
+    a, s, w = c.device()
+    ops.set_wait_limit(2)                      # the first wait not already satisfied gives up
+    try:
+        ops.gate_up(a, s, w)
+        torch.cuda.synchronize()
+    finally:
+        ops.set_wait_limit(0)
+    assert ops.device_status() == ops.ETIMEOUT
+    h, hs = ops.gate_up(a, s, w)
+    torch.cuda.synchronize()
+    check_gate_up(h.cpu().numpy(), hs.cpu().numpy(), c.a, c.s, c.pw, M, F, K, f"after a give-up, M {M} F {F}")
+    assert ops.device_status() == ops.OK
+
+
 def test_gate_up_rejects_bad_arguments():
     c = Case(2, 128, 128, seed=3)
     a, s, w = c.device()
