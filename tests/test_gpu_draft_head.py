@@ -77,6 +77,23 @@ def test_draft_head_full_size(name):
     _check_head(wl.M, wl.N, wl.K, seed=77)
 
 
+def test_draft_head_gives_up_then_the_next_call_is_exact():
+    # the 2-bit matmul gives up (its scores are then incomplete); the
+    # shortlist kernels still read in-bounds rows (a word always carries a
+    # real row), and the next call on the same workspace is exact
+    M, N, K = 2, 3000, 512
+    h2, h8, rs, a, s = _case(M, N, K, 5)
+    w, dh8, drs, da, ds = _device(h2, h8, rs, a, s)
+    ops.set_wait_limit(2)                      # the first wait not already satisfied gives up
+    try:
+        ops.draft_head(da, ds, w, dh8, drs)
+        torch.cuda.synchronize()
+    finally:
+        ops.set_wait_limit(0)
+    assert ops.device_status() == ops.ETIMEOUT
+    _check_head(M, N, K, seed=5)
+
+
 def test_draft_head_rejects_bad_arguments():
     L = ops.lib()
     import ctypes
