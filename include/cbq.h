@@ -37,7 +37,14 @@
  *     default stream) and never synchronise the host;
  *   - the return value is CBQ_OK or a negative CBQ_E* code; on an argument
  *     error nothing is launched; nothing throws across the ABI;
- *   - requires an sm_103 (GB300) or sm_100 class GPU; K % 128 == 0.
+ *   - requires an sm_103 (GB300) or sm_100 class GPU; K % 128 == 0;
+ *   - the stream-K kernel (every call that takes a workspace and runs it)
+ *     is launched as a programmatic dependent of the previous kernel on
+ *     `stream`: it may start streaming the packed weights before that kernel
+ *     has finished, and reads activations, routing and scratch or writes
+ *     outputs only after it has; so the packed weights must not be written
+ *     by the kernel launched just before the call on the same stream (copies
+ *     and host writes are fine).
  */
 #ifndef CBQ_H
 #define CBQ_H
