@@ -71,6 +71,41 @@ EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
+int encode_activation_map(CUtensorMap* out, const uint8_t* a, int M, int K, int ntok) {
+  // the last maps this thread encoded (encoding is host work on every call
+  // otherwise); a small direct-mapped table keyed on (a, M, K, ntok)
+  struct Entry {
+    const uint8_t* a = nullptr;
+    int M = 0, K = 0, ntok = 0;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 16;
+  thread_local Entry table[kEntries];
+  const uintptr_t h = (reinterpret_cast<uintptr_t>(a) >> 8) ^ static_cast<uintptr_t>(M) * 31u ^
+                      static_cast<uintptr_t>(K) * 131u ^ static_cast<uintptr_t>(ntok) * 7u;
+  Entry& e = table[h % kEntries];
+  if (e.a == a && e.M == M && e.K == K && e.ntok == ntok) {
+    *out = e.map;
+    return CBQ_OK;
+  }
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return CBQ_ECUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(ntok)};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return CBQ_ECUDA;
+  e.a = a;
+  e.M = M;
+  e.K = K;
+  e.ntok = ntok;
+  e.map = *out;
+  return CBQ_OK;
+}
+
 int device_sm_count() {
   DeviceInfo* d = nullptr;
   if (current_device_checked(&d) != CBQ_OK) return 1;

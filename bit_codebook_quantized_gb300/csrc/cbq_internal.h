@@ -75,6 +75,11 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
+// Activations a[M][K] (E4M3 bytes, row-major) as a TMA tensor whose box is one
+// 128-byte k-tile of `ntok` token rows, landed with the 128-byte swizzle (rows
+// past M read as zeros).  The map depends on (a, M, K, ntok) only, so the
+// calling thread keeps the last maps it encoded.  CBQ_OK or CBQ_ECUDA.
+int encode_activation_map(CUtensorMap* out, const uint8_t* a, int M, int K, int ntok);
 
 int device_sm_count();
 void note_launch();

@@ -1145,19 +1145,7 @@ int launch_t(const SkParams& p, const Plan& pl, cudaStream_t stream) {
 // Activations a[M][K] as a TMA tensor whose box is one k-tile of `ntok`
 // token rows: a 2-D view with a (128 B, ntok) box and the 128-byte swizzle;
 // rows past M read as zeros.
-int encode_a_map(SkParams& p, int ntok) {
-  EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return CBQ_ECUDA;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.M)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K)};
-  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(ntok)};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(&p.a_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.a), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
-             ? CBQ_OK
-             : CBQ_ECUDA;
-}
+int encode_a_map(SkParams& p, int ntok) { return encode_activation_map(&p.a_map, p.a, p.M, p.K, ntok); }
 
 int launch_planned(const SkParams& p_in, const Plan& pl, float* partial, unsigned* counters, Mode mode,
                    cudaStream_t stream, int bits = 3) {

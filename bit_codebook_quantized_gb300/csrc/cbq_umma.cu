@@ -706,19 +706,7 @@ int ntok_for(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
 // Activations a[M][K] as a TMA tensor whose box is one k-tile (128 bytes) of
 // ntok token rows, landed with the 128-byte swizzle; rows past M read as zeros.
-int encode_a_map(UmmaParams& p, int ntok) {
-  EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return CBQ_ECUDA;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.M)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K)};
-  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(ntok)};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(&p.a_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.a), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
-             ? CBQ_OK
-             : CBQ_ECUDA;
-}
+int encode_a_map(UmmaParams& p, int ntok) { return encode_activation_map(&p.a_map, p.a, p.M, p.K, ntok); }
 
 }  // namespace
 
