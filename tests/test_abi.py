@@ -197,6 +197,26 @@ def test_workspace_size_covers_counters_and_partials(L):
     assert L.cbq_grouped_workspace_size(5000, 8, 64, 1536, 2048, ctypes.byref(n)) == ops.EINVAL
 
 
+def test_draft_head_sizes(L):
+    # the 2-bit head: KN/4 code bytes, KN/32 scale bytes, 4N codebook bytes
+    c, sc, cb = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.cbq_head2_sizes(151936, 2048, ctypes.byref(c), ctypes.byref(sc), ctypes.byref(cb)) == ops.OK
+    assert (c.value, sc.value, cb.value) == (2048 * 151936 // 4, 2048 * 151936 // 32, 4 * 151936)
+    assert L.cbq_head2_sizes(100, 96, ctypes.byref(c), ctypes.byref(sc), ctypes.byref(cb)) == ops.EINVAL
+    # the draft-head workspace: the stream-K scratch (fixed area + two partial
+    # tiles per CTA; 1 CTA without a device), the scores M x N fp32 and the
+    # chunk lists M x ceil(N / 1024) x 16 words, each part rounded to 256 bytes
+    r256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    n = ctypes.c_size_t()
+    for M, N, K in [(1, 151936, 2048), (8, 1030, 256), (64, 262144, 128)]:
+        assert L.cbq_draft_head_workspace_size(M, N, K, ctypes.byref(n)) == ops.OK
+        ntok = 16 if M <= 16 else (32 if M <= 32 else 64)
+        want = r256(65536 * 4 + 512 + 2 * 128 * ntok * 4) + r256(M * N * 4) + r256(M * (-(-N // 1024)) * 16 * 8)
+        assert n.value == want, (M, N, K)
+    for M, N, K in [(0, 64, 128), (65, 64, 128), (1, 15, 128), (1, 262145, 128), (1, 64, 96), (1, 64, 0)]:
+        assert L.cbq_draft_head_workspace_size(M, N, K, ctypes.byref(n)) == ops.EINVAL, (M, N, K)
+
+
 def test_library_pack_matches_the_hand_worked_lloyd_row(golden_dir):
     # the library's quantiser (its own code) on the hand-worked Lloyd row
     from tests.test_oracle import lloyd_golden_row
