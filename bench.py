@@ -810,6 +810,23 @@ def run_single(args):
     from bit_codebook_quantized_gb300 import build as _b
     _b.build()
     dev = torch.device("cuda", 0)
+    gu = {name: (M, F, K) for name, M, F, K in GATE_UP_POINTS}
+    if args.single in gu:
+        # the fused gate-up step: matmul with the SiLU-product epilogue, then
+        # the per-token E4M3 quantisation
+        M, F, K = gu[args.single]
+        pw = synth.gen_weights(2 * F, K, seed=1)
+        w = ops.PackedWeights.from_host(pw.codes, pw.scales, pw.codebooks, 2 * F, K, device=dev)
+        a = torch.from_numpy(synth.gen_activations(M, K, seed=2)).to(dev)
+        s = torch.from_numpy(synth.gen_a_scale(M, seed=3, mode="uniform")).to(dev)
+        for _ in range(args.calls):
+            ops.gate_up(a, s, w)
+        torch.cuda.synchronize()
+        st = ops.device_status()
+        print(json.dumps({"single": args.single, "calls": args.calls, "status": st}))
+        if st != ops.OK:
+            sys.exit(1)
+        return
     if args.single in synth.budget_workloads():
         # the verify round's expert budget on seeded router logits
         T, E, k, B = synth.budget_workloads()[args.single]
@@ -874,7 +891,8 @@ def main(argv=None):
                     help="--impl reference: CPU seconds the whole run should take")
     ap.add_argument("--single", default=None,
                     help="run --calls calls of one workload (see synth.workloads(), "
-                         "synth.draft_head_workloads() and synth.budget_workloads()) and exit")
+                         "synth.draft_head_workloads(), synth.budget_workloads() and the gate-up "
+                         "points, e.g. gate_up_4096x6144_m8) and exit")
     ap.add_argument("--path", type=int, default=0, help="kernel for --single: 0 auto, 1 gemv, 2 mma, 3 stream-K")
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--per-config-calls", type=int, default=250,
