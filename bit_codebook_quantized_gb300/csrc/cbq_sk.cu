@@ -298,6 +298,18 @@ __global__ void __launch_bounds__(kThreads, 1) sk_kernel(const __grid_constant__
     Share r;
     r.u0 = geo.first_unit(b0 < geo.G ? b0 : geo.G);
     r.n_units = static_cast<int>(geo.first_unit(b1 < geo.G ? b1 : geo.G) - r.u0);
+    if constexpr (GROUPED) {
+      // whole tiles per CTA (no partial-tile fix-up) when the used experts'
+      // T tiles spread over the G CTAs with at most 10 % over the mean and a
+      // CTA's activation slots hold every k-tile of a row (MoE round: 288
+      // tiles on 152 CTAs, 31.9 -> 27.5 us)
+      const long long T = geo.U / geo.KT, G = geo.G;
+      if (geo.KT <= p.b_ktiles && T >= G && ((T + G - 1) / G) * G * 10 <= 11 * T) {
+        const long long tb0 = (b0 < G ? b0 : G) * T / G, tb1 = (b1 < G ? b1 : G) * T / G;
+        r.u0 = tb0 * geo.KT;
+        r.n_units = static_cast<int>((tb1 - tb0) * geo.KT);
+      }
+    }
     r.n_stages = (r.n_units + kUnitsPerStage - 1) / kUnitsPerStage;
     r.t_first = static_cast<int>(static_cast<uint32_t>(r.u0) / static_cast<uint32_t>(geo.KT));
     r.c_first = static_cast<int>(r.u0) - r.t_first * geo.KT;
