@@ -60,7 +60,7 @@ def _check_head(M, N, K, seed, zero_codebooks=False):
 
 @pytest.mark.parametrize("M,N,K", [(1, 200, 640), (3, 130, 256), (16, 1000, 384), (64, 300, 1024), (8, 16, 128),
                                    (2, 1024, 128), (2, 1030, 256), (1, 16 * 1024 + 7, 128), (4, 40000, 256),
-                                   (2, 100000, 256), (1, 150000, 128)])
+                                   (2, 100000, 256), (1, 150000, 128), (1, 262144, 128)])
 def test_draft_head_small(M, N, K):
     _check_head(M, N, K, seed=M + N + K)
 
