@@ -88,6 +88,9 @@ constexpr int kUnitsPerStage = 4;
 constexpr int kStageBytes = kUnitsPerStage * kUnitBytes;   // 24 KB
 constexpr int kMaxStages = 8;
 constexpr int kGroups = 3;                            // decoder groups: unit i -> group i % 3
+// the decoders step a group's stage position by kGroups units with one wrap,
+// and start it at its group number without one
+static_assert(kUnitsPerStage >= kGroups, "a group's next unit lies in this stage or the next");
 constexpr int kMaxSlots = 2;                          // decoded units in TMEM per group (at most)
 constexpr int kProdWarp = 0;                          // code stream
 constexpr int kAllocWarp = 1;                         // TMEM allocation (also group 0's MMA warp)
