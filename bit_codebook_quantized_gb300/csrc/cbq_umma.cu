@@ -220,11 +220,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
   // ---- which units does this CTA own? ----
   int n_units, u_begin, u_step;
   if constexpr (GROUPED) {
-    const int nr = p.M * p.topk;
+    const int nr = p.M * p.topk;                       // <= kThreads (64 x 8)
+    const int e_mine = tid < nr ? p.topk_idx[tid] : 0; // load issued before the flags are cleared
     for (int e = tid; e < p.E; e += kThreads) used_flag[e] = 0;
     __syncthreads();
     for (int i = tid; i < nr; i += kThreads) {
-      const int e = p.topk_idx[i];
+      const int e = i == tid ? e_mine : p.topk_idx[i];
       topk_s[i] = e;
       if (e >= 0 && e < p.E) used_flag[e] = 1;
       else raise(kErrRouting);
@@ -248,9 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const __grid_constant
     }
     __syncthreads();
     // contiguous blocks of (expert, tile) units so consecutive units share an expert
-    const int total = misc[1] * tiles;
-    u_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * total) / gridDim.x);
-    n_units = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total) / gridDim.x) - u_begin;
+    // floor(b total / G) = b q + floor(b r / G) with total = q G + r, in
+    // 32-bit arithmetic (b r < G^2)
+    const uint32_t total = static_cast<uint32_t>(misc[1] * tiles), G = gridDim.x;
+    const uint32_t q = total / G, rem = total - q * G, b = blockIdx.x;
+    u_begin = static_cast<int>(b * q + (b * rem) / G);
+    n_units = static_cast<int>((b + 1) * q + ((b + 1) * rem) / G) - u_begin;
     u_step = 1;
   } else {
     u_begin = cluster_id;
